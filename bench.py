@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Throughput of the W4A16 routed-expert MoE layer on GB300.
+
+One step = the whole layer on one batch of synthetic tokens: moe_route
+(router GEMM, softmax, top-k, renormalised weights) then moe_w4a16_forward
+(permute, INT4 expert GEMMs with SiLU*up, weighted combine). The stack
+workloads run 48 such layers, each followed by the residual + RMS rescale.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints one JSON line. Workloads (shapes from "Running 125B MoE on Three
+3090s - vLLM Edition", section 1): decode1 (T=1, the default), decode4,
+decode64, prefill512 (Zipf-skewed routing), stack_prefill4096 and
+stack_decode4 (48 layers).
+
+Timing: inputs resident in HBM; each step is a CUDA-graph replay; steps
+rotate over independent weight sets so that no step finds its experts in L2
+(their total exceeds the 129 MB L2); CUDA events on the launching stream;
+>= 3 warm-up steps. The expert kernel's own time is taken from events that
+the library records around it inside the same graphs. `e2e` repeats the
+timing through the same public calls with the step's tokens copied in from
+pinned host memory and its output copied back, inside the timed region.
+The CPU baseline is the fp64 oracle on a bounded sample of the workload.
+Multi-GPU: independent replicas (the layer has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+EXPERT_BYTES = 2_534_400          # packed INT4 + bf16 scales of one full-shape expert
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sets", type=int, default=0, help="weight sets to rotate over (0: enough to exceed L2)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def cpu_baseline(wl, seed: int, target_s: float):
+    """The fp64 oracle on a bounded sample of tokens of the workload (tok/s)."""
+    import oracle
+    T, H, E, k, I = wl.dims
+    oracle.build()
+    x = synth.hidden(max(T, 1), H, seed=seed)
+    wr = synth.router(E, H, seed=seed, layer=0)
+    bias = synth.zipf_bias(E, wl.zipf, seed=seed) if wl.zipf else None
+
+    def run(rows):
+        xs = x[rows]
+        ids, w, _ = oracle.route(xs, wr, k, bias)
+        held = np.unique(ids)
+        row = np.full(E, -1, np.int32)
+        row[held] = np.arange(len(held))
+        wts = synth.expert_weights(E, H, I, seed=seed, layer=0, experts=held)
+        t0 = time.perf_counter()
+        oracle.route(xs, wr, k, bias)
+        oracle.expert_forward(xs, ids, w.astype(np.float32), wts["w1_packed"], wts["w1_scales"],
+                              wts["w2_packed"], wts["w2_scales"], E, I, expert_row=row)
+        return time.perf_counter() - t0
+
+    cores = oracle.max_threads()
+    n = min(cores, x.shape[0])
+    rows = np.arange(n) % x.shape[0]
+    t = run(rows)
+    reps = max(1, min(64, int(target_s / max(t, 1e-3))))
+    if reps > 1:
+        rows = np.arange(n * reps) % x.shape[0]
+        t = run(rows)
+    ntok = len(rows)
+    layers = wl.layers
+    return {"value": ntok / t / layers, "unit": "tok/s", "cores": min(cores, ntok), "kind": "oracle",
+            "sample": "%d tokens of workload %s through one layer (route + experts), fp64, %.1f s%s"
+                      % (ntok, wl.name, t, "; divided by %d layers" % layers if layers > 1 else "")}
+
+
+# ------------------------------------------------------------- our arm -----
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a16_mixture_experts_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per launch of the expert kernel from a committed ncu capture, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(config)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args, rank, world, local):
+    import w4a16_mixture_experts_gb300 as moe
+    moe.build()
+    moe.lib()
+    wl = synth.WORKLOADS[args.config]
+    T, H, E, k, I = wl.dims
+    stack = wl.layers > 1
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # weight sets: the stack's 48 layers, or enough single layers to exceed L2
+    if stack:
+        nsets = wl.layers
+    elif args.sets:
+        nsets = args.sets
+    else:
+        touched = min(E, T * k) * EXPERT_BYTES
+        nsets = max(2, min(16, math.ceil(2.5 * L2_BYTES / touched)))
+    seed = args.seed + 1000 * rank
+    sets = []
+    for i in range(nsets):
+        d = synth.layer_inputs(wl, seed=seed, layer=i)
+        if not stack:
+            d["hidden"] = synth.hidden(T, H, seed=seed, layer=i)
+        sets.append({key: (v.to(dev) if v is not None else None) for key, v in d.items()})
+        if stack and i > 0:
+            sets[i]["hidden"] = None
+    x0 = sets[0]["hidden"]
+    ws = moe.workspace(T, H, E, k, I, dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    act = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    stream = torch.cuda.Stream(device=dev)
+    n_exp_launch = wl.layers
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nsets * (1 if not stack else 1))]
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ev_b))]
+    unique = [0] * nsets
+
+    def step(i, profile=False):
+        """Enqueue one step (set i for single layers; all layers for the stack)."""
+        if stack:
+            x = x0
+            for l in range(wl.layers):
+                s = sets[l]
+                if profile:
+                    moe.moe_profile_events(ev_b[l], ev_a[l])
+                moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
+                nxt = act[l % 2]
+                moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
+                                          s["w2_scales"], eps=1e-6, next=nxt, ws=ws)
+                x = nxt
+            return x
+        s = sets[i]
+        if profile:
+            moe.moe_profile_events(ev_b[i], ev_a[i])
+        moe.moe_route(s["hidden"], s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
+        moe.moe_w4a16_forward(s["hidden"], ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
+                              s["w2_scales"], out=out, ws=ws)
+        return out
+
+    with torch.cuda.stream(stream):
+        # warm-up, and the unique experts each set touches
+        for i in range(max(args.warmup, nsets if not stack else 1)):
+            step(i % nsets)
+            if not stack and i < nsets:
+                torch.cuda.current_stream().synchronize()
+                unique[i] = len(torch.unique(ids).tolist())
+        stream.synchronize()
+        if stack:
+            # unique experts per layer along the stack's own routing
+            x = x0
+            for l in range(wl.layers):
+                s = sets[l]
+                moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
+                moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
+                                          s["w2_scales"], eps=1e-6, next=act[l % 2], ws=ws)
+                stream.synchronize()
+                unique[l] = len(torch.unique(ids).tolist())
+                x = act[l % 2]
+        assert moe.moe_check_device_error(ws, stream) == 0
+
+        graphs = []
+        use_graph = not args.no_graph
+        if use_graph:
+            try:
+                for i in range(1 if stack else nsets):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        step(i, profile=True)
+                    graphs.append(g)
+                moe.moe_profile_events(None, None)
+            except Exception as exc:  # capture not possible: time eagerly
+                moe.moe_profile_events(None, None)
+                print("graph capture failed (%s); timing eager launches" % exc, file=sys.stderr)
+                graphs, use_graph = [], False
+
+        def replay(i):
+            if use_graph:
+                graphs[0 if stack else i % nsets].replay()
+            else:
+                step(i % nsets, profile=True)
+
+        for i in range(args.warmup):
+            replay(i)
+        stream.synchronize()
+        barrier(world)
+
+        clocks = Clocks(local)
+        clocks.start()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            replay(i)
+        t1.record(stream)
+        stream.synchronize()
+        ms = t0.elapsed_time(t1)
+        clk = clocks.stop()
+        moe.moe_profile_events(None, None)
+        assert moe.moe_check_device_error(ws, stream) == 0
+
+        # expert kernel durations of the last replay of each graph
+        if stack:
+            durs = [ev_b[l].elapsed_time(ev_a[l]) for l in range(wl.layers)]
+            bytes_l = [u * EXPERT_BYTES for u in unique]
+        else:
+            m = min(args.steps, nsets)
+            last = [(args.steps - 1 - j) % nsets for j in range(m)]
+            durs = [ev_b[i].elapsed_time(ev_a[i]) for i in last]
+            bytes_l = [unique[i] * EXPERT_BYTES for i in last]
+
+        # end to end: tokens in from pinned host memory, output back, every step
+        h_in = [sets[i % nsets]["hidden"].cpu().pin_memory() if not stack else x0.cpu().pin_memory()
+                for i in range(1 if stack else nsets)]
+        h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        dst_in = [x0 if stack else sets[i]["hidden"] for i in range(1 if stack else nsets)]
+        final = act[(wl.layers - 1) % 2] if stack else out
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            j = 0 if stack else i % nsets
+            dst_in[j].copy_(h_in[j], non_blocking=True)
+            replay(i)
+            h_out.copy_(final, non_blocking=True)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            j = 0 if stack else i % nsets
+            dst_in[j].copy_(h_in[j], non_blocking=True)
+            replay(i)
+            h_out.copy_(final, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        ms_e2e = e0.elapsed_time(e1)
+
+    ms = max_over_ranks(ms, world)
+    ms_e2e = max_over_ranks(ms_e2e, world)
+    launches_per_layer = 2 + (3 if T > 0 else 0) + 1 + 1   # route 2, permute 3, experts 1, combine 1
+    pk, pk_src = peaks()
+    achieved = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
+    res = {
+        "metric": "MoE layer tok/s (%s)" % wl.name,
+        "value": world * T * args.steps / (ms * 1e-3),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 activations x int4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; shapes and distributions of the pages' workload; random weights)",
+        "config": {"workload": wl.name, "T": T, "H": H, "E": E, "k": k, "I": I, "layers": wl.layers,
+                   "zipf": wl.zipf, "weight_sets": nsets,
+                   "l2": "rotating %d independent weight sets (> L2) between steps" % nsets
+                   if not stack else "48 layers x 1.3 GB of weights per step (> L2)",
+                   "graph": use_graph, "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "decode_experts_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "peak_source": pk_src + " hbm_gbs (copy)", "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": recorded_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": statistics.mean(bytes_l),
+                     "kernel_ms_per_launch": statistics.mean(durs), "launches_measured": len(durs),
+                     "unique_experts_per_launch": statistics.mean(bytes_l) / EXPERT_BYTES},
+        "e2e": {"value": world * T * args.steps / (ms_e2e * 1e-3), "unit": "tok/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": args.steps * wl.layers * launches_per_layer,
+        "clocks": clk,
+    }
+    return res
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    wl = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        if rank == 0:
+            cb = cpu_baseline(wl, args.seed, args.cpu_seconds * max(1, args.steps) / max(1, args.steps))
+            line = {"impl": "reference", "metric": "MoE layer tok/s (%s)" % wl.name, "value": cb["value"],
+                    "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                    "data": "synthetic", "config": {"workload": wl.name},
+                    "cpu_baseline": cb,
+                    "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        res["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

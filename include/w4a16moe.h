@@ -1,0 +1,187 @@
+/*
+ * w4a16moe.h - C ABI of the GB300 (sm_103a) W4A16 routed-expert MoE layer.
+ *
+ * The layer is the routed-expert block of the 125B-A6B MoE described in
+ * "Running 125B MoE on Three 3090s - vLLM Optimization Edition", section 3.3
+ * "MoE block (decode-05)": a BF16 router GEMV, softmax and top-k with
+ * renormalised weights (norm_topk_prob), the token-to-expert alignment, and
+ * the fused W4A16 expert GEMMs (gate_up, SiluAndMul, down) followed by the
+ * weighted sum over the selected experts. Shapes are those of "Running 125B
+ * MoE on Three 3090s - vLLM Edition", section 1 "Shape of This Model"
+ * (hidden 2560, 512 experts, 10 per token, moe_intermediate 640); the weight
+ * format is group A of the model card's "What is quantized" table (INT4,
+ * group size 128, symmetric, compressed-tensors pack-quantized).
+ *
+ * Conventions for every call:
+ *  - All pointers except `dims`/`bytes` outputs are DEVICE pointers of the
+ *    current CUDA device, owned by the caller; the library never allocates,
+ *    frees or synchronises inside moe_route / moe_w4a16_forward /
+ *    moe_w4a16_forward_rms / moe_permute / moe_pack_int4.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
+ *    enqueued asynchronously; results are valid once the stream reaches them.
+ *  - bf16 tensors are passed as `uint16_t*` holding IEEE bfloat16 bits.
+ *  - Every tensor is row-major and contiguous; every pointer is 16-byte
+ *    aligned.
+ *  - Supported shapes: T >= 0, H and I multiples of 128, 1 <= k <= 32,
+ *    k <= E <= 1024, H <= 8192, I <= 4096. Others return
+ *    MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *  - Argument errors are returned synchronously and enqueue nothing. A
+ *    launch failure returns MOE_ERR_CUDA. Errors seen by a kernel (an expert
+ *    id outside [0, E), an internal wait that gave up) are recorded in the
+ *    workspace's error word and reported by moe_check_device_error.
+ *  - Workspace: `ws` must hold at least moe_workspace_size() bytes and must
+ *    be all zero before its first use (the library leaves the counters it
+ *    uses at zero when a call completes). One workspace must not be used by
+ *    two calls that may run concurrently.
+ */
+#ifndef W4A16MOE_H
+#define W4A16MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size */
+    MOE_ERR_UNSUPPORTED = 2,  /* shape outside the supported set */
+    MOE_ERR_WORKSPACE = 3,    /* workspace too small */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE = 5,       /* a kernel saw an expert id outside [0, E) */
+    MOE_ERR_TIMEOUT = 6       /* a kernel's bounded wait gave up */
+} moe_status;
+
+/* Layer dimensions: T tokens, hidden H, E experts, k experts per token,
+ * expert intermediate I. The quantisation group is fixed at 128. */
+typedef struct {
+    int32_t T, H, E, k, I;
+} moe_dims;
+
+/* Static description of a status code. Never NULL. */
+MOE_API const char *moe_status_str(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+MOE_API int moe_version(void);
+
+/* Workspace bytes needed by moe_route, moe_permute and the forward calls
+ * for dims `d`. Writes *bytes; returns MOE_OK or MOE_ERR_UNSUPPORTED /
+ * MOE_ERR_INVALID_ARG. */
+MOE_API int moe_workspace_size(moe_dims d, size_t *bytes);
+
+/*
+ * Router + softmax + top-k + renormalisation ("vLLM Optimization Edition",
+ * section 3.3 "MoE block": router GEMV, topk_softmax, norm_topk_prob, and
+ * the key that sends ties to the lower expert id).
+ *
+ *   logits[t][e] = sum_h hidden[t][h] * router_w[e][h] (+ bias[e])
+ *   topk_ids[t][0..k) = the k largest logits, in order of descending logit,
+ *                       ties to the lower id; ranked in fp32
+ *   topk_w[t][j]      = softmax over the k selected logits, which equals the
+ *                       renormalised full softmax
+ *
+ * hidden   bf16 [T][H]     router_w bf16 [E][H]
+ * bias     f32 [E] or NULL (added to the logits for selection and weights)
+ * topk_ids int32 [T][k]    topk_w   f32 [T][k]   (outputs)
+ */
+MOE_API int moe_route(const uint16_t *hidden, const uint16_t *router_w, const float *bias,
+              moe_dims d, int32_t *topk_ids, float *topk_w,
+              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Routed-expert forward ("vLLM Optimization Edition", section 3.3: the fused
+ * Marlin MoE gate_up, SiluAndMul, down, and moe_sum; weights as in the model
+ * card's group A):
+ *
+ *   W1[e][n][c] = (nibble c%8 of w1_packed[e][n][c/8] - 8) * w1_scales[e][n][c/128]
+ *   W2[e][n][c] likewise from w2_packed / w2_scales
+ *   for each token t and slot j, e = topk_ids[t][j]:
+ *     g = W1[e][0:I] . x_t,  u = W1[e][I:2I] . x_t,  h = SiLU(g) * u
+ *     out[t] += topk_w[t][j] * (W2[e] . h)
+ *   out is rounded to bf16 once.
+ *
+ * hidden    bf16 [T][H]         topk_ids int32 [T][k] in [0, E)
+ * topk_w    f32 [T][k]          (taken as given; need not sum to 1)
+ * w1_packed int32 [E][2I][H/8]  (rows [0,I) gate, [I,2I) up; low nibble first)
+ * w1_scales bf16 [E][2I][H/128]
+ * w2_packed int32 [E][H][I/8]   w2_scales bf16 [E][H][I/128]
+ * out       bf16 [T][H]         (output; must not overlap any input)
+ *
+ * Accumulation is fp32; the SiLU(g)*u activation is rounded to bf16 where it
+ * feeds the down projection. An id outside [0, E) sets MOE_ERR_DEVICE in the
+ * workspace and that slot contributes nothing.
+ */
+MOE_API int moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
+                      const int32_t *w1_packed, const uint16_t *w1_scales,
+                      const int32_t *w2_packed, const uint16_t *w2_scales,
+                      uint16_t *out, moe_dims d, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Forward followed by the residual and RMS rescale used between the layers
+ * of a stack (no learned weight):
+ *   r = hidden + moe(hidden) (fp32),  next[t] = bf16(r / sqrt(mean(r^2) + eps))
+ * Same arguments as moe_w4a16_forward; `next` bf16 [T][H] may not overlap
+ * `hidden`.
+ */
+MOE_API int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
+                          const int32_t *w1_packed, const uint16_t *w1_scales,
+                          const int32_t *w2_packed, const uint16_t *w2_scales,
+                          uint16_t *next, float eps, moe_dims d, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/*
+ * Token-to-expert permutation ("vLLM Optimization Edition", section 3.3:
+ * moe_align_block_size, here without block padding): per-expert counts,
+ * their exclusive prefix sum, and the assignments a = t*k + j listed expert
+ * by expert, in increasing a within an expert. Exposed for testing; the
+ * forward calls run the same kernels.
+ *
+ * topk_ids int32 [T][k]; offsets int32 [E+1] (output); perm int32 [T*k]
+ * (output). An id outside [0, E) sets MOE_ERR_DEVICE; such assignments are
+ * left out, so offsets[E] counts only valid ones.
+ */
+MOE_API int moe_permute(const int32_t *topk_ids, moe_dims d, int32_t *offsets, int32_t *perm,
+                void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Pack signed int4 values into the storage format of the weights (model
+ * card "What is quantized", pack-quantized): packed[n][w] holds
+ * q[n][8w..8w+7] + 8, value 8w+i in bits [4i, 4i+4).
+ * q int8 [N][K] with values in [-8, 7] (others are clamped and flagged in
+ * *bad_count, a device int32 that is incremented, may be NULL);
+ * packed int32 [N][K/8]. K must be a multiple of 8.
+ */
+MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed,
+                  int32_t *bad_count, void *stream);
+
+/*
+ * Profiling aid (no counterpart on the pages): from now on, every forward
+ * call records `before_experts` on its stream just before it launches the
+ * expert kernel and `after_experts` just after it, so that the caller can
+ * time that kernel alone with cudaEventElapsedTime. Both are cudaEvent_t
+ * handles owned by the caller (created with timing enabled); while the stream
+ * is being captured into a CUDA graph they become event-record nodes. Pass
+ * NULL, NULL to stop. The setting is process-wide and not thread-safe.
+ */
+MOE_API int moe_profile_events(void *before_experts, void *after_experts);
+
+/*
+ * Synchronises `stream`, then reads and clears the workspace's error word.
+ * Returns MOE_OK, MOE_ERR_DEVICE or MOE_ERR_TIMEOUT (or MOE_ERR_CUDA if the
+ * synchronisation itself failed).
+ */
+MOE_API int moe_check_device_error(void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16MOE_H */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library must build for sm_103a, load, export every entry point that
+include/w4a16moe.h declares, and reject bad arguments synchronously, before
+touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a16_mixture_experts_gb300 as moe
+from w4a16_mixture_experts_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return moe.lib()
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("moe_route", "moe_w4a16_forward", "moe_workspace_size", "moe_permute", "moe_pack_int4",
+              "moe_check_device_error", "moe_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared():
+        assert hasattr(L, name), name
+    out = os.popen("nm -D --defined-only %s" % moe.LIB_PATH).read()
+    exported = set(re.findall(r"\bT (moe_\w+)", out))
+    assert set(declared()) <= exported
+    assert all(n in declared() for n in exported), "undeclared export"
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert moe.moe_status_str(s)
+    assert moe.moe_status_str(99) == "unknown status"
+    assert moe.moe_version() >= 100
+
+
+def test_workspace_size_and_shape_rules(L):
+    n = moe.moe_workspace_size(1, 2560, 512, 10, 640)
+    assert n > 0 and n % 256 == 0
+    assert moe.moe_workspace_size(64, 2560, 512, 10, 640) > n
+    bad = [
+        (1, 2560 + 64, 512, 10, 640),   # H not a multiple of 128
+        (1, 2560, 512, 10, 600),        # I not a multiple of 128
+        (1, 2560, 512, 33, 640),        # k > 32
+        (1, 2560, 2048, 10, 640),       # E > 1024
+        (1, 2560, 8, 10, 640),          # k > E
+        (1, 16384, 512, 10, 640),       # H > 8192
+    ]
+    for dims in bad:
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_workspace_size(*dims)
+        assert ei.value.status == 2
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_size(-1, 2560, 512, 10, 640)
+    assert ei.value.status == 1
+
+
+def _call_forward(L, dims, ptrs, ws_bytes):
+    return L.moe_w4a16_forward(*[ctypes.c_void_p(p) for p in ptrs[:7]], ctypes.c_void_p(ptrs[7]), dims,
+                               ctypes.c_void_p(ptrs[8]), ws_bytes, None)
+
+
+def test_argument_errors_are_synchronous(L):
+    """Fake, never-dereferenced addresses: every call must fail before any CUDA work."""
+    d = moe.moe_dims(4, 256, 16, 2, 128)
+    need = moe.moe_workspace_size(4, 256, 16, 2, 128)
+    good = [0x10000 * (i + 1) for i in range(9)]
+    # a null weight pointer
+    ptrs = list(good)
+    ptrs[3] = 0
+    assert _call_forward(L, d, ptrs, need) == 1
+    # a misaligned pointer
+    ptrs = list(good)
+    ptrs[0] += 8
+    assert _call_forward(L, d, ptrs, need) == 1
+    # a workspace that is too small
+    assert _call_forward(L, d, good, need - 256) == 3
+    # unsupported shape
+    assert _call_forward(L, moe.moe_dims(4, 200, 16, 2, 128), good, need) == 2
+    # route with a misaligned bias
+    assert L.moe_route(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2] + 4), d,
+                       ctypes.c_void_p(good[3]), ctypes.c_void_p(good[4]), ctypes.c_void_p(good[5]), need,
+                       None) == 1
+    # pack with K not a multiple of 8
+    assert L.moe_pack_int4(ctypes.c_void_p(good[0]), 4, 12, ctypes.c_void_p(good[1]), None, None) == 1
+    # device-error check with no workspace
+    assert L.moe_check_device_error(None, 0, None) == 1
+    # empty batch: nothing to do, no device access
+    e = moe.moe_dims(0, 256, 16, 2, 128)
+    assert L.moe_w4a16_forward(None, None, None, *[ctypes.c_void_p(p) for p in good[:4]], None, e,
+                               ctypes.c_void_p(good[5]), need, None) == 0

@@ -1,0 +1,232 @@
+"""Python binding of libw4a16moe, the GB300 (sm_103a) W4A16 routed-expert MoE layer.
+
+Argument marshalling only: each function here takes torch CUDA tensors (device
+memory and streams come from PyTorch), derives the layer dims from their
+shapes, and calls the C entry point of the same name in ``libw4a16moe.so``.
+Every step of the layer runs in the library's CUDA kernels; there is no
+fallback, and importing this module fails loudly if the library is missing.
+
+Weights follow the storage of the model card "Minachist/Qwen3.8-Flash-Next-
+INT4-Mixed-AutoRound" ("What is quantized", group A): int32 words holding
+eight int4 values q + 8, lowest nibble first, with one bf16 scale per row and
+128-wide K group. Shapes (E experts, hidden H, intermediate I):
+w1_packed [E, 2I, H/8] int32 (gate rows then up rows), w1_scales [E, 2I, H/128]
+bf16, w2_packed [E, H, I/8] int32, w2_scales [E, H, I/128] bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
+    "workspace", "moe_route", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
+    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "STATUS",
+]
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_DIR, "libw4a16moe.so")
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE", 6: "MOE_ERR_TIMEOUT"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(status, status), moe_status_str(status)))
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("I", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "moe_dims(T=%d, H=%d, E=%d, k=%d, I=%d)" % (self.T, self.H, self.E, self.k, self.I)
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libw4a16moe.so in-tree for sm_103a (nvcc)."""
+    from . import _build
+    return _build.build(force=force, verbose=verbose)
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libw4a16moe.so is not built (%s); run w4a16_mixture_experts_gb300.build()"
+                               % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        D = moe_dims
+        L.moe_status_str.argtypes, L.moe_status_str.restype = [I], ctypes.c_char_p
+        L.moe_version.argtypes, L.moe_version.restype = [], I
+        L.moe_workspace_size.argtypes, L.moe_workspace_size.restype = [D, ctypes.POINTER(Z)], I
+        L.moe_route.argtypes, L.moe_route.restype = [P, P, P, D, P, P, P, Z, P], I
+        L.moe_w4a16_forward.argtypes = [P, P, P, P, P, P, P, P, D, P, Z, P]
+        L.moe_w4a16_forward.restype = I
+        L.moe_w4a16_forward_rms.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, D, P, Z, P]
+        L.moe_w4a16_forward_rms.restype = I
+        L.moe_permute.argtypes, L.moe_permute.restype = [P, D, P, P, P, Z, P], I
+        L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
+        L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
+        L.moe_profile_events.argtypes, L.moe_profile_events.restype = [P, P], I
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+def _need(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype or t.dim() != ndim:
+        raise ValueError("%s must be %s with %d dims, got %s %s" % (name, dtype, ndim, t.dtype, tuple(t.shape)))
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+
+
+def moe_status_str(status: int) -> str:
+    return lib().moe_status_str(int(status)).decode()
+
+
+def moe_version() -> int:
+    return lib().moe_version()
+
+
+def moe_workspace_size(T: int, H: int, E: int, k: int, I: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(moe_dims(T, H, E, k, I), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def workspace(T: int, H: int, E: int, k: int, I: int, device=None) -> torch.Tensor:
+    """A zeroed uint8 workspace of moe_workspace_size bytes (owned by torch)."""
+    return torch.zeros(moe_workspace_size(T, H, E, k, I), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _ws(ws, dims: moe_dims, device):
+    if ws is None:
+        ws = workspace(dims.T, dims.H, dims.E, dims.k, dims.I, device)
+    return ws
+
+
+def moe_route(hidden, router_w, k: int, bias=None, ws=None, topk_ids=None, topk_w=None, stream=None):
+    """Router GEMM, softmax, top-k (ties to the lower id) and renormalised weights.
+
+    Returns (topk_ids int32 [T, k], topk_w f32 [T, k]).
+    """
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(router_w, "router_w", torch.bfloat16, 2)
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+    dims = moe_dims(T, H, E, k, 128)
+    ws = _ws(ws, dims, hidden.device)
+    if topk_ids is None:
+        topk_ids = torch.empty(T, k, dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, k, dtype=torch.float32, device=hidden.device)
+    _check(lib().moe_route(_p(hidden), _p(router_w), _p(bias), dims, _p(topk_ids), _p(topk_w), _p(ws),
+                           ws.numel(), _stream(stream)), "moe_route")
+    return topk_ids, topk_w
+
+
+def _expert_dims(hidden, topk_ids, w1_packed, w2_packed):
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(w1_packed, "w1_packed", torch.int32, 3)
+    _need(w2_packed, "w2_packed", torch.int32, 3)
+    T, H = hidden.shape
+    E, two_i, _ = w1_packed.shape
+    return moe_dims(T, H, E, topk_ids.shape[1], two_i // 2)
+
+
+def moe_w4a16_forward(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales,
+                      out=None, ws=None, stream=None):
+    """Routed-expert forward: bf16 out [T, H] = sum_j w_j * W2 (SiLU(W1g x) * W1u x)."""
+    dims = _expert_dims(hidden, topk_ids, w1_packed, w2_packed)
+    _need(topk_w, "topk_w", torch.float32, 2)
+    _need(w1_scales, "w1_scales", torch.bfloat16, 3)
+    _need(w2_scales, "w2_scales", torch.bfloat16, 3)
+    ws = _ws(ws, dims, hidden.device)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(lib().moe_w4a16_forward(_p(hidden), _p(topk_ids), _p(topk_w), _p(w1_packed), _p(w1_scales),
+                                   _p(w2_packed), _p(w2_scales), _p(out), dims, _p(ws), ws.numel(),
+                                   _stream(stream)), "moe_w4a16_forward")
+    return out
+
+
+def moe_w4a16_forward_rms(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales,
+                          eps: float = 1e-6, next=None, ws=None, stream=None):
+    """Forward, then next = bf16((hidden + moe) / rms(hidden + moe)) (stack epilogue)."""
+    dims = _expert_dims(hidden, topk_ids, w1_packed, w2_packed)
+    _need(topk_w, "topk_w", torch.float32, 2)
+    _need(w1_scales, "w1_scales", torch.bfloat16, 3)
+    _need(w2_scales, "w2_scales", torch.bfloat16, 3)
+    ws = _ws(ws, dims, hidden.device)
+    if next is None:
+        next = torch.empty_like(hidden)
+    _check(lib().moe_w4a16_forward_rms(_p(hidden), _p(topk_ids), _p(topk_w), _p(w1_packed), _p(w1_scales),
+                                       _p(w2_packed), _p(w2_scales), _p(next), float(eps), dims, _p(ws),
+                                       ws.numel(), _stream(stream)), "moe_w4a16_forward_rms")
+    return next
+
+
+def moe_permute(topk_ids, E: int, H: int = 128, I: int = 128, ws=None, stream=None):
+    """(offsets int32 [E+1], perm int32 [T*k]) of the stable token-to-expert permutation."""
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    T, k = topk_ids.shape
+    dims = moe_dims(T, H, E, k, I)
+    ws = _ws(ws, dims, topk_ids.device)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=topk_ids.device)
+    perm = torch.empty(T * k, dtype=torch.int32, device=topk_ids.device)
+    _check(lib().moe_permute(_p(topk_ids), dims, _p(offsets), _p(perm), _p(ws), ws.numel(), _stream(stream)),
+           "moe_permute")
+    return offsets, perm
+
+
+def moe_pack_int4(q, bad_count=None, stream=None):
+    """int32 [N, K/8] storage words of int8 q [N, K] in [-8, 7]."""
+    _need(q, "q", torch.int8, 2)
+    N, K = q.shape
+    packed = torch.empty(N, K // 8, dtype=torch.int32, device=q.device)
+    if bad_count is not None:
+        _need(bad_count, "bad_count", torch.int32, 1)
+    _check(lib().moe_pack_int4(_p(q), N, K, _p(packed), _p(bad_count), _stream(stream)), "moe_pack_int4")
+    return packed
+
+
+def moe_profile_events(before=None, after=None):
+    """Record two torch.cuda.Events (enable_timing=True, external=True) around
+    the expert kernel of every later forward call; (None, None) stops."""
+    b = None if before is None else ctypes.c_void_p(before.cuda_event)
+    a = None if after is None else ctypes.c_void_p(after.cuda_event)
+    _check(lib().moe_profile_events(b, a), "moe_profile_events")
+
+
+def moe_check_device_error(ws, stream=None) -> int:
+    """Synchronise the stream; return (and clear) the workspace's device error status."""
+    return lib().moe_check_device_error(_p(ws), ws.numel(), _stream(stream))

@@ -1,0 +1,223 @@
+// C-ABI entry points of libw4a16moe: argument checks, workspace layout and
+// kernel sequencing. No allocation, no synchronisation (except in
+// moe_check_device_error, which exists to synchronise).
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "w4a16moe.h"
+
+namespace moe {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+
+struct SmemAttr {
+    const void *func;
+    int bytes;
+    bool done[kMaxDevices];
+};
+SmemAttr g_attrs[8];
+int g_nattrs = 0;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    return dev;
+}
+}  // namespace
+
+int sm_count() {
+    const int dev = current_device();
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+cudaError_t set_smem_once(const void *func, int bytes) {
+    const int dev = current_device();
+    int i = 0;
+    for (; i < g_nattrs; ++i)
+        if (g_attrs[i].func == func) break;
+    if (i == g_nattrs) {
+        if (g_nattrs == 8) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        g_attrs[i].func = func;
+        g_attrs[i].bytes = bytes;
+        ++g_nattrs;
+    }
+    if (g_attrs[i].done[dev]) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess) g_attrs[i].done[dev] = true;
+    return err;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Null is allowed only for empty tensors.
+bool ptr_ok(const void *p, bool empty) { return empty ? (p == nullptr || aligned16(p)) : (p && aligned16(p)); }
+
+int check_dims(const moe_dims &d) {
+    if (d.T < 0 || d.H <= 0 || d.E <= 0 || d.k <= 0 || d.I <= 0) return MOE_ERR_INVALID_ARG;
+    if (d.H % kGroup || d.I % kGroup || d.H > 8192 || d.I > 4096) return MOE_ERR_UNSUPPORTED;
+    if (d.k > kMaxK || d.k > d.E || d.E > kMaxE) return MOE_ERR_UNSUPPORTED;
+    if (d.T > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+    if (!decode_supported(d)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_ws(const moe_dims &d, const void *ws, size_t ws_bytes) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < ws_layout(d).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s) {
+    return ev ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) : cudaSuccess;
+}
+
+int forward_impl(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w, const int32_t *w1_packed,
+                 const uint16_t *w1_scales, const int32_t *w2_packed, const uint16_t *w2_scales, uint16_t *out,
+                 uint16_t *next, float eps, moe_dims d, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    const bool empty = d.T == 0;
+    if (!ptr_ok(hidden, empty) || !ptr_ok(topk_ids, empty) || !ptr_ok(topk_w, empty)) return MOE_ERR_INVALID_ARG;
+    if (!ptr_ok(w1_packed, false) || !ptr_ok(w1_scales, false) || !ptr_ok(w2_packed, false) ||
+        !ptr_ok(w2_scales, false))
+        return MOE_ERR_INVALID_ARG;
+    if (!ptr_ok(next ? (const void *)next : (const void *)out, empty)) return MOE_ERR_INVALID_ARG;
+    if (next && !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+    if (empty) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ExpertArgs a{hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales};
+    cudaError_t err = launch_permute(topk_ids, d, ws, s);
+    if (err == cudaSuccess) err = record_profile_event(g_ev_before, s);
+    if (err == cudaSuccess) err = launch_decode_experts(a, d, ws, s);
+    if (err == cudaSuccess) err = record_profile_event(g_ev_after, s);
+    if (err == cudaSuccess) err = launch_combine(a, d, ws, out, next, eps, s);
+    return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size)";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+        case MOE_ERR_DEVICE: return "a kernel saw an expert id outside [0, E)";
+        case MOE_ERR_TIMEOUT: return "a kernel's bounded wait gave up";
+        default: return "unknown status";
+    }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_workspace_size(moe_dims d, size_t *bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    const int rc = check_dims(d);
+    if (rc) return rc;
+    *bytes = ws_layout(d).total;
+    return MOE_OK;
+}
+
+int moe_route(const uint16_t *hidden, const uint16_t *router_w, const float *bias, moe_dims d, int32_t *topk_ids,
+              float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    const bool empty = d.T == 0;
+    if (!ptr_ok(hidden, empty) || !ptr_ok(router_w, false) || !ptr_ok(topk_ids, empty) || !ptr_ok(topk_w, empty))
+        return MOE_ERR_INVALID_ARG;
+    if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+    if (empty) return MOE_OK;
+    return cuda_status(launch_route(hidden, router_w, bias, d, topk_ids, topk_w, ws,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
+                      const int32_t *w1_packed, const uint16_t *w1_scales, const int32_t *w2_packed,
+                      const uint16_t *w2_scales, uint16_t *out, moe_dims d, void *ws, size_t ws_bytes,
+                      void *stream) {
+    return forward_impl(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales, out, nullptr, 0.f, d,
+                        ws, ws_bytes, stream);
+}
+
+int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
+                          const int32_t *w1_packed, const uint16_t *w1_scales, const int32_t *w2_packed,
+                          const uint16_t *w2_scales, uint16_t *next, float eps, moe_dims d, void *ws,
+                          size_t ws_bytes, void *stream) {
+    if (!next && d.T > 0) return MOE_ERR_INVALID_ARG;
+    return forward_impl(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales, nullptr, next, eps, d,
+                        ws, ws_bytes, stream);
+}
+
+int moe_permute(const int32_t *topk_ids, moe_dims d, int32_t *offsets, int32_t *perm, void *ws, size_t ws_bytes,
+                void *stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    const bool empty = d.T == 0;
+    if (!ptr_ok(topk_ids, empty) || !ptr_ok(offsets, false) || !ptr_ok(perm, empty)) return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(d);
+    cudaError_t err = launch_permute(topk_ids, d, ws, s);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(offsets, ws_at<int32_t>(ws, L.offsets), sizeof(int32_t) * (d.E + 1),
+                              cudaMemcpyDeviceToDevice, s);
+    if (err == cudaSuccess && d.T > 0)
+        err = cudaMemcpyAsync(perm, ws_at<int32_t>(ws, L.perm), sizeof(int32_t) * (size_t)d.T * d.k,
+                              cudaMemcpyDeviceToDevice, s);
+    return cuda_status(err);
+}
+
+int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad_count, void *stream) {
+    if (N < 0 || K < 0 || K % 8) return MOE_ERR_INVALID_ARG;
+    const bool empty = N == 0 || K == 0;
+    if (!ptr_ok(q, empty) || !ptr_ok(packed, empty)) return MOE_ERR_INVALID_ARG;
+    if (bad_count && (reinterpret_cast<uintptr_t>(bad_count) & 3u)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_pack_int4(q, N, K, packed, bad_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_profile_events(void *before_experts, void *after_experts) {
+    if ((before_experts == nullptr) != (after_experts == nullptr)) return MOE_ERR_INVALID_ARG;
+    g_ev_before = reinterpret_cast<cudaEvent_t>(before_experts);
+    g_ev_after = reinterpret_cast<cudaEvent_t>(after_experts);
+    return MOE_OK;
+}
+
+int moe_check_device_error(void *ws, size_t ws_bytes, void *stream) {
+    if (!ws || !aligned16(ws) || ws_bytes < sizeof(Ctrl)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t err_word = 0;
+    if (cudaMemcpyAsync(&err_word, ws, sizeof(err_word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (err_word) {
+        if (cudaMemsetAsync(ws, 0, sizeof(err_word), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+        return err_word == MOE_ERR_TIMEOUT ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
+    }
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+// Device helpers shared by the kernels of libw4a16moe (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "w4a16moe.h"
+
+namespace moe {
+
+constexpr int kGroup = 128;           // quantisation group along K
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr uint32_t kSpinLimit = 1u << 22;   // polls before a wait gives up (~0.5 s)
+
+// ---- workspace layout -------------------------------------------------------
+// A fixed control block followed by 256-byte aligned regions; offsets depend
+// only on the dims, so host and device agree without storing them.
+struct Ctrl {
+    uint32_t error;          // first MOE_ERR_DEVICE / MOE_ERR_TIMEOUT seen
+    uint32_t pad0;
+    uint32_t n_active;       // experts with at least one assignment
+    uint32_t pad1[61];
+};
+static_assert(sizeof(Ctrl) == 256, "control block");
+
+struct WsLayout {
+    size_t ctrl;         // Ctrl
+    size_t partial;      // f32 [ksplit][T][E] router partial logits
+    size_t counts;       // i32 [E]        per-expert assignment counts
+    size_t offsets;      // i32 [E+1]
+    size_t active;       // i32 [E]        active expert ids, increasing
+    size_t done1;        // u32 [E]        per active expert: finished gate_up tasks
+    size_t chunk;        // i32 [nchunk][E] per-chunk counts -> per-chunk bases
+    size_t perm;         // i32 [T*k]      slot -> assignment
+    size_t inv;          // i32 [T*k]      assignment -> slot (-1: dropped)
+    size_t hbuf;         // bf16 [T*k][I]  SiLU(g)*u per slot (fragment order)
+    size_t ybuf;         // f32 [T*k][H]   down-projection output per slot
+    size_t total;
+    int ksplit;
+    int nchunk;
+};
+
+constexpr int kPermChunk = 1024;      // assignments per permute CTA
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Router K split: small batches split K across CTAs so that enough SMs pull
+// the router weight; each split must be a whole number of 32-wide K blocks.
+inline int router_ksplit(const moe_dims &d) {
+    if (d.T > 64) return 1;
+    for (int s = 16; s > 1; s >>= 1)
+        if (d.H % (32 * s) == 0 && s <= d.H / 128) return s;
+    return 1;
+}
+
+inline WsLayout ws_layout(const moe_dims &d) {
+    WsLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    const size_t T = (size_t)d.T, E = (size_t)d.E, k = (size_t)d.k;
+    const size_t H = (size_t)d.H, I = (size_t)d.I;
+    L.ksplit = router_ksplit(d);
+    L.nchunk = (int)((T * k + kPermChunk - 1) / kPermChunk);
+    L.ctrl = take(sizeof(Ctrl));
+    L.partial = take((size_t)L.ksplit * T * E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.active = take(E * 4);
+    L.done1 = take(E * 4);
+    L.chunk = take((size_t)(L.nchunk > 0 ? L.nchunk : 1) * E * 4);
+    L.perm = take(T * k * 4);
+    L.inv = take(T * k * 4);
+    L.hbuf = take(T * k * I * 2);
+    L.ybuf = take(T * k * H * 4);
+    L.total = o;
+    return L;
+}
+
+template <typename P>
+__host__ __device__ inline P *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<P *>(reinterpret_cast<char *>(ws) + off);
+}
+
+// ---- error word -------------------------------------------------------------
+__device__ inline void set_error(Ctrl *c, uint32_t code) { atomicCAS(&c->error, 0u, code); }
+
+// ---- small PTX wrappers -----------------------------------------------------
+__device__ inline uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ inline void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase. Returns false if it gave up.
+__device__ inline bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ inline uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ inline void red_release_add_u32(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ inline uint4 ld_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ inline uint4 ld_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ inline uint4 lds_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+// D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ inline void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- INT4 -> bf16x2 ---------------------------------------------------------
+// Word w holds nibbles n0..n7 (low first), each = q + 8. Pair j (0..3) is
+// (n_j, n_{j+4}) as bf16x2 with n_j in the low half, converted to q exactly:
+// OR-ing a nibble into the mantissa of 128.0 (0x4300) gives 128 + n, and
+// subtracting 136 leaves n - 8, both exact in bf16.
+__device__ inline uint32_t int4_pair_bias(uint32_t w, int j) {
+    return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+}
+
+__device__ inline uint32_t bf16x2_sub136(uint32_t v) {
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(136.0f, 136.0f);
+    __nv_bfloat162 r = __hsub2(a, c);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ inline uint32_t int4_pair(uint32_t w, int j) { return bf16x2_sub136(int4_pair_bias(w, j)); }
+
+__device__ inline float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ inline float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+}  // namespace moe

@@ -1,0 +1,45 @@
+// Host-side launchers of the libw4a16moe kernels (all enqueue on `s`).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "w4a16moe.h"
+
+namespace moe {
+
+// Raises a kernel's dynamic shared memory limit once per device.
+cudaError_t set_smem_once(const void *func, int bytes);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
+                         int32_t *ids, float *w, void *ws, cudaStream_t s);
+
+cudaError_t launch_permute(const int32_t *ids, const moe_dims &d, void *ws, cudaStream_t s);
+
+struct ExpertArgs {
+    const uint16_t *x;
+    const int32_t *ids;
+    const float *topk_w;
+    const int32_t *w1p;
+    const uint16_t *w1s;
+    const int32_t *w2p;
+    const uint16_t *w2s;
+};
+
+// Decode-shaped expert path (skinny GEMMs on mma.sync, register dequant):
+// fills the per-slot down-projection buffer of the workspace.
+cudaError_t launch_decode_experts(const ExpertArgs &a, const moe_dims &d, void *ws, cudaStream_t s);
+// True if the decode kernel supports these dims (its shared-memory stages fit).
+bool decode_supported(const moe_dims &d);
+
+// out[t] = bf16(sum_j w[t][j] * y[slot(t, j)]); with `next` set instead:
+// next[t] = bf16(rms_rescale(x[t] + that sum)).
+cudaError_t launch_combine(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
+                           float eps, cudaStream_t s);
+
+cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
+                             cudaStream_t s);
+
+}  // namespace moe

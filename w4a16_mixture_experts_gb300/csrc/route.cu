@@ -1,0 +1,169 @@
+// Router GEMM and the fused softmax / top-k / renormalisation.
+//
+// "Running 125B MoE on Three 3090s - vLLM Optimization Edition", section 3.3
+// "MoE block (decode-05)": the router GEMV, topk_softmax, and the two facts
+// used here: with norm_topk_prob the full softmax denominator cancels, so a
+// softmax over the k selected logits gives the weights; and top-k over keys
+// that pack an order-preserving logit above (max - expert id) yields value
+// and id in one max, ties going to the lower id. The keys here carry the
+// fp32 logit (32 bits) instead of a bf16 one, so that ranking resolves gaps
+// far below a bf16 ulp.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Partial logits: partial[kb][t][e] = sum over K split kb of x[t][:] . Wr[e][:].
+//
+// One warp computes 16 experts x (8*NT) tokens over H/ksplit of K with
+// mma.sync m16n8k16 (router rows as A, tokens as B). Both operands come
+// straight from global memory as 16-byte chunks: a chunk of 8 consecutive K
+// values of one row feeds two k-steps (values 0-3 to the first, 4-7 to the
+// second), the same physical-K assignment being used for A and B, so the dot
+// product is unchanged. Grid: (ceil(E/64), ksplit, ceil(T/(8*NT))), 4 warps.
+template <int NT>
+__global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__restrict__ x,
+                                                           const uint16_t *__restrict__ wr,
+                                                           float *__restrict__ partial, int T, int H,
+                                                           int E) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int ksplit = gridDim.y, kb = blockIdx.y;
+    const int kpart = H / ksplit;
+    const int e0 = blockIdx.x * 64 + warp * 16;
+    const int t0 = blockIdx.z * (8 * NT);
+    if (e0 >= E) return;
+
+    const int ra = e0 + g, rb = e0 + g + 8;
+    const bool va = ra < E, vb = rb < E;
+    const uint16_t *pa = wr + (size_t)(va ? ra : 0) * H + kb * kpart + 8 * tig;
+    const uint16_t *pb = wr + (size_t)(vb ? rb : 0) * H + kb * kpart + 8 * tig;
+    const uint16_t *px[NT];
+    bool vx[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int t = t0 + 8 * nt + g;
+        vx[nt] = t < T;
+        px[nt] = x + (size_t)(vx[nt] ? t : 0) * H + kb * kpart + 8 * tig;
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll 2
+    for (int kk = 0; kk < kpart; kk += 32) {
+        const uint4 A0 = va ? ld_nc_v4(pa + kk) : zero;
+        const uint4 A1 = vb ? ld_nc_v4(pb + kk) : zero;
+        uint4 B[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) B[nt] = vx[nt] ? ld_nc_v4(px[nt] + kk) : zero;
+        const uint32_t a0[4] = {A0.x, A1.x, A0.y, A1.y};
+        const uint32_t a1[4] = {A0.z, A1.z, A0.w, A1.w};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16_16816(acc[nt], a0, B[nt].x, B[nt].y);
+            mma_bf16_16816(acc[nt], a1, B[nt].z, B[nt].w);
+        }
+    }
+    float *out = partial + (size_t)kb * T * E;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int tc = t0 + 8 * nt + 2 * tig;
+        if (tc < T) {
+            if (va) out[(size_t)tc * E + ra] = acc[nt][0];
+            if (vb) out[(size_t)tc * E + rb] = acc[nt][2];
+        }
+        if (tc + 1 < T) {
+            if (va) out[(size_t)(tc + 1) * E + ra] = acc[nt][1];
+            if (vb) out[(size_t)(tc + 1) * E + rb] = acc[nt][3];
+        }
+    }
+}
+
+// Order-preserving map of an fp32 value onto uint32.
+__device__ inline uint32_t f32_order_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ inline float f32_from_order_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ---------------------------------------------------------------------------
+// Top-k: one warp per token. Lane l holds experts l, l+32, ... as 64-bit keys
+// (order key of the fp32 logit << 32 | 0xffffffff - id). Each of the k
+// rounds takes the warp maximum (unique, because ids differ), removes it, and
+// records it. Weights: softmax over the selected logits in fp32.
+constexpr int kTopkMaxPer = kMaxE / 32;
+
+__global__ void __launch_bounds__(128) route_topk_kernel(const float *__restrict__ partial, int ksplit,
+                                                         const float *__restrict__ bias, int T, int E,
+                                                         int k, int32_t *__restrict__ ids,
+                                                         float *__restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int nper = (E + 31) / 32;
+    uint64_t key[kTopkMaxPer];
+#pragma unroll
+    for (int i = 0; i < kTopkMaxPer; ++i) {
+        key[i] = 0;
+        const int e = lane + 32 * i;
+        if (i < nper && e < E) {
+            float l = 0.f;
+            for (int s = 0; s < ksplit; ++s) l += partial[((size_t)s * T + t) * E + e];
+            if (bias) l += bias[e];
+            key[i] = ((uint64_t)f32_order_key(l) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+        }
+    }
+    uint64_t mine = 0;   // lane j keeps the j-th selected key
+    for (int j = 0; j < k; ++j) {
+        uint64_t m = 0;
+#pragma unroll
+        for (int i = 0; i < kTopkMaxPer; ++i) m = key[i] > m ? key[i] : m;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, m, off);
+            m = o > m ? o : m;
+        }
+#pragma unroll
+        for (int i = 0; i < kTopkMaxPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+        if (lane == j) mine = m;
+    }
+    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
+    const float l = f32_from_order_key((uint32_t)(mine >> 32));
+    const float p = lane < k ? expf(l - lmax) : 0.f;
+    float z = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+        w[(size_t)t * k + lane] = p / z;
+    }
+}
+
+cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
+                         int32_t *ids, float *w, void *ws, cudaStream_t s) {
+    const WsLayout L = ws_layout(d);
+    float *partial = ws_at<float>(ws, L.partial);
+    const int ksplit = L.ksplit;
+    const int tt = d.T <= 64 ? d.T : 64;
+    int nt = 1;
+    while (8 * nt < tt) nt <<= 1;
+    dim3 grid((d.E + 63) / 64, ksplit, (d.T + 8 * nt - 1) / (8 * nt));
+    switch (nt) {
+        case 1: route_logits_kernel<1><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
+        case 2: route_logits_kernel<2><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
+        case 4: route_logits_kernel<4><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
+        default: route_logits_kernel<8><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
+    }
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    route_topk_kernel<<<(d.T + 3) / 4, 128, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
