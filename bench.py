@@ -34,7 +34,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -155,16 +154,21 @@ def max_over_ranks(v: float, world: int) -> float:
 # ------------------------------------------------------------ CPU baseline --
 
 def cpu_baseline(wl, seed: int, target_s: float):
-    """The fp64 oracle on a bounded sample of tokens of the workload (tok/s)."""
+    """The fp64 oracle, as it stands, on a bounded sample of the workload's tokens (tok/s).
+
+    The layer is independent per token, so a sample of n tokens through one layer
+    measures the same per-token work as the workload; n is sized from a short
+    probe so that the timed run takes about target_s seconds.
+    """
     import oracle
     T, H, E, k, I = wl.dims
     oracle.build()
-    x = synth.hidden(max(T, 1), H, seed=seed)
+    cores = oracle.max_threads()
     wr = synth.router(E, H, seed=seed, layer=0)
     bias = synth.zipf_bias(E, wl.zipf, seed=seed) if wl.zipf else None
 
-    def run(rows):
-        xs = x[rows]
+    def run(n):
+        xs = synth.hidden(n, H, seed=seed, layer=101)
         ids, w, _ = oracle.route(xs, wr, k, bias)
         held = np.unique(ids)
         row = np.full(E, -1, np.int32)
@@ -176,19 +180,14 @@ def cpu_baseline(wl, seed: int, target_s: float):
                               wts["w2_packed"], wts["w2_scales"], E, I, expert_row=row)
         return time.perf_counter() - t0
 
-    cores = oracle.max_threads()
-    n = min(cores, x.shape[0])
-    rows = np.arange(n) % x.shape[0]
-    t = run(rows)
-    reps = max(1, min(64, int(target_s / max(t, 1e-3))))
-    if reps > 1:
-        rows = np.arange(n * reps) % x.shape[0]
-        t = run(rows)
-    ntok = len(rows)
-    layers = wl.layers
-    return {"value": ntok / t / layers, "unit": "tok/s", "cores": min(cores, ntok), "kind": "oracle",
-            "sample": "%d tokens of workload %s through one layer (route + experts), fp64, %.1f s%s"
-                      % (ntok, wl.name, t, "; divided by %d layers" % layers if layers > 1 else "")}
+    n = cores
+    t = run(n)
+    n = max(cores, min(8192, int(n * target_s / max(t, 1e-3)) // cores * cores))
+    t = run(n)
+    return {"value": n / t / wl.layers, "unit": "tok/s", "cores": min(cores, n), "kind": "oracle",
+            "sample": "%d seeded tokens through one layer of workload %s (route + experts), fp64, %.1f s%s"
+                      % (n, wl.name, t, "; per-token rate divided by %d layers" % wl.layers
+                         if wl.layers > 1 else "")}
 
 
 # ------------------------------------------------------------- our arm -----
@@ -253,6 +252,8 @@ def run_ours(args, rank, world, local):
     ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nsets * (1 if not stack else 1))]
     ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ev_b))]
     unique = [0] * nsets
+    for e in ev_b + ev_a:       # torch only lets recorded events be timed; the library re-records them
+        e.record(stream)
 
     def step(i, profile=False):
         """Enqueue one step (set i for single layers; all layers for the stack)."""
@@ -414,7 +415,7 @@ def main():
     wl = synth.WORKLOADS[args.config]
     if args.impl == "reference":
         if rank == 0:
-            cb = cpu_baseline(wl, args.seed, args.cpu_seconds * max(1, args.steps) / max(1, args.steps))
+            cb = cpu_baseline(wl, args.seed, args.cpu_seconds)
             line = {"impl": "reference", "metric": "MoE layer tok/s (%s)" % wl.name, "value": cb["value"],
                     "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

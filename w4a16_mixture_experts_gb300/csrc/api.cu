@@ -105,7 +105,14 @@ int forward_impl(const uint16_t *hidden, const int32_t *topk_ids, const float *t
     if (empty) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ExpertArgs a{hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales};
-    cudaError_t err = launch_permute(topk_ids, d, ws, s);
+    cudaError_t err;
+    if (fused_supported(d)) {
+        err = record_profile_event(g_ev_before, s);
+        if (err == cudaSuccess) err = launch_decode_fused(a, d, ws, out, next, eps, s);
+        if (err == cudaSuccess) err = record_profile_event(g_ev_after, s);
+        return cuda_status(err);
+    }
+    err = launch_permute(topk_ids, d, ws, s);
     if (err == cudaSuccess) err = record_profile_event(g_ev_before, s);
     if (err == cudaSuccess) err = launch_decode_experts(a, d, ws, s);
     if (err == cudaSuccess) err = record_profile_event(g_ev_after, s);

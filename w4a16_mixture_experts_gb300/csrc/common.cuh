@@ -31,7 +31,11 @@ struct WsLayout {
     size_t counts;       // i32 [E]        per-expert assignment counts
     size_t offsets;      // i32 [E+1]
     size_t active;       // i32 [E]        active expert ids, increasing
-    size_t done1;        // u32 [E]        per active expert: finished gate_up tasks
+    size_t done1;        // u32 [E]        per expert: finished gate_up tasks
+    size_t done2;        // u32 [E]        per expert: finished down tasks
+    size_t ticket;       // u32 [T][H/32]  per output block: finished slots
+    size_t rowdone;      // u32 [T]        per token: finished output blocks
+    size_t rbuf;         // f32 [T][H]     residual sums (stack epilogue)
     size_t chunk;        // i32 [nchunk][E] per-chunk counts -> per-chunk bases
     size_t perm;         // i32 [T*k]      slot -> assignment
     size_t inv;          // i32 [T*k]      assignment -> slot (-1: dropped)
@@ -69,6 +73,10 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);
     L.done1 = take(E * 4);
+    L.done2 = take(E * 4);
+    L.ticket = take(T * (H / 32) * 4);
+    L.rowdone = take(T * 4);
+    L.rbuf = take(T <= 64 ? T * H * 4 : 0);
     L.chunk = take((size_t)(L.nchunk > 0 ? L.nchunk : 1) * E * 4);
     L.perm = take(T * k * 4);
     L.inv = take(T * k * 4);
@@ -134,6 +142,16 @@ __device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled TMA load of the box at (c0 = inner element, c1 = row), completing on `bar`.
+// c0 * element size must be a multiple of 16 bytes.
+__device__ inline void tma_load_2d(void *dst, const void *tmap, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -1,0 +1,808 @@
+// Fused decode forward: permute, W4A16 expert GEMMs and combine in one launch.
+//
+// Computes the fused Marlin MoE of "Running 125B MoE on Three 3090s - vLLM
+// Optimization Edition", section 3.3 "MoE block" (moe_align_block_size,
+// gate_up, SiluAndMul, down, moe_sum) for small batches (T <= 64), on
+// symmetric INT4 group-128 weights (model card, "What is quantized", group A).
+// At decode the layer streams ~2.5 MB of packed weights per active expert
+// and does a few FLOPs per byte, so everything here serves the byte stream:
+//
+//  * One persistent CTA per SM, 8 warps. Each CTA first derives the whole
+//    token-to-expert permutation from topk_ids in shared memory (every CTA
+//    computes the same result), so no separate permute launch sits on the
+//    critical path. Small batches rank each assignment by comparison
+//    (slot = #assignments with a lower expert + #earlier ones with the same
+//    expert); larger ones use a histogram and prefix sum over the experts.
+//  * Work is a list of tasks: gate_up tasks (8 gate rows and the matching 8
+//    up rows of one expert, all of K) then down tasks (32 output rows of one
+//    expert, all of K = I). Each CTA takes a contiguous range of each list and
+//    deals the concatenation round-robin to its warps, so every warp runs its
+//    gate_up tasks before its down tasks.
+//  * A task is streamed as ~10 KB chunks (gate_up: K in pieces of 10 groups,
+//    loaded as two 2-D TMA boxes; down: one 1-D bulk copy) through a 2-stage
+//    shared-memory ring per warp completed on mbarriers, so a warp always has
+//    its next chunk in flight, including the first chunk of its next task.
+//  * Weights are dequantised in registers into mma.sync m16n8k16 A fragments
+//    (bf16 holds q in [-8, 7] exactly); each group's fp32 partial sum is
+//    scaled by its bf16 scale, so W = q * scale is never rounded. Tokens are
+//    the N = 8 side. Activations for small T are staged once per CTA in
+//    shared memory, already in fragment order.
+//  * A down task of expert e waits (bounded, acquire) until all gate_up tasks
+//    of e have published SiLU(g)*u (bf16, stored in fragment order), then
+//    loads it from L2 into registers.
+//  * The combine is fused: after writing its fp32 down outputs, a down task
+//    counts, per (token, 32-row block), how many of the token's slots are
+//    done; the task that completes a block sums the slots in slot order and
+//    writes the bf16 output (in the stack variant: residual + RMS rescale
+//    once the token's last block is done). All counters reset themselves.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kFW = 8;               // warps per CTA
+constexpr int kGC = 10;              // quantisation groups per gate_up chunk
+constexpr int kP2Rows = 32;          // output rows per down task
+constexpr int kMaxNT = 8;            // token tiles of 8 per expert (T <= 64)
+constexpr int kFastN = 256;          // assignments ranked by comparison
+constexpr int kFusedMaxT = 64;
+constexpr int kFusedMaxN = 2048;     // T * k
+constexpr int kFusedSmem = 232448 - 512;   // per-block opt-in limit, less static shared memory
+
+struct FusedParams {
+    CUtensorMap tm_w1;   // int32 [E*2I][H/8], box (gcw words, 8 rows)
+    const uint16_t *x;
+    const int32_t *ids;
+    const float *topk_w;
+    const uint16_t *w1s;
+    const int32_t *w2p;
+    const uint16_t *w2s;
+    uint16_t *out;       // bf16 [T][H], or nullptr in the stack variant
+    uint16_t *next;      // bf16 [T][H] stack variant output
+    float eps;
+    Ctrl *ctrl;
+    uint32_t *done1;     // [E] finished gate_up tasks
+    uint32_t *done2;     // [E] finished down tasks
+    uint32_t *ticket;    // [T][H/32] finished slots per output block
+    uint32_t *rowdone;   // [T] finished output blocks (stack variant)
+    uint16_t *hbuf;      // bf16 [T*k][I], fragment order
+    float *ybuf;         // f32 [T*k][H]
+    float *rbuf;         // f32 [T][H] residual sums (stack variant)
+    int T, H, E, k, I;
+    int gcw;             // words per gate_up chunk row (groups per chunk * 16)
+    int nkc;             // chunks per gate_up task
+    uint32_t stage_bytes;
+    uint32_t pro_off;    // offset of the permutation arrays
+    uint32_t xs_off;     // offset of the staged activations (0: not staged)
+};
+
+struct FusedLayout {
+    uint32_t stage_bytes, pro_off, xs_off, total;
+    int gcw, nkc;
+    bool ok;
+};
+
+inline uint32_t fused_pro_bytes(const moe_dims &d) {
+    const size_t n = (size_t)d.T * d.k;
+    return (uint32_t)(align_up(n * 2, 16) * 3 + align_up(d.E * 4, 16) + align_up((d.E + 1) * 2, 16) +
+                      align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
+}
+
+// Shared memory: 2 stages per warp | permutation arrays | staged activations (if they fit).
+inline FusedLayout fused_layout(const moe_dims &d) {
+    FusedLayout L{};
+    const int G1 = d.H / 128, G2 = d.I / 128;
+    const int gc = G1 < kGC ? G1 : kGC;
+    L.gcw = gc * 16;
+    L.nkc = (G1 + gc - 1) / gc;
+    const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
+    const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
+    L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
+    L.pro_off = 2 * kFW * L.stage_bytes;
+    const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2;
+    const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
+    L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
+    L.total = L.xs_off ? base + xs_bytes : base;
+    // scratch of the prologue lives in the stage area
+    const uint32_t scratch = kFW * d.E * 2 + 2 * d.E * 4 + 3 * kFastN * 4;
+    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= 2 * kFW * L.stage_bytes && d.T <= kFusedMaxT &&
+           d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
+    return L;
+}
+
+bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
+
+struct Pro {   // permutation arrays in shared memory
+    int16_t *ids, *perm, *inv;
+    int32_t *cnt;
+    int16_t *offs, *act, *aoff, *acnt, *kv;
+    uint64_t *bar;
+    int *nact;
+};
+
+__device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
+    Pro v;
+    const int n = p.T * p.k;
+    uint8_t *q = smem + p.pro_off;
+    auto take = [&](size_t bytes) { uint8_t *r = q; q += (bytes + 15) / 16 * 16; return r; };
+    v.ids = reinterpret_cast<int16_t *>(take(n * 2));
+    v.perm = reinterpret_cast<int16_t *>(take(n * 2));
+    v.inv = reinterpret_cast<int16_t *>(take(n * 2));
+    v.cnt = reinterpret_cast<int32_t *>(take(p.E * 4));
+    v.offs = reinterpret_cast<int16_t *>(take((p.E + 1) * 2));
+    v.act = reinterpret_cast<int16_t *>(take(p.E * 2));
+    v.aoff = reinterpret_cast<int16_t *>(take(p.E * 2));
+    v.acnt = reinterpret_cast<int16_t *>(take(p.E * 2));
+    v.kv = reinterpret_cast<int16_t *>(take(p.T * 2));
+    v.bar = reinterpret_cast<uint64_t *>(take(4 * kFW * 8));
+    v.nact = reinterpret_cast<int *>(take(16));
+    return v;
+}
+
+// Exclusive scan over the CTA (kFW warps) of one int per thread; *total gets the sum.
+__device__ inline int cta_exclusive_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int s = lane < kFW ? warp_sums[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, si, off);
+            if (lane >= off) si += o;
+        }
+        if (lane < kFW) warp_sums[lane] = si - s;
+        if (lane == kFW - 1) *total = si;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// The stable permutation, in every CTA: the slot of assignment a is
+// #{valid a' with a lower expert} + #{a' < a with the same expert}.
+__device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v) {
+    __shared__ int warp_sums[kFW];
+    __shared__ int total, nact_s;
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int n = p.T * p.k, E = p.E;
+    const bool fast = n <= kFastN && n <= nthr;
+
+    // issue the id loads first, then stage the activations while they fly
+    int id_reg = -1;
+    if (fast && tid < n) id_reg = p.ids[tid];
+    if (p.xs_off) {
+        uint4 *xs = reinterpret_cast<uint4 *>(smem + p.xs_off);
+        const int nch = p.T * p.H / 8;
+        for (int i = tid; i < nch; i += nthr) {
+            const uint4 c = ld_nc_v4(p.x + (size_t)i * 8);
+            xs[i] = make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632),
+                               __byte_perm(c.y, c.w, 0x5410), __byte_perm(c.y, c.w, 0x7632));
+        }
+    }
+    bool bad = false;
+    if (fast) {
+        if (tid < n) {
+            if (id_reg < 0 || id_reg >= E) {
+                id_reg = -1;
+                bad = true;
+            }
+            v.ids[tid] = (int16_t)id_reg;
+        }
+    } else {
+        for (int a = tid; a < n; a += nthr) {
+            int e = p.ids[a];
+            if (e < 0 || e >= E) {
+                e = -1;
+                bad = true;
+            }
+            v.ids[a] = (int16_t)e;
+        }
+    }
+    if (bad && blockIdx.x == 0) set_error(p.ctrl, MOE_ERR_DEVICE);
+    if (tid == 0) nact_s = 0;
+    __syncthreads();
+    for (int t = tid; t < p.T; t += nthr) {
+        int c = 0;
+        for (int j = 0; j < p.k; ++j) c += v.ids[t * p.k + j] >= 0;
+        v.kv[t] = (int16_t)c;
+    }
+
+    if (fast) {
+        int32_t *is_lead = reinterpret_cast<int32_t *>(smem);   // scratch in the stage area
+        const int a = tid;
+        int e = -1, cl = 0, rk = 0, ct = 0;
+        if (a < n) {
+            e = v.ids[a];
+            is_lead[a] = 0;
+            if (e < 0) {
+                v.inv[a] = -1;
+            } else {
+                for (int a2 = 0; a2 < n; ++a2) {
+                    const int e2 = v.ids[a2];
+                    cl += (e2 >= 0) & (e2 < e);
+                    ct += e2 == e;
+                    rk += (e2 == e) & (a2 < a);
+                }
+                const int slot = cl + rk;
+                v.perm[slot] = (int16_t)a;
+                v.inv[a] = (int16_t)slot;
+                if (rk == 0) {
+                    is_lead[a] = 1;
+                    atomicAdd(&nact_s, 1);
+                }
+            }
+        }
+        __syncthreads();
+        if (a < n && e >= 0 && rk == 0) {
+            int ai = 0;
+            for (int a2 = 0; a2 < n; ++a2) ai += is_lead[a2] & (v.ids[a2] < e);
+            v.act[ai] = (int16_t)e;
+            v.aoff[ai] = (int16_t)cl;
+            v.acnt[ai] = (int16_t)ct;
+        }
+        if (tid == 0) *v.nact = nact_s;
+    } else {
+        for (int e = tid; e < E; e += nthr) v.cnt[e] = 0;
+        __syncthreads();
+        for (int a = tid; a < n; a += nthr)
+            if (v.ids[a] >= 0) atomicAdd(&v.cnt[v.ids[a]], 1);
+        __syncthreads();
+        // offsets and active list: each thread owns ceil(E/nthr) consecutive experts
+        const int per = (E + nthr - 1) / nthr;
+        const int e0 = tid * per;
+        int sum = 0, nz = 0;
+        for (int i = 0; i < per; ++i)
+            if (e0 + i < E) {
+                sum += v.cnt[e0 + i];
+                nz += v.cnt[e0 + i] > 0;
+            }
+        const int off0 = cta_exclusive_scan(sum, warp_sums, &total);
+        const int all = total;
+        const int act0 = cta_exclusive_scan(nz, warp_sums, &total);
+        const int nact = total;
+        {
+            int o = off0, ai = act0;
+            for (int i = 0; i < per; ++i)
+                if (e0 + i < E) {
+                    const int c = v.cnt[e0 + i];
+                    v.offs[e0 + i] = (int16_t)o;
+                    if (c > 0) {
+                        v.act[ai] = (int16_t)(e0 + i);
+                        v.aoff[ai] = (int16_t)o;
+                        v.acnt[ai] = (int16_t)c;
+                        ++ai;
+                    }
+                    o += c;
+                }
+        }
+        if (tid == 0) {
+            v.offs[E] = (int16_t)all;
+            *v.nact = nact;
+        }
+        // stable scatter in chunks of nthr assignments; scratch in the stage area
+        uint16_t *wc = reinterpret_cast<uint16_t *>(smem);              // [kFW][E]
+        int32_t *run = reinterpret_cast<int32_t *>(smem + kFW * E * 2);  // [E]
+        int32_t *tot = run + E;                                          // [E]
+        for (int e = tid; e < E; e += nthr) run[e] = 0;
+        for (int base = 0; base < n; base += nthr) {
+            for (int i = tid; i < kFW * E; i += nthr) wc[i] = 0;
+            __syncthreads();
+            const int a = base + tid;
+            const int e = a < n ? v.ids[a] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            if (e >= 0 && rank == 0) wc[warp * E + e] = (uint16_t)__popc(same);
+            __syncthreads();
+            for (int x = tid; x < E; x += nthr) {
+                int r = 0;
+                for (int w = 0; w < kFW; ++w) {
+                    const int c = wc[w * E + x];
+                    wc[w * E + x] = (uint16_t)r;
+                    r += c;
+                }
+                tot[x] = r;
+            }
+            __syncthreads();
+            if (a < n) {
+                if (e >= 0) {
+                    const int slot = v.offs[e] + run[e] + wc[warp * E + e] + rank;
+                    v.perm[slot] = (int16_t)a;
+                    v.inv[a] = (int16_t)slot;
+                } else {
+                    v.inv[a] = -1;
+                }
+            }
+            __syncthreads();
+            for (int x = tid; x < E; x += nthr) run[x] += tot[x];
+        }
+    }
+    __syncthreads();
+    // tokens with no valid slot still get an output: zero, or the rescaled residual
+    if (blockIdx.x == 0 && warp == 0)
+        for (int t = 0; t < p.T; ++t)
+            if (v.kv[t] == 0) {
+                if (p.out) {
+                    for (int c = lane; c < p.H; c += 32) p.out[(size_t)t * p.H + c] = 0;
+                } else {
+                    float ss = 0.f;
+                    for (int c = lane; c < p.H; c += 32) {
+                        const float r = bf16_bits_to_f32(p.x[(size_t)t * p.H + c]);
+                        ss += r * r;
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                    const float scale = rsqrtf(ss / (float)p.H + p.eps);
+                    for (int c = lane; c < p.H; c += 32) {
+                        const __nv_bfloat16 b =
+                            __float2bfloat16_rn(bf16_bits_to_f32(p.x[(size_t)t * p.H + c]) * scale);
+                        p.next[(size_t)t * p.H + c] = *reinterpret_cast<const uint16_t *>(&b);
+                    }
+                }
+            }
+    __syncthreads();
+}
+
+__device__ inline uint32_t fw_word(const uint4 &v, int m) {
+    return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
+}
+
+// ---- the warp's chunk sequence ------------------------------------------------
+struct Seq {       // position in the warp's list of tasks, and chunk within the task
+    int pos, chunk;
+};
+
+struct WarpList {
+    int b1, m1, b2, m2, warp, n1, nkc;
+    // task at list position `pos` of this warp, or -1 past the end
+    __device__ int task(int pos) const {
+        const int i = warp + pos * kFW;
+        if (i < m1) return b1 + i;
+        if (i < m1 + m2) return n1 + b2 + (i - m1);
+        return -1;
+    }
+    __device__ void advance(Seq &s) const {
+        const int tk = task(s.pos);
+        if (++s.chunk >= (tk < n1 ? nkc : 1)) {
+            s.chunk = 0;
+            ++s.pos;
+        }
+    }
+};
+
+__device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int task, int chunk, int n1, uint8_t *stage,
+                               uint64_t *bar, int lane) {
+    if (lane != 0) return;
+    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
+    if (task < n1) {
+        const int a = task / tp1, r = task - a * tp1;
+        const int e = v.act[a];
+        const int G1 = p.H / 128;
+        const uint32_t box = 8u * p.gcw * 4;
+        const int row = e * 2 * p.I + 8 * r;
+        mbar_arrive_expect_tx(bar, 2 * box + 32 * G1);
+        tma_load_2d(stage, &p.tm_w1, chunk * p.gcw, row, bar);
+        tma_load_2d(stage + box, &p.tm_w1, chunk * p.gcw, row + p.I, bar);
+        bulk_g2s(stage + 2 * box, p.w1s + (size_t)row * G1, 16 * G1, bar);
+        bulk_g2s(stage + 2 * box + 16 * G1, p.w1s + (size_t)(row + p.I) * G1, 16 * G1, bar);
+    } else {
+        const int t2 = task - n1;
+        const int a = t2 / tp2, c = t2 - a * tp2;
+        const int e = v.act[a];
+        const int G2 = p.I / 128;
+        const uint32_t rb = p.I / 2;
+        mbar_arrive_expect_tx(bar, kP2Rows * rb + kP2Rows * G2 * 2);
+        bulk_g2s(stage, reinterpret_cast<const char *>(p.w2p) + ((size_t)e * p.H + kP2Rows * c) * rb, kP2Rows * rb,
+                 bar);
+        bulk_g2s(stage + kP2Rows * rb, p.w2s + ((size_t)e * p.H + kP2Rows * c) * G2, kP2Rows * G2 * 2, bar);
+    }
+}
+
+// ---- gate_up ----------------------------------------------------------------
+// Lane (g, tig) holds, for group q, words 4*tig..4*tig+3 of A rows g (gate)
+// and g+8 (up). Word m covers K = base..base+7, base = 128q + 32tig + 8m;
+// k-step 2m+h takes nibble pairs (2h, 2h+4) for the low fragment slots and
+// (2h+1, 2h+5) for the high ones, so the B fragment of token g is the
+// activation chunk base..base+7 in the order (0,4),(1,5),(2,6),(3,7).
+template <bool kStaged>
+__device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int task, int chunk, const uint8_t *stage,
+                                       const uint8_t *smem, int lane, float (&acc)[kMaxNT][4]) {
+    const int tp1 = p.I / 8;
+    const int a = task / tp1;
+    const int s0 = v.aoff[a], ne = v.acnt[a];
+    const int nt_n = (ne + 7) >> 3;
+    const int g = lane >> 2, tig = lane & 3;
+    const int G1 = p.H / 128;
+    const int gc = p.gcw / 16;
+    const int q0 = chunk * gc;
+    const int qn = G1 - q0 < gc ? G1 - q0 : gc;
+    const uint32_t rowb = p.gcw * 4;
+    const uint8_t *rg = stage + g * rowb + 16 * tig;
+    const uint8_t *ru = stage + 8 * rowb + g * rowb + 16 * tig;
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + 16 * rowb);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    if (chunk == 0) {
+#pragma unroll
+        for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    }
+    for (int nt = 0; nt < nt_n; ++nt) {
+        // activation row of the token in column g of this N tile
+        const int j = 8 * nt + g;
+        const bool vx = j < ne;
+        const int tok = vx ? v.perm[s0 + j] / p.k : 0;
+        const uint4 *xb;
+        if (kStaged)
+            xb = reinterpret_cast<const uint4 *>(smem + p.xs_off) + (size_t)tok * (p.H / 8) + 4 * tig;
+        else
+            xb = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.H + 32 * tig);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+        for (int qq = 0; qq < qn; ++qq) {
+            const int q = q0 + qq;
+            const uint4 wg = lds_v4(rg + 64 * qq), wu = lds_v4(ru + 64 * qq);
+            const float sg = bf16_bits_to_f32(sc[g * G1 + q]);
+            const float su = bf16_bits_to_f32(sc[(8 + g) * G1 + q]);
+            uint4 X[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                X[m] = vx ? (kStaged ? xb[16 * q + m] : ld_nc_v4(xb + 16 * q + m)) : zero;
+                if (!kStaged)
+                    X[m] = make_uint4(__byte_perm(X[m].x, X[m].z, 0x5410), __byte_perm(X[m].x, X[m].z, 0x7632),
+                                      __byte_perm(X[m].y, X[m].w, 0x5410), __byte_perm(X[m].y, X[m].w, 0x7632));
+            }
+            // one accumulator per word keeps the mma chains two deep
+            float c[4][4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t xg = fw_word(wg, m), xu = fw_word(wu, m);
+                const uint32_t f0[4] = {int4_pair(xg, 0), int4_pair(xu, 0), int4_pair(xg, 1), int4_pair(xu, 1)};
+                const uint32_t f1[4] = {int4_pair(xg, 2), int4_pair(xu, 2), int4_pair(xg, 3), int4_pair(xu, 3)};
+                c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
+                mma_bf16_16816(c[m], f0, X[m].x, X[m].y);
+                mma_bf16_16816(c[m], f1, X[m].z, X[m].w);
+            }
+            a0 += sg * ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0]));
+            a1 += sg * ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1]));
+            a2 += su * ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2]));
+            a3 += su * ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxNT; ++i)
+            if (i == nt) {
+                acc[i][0] += a0;
+                acc[i][1] += a1;
+                acc[i][2] += a2;
+                acc[i][3] += a3;
+            }
+    }
+}
+
+// h for intermediate row 8r+g, tokens 8nt+2tig(+1): chunk r, position 2*(g%4) + g/4.
+__device__ inline void f_gate_up_store(const FusedParams &p, const Pro &v, int task, int lane,
+                                       const float (&acc)[kMaxNT][4]) {
+    const int tp1 = p.I / 8;
+    const int a = task / tp1, r = task - a * tp1;
+    const int s0 = v.aoff[a], ne = v.acnt[a];
+    const int g = lane >> 2, tig = lane & 3;
+    const int pos = 2 * (g & 3) + (g >> 2);
+#pragma unroll
+    for (int nt = 0; nt < kMaxNT; ++nt)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int j = 8 * nt + 2 * tig + b;
+            if (j < ne) {
+                const float hv = silu(acc[nt][b]) * acc[nt][2 + b];
+                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                p.hbuf[(size_t)(s0 + j) * p.I + 8 * r + pos] = *reinterpret_cast<const uint16_t *>(&hb);
+            }
+        }
+}
+
+// ---- down + fused combine ----------------------------------------------------
+__device__ __noinline__ void f_combine_block(const FusedParams &p, const Pro &v, int t, int c, int lane) {
+    const int n = kP2Rows * c + lane;
+    float s = 0.f;
+    for (int j = 0; j < p.k; ++j) {
+        const int slot = v.inv[t * p.k + j];
+        if (slot < 0) continue;
+        s += p.topk_w[(size_t)t * p.k + j] * __ldcg(p.ybuf + (size_t)slot * p.H + n);
+    }
+    if (p.out) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(s);
+        p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
+    } else {
+        p.rbuf[(size_t)t * p.H + n] = s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]);
+    }
+}
+
+__device__ __noinline__ void f_rms_row(const FusedParams &p, int t, int lane) {
+    float ss = 0.f;
+    for (int n = lane; n < p.H; n += 32) {
+        const float r = __ldcg(p.rbuf + (size_t)t * p.H + n);
+        ss += r * r;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float scale = rsqrtf(ss / (float)p.H + p.eps);
+    for (int n = lane; n < p.H; n += 32) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(__ldcg(p.rbuf + (size_t)t * p.H + n) * scale);
+        p.next[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
+    }
+}
+
+__device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const uint8_t *stage, int lane) {
+    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
+    const int a = t2 / tp2, c = t2 - a * tp2;
+    const int e = v.act[a];
+    const int s0 = v.aoff[a], ne = v.acnt[a];
+    const int g = lane >> 2, tig = lane & 3;
+    const int G2 = p.I / 128;
+    const uint32_t rb = p.I / 2;
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + kP2Rows * rb);
+
+    // wait until every gate_up task of expert e has published its h
+    uint32_t ok = 1;
+    if (lane == 0) {
+        uint32_t i = 0;
+        while (ld_acquire_u32(&p.done1[e]) < (uint32_t)tp1) {
+            if (++i > kSpinLimit) {
+                ok = 0;
+                set_error(p.ctrl, MOE_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    if (!ok) return false;
+
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int np = 0; np < ne; np += 8) {
+        const int j = np + g;
+        const bool valid = j < ne;
+        const uint4 *hb = reinterpret_cast<const uint4 *>(p.hbuf + (size_t)(s0 + (valid ? j : 0)) * p.I) + 4 * tig;
+        float acc[2][4];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+        uint4 Yn[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) Yn[m] = valid ? ld_cg_v4(hb + m) : zero;
+#pragma unroll 1
+        for (int q = 0; q < G2; ++q) {
+            uint4 Y[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) Y[m] = Yn[m];
+            if (q + 1 < G2) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) Yn[m] = valid ? ld_cg_v4(hb + 16 * (q + 1) + m) : zero;
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int R = 16 * s + g;
+                const uint4 w0 = lds_v4(stage + R * rb + 64 * q + 16 * tig);
+                const uint4 w1 = lds_v4(stage + (R + 8) * rb + 64 * q + 16 * tig);
+                const float s0v = bf16_bits_to_f32(sc[R * G2 + q]);
+                const float s1v = bf16_bits_to_f32(sc[(R + 8) * G2 + q]);
+                float c[4][4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t x0 = fw_word(w0, m), x1 = fw_word(w1, m);
+                    const uint32_t f0[4] = {int4_pair(x0, 0), int4_pair(x1, 0), int4_pair(x0, 1), int4_pair(x1, 1)};
+                    const uint32_t f1[4] = {int4_pair(x0, 2), int4_pair(x1, 2), int4_pair(x0, 3), int4_pair(x1, 3)};
+                    c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
+                    mma_bf16_16816(c[m], f0, Y[m].x, Y[m].y);
+                    mma_bf16_16816(c[m], f1, Y[m].z, Y[m].w);
+                }
+                acc[s][0] += s0v * ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0]));
+                acc[s][1] += s0v * ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1]));
+                acc[s][2] += s1v * ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2]));
+                acc[s][3] += s1v * ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int jj = np + 2 * tig + b;
+                if (jj < ne) {
+                    float *yr = p.ybuf + (size_t)(s0 + jj) * p.H + kP2Rows * c + 16 * s + g;
+                    yr[0] = acc[s][b];
+                    yr[8] = acc[s][2 + b];
+                }
+            }
+    }
+
+    // fused combine: count this task's slots per (token, block); complete blocks
+    __threadfence();
+    __syncwarp();
+    for (int j0 = 0; j0 < ne; j0 += 32) {
+        const int j = j0 + lane;
+        int t = -1;
+        bool fin = false;
+        if (j < ne) {
+            t = v.perm[s0 + j] / p.k;
+            const uint32_t old = atomicAdd(&p.ticket[(size_t)t * tp2 + c], 1u);
+            fin = old + 1 == (uint32_t)v.kv[t];
+            if (fin) p.ticket[(size_t)t * tp2 + c] = 0;
+        }
+        unsigned m = __ballot_sync(0xffffffffu, fin);
+        if (m) __threadfence();
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int tt = __shfl_sync(0xffffffffu, t, src);
+            f_combine_block(p, v, tt, c, lane);
+            if (!p.out) {
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0) {
+                    last = atomicAdd(&p.rowdone[tt], 1u) + 1 == (uint32_t)tp2;
+                    if (last) p.rowdone[tt] = 0;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    f_rms_row(p, tt, lane);
+                }
+            }
+        }
+    }
+    // the last down task of expert e resets the expert's counters
+    if (lane == 0) {
+        __threadfence();
+        if (atomicAdd(&p.done2[e], 1u) + 1 == (uint32_t)tp2) {
+            p.done1[e] = 0;
+            p.done2[e] = 0;
+        }
+    }
+    return true;
+}
+
+// ---- kernel -----------------------------------------------------------------
+template <bool kStaged>
+__global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_constant__ FusedParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w1) : "memory");
+    const Pro v = pro_views(smem, p);
+    fused_prologue(p, smem, v);
+
+    const int nact = *v.nact;
+    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
+    const int n1 = nact * tp1, n2 = nact * tp2;
+    const int C = gridDim.x, cb = blockIdx.x;
+    WarpList L;
+    L.b1 = (int)((long long)n1 * cb / C);
+    L.m1 = (int)((long long)n1 * (cb + 1) / C) - L.b1;
+    L.b2 = (int)((long long)n2 * cb / C);
+    L.m2 = (int)((long long)n2 * (cb + 1) / C) - L.b2;
+    L.warp = warp;
+    L.n1 = n1;
+    L.nkc = p.nkc;
+    uint8_t *stages = smem + (size_t)warp * 2 * p.stage_bytes;
+    uint64_t *bar = v.bar + 2 * warp;
+    if (lane == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+    }
+    fence_mbar_init();
+    __syncwarp();
+
+    Seq ahead{0, 0};
+    for (int s = 0; s < 2; ++s) {
+        const int tk = L.task(ahead.pos);
+        if (tk < 0) break;
+        f_issue(p, v, tk, ahead.chunk, n1, stages + s * p.stage_bytes, &bar[s], lane);
+        L.advance(ahead);
+    }
+    float acc[kMaxNT][4];
+    uint32_t phase[2] = {0u, 0u};
+    Seq cur{0, 0};
+    for (int st = 0;; st ^= 1) {
+        const int tk = L.task(cur.pos);
+        if (tk < 0) break;
+        uint8_t *stage = stages + st * p.stage_bytes;
+        if (!mbar_wait(&bar[st], phase[st])) {
+            // a copy did not land in time: record it, give the other stage's
+            // copy one more bounded wait, and stop
+            if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+            mbar_wait(&bar[st ^ 1], phase[st ^ 1]);
+            return;
+        }
+        phase[st] ^= 1u;
+        if (tk < n1) {
+            f_gate_up_chunk<kStaged>(p, v, tk, cur.chunk, stage, smem, lane, acc);
+            if (cur.chunk == p.nkc - 1) {
+                f_gate_up_store(p, v, tk, lane, acc);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) red_release_add_u32(&p.done1[v.act[tk / tp1]], 1u);
+            }
+        } else {
+            f_down(p, v, tk - n1, stage, lane);
+        }
+        __syncwarp();
+        const int nx = L.task(ahead.pos);
+        if (nx >= 0) {
+            fence_proxy_async_smem();
+            f_issue(p, v, nx, ahead.chunk, n1, stage, &bar[st], lane);
+            L.advance(ahead);
+        }
+        L.advance(cur);
+    }
+}
+
+cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
+                                float eps, cudaStream_t s) {
+    const WsLayout W = ws_layout(d);
+    const FusedLayout L = fused_layout(d);
+    if (!L.ok) return cudaErrorInvalidValue;
+    FusedParams p;
+    cudaError_t err = encode_tmap_2d(&p.tm_w1, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w1p, (uint64_t)d.H / 8,
+                                     (uint64_t)d.E * 2 * d.I, (uint64_t)d.H / 2, (uint32_t)L.gcw, 8u,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    p.x = a.x;
+    p.ids = a.ids;
+    p.topk_w = a.topk_w;
+    p.w1s = a.w1s;
+    p.w2p = a.w2p;
+    p.w2s = a.w2s;
+    p.out = next ? nullptr : out;
+    p.next = next;
+    p.eps = eps;
+    p.ctrl = ws_at<Ctrl>(ws, W.ctrl);
+    p.done1 = ws_at<uint32_t>(ws, W.done1);
+    p.done2 = ws_at<uint32_t>(ws, W.done2);
+    p.ticket = ws_at<uint32_t>(ws, W.ticket);
+    p.rowdone = ws_at<uint32_t>(ws, W.rowdone);
+    p.hbuf = ws_at<uint16_t>(ws, W.hbuf);
+    p.ybuf = ws_at<float>(ws, W.ybuf);
+    p.rbuf = ws_at<float>(ws, W.rbuf);
+    p.T = d.T;
+    p.H = d.H;
+    p.E = d.E;
+    p.k = d.k;
+    p.I = d.I;
+    p.gcw = L.gcw;
+    p.nkc = L.nkc;
+    p.stage_bytes = L.stage_bytes;
+    p.pro_off = L.pro_off;
+    p.xs_off = L.xs_off;
+
+    const bool staged = L.xs_off != 0;
+    const void *fn = staged ? reinterpret_cast<const void *>(decode_fused_kernel<true>)
+                            : reinterpret_cast<const void *>(decode_fused_kernel<false>);
+    err = set_smem_once(fn, kFusedSmem);
+    if (err != cudaSuccess) return err;
+    const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
+    const long long max_tasks = max_active * (d.I / 8 + d.H / kP2Rows);
+    long long grid = (max_tasks + kFW - 1) / kFW;
+    if (grid > sm_count()) grid = sm_count();
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kFW * 32);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, p);
+}
+
+}  // namespace moe

@@ -1,6 +1,7 @@
 // Host-side launchers of the libw4a16moe kernels (all enqueue on `s`).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "w4a16moe.h"
@@ -9,6 +10,11 @@ namespace moe {
 
 // Raises a kernel's dynamic shared memory limit once per device.
 cudaError_t set_smem_once(const void *func, int bytes);
+
+// 2-D tiled TMA descriptor over a row-major [rows][inner] tensor.
+cudaError_t encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base,
+                           uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                           uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
@@ -33,6 +39,11 @@ struct ExpertArgs {
 cudaError_t launch_decode_experts(const ExpertArgs &a, const moe_dims &d, void *ws, cudaStream_t s);
 // True if the decode kernel supports these dims (its shared-memory stages fit).
 bool decode_supported(const moe_dims &d);
+
+// Fused decode forward (T <= 64): permute, experts and combine in one launch.
+bool fused_supported(const moe_dims &d);
+cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
+                                float eps, cudaStream_t s);
 
 // out[t] = bf16(sum_j w[t][j] * y[slot(t, j)]); with `next` set instead:
 // next[t] = bf16(rms_rescale(x[t] + that sum)).

@@ -93,44 +93,65 @@ __device__ inline float f32_from_order_key(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------
-// Top-k: one warp per token. Lane l holds experts l, l+32, ... as 64-bit keys
-// (order key of the fp32 logit << 32 | 0xffffffff - id). Each of the k
-// rounds takes the warp maximum (unique, because ids differ), removes it, and
-// records it. Weights: softmax over the selected logits in fp32.
-constexpr int kTopkMaxPer = kMaxE / 32;
+// Top-k: one CTA of 256 threads per token. Thread i sums the K-split partial
+// logits of experts i, i+256, ... and forms their 64-bit keys (order key of
+// the fp32 logit << 32 | 0xffffffff - id). Each warp extracts its own k
+// largest keys (k rounds of a two-step warp max with redux.sync: first the
+// logit half, then the id half among the lanes holding that logit); warp 0
+// then takes the k largest of the 8 warps' candidates. Keys are unique, so
+// every maximum has exactly one holder. Weights: softmax over the selected
+// logits in fp32.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkPer = kMaxE / kTopkThreads;
 
-__global__ void __launch_bounds__(128) route_topk_kernel(const float *__restrict__ partial, int ksplit,
-                                                         const float *__restrict__ bias, int T, int E,
-                                                         int k, int32_t *__restrict__ ids,
-                                                         float *__restrict__ w) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const int nper = (E + 31) / 32;
-    uint64_t key[kTopkMaxPer];
+__device__ inline uint64_t warp_max_key(uint64_t m) {
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32) == hi ? (uint32_t)m : 0u);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ partial, int ksplit,
+                                                                  const float *__restrict__ bias, int T, int E,
+                                                                  int k, int32_t *__restrict__ ids,
+                                                                  float *__restrict__ w) {
+    __shared__ uint64_t cand[kTopkThreads / 32][kMaxK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x;
+    uint64_t key[kTopkPer];
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPer; ++i) {
+    for (int i = 0; i < kTopkPer; ++i) {
         key[i] = 0;
-        const int e = lane + 32 * i;
-        if (i < nper && e < E) {
+        const int e = threadIdx.x + kTopkThreads * i;
+        if (e < E) {
             float l = 0.f;
             for (int s = 0; s < ksplit; ++s) l += partial[((size_t)s * T + t) * E + e];
             if (bias) l += bias[e];
             key[i] = ((uint64_t)f32_order_key(l) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
         }
     }
-    uint64_t mine = 0;   // lane j keeps the j-th selected key
     for (int j = 0; j < k; ++j) {
         uint64_t m = 0;
 #pragma unroll
-        for (int i = 0; i < kTopkMaxPer; ++i) m = key[i] > m ? key[i] : m;
+        for (int i = 0; i < kTopkPer; ++i) m = key[i] > m ? key[i] : m;
+        m = warp_max_key(m);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, m, off);
-            m = o > m ? o : m;
-        }
+        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+        if (lane == 0) cand[warp][j] = m;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // lane l holds candidate slot l of every warp's list
+    uint64_t c[kTopkThreads / 32];
 #pragma unroll
-        for (int i = 0; i < kTopkMaxPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+    for (int v = 0; v < kTopkThreads / 32; ++v) c[v] = lane < k ? cand[v][lane] : 0;
+    uint64_t mine = 0;
+    for (int j = 0; j < k; ++j) {
+        uint64_t m = 0;
+#pragma unroll
+        for (int v = 0; v < kTopkThreads / 32; ++v) m = c[v] > m ? c[v] : m;
+        m = warp_max_key(m);
+#pragma unroll
+        for (int v = 0; v < kTopkThreads / 32; ++v) c[v] = c[v] == m ? 0 : c[v];
         if (lane == j) mine = m;
     }
     const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
@@ -162,7 +183,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_topk_kernel<<<(d.T + 3) / 4, 128, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+    route_topk_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
     return cudaGetLastError();
 }
 
