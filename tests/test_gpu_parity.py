@@ -312,3 +312,56 @@ def test_forward_rms_stack_step():
     ref_out = forward_ref(h, ids, w32, E, I)
     _, ref_next = oracle.residual_rms(h["hidden"], ref_out, eps=1e-6)
     assert_close(nxt.float().cpu().numpy(), ref_next, "rms")
+
+
+# ------------------------------------------------------- prefill (tcgen05) ----
+
+@pytest.mark.parametrize("T,H,E,k,I", [
+    (80, 256, 16, 2, 128),      # just above the decode limit
+    (129, 128, 1, 1, 128),      # one expert: a full 128-token chunk and a 1-token chunk
+    (300, 384, 4, 2, 256),      # hot experts spanning three chunks, odd group count
+    (200, 512, 64, 8, 384),     # many small experts, ragged N tiles
+])
+def test_prefill_forward_parity(T, H, E, k, I):
+    seed = T * 7 + E
+    x = synth.hidden(T, H, seed=seed)
+    wts = synth.expert_weights(E, H, I, seed=seed)
+    ids, w = synth.random_topk(T, E, k, seed=seed)
+    W = [wts[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
+    ws = moe.workspace(T, H, E, k, I)
+    out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W, ws=ws)
+    assert moe.moe_check_device_error(ws) == 0
+    ref = oracle.expert_forward(x, ids, w, wts["w1_packed"], wts["w1_scales"], wts["w2_packed"],
+                                wts["w2_scales"], E, I)
+    assert_close(out.float().cpu().numpy(), ref, "prefill T=%d H=%d E=%d k=%d I=%d" % (T, H, E, k, I))
+    # the workspace is left clean: a second call gives the same result
+    out2 = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W, ws=ws)
+    assert_close(out2.float().cpu().numpy(), ref, "second call")
+
+
+def test_prefill_full_shape_sampled():
+    """T = 4096 at the full layer shape, uniform routing, checked on sampled tokens."""
+    wl = synth.WORKLOADS["stack_prefill4096"]
+    T, H, E, k, I = wl.dims
+    x = synth.hidden(T, H, seed=11)
+    wts = synth.expert_weights(E, H, I, seed=11)
+    ids, w = synth.random_topk(T, E, k, seed=11)
+    W = [wts[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
+    out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W).float().cpu().numpy()
+    rows = np.sort(np.random.default_rng(11).choice(T, 16, replace=False))
+    ref = oracle.expert_forward(x[rows], ids[rows], w[rows], wts["w1_packed"], wts["w1_scales"],
+                                wts["w2_packed"], wts["w2_scales"], E, I)
+    assert_close(out[rows], ref, "T=4096 sampled")
+
+
+def test_prefill_rms_stack_step():
+    T, H, E, k, I = 96, 256, 8, 2, 128
+    x = synth.hidden(T, H, seed=4)
+    wts = synth.expert_weights(E, H, I, seed=4)
+    ids, w = synth.random_topk(T, E, k, seed=4)
+    W = [wts[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
+    nxt = moe.moe_w4a16_forward_rms(x.cuda(), ids.cuda(), w.cuda(), *W, eps=1e-6)
+    ref_out = oracle.expert_forward(x, ids, w, wts["w1_packed"], wts["w1_scales"], wts["w2_packed"],
+                                    wts["w2_scales"], E, I)
+    _, ref_next = oracle.residual_rms(x, ref_out, eps=1e-6)
+    assert_close(nxt.float().cpu().numpy(), ref_next, "prefill rms")

@@ -71,7 +71,7 @@ int check_dims(const moe_dims &d) {
     if (d.H % kGroup || d.I % kGroup || d.H > 8192 || d.I > 4096) return MOE_ERR_UNSUPPORTED;
     if (d.k > kMaxK || d.k > d.E || d.E > kMaxE) return MOE_ERR_UNSUPPORTED;
     if (d.T > (1 << 20)) return MOE_ERR_UNSUPPORTED;
-    if (!decode_supported(d)) return MOE_ERR_UNSUPPORTED;
+    if (!prefill_supported(d)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -113,10 +113,7 @@ int forward_impl(const uint16_t *hidden, const int32_t *topk_ids, const float *t
         return cuda_status(err);
     }
     err = launch_permute(topk_ids, d, ws, s);
-    if (err == cudaSuccess) err = record_profile_event(g_ev_before, s);
-    if (err == cudaSuccess) err = launch_decode_experts(a, d, ws, s);
-    if (err == cudaSuccess) err = record_profile_event(g_ev_after, s);
-    if (err == cudaSuccess) err = launch_combine(a, d, ws, out, next, eps, s);
+    if (err == cudaSuccess) err = launch_prefill(a, d, ws, out, next, eps, g_ev_before, g_ev_after, s);
     return cuda_status(err);
 }
 

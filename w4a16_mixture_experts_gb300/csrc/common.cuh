@@ -40,7 +40,10 @@ struct WsLayout {
     size_t perm;         // i32 [T*k]      slot -> assignment
     size_t inv;          // i32 [T*k]      assignment -> slot (-1: dropped)
     size_t hbuf;         // bf16 [T*k][I]  SiLU(g)*u per slot (fragment order)
-    size_t ybuf;         // f32 [T*k][H]   down-projection output per slot
+    size_t ybuf;         // f32 [T*k][H]   down-projection output per slot (decode path)
+    size_t xperm;        // bf16 [T][H]    activations in fragment order (prefill path)
+    size_t out_acc;      // f32 [T][H]     weighted output accumulator (prefill path)
+    size_t chunk_base;   // i32 [E+1]      first 128-token chunk per active expert (prefill path)
     size_t total;
     int ksplit;
     int nchunk;
@@ -81,7 +84,11 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.perm = take(T * k * 4);
     L.inv = take(T * k * 4);
     L.hbuf = take(T * k * I * 2);
-    L.ybuf = take(T * k * H * 4);
+    const bool small = T <= 64;
+    L.ybuf = take(small ? T * k * H * 4 : 0);
+    L.xperm = take(small ? 0 : T * H * 2);
+    L.out_acc = take(small ? 0 : T * H * 4);
+    L.chunk_base = take((E + 1) * 4);
     L.total = o;
     return L;
 }

@@ -34,21 +34,17 @@ struct ExpertArgs {
     const uint16_t *w2s;
 };
 
-// Decode-shaped expert path (skinny GEMMs on mma.sync, register dequant):
-// fills the per-slot down-projection buffer of the workspace.
-cudaError_t launch_decode_experts(const ExpertArgs &a, const moe_dims &d, void *ws, cudaStream_t s);
-// True if the decode kernel supports these dims (its shared-memory stages fit).
-bool decode_supported(const moe_dims &d);
+// Prefill expert path (tcgen05 grouped GEMMs; needs launch_permute first):
+// x reordering, gate_up, down, and the conversion of the fp32 accumulator.
+// The two events (may be null) bracket the gate_up and down kernels.
+bool prefill_supported(const moe_dims &d);
+cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
+                           cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t s);
 
 // Fused decode forward (T <= 64): permute, experts and combine in one launch.
 bool fused_supported(const moe_dims &d);
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
                                 float eps, cudaStream_t s);
-
-// out[t] = bf16(sum_j w[t][j] * y[slot(t, j)]); with `next` set instead:
-// next[t] = bf16(rms_rescale(x[t] + that sum)).
-cudaError_t launch_combine(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
-                           float eps, cudaStream_t s);
 
 cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
                              cudaStream_t s);

@@ -1,0 +1,538 @@
+// Prefill expert path (T > 64): W4A16 grouped GEMMs on the tcgen05 tensor core.
+//
+// Same computation as the fused Marlin MoE of "Running 125B MoE on Three
+// 3090s - vLLM Optimization Edition", section 3.3 "MoE block" (gate_up,
+// SiluAndMul, down, weighted sum), for batches where each expert sees many
+// tokens. Section 3.3's W8A16 lesson (decode tiles do not carry over to
+// prefill) is why this is a separate kernel. Two launches of one
+// warp-specialised persistent kernel:
+//
+//   gate_up: tile = (expert, 64 intermediate rows i0.., up to 128 tokens).
+//            A = 128 weight rows (gate row i and up row i interleaved), K = H.
+//            Epilogue: h = SiLU(g) * u, rounded to bf16, stored per slot.
+//   down:    tile = (expert, 128 output rows, up to 128 tokens), K = I.
+//            Epilogue: out_acc[t] += topk_w * y (fp32 reduction in L2).
+//
+// Per 64-wide K step:
+//   * one TMA tile of packed INT4 (128 rows x 32 bytes) lands in shared
+//     memory (warp 8 lane 0, mbarrier complete_tx);
+//   * 128 producer threads gather the token rows of the activations (64 bf16
+//     each) with cp.async into the 128-byte-swizzled K-major layout the MMA
+//     descriptor reads;
+//   * 128 dequant threads (one per weight row) turn 64 nibbles into bf16
+//     q*scale in registers and write them straight into tensor memory as the
+//     A operand (tcgen05.st), so A never touches shared memory;
+//   * one thread issues 4 tcgen05.mma (M=128, N=tokens, K=16) into an fp32
+//     TMEM accumulator; tcgen05.commit releases the stage.
+// The accumulator is double-buffered in TMEM so 128 epilogue threads drain
+// one tile while the next one accumulates.
+//
+// Weights enter A as W = bf16(q * scale) (one rounding per weight). Nibble
+// pairs (j, j+4) of each word fill one 32-bit TMEM column, so the
+// activations are kept in the matching order within each 8-element chunk
+// (0,4,1,5,2,6,3,7): x is rewritten into that order once per call, and the
+// gate_up epilogue stores h in it directly.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+
+constexpr int kPS = 6;             // pipeline stages
+constexpr int kPN = 128;           // max tokens per tile (columns of one TMEM accumulator)
+constexpr int kPG = 64;            // max quantisation groups along K (K <= 8192)
+constexpr int kPThreads = 13 * 32; // warps 0-3 dequant, 4-7 epilogue, 8-11 B producer, 12 MMA
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAStage0 = 2 * kPN;   // TMEM columns: 2 accumulators, then A stages of 32 columns
+constexpr uint32_t kBBytes = kPN * 128;  // one B stage: 128 rows x 64 bf16
+constexpr uint32_t kRawBytes = 128 * 32; // one packed-INT4 stage: 128 rows x 64 nibbles
+constexpr uint32_t kScaleBytes = 128 * kPG * 2;
+
+struct PrefillSmem {   // offsets from the 1024-aligned base
+    static constexpr uint32_t b = 0;
+    static constexpr uint32_t raw = b + kPS * kBBytes;
+    static constexpr uint32_t sc = raw + kPS * kRawBytes;
+    static constexpr uint32_t bars = sc + 2 * kScaleBytes;
+    static constexpr uint32_t nbars = 4 * kPS + 8;
+    static constexpr uint32_t tmem_slot = bars + nbars * 8;
+    static constexpr uint32_t total = tmem_slot + 16;
+};
+constexpr uint32_t kPrefillSmem = PrefillSmem::total + 1024;   // + alignment slack
+
+struct PrefillParams {
+    CUtensorMap tm_w;          // int32 [rows][K/8], box (8 words, 64 rows)
+    const uint16_t *b_src;     // gate_up: x in fragment order [T][H]; down: h [T*k][I]
+    const uint16_t *scales;    // bf16 [rows][K/128]
+    const int32_t *offsets;    // [E+1] slot offsets per expert
+    const int32_t *active;     // active experts, increasing
+    const int32_t *chunk_base; // [n_active+1] first 128-token chunk of each active expert
+    const int32_t *perm;       // slot -> assignment t*k+j
+    const float *topk_w;
+    const Ctrl *ctrl;
+    Ctrl *ctrl_rw;
+    uint16_t *hbuf;            // gate_up output, bf16 [T*k][I] fragment order
+    float *out_acc;            // down output, f32 [T][H]
+    int T, H, E, k, I;
+    int K;                     // reduction length: H (gate_up) or I (down)
+    int mb;                    // row blocks per expert: I/64 (gate_up) or H/128 (down)
+    int down;                  // 0: gate_up, 1: down
+};
+
+struct Tile {
+    int e, s0, nv, n16, m;
+};
+
+// tile t -> (expert, token chunk, row block); chunks of each expert are
+// consecutive, and the row blocks of one chunk are consecutive tiles.
+__device__ inline Tile decode_tile(const PrefillParams &p, int nact, int t) {
+    const int c = t / p.mb;
+    Tile r;
+    r.m = t - c * p.mb;
+    int lo = 0, hi = nact;   // largest a with chunk_base[a] <= c
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.chunk_base[mid] <= c) lo = mid;
+        else hi = mid;
+    }
+    const int a = lo;
+    const int e = p.active[a];
+    const int chunk = c - p.chunk_base[a];
+    const int cnt = p.offsets[e + 1] - p.offsets[e];
+    r.e = e;
+    r.s0 = p.offsets[e] + chunk * kPN;
+    r.nv = min(kPN, cnt - chunk * kPN);
+    r.n16 = (r.nv + 15) & ~15;
+    return r;
+}
+
+__device__ inline void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ inline void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once all of this thread's prior cp.async have landed.
+__device__ inline void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ inline bool pwait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort_flag) return false;
+    }
+    return false;
+}
+
+__device__ inline void fail(const PrefillParams &p, volatile int *abort_flag) {
+    *abort_flag = 1;
+    set_error(p.ctrl_rw, MOE_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sB = smem + PrefillSmem::b;
+    uint8_t *sRaw = smem + PrefillSmem::raw;
+    uint16_t *sSc = reinterpret_cast<uint16_t *>(smem + PrefillSmem::sc);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PrefillSmem::bars);
+    uint64_t *raw_full = bars;              // [kPS] TMA tile (+tx) and 128 cp.async producers
+    uint64_t *a_full = bars + kPS;          // [kPS] 128 dequant threads
+    uint64_t *stage_empty = bars + 2 * kPS; // [kPS] MMA commit
+    uint64_t *acc_full = bars + 3 * kPS;    // [2] MMA commit
+    uint64_t *acc_empty = acc_full + 2;     // [2] 128 epilogue threads
+    uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
+    uint64_t *sc_empty = sc_full + 2;       // [2] 128 dequant threads
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PrefillSmem::tmem_slot);
+    __shared__ int abort_s;
+    volatile int *abort_flag = &abort_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        abort_s = 0;
+        for (int s = 0; s < kPS; ++s) {
+            mbar_init(&raw_full[s], 1 + 128);
+            mbar_init(&a_full[s], 128);
+            mbar_init(&stage_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+            mbar_init(&sc_full[b], 1);
+            mbar_init(&sc_empty[b], 128);
+        }
+        fence_mbar_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w) : "memory");
+    }
+    if (warp == 12) {
+        tc::alloc(tmem_slot, kTmemCols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int nact = (int)p.ctrl->n_active;
+    const int ntiles = nact > 0 ? p.chunk_base[nact] * p.mb : 0;
+    const int nks = p.K / 64;
+    const int G = p.K / 128;
+
+    if (warp < 4) {
+        // ------------------------------------------------ dequant: one weight row per thread
+        const int r = threadIdx.x;   // tile row, TMEM lane
+        const int raw_off = p.down ? r * 32 : (r & 1) * 2048 + (r >> 1) * 32;
+        const int sc_row = p.down ? r : (r & 1) * 64 + (r >> 1);
+        uint32_t g = 0;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            const int tb = lt & 1;
+            if (!pwait(&sc_full[tb], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
+            const uint16_t *sc = sSc + tb * (kScaleBytes / 2) + sc_row * G;
+            bool ok = true;
+            for (int ks = 0; ks < nks; ++ks, ++g) {
+                const int s = g % kPS;
+                if (!pwait(&raw_full[s], (g / kPS) & 1, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                const uint8_t *rr = sRaw + s * kRawBytes + raw_off;
+                const uint4 w0 = lds_v4(rr), w1 = lds_v4(rr + 16);
+                const uint32_t sb = sc[ks >> 1];
+                const uint32_t s2u = sb | (sb << 16);
+                const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
+                uint32_t v[32];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t w = m < 4 ? (m == 0 ? w0.x : m == 1 ? w0.y : m == 2 ? w0.z : w0.w)
+                                             : (m == 4 ? w1.x : m == 5 ? w1.y : m == 6 ? w1.z : w1.w);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t q = int4_pair(w, j);
+                        __nv_bfloat162 qv = *reinterpret_cast<__nv_bfloat162 *>(&q);
+                        qv = __hmul2(qv, s2);
+                        v[4 * m + j] = *reinterpret_cast<uint32_t *>(&qv);
+                    }
+                }
+                tc::st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + kAStage0 + s * 32, v);
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(&a_full[s]);
+            }
+            if (!ok) { fail(p, abort_flag); break; }
+            mbar_arrive(&sc_empty[tb]);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------ epilogue: one accumulator row per thread
+        const int q = warp - 4;
+        const int r = 32 * q + lane;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            const Tile T = decode_tile(p, nact, t);
+            const int b = lt & 1;
+            if (!pwait(&acc_full[b], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
+            tc::fence_after();
+            const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + b * kPN;
+            for (int c0 = 0; c0 < T.nv; c0 += 16) {
+                float v[16];
+                tc::ld_32x32b_x16(dbase + c0, v);
+                tc::wait_ld();
+                if (!p.down) {
+                    // rows 2i (gate) and 2i+1 (up) of intermediate i0 + i sit in adjacent lanes
+                    const int i = T.m * 64 + (r >> 1);
+                    const int pos = 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float other = __shfl_xor_sync(0xffffffffu, v[u], 1);
+                        if (c0 + u < T.nv && !(lane & 1)) {
+                            const float hv = silu(v[u]) * other;
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                            p.hbuf[(size_t)(T.s0 + c0 + u) * p.I + pos] = *reinterpret_cast<const uint16_t *>(&hb);
+                        }
+                    }
+                } else {
+                    const int n = T.m * 128 + r;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        if (c0 + u < T.nv) {
+                            const int a = p.perm[T.s0 + c0 + u];
+                            const int tok = a / p.k;
+                            const float w = p.topk_w[a];
+                            atomicAdd(p.out_acc + (size_t)tok * p.H + n, w * v[u]);
+                        }
+                    }
+                }
+            }
+            tc::fence_before();
+            mbar_arrive(&acc_empty[b]);
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------ producers: INT4 tile (TMA) + activation rows (cp.async)
+        const int r = threadIdx.x - 256;   // B row (token column of the tile)
+        uint32_t g = 0;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            const Tile T = decode_tile(p, nact, t);
+            const int tb = lt & 1;
+            // scales of the tile's 128 rows, all groups
+            if (r == 0) {
+                if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); }
+                else {
+                    uint16_t *dst = sSc + tb * (kScaleBytes / 2);
+                    if (!p.down) {
+                        const size_t row = (size_t)T.e * 2 * p.I + T.m * 64;
+                        mbar_arrive_expect_tx(&sc_full[tb], 2 * 64 * G * 2);
+                        bulk_g2s(dst, p.scales + row * G, 64 * G * 2, &sc_full[tb]);
+                        bulk_g2s(dst + 64 * G, p.scales + (row + p.I) * G, 64 * G * 2, &sc_full[tb]);
+                    } else {
+                        const size_t row = (size_t)T.e * p.H + T.m * 128;
+                        mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
+                        bulk_g2s(dst, p.scales + row * G, 128 * G * 2, &sc_full[tb]);
+                    }
+                }
+            }
+            // the activation row this thread gathers
+            const int rr = r < T.nv ? r : 0;
+            const uint16_t *src;
+            if (!p.down) {
+                const int a = p.perm[T.s0 + rr];
+                src = p.b_src + (size_t)(a / p.k) * p.H;
+            } else {
+                src = p.b_src + (size_t)(T.s0 + rr) * p.I;
+            }
+            bool ok = true;
+            for (int ks = 0; ks < nks; ++ks, ++g) {
+                const int s = g % kPS;
+                if (!pwait(&stage_empty[s], ((g / kPS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (r == 0) {
+                    mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
+                    uint8_t *dst = sRaw + s * kRawBytes;
+                    if (!p.down) {
+                        const int row = T.e * 2 * p.I + T.m * 64;
+                        tma_load_2d(dst, &p.tm_w, ks * 8, row, &raw_full[s]);
+                        tma_load_2d(dst + 2048, &p.tm_w, ks * 8, row + p.I, &raw_full[s]);
+                    } else {
+                        const int row = T.e * p.H + T.m * 128;
+                        tma_load_2d(dst, &p.tm_w, ks * 8, row, &raw_full[s]);
+                        tma_load_2d(dst + 2048, &p.tm_w, ks * 8, row + 64, &raw_full[s]);
+                    }
+                }
+                if (r < T.n16) {
+                    // 128-byte swizzle: 16-byte chunk c of row r goes to chunk c ^ (r % 8)
+                    uint8_t *row_dst = sB + s * kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                    const uint16_t *row_src = src + ks * 64;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) cp_async_16(row_dst + ((c ^ (r & 7)) << 4), row_src + 8 * c);
+                }
+                cp_async_arrive(&raw_full[s]);
+            }
+            if (!ok) { fail(p, abort_flag); break; }
+        }
+        // every issued copy must land before the CTA may exit
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        // ------------------------------------------------ MMA issuer
+        uint32_t g = 0;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            const Tile T = decode_tile(p, nact, t);
+            const int b = lt & 1;
+            if (!pwait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+            tc::fence_after();
+            const uint32_t d = tmem + b * kPN;
+            const uint32_t idesc = tc::idesc_bf16(128, T.n16);
+            bool ok = true;
+            for (int ks = 0; ks < nks; ++ks, ++g) {
+                const int s = g % kPS;
+                if (!pwait(&a_full[s], (g / kPS) & 1, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                if (lane == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    const uint64_t bdesc = tc::sdesc_sw128(sB + s * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(d, tmem + kAStage0 + s * 32 + kk * 8, bdesc + (uint64_t)(kk * 2), idesc,
+                                   (ks | kk) != 0);
+                    tc::commit(&stage_empty[s]);
+                }
+                __syncwarp();
+            }
+            if (!ok) { fail(p, abort_flag); break; }
+            if (lane == 0) tc::commit(&acc_full[b]);
+            __syncwarp();
+        }
+    }
+
+    // all tensor-core work of this CTA has been consumed by the epilogue (or the
+    // CTA aborted); free the tensor memory
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 12) tc::dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// x -> fragment order within each 8-element chunk: (0,4,1,5,2,6,3,7).
+__global__ void xperm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int64_t nchunks) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= nchunks) return;
+    const uint4 c = ld_nc_v4(x + 8 * i);
+    *reinterpret_cast<uint4 *>(xp + 8 * i) =
+        make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632), __byte_perm(c.y, c.w, 0x5410),
+                   __byte_perm(c.y, c.w, 0x7632));
+}
+
+// One CTA: first 128-token chunk of each active expert (exclusive scan over
+// the active list, in expert order).
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(const int32_t *__restrict__ counts, int E,
+                                                          int32_t *__restrict__ chunk_base) {
+    __shared__ int warp_sums[32];
+    const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+    const int c = e < E ? (counts[e] + kPN - 1) / kPN : 0;
+    const int act = e < E && counts[e] > 0;
+    // two inclusive scans at once: chunks and active flags
+    int ic = c, ia = act;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int oc = __shfl_up_sync(0xffffffffu, ic, off), oa = __shfl_up_sync(0xffffffffu, ia, off);
+        if (lane >= off) {
+            ic += oc;
+            ia += oa;
+        }
+    }
+    __shared__ int wa[32];
+    if (lane == 31) {
+        warp_sums[w] = ic;
+        wa[w] = ia;
+    }
+    __syncthreads();
+    if (w == 0) {
+        int sc = warp_sums[lane], sa = wa[lane];
+        int xc = sc, xa = sa;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oc = __shfl_up_sync(0xffffffffu, xc, off), oa = __shfl_up_sync(0xffffffffu, xa, off);
+            if (lane >= off) {
+                xc += oc;
+                xa += oa;
+            }
+        }
+        warp_sums[lane] = xc - sc;
+        wa[lane] = xa - sa;
+    }
+    __syncthreads();
+    const int base_c = warp_sums[w] + ic - c;   // exclusive
+    const int base_a = wa[w] + ia - act;
+    if (act) chunk_base[base_a] = base_c;
+    if (e == E - 1) chunk_base[base_a + act] = base_c + c;
+}
+
+// out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue), then out_acc = 0.
+__global__ void __launch_bounds__(256) acc_convert_kernel(float *__restrict__ acc, const uint16_t *__restrict__ x,
+                                                          int H, float eps, uint16_t *__restrict__ out,
+                                                          uint16_t *__restrict__ next) {
+    __shared__ float red[8];
+    const int t = blockIdx.x;
+    float *row = acc + (size_t)t * H;
+    if (!next) {
+        for (int n = 4 * threadIdx.x; n < H; n += 1024) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + n);
+            *reinterpret_cast<float4 *>(row + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(out + (size_t)t * H + n) = u;
+        }
+        return;
+    }
+    float ss = 0.f;
+    for (int n = threadIdx.x; n < H; n += 256) {
+        const float r = row[n] + bf16_bits_to_f32(x[(size_t)t * H + n]);
+        ss += r * r;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float scale = rsqrtf(tot / (float)H + eps);
+    for (int n = threadIdx.x; n < H; n += 256) {
+        const float r = row[n] + bf16_bits_to_f32(x[(size_t)t * H + n]);
+        row[n] = 0.f;
+        const __nv_bfloat16 b = __float2bfloat16_rn(r * scale);
+        next[(size_t)t * H + n] = *reinterpret_cast<const uint16_t *>(&b);
+    }
+}
+
+bool prefill_supported(const moe_dims &d) {
+    return d.H % 128 == 0 && d.I % 128 == 0 && d.H / 128 <= kPG && d.I / 128 <= kPG && d.I % 64 == 0;
+}
+
+cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
+                           cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t s) {
+    const WsLayout W = ws_layout(d);
+    uint16_t *xperm = ws_at<uint16_t>(ws, W.xperm);
+    float *out_acc = ws_at<float>(ws, W.out_acc);
+    int32_t *chunk_base = ws_at<int32_t>(ws, W.chunk_base);
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmem);
+    if (err != cudaSuccess) return err;
+
+    const int64_t nch = (int64_t)d.T * d.H / 8;
+    xperm_kernel<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(a.x, xperm, nch);
+    chunk_scan_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), d.E, chunk_base);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    PrefillParams p;
+    p.offsets = ws_at<int32_t>(ws, W.offsets);
+    p.active = ws_at<int32_t>(ws, W.active);
+    p.chunk_base = chunk_base;
+    p.perm = ws_at<int32_t>(ws, W.perm);
+    p.topk_w = a.topk_w;
+    p.ctrl = ws_at<Ctrl>(ws, W.ctrl);
+    p.ctrl_rw = ws_at<Ctrl>(ws, W.ctrl);
+    p.hbuf = ws_at<uint16_t>(ws, W.hbuf);
+    p.out_acc = out_acc;
+    p.T = d.T;
+    p.H = d.H;
+    p.E = d.E;
+    p.k = d.k;
+    p.I = d.I;
+    const unsigned grid = (unsigned)sm_count();
+
+    // gate_up: K = H, 64 intermediate rows (x2 for gate and up) per tile
+    err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w1p, (uint64_t)d.H / 8, (uint64_t)d.E * 2 * d.I,
+                         (uint64_t)d.H / 2, 8u, 64u, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    if (ev_before && (err = cudaEventRecordWithFlags(ev_before, s, cudaEventRecordExternal)) != cudaSuccess) return err;
+    p.b_src = xperm;
+    p.scales = a.w1s;
+    p.K = d.H;
+    p.mb = d.I / 64;
+    p.down = 0;
+    prefill_kernel<<<grid, kPThreads, kPrefillSmem, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    // down: K = I, 128 output rows per tile
+    err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w2p, (uint64_t)d.I / 8, (uint64_t)d.E * d.H,
+                         (uint64_t)d.I / 2, 8u, 64u, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    p.b_src = p.hbuf;
+    p.scales = a.w2s;
+    p.K = d.I;
+    p.mb = d.H / 128;
+    p.down = 1;
+    prefill_kernel<<<grid, kPThreads, kPrefillSmem, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (ev_after && (err = cudaEventRecordWithFlags(ev_after, s, cudaEventRecordExternal)) != cudaSuccess) return err;
+
+    acc_convert_kernel<<<d.T, 256, 0, s>>>(out_acc, a.x, d.H, eps, next ? nullptr : out, next);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
