@@ -43,18 +43,21 @@ namespace moe {
 constexpr int kPS = 6;             // pipeline stages
 constexpr int kPN = 128;           // max tokens per tile (columns of one TMEM accumulator)
 constexpr int kPG = 64;            // max quantisation groups along K (K <= 8192)
-constexpr int kPThreads = 13 * 32; // warps 0-3 dequant, 4-7 epilogue, 8-11 B producer, 12 MMA
+constexpr int kPThreads = 17 * 32; // warps 0-7 dequant (two groups), 8-11 epilogue, 12-15 B producer, 16 MMA
+constexpr int kWEpi = 8, kWProd = 12, kWMma = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAStage0 = 2 * kPN;   // TMEM columns: 2 accumulators, then A stages of 32 columns
 constexpr uint32_t kBBytes = kPN * 128;  // one B stage: 128 rows x 64 bf16
 constexpr uint32_t kRawBytes = 128 * 32; // one packed-INT4 stage: 128 rows x 64 nibbles
 constexpr uint32_t kScaleBytes = 128 * kPG * 2;
+constexpr uint32_t kEpiBytes = 16 * 128 * 4;   // one epilogue staging buffer: 16 token columns x 128 rows f32
 
 struct PrefillSmem {   // offsets from the 1024-aligned base
     static constexpr uint32_t b = 0;
     static constexpr uint32_t raw = b + kPS * kBBytes;
     static constexpr uint32_t sc = raw + kPS * kRawBytes;
-    static constexpr uint32_t bars = sc + 2 * kScaleBytes;
+    static constexpr uint32_t epi = sc + 2 * kScaleBytes;
+    static constexpr uint32_t bars = epi + 2 * kEpiBytes;
     static constexpr uint32_t nbars = 4 * kPS + 8;
     static constexpr uint32_t tmem_slot = bars + nbars * 8;
     static constexpr uint32_t total = tmem_slot + 16;
@@ -147,9 +150,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint64_t *acc_full = bars + 3 * kPS;    // [2] MMA commit
     uint64_t *acc_empty = acc_full + 2;     // [2] 128 epilogue threads
     uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
-    uint64_t *sc_empty = sc_full + 2;       // [2] 128 dequant threads
+    uint64_t *sc_empty = sc_full + 2;       // [2] 256 dequant threads
+    uint8_t *sEpi = smem + PrefillSmem::epi;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PrefillSmem::tmem_slot);
     __shared__ int abort_s;
+    __shared__ float col_w[kPN];
+    __shared__ int col_tok[kPN];
     volatile int *abort_flag = &abort_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,12 +170,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 128);
             mbar_init(&sc_full[b], 1);
-            mbar_init(&sc_empty[b], 128);
+            mbar_init(&sc_empty[b], 256);
         }
         fence_mbar_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w) : "memory");
     }
-    if (warp == 12) {
+    if (warp == kWMma) {
         tc::alloc(tmem_slot, kTmemCols);
         tc::relinquish();
     }
@@ -183,9 +189,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     const int nks = p.K / 64;
     const int G = p.K / 128;
 
-    if (warp < 4) {
-        // ------------------------------------------------ dequant: one weight row per thread
-        const int r = threadIdx.x;   // tile row, TMEM lane
+    if (warp < kWEpi) {
+        // ------------------------------------------------ dequant: one weight row per thread; group
+        // 0 (warps 0-3) takes the even stages, group 1 (warps 4-7) the odd ones
+        const int grp = warp >> 2;
+        const int r = threadIdx.x & 127;   // tile row, TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int raw_off = p.down ? r * 32 : (r & 1) * 2048 + (r >> 1) * 32;
         const int sc_row = p.down ? r : (r & 1) * 64 + (r >> 1);
         uint32_t g = 0;
@@ -197,6 +206,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             bool ok = true;
             for (int ks = 0; ks < nks; ++ks, ++g) {
                 const int s = g % kPS;
+                if ((s & 1) != grp) continue;
                 if (!pwait(&raw_full[s], (g / kPS) & 1, abort_flag)) { ok = false; break; }
                 tc::fence_after();
                 const uint8_t *rr = sRaw + s * kRawBytes + raw_off;
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                         v[4 * m + j] = *reinterpret_cast<uint32_t *>(&qv);
                     }
                 }
-                tc::st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + kAStage0 + s * 32, v);
+                tc::st_32x32b_x32(tmem + lane_base + kAStage0 + s * 32, v);
                 tc::wait_st();
                 tc::fence_before();
                 mbar_arrive(&a_full[s]);
@@ -225,53 +235,87 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             if (!ok) { fail(p, abort_flag); break; }
             mbar_arrive(&sc_empty[tb]);
         }
-    } else if (warp < 8) {
+    } else if (warp < kWProd) {
         // ------------------------------------------------ epilogue: one accumulator row per thread
-        const int q = warp - 4;
+        const int q = warp - kWEpi;
         const int r = 32 * q + lane;
-        int lt = 0;
+        const int et = threadIdx.x - 32 * kWEpi;   // 0..127
+        int lt = 0, nbuf = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = decode_tile(p, nact, t);
             const int b = lt & 1;
             if (!pwait(&acc_full[b], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
             tc::fence_after();
             const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + b * kPN;
-            for (int c0 = 0; c0 < T.nv; c0 += 16) {
+            if (p.down) {
+                // routing weight and token of every column of the tile
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (et < T.nv) {
+                    const int a = p.perm[T.s0 + et];
+                    col_w[et] = p.topk_w[a];
+                    col_tok[et] = a / p.k;
+                } else {
+                    col_w[et] = 0.f;
+                    col_tok[et] = 0;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            for (int c0 = 0; c0 < T.nv; c0 += 16, ++nbuf) {
                 float v[16];
                 tc::ld_32x32b_x16(dbase + c0, v);
                 tc::wait_ld();
+                uint8_t *stg = sEpi + (nbuf & 1) * kEpiBytes;
+                // the staging buffer's previous bulk operations must have read it
+                if (et < 16) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (!p.down) {
-                    // rows 2i (gate) and 2i+1 (up) of intermediate i0 + i sit in adjacent lanes
-                    const int i = T.m * 64 + (r >> 1);
-                    const int pos = 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1);
+                    // rows 2i (gate) and 2i+1 (up) of intermediate i0 + i sit in adjacent lanes;
+                    // h goes to its fragment-order position inside the tile's 64-wide block
+                    const int il = r >> 1;
+                    const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
+                    uint16_t *hs = reinterpret_cast<uint16_t *>(stg);   // [16 columns][64]
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const float other = __shfl_xor_sync(0xffffffffu, v[u], 1);
-                        if (c0 + u < T.nv && !(lane & 1)) {
-                            const float hv = silu(v[u]) * other;
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                            p.hbuf[(size_t)(T.s0 + c0 + u) * p.I + pos] = *reinterpret_cast<const uint16_t *>(&hb);
+                        if (!(lane & 1)) {
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(v[u]) * other);
+                            hs[u * 64 + pl] = *reinterpret_cast<const uint16_t *>(&hb);
                         }
                     }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (et < 16 && c0 + et < T.nv) {
+                        uint16_t *dst = p.hbuf + (size_t)(T.s0 + c0 + et) * p.I + T.m * 64;
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 128;" ::"l"(dst),
+                                     "r"(smem_u32(hs + et * 64))
+                                     : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
                 } else {
-                    const int n = T.m * 128 + r;
+                    // weighted rows, then one 512-byte reduce-add per token column
+                    float *ys = reinterpret_cast<float *>(stg);   // [16 columns][128 rows]
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        if (c0 + u < T.nv) {
-                            const int a = p.perm[T.s0 + c0 + u];
-                            const int tok = a / p.k;
-                            const float w = p.topk_w[a];
-                            atomicAdd(p.out_acc + (size_t)tok * p.H + n, w * v[u]);
-                        }
+                    for (int u = 0; u < 16; ++u) ys[u * 128 + r] = col_w[c0 + u] * v[u];
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (et < 16 && c0 + et < T.nv) {
+                        float *dst = p.out_acc + (size_t)col_tok[c0 + et] * p.H + T.m * 128;
+                        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 512;" ::"l"(
+                                         dst),
+                                     "r"(smem_u32(ys + et * 128))
+                                     : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }
             }
             tc::fence_before();
             mbar_arrive(&acc_empty[b]);
         }
-    } else if (warp < 12) {
+        // bulk stores / reductions must finish before the CTA exits
+        if (et < 16) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    } else if (warp < kWMma) {
         // ------------------------------------------------ producers: INT4 tile (TMA) + activation rows (cp.async)
-        const int r = threadIdx.x - 256;   // B row (token column of the tile)
+        const int r = threadIdx.x - 32 * kWProd;   // B row (token column of the tile)
         uint32_t g = 0;
         int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
@@ -371,7 +415,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    if (warp == 12) tc::dealloc(tmem, kTmemCols);
+    if (warp == kWMma) tc::dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
