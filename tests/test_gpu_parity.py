@@ -196,8 +196,10 @@ def test_forward_prefill512_zipf_sampled():
     wl, h, g = layer("prefill512")
     T, H, E, k, I = wl.dims
     ids_g, w_g = moe.moe_route(g["hidden"], g["router_w"], k, bias=g["bias"])
+    ws = moe.workspace(T, H, E, k, I)
     out = moe.moe_w4a16_forward(g["hidden"], ids_g, w_g, g["w1_packed"], g["w1_scales"], g["w2_packed"],
-                                g["w2_scales"])
+                                g["w2_scales"], ws=ws)
+    assert moe.moe_check_device_error(ws) == 0
     rows = np.sort(np.random.default_rng(1).choice(T, 24, replace=False))
     ids, w = ids_g.cpu().numpy()[rows], w_g.cpu().numpy()[rows]
     # the routing the GPU used is itself checked above; here it is an input
@@ -347,7 +349,9 @@ def test_prefill_full_shape_sampled():
     wts = synth.expert_weights(E, H, I, seed=11)
     ids, w = synth.random_topk(T, E, k, seed=11)
     W = [wts[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
-    out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W).float().cpu().numpy()
+    ws = moe.workspace(T, H, E, k, I)
+    out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W, ws=ws).float().cpu().numpy()
+    assert moe.moe_check_device_error(ws) == 0
     rows = np.sort(np.random.default_rng(11).choice(T, 16, replace=False))
     ref = oracle.expert_forward(x[rows], ids[rows], w[rows], wts["w1_packed"], wts["w1_scales"],
                                 wts["w2_packed"], wts["w2_scales"], E, I)

@@ -40,29 +40,39 @@
 
 namespace moe {
 
-constexpr int kPS = 6;             // pipeline stages
+constexpr int kRR = 16;            // packed-INT4 ring (HBM stream)
+constexpr int kRB = 8;             // activation ring (L2 stream)
+constexpr int kRA = 8;             // dequantised-A ring in tensor memory
 constexpr int kPN = 128;           // max tokens per tile (columns of one TMEM accumulator)
 constexpr int kPG = 64;            // max quantisation groups along K (K <= 8192)
-constexpr int kPThreads = 17 * 32; // warps 0-7 dequant (two groups), 8-11 epilogue, 12-15 B producer, 16 MMA
-constexpr int kWEpi = 8, kWProd = 12, kWMma = 16;
+constexpr int kWEpi = 8, kWRaw = 12, kWProd = 13, kWMma = 17;
+constexpr int kPThreads = 18 * 32; // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
+                                   // 13-16 activation producers, 17 MMA
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAStage0 = 2 * kPN;   // TMEM columns: 2 accumulators, then A stages of 32 columns
-constexpr uint32_t kBBytes = kPN * 128;  // one B stage: 128 rows x 64 bf16
+constexpr uint32_t kAStage0 = 2 * kPN;   // TMEM columns: 2 accumulators, then A slots of 32 columns
+constexpr uint32_t kBBytes = kPN * 128;  // one activation stage: 128 rows x 64 bf16
 constexpr uint32_t kRawBytes = 128 * 32; // one packed-INT4 stage: 128 rows x 64 nibbles
-constexpr uint32_t kScaleBytes = 128 * kPG * 2;
 constexpr uint32_t kEpiBytes = 16 * 128 * 4;   // one epilogue staging buffer: 16 token columns x 128 rows f32
+constexpr uint32_t kPrefillSmemMax = 232448 - 2048;
 
-struct PrefillSmem {   // offsets from the 1024-aligned base
-    static constexpr uint32_t b = 0;
-    static constexpr uint32_t raw = b + kPS * kBBytes;
-    static constexpr uint32_t sc = raw + kPS * kRawBytes;
-    static constexpr uint32_t epi = sc + 2 * kScaleBytes;
-    static constexpr uint32_t bars = epi + 2 * kEpiBytes;
-    static constexpr uint32_t nbars = 4 * kPS + 8;
-    static constexpr uint32_t tmem_slot = bars + nbars * 8;
-    static constexpr uint32_t total = tmem_slot + 16;
+struct PrefillLayout {   // shared-memory offsets from the 1024-aligned base; scales sized by K
+    uint32_t b, raw, sc, sc_bytes, epi, bars, tmem_slot, total;
 };
-constexpr uint32_t kPrefillSmem = PrefillSmem::total + 1024;   // + alignment slack
+static_assert(kRA == kRB, "the A slots and B stages are released by one barrier");
+constexpr int kNBars = 2 * kRR + 3 * kRA + 8;
+
+__host__ __device__ inline PrefillLayout prefill_layout(int G) {
+    PrefillLayout L;
+    L.b = 0;
+    L.raw = L.b + kRB * kBBytes;
+    L.sc = L.raw + kRR * kRawBytes;
+    L.sc_bytes = (uint32_t)(128 * G * 2 + 127) / 128 * 128;
+    L.epi = L.sc + 2 * L.sc_bytes;
+    L.bars = L.epi + 2 * kEpiBytes;
+    L.tmem_slot = L.bars + kNBars * 8;
+    L.total = L.tmem_slot + 16 + 1024;   // + alignment slack
+    return L;
+}
 
 struct PrefillParams {
     CUtensorMap tm_w;          // int32 [rows][K/8], box (8 words, 64 rows)
@@ -81,6 +91,7 @@ struct PrefillParams {
     int K;                     // reduction length: H (gate_up) or I (down)
     int mb;                    // row blocks per expert: I/64 (gate_up) or H/128 (down)
     int down;                  // 0: gate_up, 1: down
+    PrefillLayout L;
 };
 
 struct Tile {
@@ -140,19 +151,22 @@ __device__ inline void fail(const PrefillParams &p, volatile int *abort_flag) {
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sB = smem + PrefillSmem::b;
-    uint8_t *sRaw = smem + PrefillSmem::raw;
-    uint16_t *sSc = reinterpret_cast<uint16_t *>(smem + PrefillSmem::sc);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PrefillSmem::bars);
-    uint64_t *raw_full = bars;              // [kPS] TMA tile (+tx) and 128 cp.async producers
-    uint64_t *a_full = bars + kPS;          // [kPS] 128 dequant threads
-    uint64_t *stage_empty = bars + 2 * kPS; // [kPS] MMA commit
-    uint64_t *acc_full = bars + 3 * kPS;    // [2] MMA commit
+    const PrefillLayout &L = p.L;
+    uint8_t *sB = smem + L.b;
+    uint8_t *sRaw = smem + L.raw;
+    uint16_t *sSc = reinterpret_cast<uint16_t *>(smem + L.sc);
+    uint8_t *sEpi = smem + L.epi;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *raw_full = bars;              // [kRR] INT4 TMA (+tx)
+    uint64_t *raw_empty = raw_full + kRR;   // [kRR] 128 dequant threads have read the words
+    uint64_t *b_full = raw_empty + kRR;     // [kRB] 128 activation producers (copies landed and fenced)
+    uint64_t *a_full = b_full + kRB;        // [kRA] 128 dequant threads (tcgen05.st done)
+    uint64_t *ab_empty = a_full + kRA;      // [kRA] MMA commit: A slot and B stage g % 8 are free
+    uint64_t *acc_full = ab_empty + kRA;    // [2] MMA commit
     uint64_t *acc_empty = acc_full + 2;     // [2] 128 epilogue threads
     uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
     uint64_t *sc_empty = sc_full + 2;       // [2] 256 dequant threads
-    uint8_t *sEpi = smem + PrefillSmem::epi;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PrefillSmem::tmem_slot);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
     __shared__ int abort_s;
     __shared__ float col_w[kPN];
     __shared__ int col_tok[kPN];
@@ -161,10 +175,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         abort_s = 0;
-        for (int s = 0; s < kPS; ++s) {
-            mbar_init(&raw_full[s], 1 + 128);
-            mbar_init(&a_full[s], 128);
-            mbar_init(&stage_empty[s], 1);
+        for (int i = 0; i < kRR; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], 128);
+        }
+        for (int i = 0; i < kRB; ++i) {
+            mbar_init(&b_full[i], 128);
+            mbar_init(&a_full[i], 128);
+            mbar_init(&ab_empty[i], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -191,7 +209,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
 
     if (warp < kWEpi) {
         // ------------------------------------------------ dequant: one weight row per thread; group
-        // 0 (warps 0-3) takes the even stages, group 1 (warps 4-7) the odd ones
+        // 0 (warps 0-3) takes the even K steps, group 1 (warps 4-7) the odd ones
         const int grp = warp >> 2;
         const int r = threadIdx.x & 127;   // tile row, TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -202,14 +220,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const int tb = lt & 1;
             if (!pwait(&sc_full[tb], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
-            const uint16_t *sc = sSc + tb * (kScaleBytes / 2) + sc_row * G;
+            const uint16_t *sc = sSc + tb * (L.sc_bytes / 2) + sc_row * G;
             bool ok = true;
             for (int ks = 0; ks < nks; ++ks, ++g) {
-                const int s = g % kPS;
-                if ((s & 1) != grp) continue;
-                if (!pwait(&raw_full[s], (g / kPS) & 1, abort_flag)) { ok = false; break; }
-                tc::fence_after();
-                const uint8_t *rr = sRaw + s * kRawBytes + raw_off;
+                if ((int)(g & 1) != grp) continue;
+                const int sr = g % kRR, sa = g % kRA;
+                if (!pwait(&raw_full[sr], (g / kRR) & 1, abort_flag)) { ok = false; break; }
+                const uint8_t *rr = sRaw + sr * kRawBytes + raw_off;
                 const uint4 w0 = lds_v4(rr), w1 = lds_v4(rr + 16);
                 const uint32_t sb = sc[ks >> 1];
                 const uint32_t s2u = sb | (sb << 16);
@@ -227,15 +244,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                         v[4 * m + j] = *reinterpret_cast<uint32_t *>(&qv);
                     }
                 }
-                tc::st_32x32b_x32(tmem + lane_base + kAStage0 + s * 32, v);
+                // The words are consumed (v depends on them), so the loads have landed;
+                // order them before the TMA that will refill the slot.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&raw_empty[sr]);
+                // the MMA must have finished reading this tensor-memory slot
+                if (!pwait(&ab_empty[sa], ((g / kRA) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                tc::st_32x32b_x32(tmem + lane_base + kAStage0 + sa * 32, v);
                 tc::wait_st();
                 tc::fence_before();
-                mbar_arrive(&a_full[s]);
+                mbar_arrive(&a_full[sa]);
             }
             if (!ok) { fail(p, abort_flag); break; }
             mbar_arrive(&sc_empty[tb]);
         }
-    } else if (warp < kWProd) {
+    } else if (warp < kWRaw) {
         // ------------------------------------------------ epilogue: one accumulator row per thread
         const int q = warp - kWEpi;
         const int r = 32 * q + lane;
@@ -265,8 +289,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 tc::ld_32x32b_x16(dbase + c0, v);
                 tc::wait_ld();
                 uint8_t *stg = sEpi + (nbuf & 1) * kEpiBytes;
-                // the staging buffer's previous bulk operations must have read it
-                if (et < 16) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                // every earlier bulk operation of this thread must have read its staging
+                // buffer (a thread may skip chunks at a ragged tile end, so counting groups
+                // back to the same buffer is not enough)
+                if (et < 16) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (!p.down) {
                     // rows 2i (gate) and 2i+1 (up) of intermediate i0 + i sit in adjacent lanes;
@@ -300,10 +326,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     asm volatile("bar.sync 1, 128;" ::: "memory");
                     if (et < 16 && c0 + et < T.nv) {
                         float *dst = p.out_acc + (size_t)col_tok[c0 + et] * p.H + T.m * 128;
-                        asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 512;" ::"l"(
-                                         dst),
-                                     "r"(smem_u32(ys + et * 128))
-                                     : "memory");
+                        asm volatile(
+                            "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 512;" ::"l"(dst),
+                            "r"(smem_u32(ys + et * 128))
+                            : "memory");
                         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }
@@ -313,32 +339,58 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         }
         // bulk stores / reductions must finish before the CTA exits
         if (et < 16) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    } else if (warp == kWRaw) {
+        // ------------------------------------------------ INT4 tiles and scales: one TMA thread
+        if (lane == 0) {
+            uint32_t g = 0;
+            int lt = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+                const Tile T = decode_tile(p, nact, t);
+                const int tb = lt & 1;
+                if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+                uint16_t *dst = sSc + tb * (L.sc_bytes / 2);
+                if (!p.down) {
+                    const size_t row = (size_t)T.e * 2 * p.I + T.m * 64;
+                    mbar_arrive_expect_tx(&sc_full[tb], 2 * 64 * G * 2);
+                    bulk_g2s(dst, p.scales + row * G, 64 * G * 2, &sc_full[tb]);
+                    bulk_g2s(dst + 64 * G, p.scales + (row + p.I) * G, 64 * G * 2, &sc_full[tb]);
+                } else {
+                    const size_t row = (size_t)T.e * p.H + T.m * 128;
+                    mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
+                    bulk_g2s(dst, p.scales + row * G, 128 * G * 2, &sc_full[tb]);
+                }
+                bool ok = true;
+                const int row = p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
+                const int row2 = row + (p.down ? 64 : p.I);
+                for (int ks = 0; ks < nks; ++ks, ++g) {
+                    const int sr = g % kRR;
+                    if (!pwait(&raw_empty[sr], ((g / kRR) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&raw_full[sr], kRawBytes);
+                    uint8_t *rdst = sRaw + sr * kRawBytes;
+                    tma_load_2d(rdst, &p.tm_w, ks * 8, row, &raw_full[sr]);
+                    tma_load_2d(rdst + 2048, &p.tm_w, ks * 8, row2, &raw_full[sr]);
+                }
+                if (!ok) { fail(p, abort_flag); break; }
+            }
+            // the consumers waited on every issued INT4 tile, except after an abort:
+            // then give the outstanding ones a bounded wait before the CTA exits
+            if (*abort_flag)
+                for (uint32_t gg = g > (uint32_t)kRR ? g - kRR : 0; gg < g; ++gg)
+                    mbar_wait(&raw_full[gg % kRR], (gg / kRR) & 1);
+        }
     } else if (warp < kWMma) {
-        // ------------------------------------------------ producers: INT4 tile (TMA) + activation rows (cp.async)
+        // ------------------------------------------------ activation rows (cp.async, 128-byte swizzle)
+        // Each K step is one cp.async group. The tensor core reads through the async
+        // proxy, so a stage is published only after this thread's copies into it have
+        // landed and been fenced: kLag steps after they were issued.
+        constexpr int kLag = 4;
+        static_assert(kLag < kRB, "a producer must not wait on a stage it has not published");
         const int r = threadIdx.x - 32 * kWProd;   // B row (token column of the tile)
         uint32_t g = 0;
         int lt = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
             const Tile T = decode_tile(p, nact, t);
-            const int tb = lt & 1;
-            // scales of the tile's 128 rows, all groups
-            if (r == 0) {
-                if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); }
-                else {
-                    uint16_t *dst = sSc + tb * (kScaleBytes / 2);
-                    if (!p.down) {
-                        const size_t row = (size_t)T.e * 2 * p.I + T.m * 64;
-                        mbar_arrive_expect_tx(&sc_full[tb], 2 * 64 * G * 2);
-                        bulk_g2s(dst, p.scales + row * G, 64 * G * 2, &sc_full[tb]);
-                        bulk_g2s(dst + 64 * G, p.scales + (row + p.I) * G, 64 * G * 2, &sc_full[tb]);
-                    } else {
-                        const size_t row = (size_t)T.e * p.H + T.m * 128;
-                        mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
-                        bulk_g2s(dst, p.scales + row * G, 128 * G * 2, &sc_full[tb]);
-                    }
-                }
-            }
-            // the activation row this thread gathers
             const int rr = r < T.nv ? r : 0;
             const uint16_t *src;
             if (!p.down) {
@@ -347,36 +399,29 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             } else {
                 src = p.b_src + (size_t)(T.s0 + rr) * p.I;
             }
-            bool ok = true;
             for (int ks = 0; ks < nks; ++ks, ++g) {
-                const int s = g % kPS;
-                if (!pwait(&stage_empty[s], ((g / kPS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                if (r == 0) {
-                    mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
-                    uint8_t *dst = sRaw + s * kRawBytes;
-                    if (!p.down) {
-                        const int row = T.e * 2 * p.I + T.m * 64;
-                        tma_load_2d(dst, &p.tm_w, ks * 8, row, &raw_full[s]);
-                        tma_load_2d(dst + 2048, &p.tm_w, ks * 8, row + p.I, &raw_full[s]);
-                    } else {
-                        const int row = T.e * p.H + T.m * 128;
-                        tma_load_2d(dst, &p.tm_w, ks * 8, row, &raw_full[s]);
-                        tma_load_2d(dst + 2048, &p.tm_w, ks * 8, row + 64, &raw_full[s]);
-                    }
-                }
+                const int sb = g % kRB;
+                if (!pwait(&ab_empty[sb], ((g / kRB) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 if (r < T.n16) {
-                    // 128-byte swizzle: 16-byte chunk c of row r goes to chunk c ^ (r % 8)
-                    uint8_t *row_dst = sB + s * kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                    // 16-byte chunk c of row r goes to chunk c ^ (r % 8)
+                    uint8_t *row_dst = sB + sb * kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
                     const uint16_t *row_src = src + ks * 64;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) cp_async_16(row_dst + ((c ^ (r & 7)) << 4), row_src + 8 * c);
                 }
-                cp_async_arrive(&raw_full[s]);
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (g >= (uint32_t)kLag) {
+                    asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(&b_full[(g - kLag) % kRB]);
+                }
             }
-            if (!ok) { fail(p, abort_flag); break; }
         }
-        // every issued copy must land before the CTA may exit
+        if (!ok) fail(p, abort_flag);
+        // publish the last stages
         asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (uint32_t gg = g > (uint32_t)kLag ? g - kLag : 0; gg < g; ++gg) mbar_arrive(&b_full[gg % kRB]);
     } else {
         // ------------------------------------------------ MMA issuer
         uint32_t g = 0;
@@ -390,17 +435,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const uint32_t idesc = tc::idesc_bf16(128, T.n16);
             bool ok = true;
             for (int ks = 0; ks < nks; ++ks, ++g) {
-                const int s = g % kPS;
-                if (!pwait(&a_full[s], (g / kPS) & 1, abort_flag)) { ok = false; break; }
+                const int sa = g % kRA, sb = g % kRB;
+                if (!pwait(&a_full[sa], (g / kRA) & 1, abort_flag) || !pwait(&b_full[sb], (g / kRB) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc::fence_after();
                 if (lane == 0) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    const uint64_t bdesc = tc::sdesc_sw128(sB + s * kBBytes);
+                    const uint64_t bdesc = tc::sdesc_sw128(sB + sb * kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(d, tmem + kAStage0 + s * 32 + kk * 8, bdesc + (uint64_t)(kk * 2), idesc,
+                        tc::mma_ts(d, tmem + kAStage0 + sa * 32 + kk * 8, bdesc + (uint64_t)(kk * 2), idesc,
                                    (ks | kk) != 0);
-                    tc::commit(&stage_empty[s]);
+                    tc::commit(&ab_empty[sa]);   // one commit: A slot and B stage share the index
                 }
                 __syncwarp();
             }
@@ -515,7 +562,8 @@ __global__ void __launch_bounds__(256) acc_convert_kernel(float *__restrict__ ac
 }
 
 bool prefill_supported(const moe_dims &d) {
-    return d.H % 128 == 0 && d.I % 128 == 0 && d.H / 128 <= kPG && d.I / 128 <= kPG && d.I % 64 == 0;
+    const int gmax = d.H > d.I ? d.H / 128 : d.I / 128;
+    return d.H % 128 == 0 && d.I % 128 == 0 && gmax <= kPG && prefill_layout(gmax).total <= kPrefillSmemMax;
 }
 
 cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
@@ -524,7 +572,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     uint16_t *xperm = ws_at<uint16_t>(ws, W.xperm);
     float *out_acc = ws_at<float>(ws, W.out_acc);
     int32_t *chunk_base = ws_at<int32_t>(ws, W.chunk_base);
-    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmem);
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
     const int64_t nch = (int64_t)d.T * d.H / 8;
@@ -559,7 +607,8 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.K = d.H;
     p.mb = d.I / 64;
     p.down = 0;
-    prefill_kernel<<<grid, kPThreads, kPrefillSmem, s>>>(p);
+    p.L = prefill_layout(p.K / 128);
+    prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // down: K = I, 128 output rows per tile
@@ -571,7 +620,8 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.K = d.I;
     p.mb = d.H / 128;
     p.down = 1;
-    prefill_kernel<<<grid, kPThreads, kPrefillSmem, s>>>(p);
+    p.L = prefill_layout(p.K / 128);
+    prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (ev_after && (err = cudaEventRecordWithFlags(ev_after, s, cudaEventRecordExternal)) != cudaSuccess) return err;
 
