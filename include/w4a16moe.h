@@ -138,6 +138,37 @@ MOE_API int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_id
                           void *stream);
 
 /*
+ * moe_w4a16_forward for decode batches without a caller workspace. The pages
+ * have no counterpart: this entry point exists for callers that cannot
+ * provide or allocate a device scratch buffer where they run the layer (a
+ * fully carved memory pool, a plugin signature without a workspace argument,
+ * a loop where cudaMalloc's device-wide synchronisation is not acceptable).
+ *
+ * Same computation and arguments as moe_w4a16_forward minus ws/ws_bytes. The
+ * scratch is a 16 MiB array that the library holds in device memory, one per
+ * device per process; the call allocates and frees nothing.
+ *  - Served shapes: those of the fused decode path (T <= 64) whose
+ *    moe_workspace_size() is at most 16 MiB (T = 64 at H 2560, E 512, k 10,
+ *    I 640 needs about 10 MiB). A larger workspace size returns
+ *    MOE_ERR_WORKSPACE and T > 64 returns MOE_ERR_UNSUPPORTED, in both cases
+ *    before anything is enqueued. T = 0 returns MOE_OK.
+ *  - The first call on a device looks up the array's device address (which
+ *    may load the module that holds it); make that call before any stream
+ *    capture begins.
+ *  - Each call first clears the kernel's completion counters in the array
+ *    (one cudaMemsetAsync on `stream`), so nothing needs to be zero
+ *    beforehand and an earlier call of another shape does not matter.
+ *  - Calls on the same device that may overlap in time (other streams, other
+ *    host threads) race on the array and give wrong results.
+ *  - Ids outside [0, E) contribute nothing; the error word the kernel sets
+ *    stays inside the array and is not reported.
+ */
+MOE_API int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
+                              const int32_t *w1_packed, const uint16_t *w1_scales,
+                              const int32_t *w2_packed, const uint16_t *w2_scales,
+                              uint16_t *out, moe_dims d, void *stream);
+
+/*
  * Token-to-expert permutation ("vLLM Optimization Edition", section 3.3:
  * moe_align_block_size, here without block padding): per-expert counts,
  * their exclusive prefix sum, and the assignments a = t*k + j listed expert

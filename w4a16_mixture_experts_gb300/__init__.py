@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
     "workspace", "moe_route", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
-    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "STATUS",
+    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc", "STATUS",
 ]
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.moe_w4a16_forward.restype = I
         L.moe_w4a16_forward_rms.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, D, P, Z, P]
         L.moe_w4a16_forward_rms.restype = I
+        L.moe_w4a16_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, D, P]
+        L.moe_w4a16_forward_noalloc.restype = I
         L.moe_permute.argtypes, L.moe_permute.restype = [P, D, P, P, P, Z, P], I
         L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
@@ -176,6 +178,24 @@ def moe_w4a16_forward(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed,
     _check(lib().moe_w4a16_forward(_p(hidden), _p(topk_ids), _p(topk_w), _p(w1_packed), _p(w1_scales),
                                    _p(w2_packed), _p(w2_scales), _p(out), dims, _p(ws), ws.numel(),
                                    _stream(stream)), "moe_w4a16_forward")
+    return out
+
+
+def moe_w4a16_forward_noalloc(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales,
+                              out=None, stream=None):
+    """moe_w4a16_forward for decode batches (T <= 64) with the library's own static scratch.
+
+    No workspace is passed or allocated; calls on one device must not overlap.
+    """
+    dims = _expert_dims(hidden, topk_ids, w1_packed, w2_packed)
+    _need(topk_w, "topk_w", torch.float32, 2)
+    _need(w1_scales, "w1_scales", torch.bfloat16, 3)
+    _need(w2_scales, "w2_scales", torch.bfloat16, 3)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(lib().moe_w4a16_forward_noalloc(_p(hidden), _p(topk_ids), _p(topk_w), _p(w1_packed), _p(w1_scales),
+                                           _p(w2_packed), _p(w2_scales), _p(out), dims, _stream(stream)),
+           "moe_w4a16_forward_noalloc")
     return out
 
 
