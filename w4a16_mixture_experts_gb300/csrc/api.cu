@@ -55,6 +55,17 @@ cudaError_t set_smem_once(const void *func, int bytes) {
     return err;
 }
 
+// A plain record outside stream capture; inside a capture, an external event
+// node, so that the event can still be timed after each graph replay.
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s) {
+    if (!ev) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess) return err;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                               : cudaEventRecord(ev, s);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -84,10 +95,6 @@ int check_ws(const moe_dims &d, const void *ws, size_t ws_bytes) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
-
-cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s) {
-    return ev ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) : cudaSuccess;
-}
 
 int forward_impl(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w, const int32_t *w1_packed,
                  const uint16_t *w1_scales, const int32_t *w2_packed, const uint16_t *w2_scales, uint16_t *out,

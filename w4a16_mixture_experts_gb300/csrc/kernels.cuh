@@ -19,6 +19,9 @@ cudaError_t encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Records a caller's profiling event on `s` (nothing for a null event).
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s);
+
 cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
                          int32_t *ids, float *w, void *ws, cudaStream_t s);
 

@@ -8,24 +8,32 @@
 // warp-specialised persistent kernel:
 //
 //   gate_up: tile = (expert, 64 intermediate rows i0.., up to 128 tokens).
-//            A = 128 weight rows (gate row i and up row i interleaved), K = H.
-//            Epilogue: h = SiLU(g) * u, rounded to bf16, stored per slot.
+//            A = 128 weight rows: gate row i0+i in TMEM lane 2i, the
+//            matching up row in lane 2i+1; K = H.
+//            Epilogue: h = SiLU(g) * u (lane pairs meet by one shuffle),
+//            rounded to bf16 and stored per slot.
 //   down:    tile = (expert, 128 output rows, up to 128 tokens), K = I.
-//            Epilogue: out_acc[t] += topk_w * y (fp32 reduction in L2).
+//            Epilogue: out_acc[t] += topk_w * y (fp32 reductions in L2).
 //
-// Per 64-wide K step:
-//   * one TMA tile of packed INT4 (128 rows x 32 bytes) lands in shared
-//     memory (warp 8 lane 0, mbarrier complete_tx);
-//   * 128 producer threads gather the token rows of the activations (64 bf16
-//     each) with cp.async into the 128-byte-swizzled K-major layout the MMA
-//     descriptor reads;
-//   * 128 dequant threads (one per weight row) turn 64 nibbles into bf16
-//     q*scale in registers and write them straight into tensor memory as the
-//     A operand (tcgen05.st), so A never touches shared memory;
-//   * one thread issues 4 tcgen05.mma (M=128, N=tokens, K=16) into an fp32
-//     TMEM accumulator; tcgen05.commit releases the stage.
-// The accumulator is double-buffered in TMEM so 128 epilogue threads drain
-// one tile while the next one accumulates.
+// One pipeline stage is one quantisation group (128 of K):
+//   * warp 12 lane 0 loads the stage's packed INT4 (128 rows x 64 bytes) with
+//     two 2-D TMA copies in the 64-byte swizzle, which spreads the dequant
+//     threads' 16-byte shared loads over the banks (consecutive rows of one
+//     box are conflict-free; gate_up's paired lanes read two boxes and meet
+//     2-way);
+//   * 128 producer threads gather the stage's activation rows (128 bf16 per
+//     token, sixteen lanes per row) with cp.async into two 128-byte-swizzled
+//     K-major blocks, the layout the MMA's shared-memory descriptor reads;
+//   * 128 dequant threads (one per weight row; two groups take alternate
+//     stages) turn 128 nibbles into bf16 q*scale in registers and write them
+//     straight into tensor memory as the A operand (tcgen05.st);
+//   * the MMA warp issues 8 tcgen05.mma (M=128, N=tokens, K=16) from one
+//     elected lane into an fp32 TMEM accumulator; one tcgen05.commit frees
+//     the stage's A slot and activation buffer.
+// Issuing the MMAs from a tight, unrolled, warp-uniform sequence matters: a
+// 128x128x16 MMA takes about 64 SM cycles, so per-instruction issue overhead
+// of the same order halves the tensor rate. The accumulator is double-buffered
+// in TMEM so 128 epilogue threads drain one tile while the next accumulates.
 //
 // Weights enter A as W = bf16(q * scale) (one rounding per weight). Nibble
 // pairs (j, j+4) of each word fill one 32-bit TMEM column, so the
@@ -40,42 +48,47 @@
 
 namespace moe {
 
-constexpr int kRR = 16;            // packed-INT4 ring (HBM stream)
-constexpr int kRB = 8;             // activation ring (L2 stream)
-constexpr int kRA = 8;             // dequantised-A ring in tensor memory
-constexpr int kPN = 128;           // max tokens per tile (columns of one TMEM accumulator)
-constexpr int kPG = 64;            // max quantisation groups along K (K <= 8192)
+constexpr int kKS = 128;             // K per pipeline stage: one quantisation group
+constexpr int kRR = 8;               // packed-INT4 stages (HBM stream)
+constexpr int kRS = 4;               // A slots in TMEM = activation stages in smem (freed together)
+constexpr int kPN = 128;             // max tokens per tile (columns of one TMEM accumulator)
 constexpr int kWEpi = 8, kWRaw = 12, kWProd = 13, kWMma = 17;
-constexpr int kPThreads = 18 * 32; // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
-                                   // 13-16 activation producers, 17 MMA
+constexpr int kNProdW = kWMma - kWProd;   // activation producer warps
+constexpr int kNProd = 32 * kNProdW;      // activation producer threads
+constexpr int kPThreads = 18 * 32;   // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
+                                     // 13-16 activation producers, 17 MMA
+constexpr int kLag = 2;              // stages a producer keeps in flight before publishing
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAStage0 = 2 * kPN;   // TMEM columns: 2 accumulators, then A slots of 32 columns
-constexpr uint32_t kBBytes = kPN * 128;  // one activation stage: 128 rows x 64 bf16
-constexpr uint32_t kRawBytes = 128 * 32; // one packed-INT4 stage: 128 rows x 64 nibbles
-constexpr uint32_t kEpiBytes = 16 * 128 * 4;   // one epilogue staging buffer: 16 token columns x 128 rows f32
-constexpr uint32_t kPrefillSmemMax = 232448 - 2048;
+constexpr uint32_t kAStage0 = 2 * kPN;          // TMEM columns: 2 accumulators, then the A slots
+constexpr uint32_t kACols = kKS / 2;            // 64 columns (bf16 pairs) per A slot
+constexpr uint32_t kBKBlock = kPN * 128;        // 128 token rows x 64 bf16: one 128-byte-swizzle K block
+constexpr uint32_t kBBytes = 2 * kBKBlock;      // one activation stage: two K blocks
+constexpr uint32_t kRawHalf = 64 * 64;          // 64 weight rows x 16 words
+constexpr uint32_t kRawBytes = 2 * kRawHalf;    // one packed-INT4 stage
+constexpr uint32_t kPrefillSmemMax = 232448 - 1024;   // dynamic; the static part is a few bytes
+static_assert(kAStage0 + kRS * kACols <= kTmemCols, "tensor memory budget");
+static_assert(kLag < kRS, "a producer must not wait on a stage it has not published");
 
 struct PrefillLayout {   // shared-memory offsets from the 1024-aligned base; scales sized by K
-    uint32_t b, raw, sc, sc_bytes, epi, bars, tmem_slot, total;
+    uint32_t b, raw, sc, sc_bytes, cols, bars, tmem_slot, total;
 };
-static_assert(kRA == kRB, "the A slots and B stages are released by one barrier");
-constexpr int kNBars = 2 * kRR + 3 * kRA + 8;
+constexpr int kNBars = 2 * kRR + 3 * kRS + 8;
 
 __host__ __device__ inline PrefillLayout prefill_layout(int G) {
     PrefillLayout L;
     L.b = 0;
-    L.raw = L.b + kRB * kBBytes;
+    L.raw = L.b + kRS * kBBytes;
     L.sc = L.raw + kRR * kRawBytes;
     L.sc_bytes = (uint32_t)(128 * G * 2 + 127) / 128 * 128;
-    L.epi = L.sc + 2 * L.sc_bytes;
-    L.bars = L.epi + 2 * kEpiBytes;
+    L.cols = L.sc + 2 * L.sc_bytes;           // per token column: f32 weight, i32 token, i32 source row
+    L.bars = L.cols + 3 * 4 * kPN;
     L.tmem_slot = L.bars + kNBars * 8;
     L.total = L.tmem_slot + 16 + 1024;   // + alignment slack
     return L;
 }
 
 struct PrefillParams {
-    CUtensorMap tm_w;          // int32 [rows][K/8], box (8 words, 64 rows)
+    CUtensorMap tm_w;          // int32 [rows][K/8], box (16 words, 64 rows), 64-byte swizzle
     const uint16_t *b_src;     // gate_up: x in fragment order [T][H]; down: h [T*k][I]
     const uint16_t *scales;    // bf16 [rows][K/128]
     const int32_t *offsets;    // [E+1] slot offsets per expert
@@ -129,9 +142,11 @@ __device__ inline void cp_async_16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Arrive on `bar` once all of this thread's prior cp.async have landed.
-__device__ inline void cp_async_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// One lane of the (converged) warp returns true.
+__device__ inline bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -143,9 +158,36 @@ __device__ inline bool pwait(uint64_t *bar, uint32_t parity, volatile int *abort
     return false;
 }
 
+// Named barrier 1 over the 128 epilogue threads, returning the AND of `v`.
+__device__ inline bool bar_and_128(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 __device__ inline void fail(const PrefillParams &p, volatile int *abort_flag) {
     *abort_flag = 1;
     set_error(p.ctrl_rw, MOE_ERR_TIMEOUT);
+}
+
+// 8 words (64 nibbles) of one weight row -> 32 TMEM columns: the bf16 pairs
+// (j, j+4) of each word, times the group scale.
+__device__ inline void dequant8(const uint4 &a, const uint4 &b, __nv_bfloat162 s2, uint32_t (&v)[32]) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t q = int4_pair(w[m], j);
+            __nv_bfloat162 qv = *reinterpret_cast<__nv_bfloat162 *>(&q);
+            qv = __hmul2(qv, s2);
+            v[4 * m + j] = *reinterpret_cast<uint32_t *>(&qv);
+        }
 }
 
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -155,21 +197,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint8_t *sB = smem + L.b;
     uint8_t *sRaw = smem + L.raw;
     uint16_t *sSc = reinterpret_cast<uint16_t *>(smem + L.sc);
-    uint8_t *sEpi = smem + L.epi;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *raw_full = bars;              // [kRR] INT4 TMA (+tx)
-    uint64_t *raw_empty = raw_full + kRR;   // [kRR] 128 dequant threads have read the words
-    uint64_t *b_full = raw_empty + kRR;     // [kRB] 128 activation producers (copies landed and fenced)
-    uint64_t *a_full = b_full + kRB;        // [kRA] 128 dequant threads (tcgen05.st done)
-    uint64_t *ab_empty = a_full + kRA;      // [kRA] MMA commit: A slot and B stage g % 8 are free
-    uint64_t *acc_full = ab_empty + kRA;    // [2] MMA commit
+    uint64_t *raw_empty = raw_full + kRR;   // [kRR] the 128 dequant threads of the stage's group
+    uint64_t *b_full = raw_empty + kRR;     // [kRS] activation producers (copies landed and fenced)
+    uint64_t *a_full = b_full + kRS;        // [kRS] 128 dequant threads (tcgen05.st done)
+    uint64_t *ab_empty = a_full + kRS;      // [kRS] MMA commit: A slot and activation stage are free
+    uint64_t *acc_full = ab_empty + kRS;    // [2] MMA commit
     uint64_t *acc_empty = acc_full + 2;     // [2] 128 epilogue threads
     uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
     uint64_t *sc_empty = sc_full + 2;       // [2] 256 dequant threads
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
+    float *col_w = reinterpret_cast<float *>(smem + L.cols);     // epilogue (down): routing weight
+    int *col_tok = reinterpret_cast<int *>(col_w + kPN);          // epilogue (down): token
+    int *row_idx = col_tok + kPN;                                 // producers: source row
     __shared__ int abort_s;
-    __shared__ float col_w[kPN];
-    __shared__ int col_tok[kPN];
     volatile int *abort_flag = &abort_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -179,8 +221,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 128);
         }
-        for (int i = 0; i < kRB; ++i) {
-            mbar_init(&b_full[i], 128);
+        for (int i = 0; i < kRS; ++i) {
+            mbar_init(&b_full[i], kNProd);
             mbar_init(&a_full[i], 128);
             mbar_init(&ab_empty[i], 1);
         }
@@ -204,54 +246,50 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
 
     const int nact = (int)p.ctrl->n_active;
     const int ntiles = nact > 0 ? p.chunk_base[nact] * p.mb : 0;
-    const int nks = p.K / 64;
-    const int G = p.K / 128;
+    const int G = p.K / kKS;   // stages per tile
 
     if (warp < kWEpi) {
         // ------------------------------------------------ dequant: one weight row per thread; group
-        // 0 (warps 0-3) takes the even K steps, group 1 (warps 4-7) the odd ones
+        // 0 (warps 0-3) takes the even stages, group 1 (warps 4-7) the odd ones
         const int grp = warp >> 2;
-        const int r = threadIdx.x & 127;   // tile row, TMEM lane
+        const int r = threadIdx.x & 127;   // tile row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int raw_off = p.down ? r * 32 : (r & 1) * 2048 + (r >> 1) * 32;
-        const int sc_row = p.down ? r : (r & 1) * 64 + (r >> 1);
+        // TMA box (half of the stage) and row within it: gate_up puts gate row i in lane 2i and
+        // up row i in lane 2i+1, so the epilogue pairs them with one shuffle; down is in order
+        const int half = p.down ? r >> 6 : r & 1;
+        const int br = p.down ? r & 63 : r >> 1;
+        const int rbase = half * (int)kRawHalf + br * 64;
+        const int rot = (br >> 1) & 3;     // 64-byte swizzle: 16-byte chunk c sits at c ^ rot
         uint32_t g = 0;
         int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const int tb = lt & 1;
             if (!pwait(&sc_full[tb], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
-            const uint16_t *sc = sSc + tb * (L.sc_bytes / 2) + sc_row * G;
+            const uint16_t *sc = sSc + tb * (L.sc_bytes / 2) + (half * 64 + br) * G;
             bool ok = true;
-            for (int ks = 0; ks < nks; ++ks, ++g) {
+            for (int ks = 0; ks < G; ++ks, ++g) {
                 if ((int)(g & 1) != grp) continue;
-                const int sr = g % kRR, sa = g % kRA;
+                const int sr = g % kRR, sa = g % kRS;
                 if (!pwait(&raw_full[sr], (g / kRR) & 1, abort_flag)) { ok = false; break; }
-                const uint8_t *rr = sRaw + sr * kRawBytes + raw_off;
-                const uint4 w0 = lds_v4(rr), w1 = lds_v4(rr + 16);
-                const uint32_t sb = sc[ks >> 1];
+                const uint8_t *rr = sRaw + sr * kRawBytes + rbase;
+                const uint4 c0 = lds_v4(rr + 16 * (0 ^ rot)), c1 = lds_v4(rr + 16 * (1 ^ rot));
+                const uint4 c2 = lds_v4(rr + 16 * (2 ^ rot)), c3 = lds_v4(rr + 16 * (3 ^ rot));
+                const uint32_t sb = sc[ks];
                 const uint32_t s2u = sb | (sb << 16);
                 const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
-                uint32_t v[32];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const uint32_t w = m < 4 ? (m == 0 ? w0.x : m == 1 ? w0.y : m == 2 ? w0.z : w0.w)
-                                             : (m == 4 ? w1.x : m == 5 ? w1.y : m == 6 ? w1.z : w1.w);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t q = int4_pair(w, j);
-                        __nv_bfloat162 qv = *reinterpret_cast<__nv_bfloat162 *>(&q);
-                        qv = __hmul2(qv, s2);
-                        v[4 * m + j] = *reinterpret_cast<uint32_t *>(&qv);
-                    }
-                }
+                uint32_t v0[32], v1[32];
+                dequant8(c0, c1, s2, v0);
+                dequant8(c2, c3, s2, v1);
                 // The words are consumed (v depends on them), so the loads have landed;
-                // order them before the TMA that will refill the slot.
+                // order them before the TMA that will refill the stage.
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(&raw_empty[sr]);
                 // the MMA must have finished reading this tensor-memory slot
-                if (!pwait(&ab_empty[sa], ((g / kRA) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!pwait(&ab_empty[sa], ((g / kRS) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 tc::fence_after();
-                tc::st_32x32b_x32(tmem + lane_base + kAStage0 + sa * 32, v);
+                const uint32_t ta = tmem + lane_base + kAStage0 + sa * kACols;
+                tc::st_32x32b_x32(ta, v0);
+                tc::st_32x32b_x32(ta + 32, v1);
                 tc::wait_st();
                 tc::fence_before();
                 mbar_arrive(&a_full[sa]);
@@ -260,87 +298,62 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             mbar_arrive(&sc_empty[tb]);
         }
     } else if (warp < kWRaw) {
-        // ------------------------------------------------ epilogue: one accumulator row per thread
+        // ------------------------------------------------ epilogue: one accumulator row per thread,
+        // written straight to global memory (h as bf16 stores, down as fp32 reductions in L2)
         const int q = warp - kWEpi;
-        const int r = 32 * q + lane;
-        const int et = threadIdx.x - 32 * kWEpi;   // 0..127
-        int lt = 0, nbuf = 0;
+        const int et = threadIdx.x - 32 * kWEpi;   // 0..127 = TMEM lane = tile row
+        // gate_up: this lane pair's intermediate row and its fragment-order position
+        const int il = et >> 1;
+        const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
+        int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = decode_tile(p, nact, t);
             const int b = lt & 1;
-            if (!pwait(&acc_full[b], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
+            // the 128 epilogue threads share named barrier 1: they give up together
+            if (!bar_and_128(pwait(&acc_full[b], (lt >> 1) & 1, abort_flag))) { fail(p, abort_flag); break; }
             tc::fence_after();
             const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + b * kPN;
             if (p.down) {
-                // routing weight and token of every column of the tile
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                // routing weight and token of every column of the tile (the previous tile's
+                // readers passed the barrier above before these are rewritten)
                 if (et < T.nv) {
                     const int a = p.perm[T.s0 + et];
                     col_w[et] = p.topk_w[a];
                     col_tok[et] = a / p.k;
-                } else {
-                    col_w[et] = 0.f;
-                    col_tok[et] = 0;
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-            }
-            for (int c0 = 0; c0 < T.nv; c0 += 16, ++nbuf) {
-                float v[16];
-                tc::ld_32x32b_x16(dbase + c0, v);
-                tc::wait_ld();
-                uint8_t *stg = sEpi + (nbuf & 1) * kEpiBytes;
-                // every earlier bulk operation of this thread must have read its staging
-                // buffer (a thread may skip chunks at a ragged tile end, so counting groups
-                // back to the same buffer is not enough)
-                if (et < 16) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (!p.down) {
-                    // rows 2i (gate) and 2i+1 (up) of intermediate i0 + i sit in adjacent lanes;
-                    // h goes to its fragment-order position inside the tile's 64-wide block
-                    const int il = r >> 1;
-                    const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
-                    uint16_t *hs = reinterpret_cast<uint16_t *>(stg);   // [16 columns][64]
+                float *orow = p.out_acc + T.m * 128 + et;
+                for (int c0 = 0; c0 < T.nv; c0 += 16) {
+                    float v[16];
+                    tc::ld_32x32b_x16(dbase + c0, v);
+                    tc::wait_ld();
+                    const int nu = min(16, T.nv - c0);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        if (u < nu) atomicAdd(orow + (size_t)col_tok[c0 + u] * p.H, col_w[c0 + u] * v[u]);
+                }
+            } else {
+                uint16_t *hrow = p.hbuf + (size_t)T.s0 * p.I + T.m * 64 + pl;
+                for (int c0 = 0; c0 < T.nv; c0 += 16) {
+                    float v[16];
+                    tc::ld_32x32b_x16(dbase + c0, v);
+                    tc::wait_ld();
+                    const int nu = min(16, T.nv - c0);
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const float other = __shfl_xor_sync(0xffffffffu, v[u], 1);
-                        if (!(lane & 1)) {
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(v[u]) * other);
-                            hs[u * 64 + pl] = *reinterpret_cast<const uint16_t *>(&hb);
+                        const float up = __shfl_xor_sync(0xffffffffu, v[u], 1);
+                        if (!(et & 1) && u < nu) {
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(v[u]) * up);
+                            hrow[(size_t)(c0 + u) * p.I] = *reinterpret_cast<const uint16_t *>(&hb);
                         }
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (et < 16 && c0 + et < T.nv) {
-                        uint16_t *dst = p.hbuf + (size_t)(T.s0 + c0 + et) * p.I + T.m * 64;
-                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 128;" ::"l"(dst),
-                                     "r"(smem_u32(hs + et * 64))
-                                     : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    }
-                } else {
-                    // weighted rows, then one 512-byte reduce-add per token column
-                    float *ys = reinterpret_cast<float *>(stg);   // [16 columns][128 rows]
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) ys[u * 128 + r] = col_w[c0 + u] * v[u];
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (et < 16 && c0 + et < T.nv) {
-                        float *dst = p.out_acc + (size_t)col_tok[c0 + et] * p.H + T.m * 128;
-                        asm volatile(
-                            "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 512;" ::"l"(dst),
-                            "r"(smem_u32(ys + et * 128))
-                            : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     }
                 }
             }
             tc::fence_before();
             mbar_arrive(&acc_empty[b]);
         }
-        // bulk stores / reductions must finish before the CTA exits
-        if (et < 16) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     } else if (warp == kWRaw) {
-        // ------------------------------------------------ INT4 tiles and scales: one TMA thread
+        // ------------------------------------------------ INT4 stages and scales: one TMA thread
         if (lane == 0) {
             uint32_t g = 0;
             int lt = 0;
@@ -348,31 +361,25 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 const Tile T = decode_tile(p, nact, t);
                 const int tb = lt & 1;
                 if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+                // weight rows of TMEM lanes 0-63 and 64-127
+                const int row_a = p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
+                const int row_b = row_a + (p.down ? 64 : p.I);
                 uint16_t *dst = sSc + tb * (L.sc_bytes / 2);
-                if (!p.down) {
-                    const size_t row = (size_t)T.e * 2 * p.I + T.m * 64;
-                    mbar_arrive_expect_tx(&sc_full[tb], 2 * 64 * G * 2);
-                    bulk_g2s(dst, p.scales + row * G, 64 * G * 2, &sc_full[tb]);
-                    bulk_g2s(dst + 64 * G, p.scales + (row + p.I) * G, 64 * G * 2, &sc_full[tb]);
-                } else {
-                    const size_t row = (size_t)T.e * p.H + T.m * 128;
-                    mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
-                    bulk_g2s(dst, p.scales + row * G, 128 * G * 2, &sc_full[tb]);
-                }
+                mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
+                bulk_g2s(dst, p.scales + (size_t)row_a * G, 64 * G * 2, &sc_full[tb]);
+                bulk_g2s(dst + 64 * G, p.scales + (size_t)row_b * G, 64 * G * 2, &sc_full[tb]);
                 bool ok = true;
-                const int row = p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
-                const int row2 = row + (p.down ? 64 : p.I);
-                for (int ks = 0; ks < nks; ++ks, ++g) {
+                for (int ks = 0; ks < G; ++ks, ++g) {
                     const int sr = g % kRR;
                     if (!pwait(&raw_empty[sr], ((g / kRR) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&raw_full[sr], kRawBytes);
                     uint8_t *rdst = sRaw + sr * kRawBytes;
-                    tma_load_2d(rdst, &p.tm_w, ks * 8, row, &raw_full[sr]);
-                    tma_load_2d(rdst + 2048, &p.tm_w, ks * 8, row2, &raw_full[sr]);
+                    tma_load_2d(rdst, &p.tm_w, ks * 16, row_a, &raw_full[sr]);
+                    tma_load_2d(rdst + kRawHalf, &p.tm_w, ks * 16, row_b, &raw_full[sr]);
                 }
                 if (!ok) { fail(p, abort_flag); break; }
             }
-            // the consumers waited on every issued INT4 tile, except after an abort:
+            // the consumers waited on every issued INT4 stage, except after an abort:
             // then give the outstanding ones a bounded wait before the CTA exits
             if (*abort_flag)
                 for (uint32_t gg = g > (uint32_t)kRR ? g - kRR : 0; gg < g; ++gg)
@@ -380,40 +387,51 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         }
     } else if (warp < kWMma) {
         // ------------------------------------------------ activation rows (cp.async, 128-byte swizzle)
-        // Each K step is one cp.async group. The tensor core reads through the async
-        // proxy, so a stage is published only after this thread's copies into it have
-        // landed and been fenced: kLag steps after they were issued.
-        constexpr int kLag = 4;
-        static_assert(kLag < kRB, "a producer must not wait on a stage it has not published");
-        const int r = threadIdx.x - 32 * kWProd;   // B row (token column of the tile)
+        // Sixteen lanes copy one token row's 256 bytes of the stage, so each warp
+        // instruction reads two contiguous 256-byte runs. Each stage is one cp.async
+        // group. The tensor core reads through the async proxy, so a stage is
+        // published only after this thread's copies into it have landed and been
+        // fenced: kLag stages after they were issued.
+        const int wp = warp - kWProd;
+        const int row0 = 2 * wp + (lane >> 4);
+        const int kb = (lane >> 3) & 1, cc = lane & 7;   // K block and 16-byte chunk of this lane
         uint32_t g = 0;
         int lt = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
             const Tile T = decode_tile(p, nact, t);
-            const int rr = r < T.nv ? r : 0;
-            const uint16_t *src;
-            if (!p.down) {
-                const int a = p.perm[T.s0 + rr];
-                src = p.b_src + (size_t)(a / p.k) * p.H;
-            } else {
-                src = p.b_src + (size_t)(T.s0 + rr) * p.I;
-            }
-            for (int ks = 0; ks < nks; ++ks, ++g) {
-                const int sb = g % kRB;
-                if (!pwait(&ab_empty[sb], ((g / kRB) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                if (r < T.n16) {
-                    // 16-byte chunk c of row r goes to chunk c ^ (r % 8)
-                    uint8_t *row_dst = sB + sb * kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
-                    const uint16_t *row_src = src + ks * 64;
+            // source row of each token column this warp copies: lane l fills rows
+            // 2*kNProdW*l + 2*wp and the next one, which only this warp reads
+            __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) cp_async_16(row_dst + ((c ^ (r & 7)) << 4), row_src + 8 * c);
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int r = 2 * kNProdW * lane + 2 * wp + s2;
+                if (r < T.n16) {
+                    const int rr = r < T.nv ? r : 0;   // padding columns repeat a valid row
+                    row_idx[r] = p.down ? T.s0 + rr : p.perm[T.s0 + rr] / p.k;
                 }
+            }
+            __syncwarp();
+            const uint16_t *src_k = p.b_src + kb * 64 + 8 * cc;
+            const size_t row_len = p.down ? (size_t)p.I : (size_t)p.H;
+            uint8_t *dst_k = sB + kb * kBKBlock;
+            for (int ks = 0; ks < G; ++ks, ++g) {
+                const int sb = g % kRS;
+                // every wait gives up the same way in all lanes, so the warp never splits
+                if (!__all_sync(0xffffffffu, pwait(&ab_empty[sb], ((g / kRS) & 1) ^ 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst_s = dst_k + sb * kBBytes;
+                for (int r = row0; r < T.n16; r += 2 * kNProdW)
+                    // chunk cc of row r goes to chunk cc ^ (r % 8) of its 128-byte line
+                    cp_async_16(dst_s + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4),
+                                src_k + (size_t)row_idx[r] * row_len + ks * kKS);
                 asm volatile("cp.async.commit_group;" ::: "memory");
                 if (g >= (uint32_t)kLag) {
                     asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_arrive(&b_full[(g - kLag) % kRB]);
+                    mbar_arrive(&b_full[(g - kLag) % kRS]);
                 }
             }
         }
@@ -421,38 +439,46 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         // publish the last stages
         asm volatile("cp.async.wait_all;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (uint32_t gg = g > (uint32_t)kLag ? g - kLag : 0; gg < g; ++gg) mbar_arrive(&b_full[gg % kRB]);
+        for (uint32_t gg = g > (uint32_t)kLag ? g - kLag : 0; gg < g; ++gg) mbar_arrive(&b_full[gg % kRS]);
     } else {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer: the whole warp waits, one
+        // elected lane issues the stage's 8 MMAs and the commit
         uint32_t g = 0;
         int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = decode_tile(p, nact, t);
             const int b = lt & 1;
-            if (!pwait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+            if (!__all_sync(0xffffffffu, pwait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, abort_flag))) {
+                fail(p, abort_flag);
+                break;
+            }
             tc::fence_after();
             const uint32_t d = tmem + b * kPN;
             const uint32_t idesc = tc::idesc_bf16(128, T.n16);
             bool ok = true;
-            for (int ks = 0; ks < nks; ++ks, ++g) {
-                const int sa = g % kRA, sb = g % kRB;
-                if (!pwait(&a_full[sa], (g / kRA) & 1, abort_flag) || !pwait(&b_full[sb], (g / kRB) & 1, abort_flag)) {
+            for (int ks = 0; ks < G; ++ks, ++g) {
+                const int s = g % kRS;
+                const uint32_t par = (g / kRS) & 1;
+                const bool ready = pwait(&a_full[s], par, abort_flag) && pwait(&b_full[s], par, abort_flag);
+                if (!__all_sync(0xffffffffu, ready)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
-                if (lane == 0) {
-                    const uint64_t bdesc = tc::sdesc_sw128(sB + sb * kBBytes);
+                if (elect_one()) {
+                    const uint64_t bd0 = tc::sdesc_sw128(sB + s * kBBytes);
+                    const uint64_t bd1 = tc::sdesc_sw128(sB + s * kBBytes + kBKBlock);
+                    const uint32_t a0 = tmem + kAStage0 + s * kACols;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(d, tmem + kAStage0 + sa * 32 + kk * 8, bdesc + (uint64_t)(kk * 2), idesc,
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(d, a0 + kk * 8, (kk < 4 ? bd0 : bd1) + (uint64_t)((kk & 3) * 2), idesc,
                                    (ks | kk) != 0);
-                    tc::commit(&ab_empty[sa]);   // one commit: A slot and B stage share the index
+                    tc::commit(&ab_empty[s]);   // one commit: A slot and activation stage share the index
                 }
                 __syncwarp();
             }
             if (!ok) { fail(p, abort_flag); break; }
-            if (lane == 0) tc::commit(&acc_full[b]);
+            if (elect_one()) tc::commit(&acc_full[b]);
             __syncwarp();
         }
     }
@@ -464,7 +490,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_after();
     if (warp == kWMma) tc::dealloc(tmem, kTmemCols);
 }
-
 // ---------------------------------------------------------------------------
 // x -> fragment order within each 8-element chunk: (0,4,1,5,2,6,3,7).
 __global__ void xperm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int64_t nchunks) {
@@ -563,7 +588,7 @@ __global__ void __launch_bounds__(256) acc_convert_kernel(float *__restrict__ ac
 
 bool prefill_supported(const moe_dims &d) {
     const int gmax = d.H > d.I ? d.H / 128 : d.I / 128;
-    return d.H % 128 == 0 && d.I % 128 == 0 && gmax <= kPG && prefill_layout(gmax).total <= kPrefillSmemMax;
+    return d.H % 128 == 0 && d.I % 128 == 0 && prefill_layout(gmax).total <= kPrefillSmemMax;
 }
 
 cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
@@ -599,31 +624,31 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
 
     // gate_up: K = H, 64 intermediate rows (x2 for gate and up) per tile
     err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w1p, (uint64_t)d.H / 8, (uint64_t)d.E * 2 * d.I,
-                         (uint64_t)d.H / 2, 8u, 64u, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         (uint64_t)d.H / 2, 16u, 64u, CU_TENSOR_MAP_SWIZZLE_64B);
     if (err != cudaSuccess) return err;
-    if (ev_before && (err = cudaEventRecordWithFlags(ev_before, s, cudaEventRecordExternal)) != cudaSuccess) return err;
+    if ((err = record_profile_event(ev_before, s)) != cudaSuccess) return err;
     p.b_src = xperm;
     p.scales = a.w1s;
     p.K = d.H;
     p.mb = d.I / 64;
     p.down = 0;
-    p.L = prefill_layout(p.K / 128);
+    p.L = prefill_layout(p.K / kKS);
     prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // down: K = I, 128 output rows per tile
     err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w2p, (uint64_t)d.I / 8, (uint64_t)d.E * d.H,
-                         (uint64_t)d.I / 2, 8u, 64u, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         (uint64_t)d.I / 2, 16u, 64u, CU_TENSOR_MAP_SWIZZLE_64B);
     if (err != cudaSuccess) return err;
     p.b_src = p.hbuf;
     p.scales = a.w2s;
     p.K = d.I;
     p.mb = d.H / 128;
     p.down = 1;
-    p.L = prefill_layout(p.K / 128);
+    p.L = prefill_layout(p.K / kKS);
     prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (ev_after && (err = cudaEventRecordWithFlags(ev_after, s, cudaEventRecordExternal)) != cudaSuccess) return err;
+    if ((err = record_profile_event(ev_after, s)) != cudaSuccess) return err;
 
     acc_convert_kernel<<<d.T, 256, 0, s>>>(out_acc, a.x, d.H, eps, next ? nullptr : out, next);
     return cudaGetLastError();
