@@ -41,9 +41,10 @@ struct WsLayout {
     size_t inv;          // i32 [T*k]      assignment -> slot (-1: dropped)
     size_t hbuf;         // bf16 [T*k][I]  SiLU(g)*u per slot (fragment order)
     size_t ybuf;         // f32 [T*k][H]   down-projection output per slot (decode path)
-    size_t xperm;        // bf16 [T][H]    activations in fragment order (prefill path)
+    size_t xperm;        // bf16 [T*k][H]  activations per slot, fragment order (prefill path)
     size_t out_acc;      // f32 [T][H]     weighted output accumulator (prefill path)
     size_t chunk_base;   // i32 [E+1]      first 128-token chunk per active expert (prefill path)
+    size_t chunk_info;   // i32x4 [T*k/128+E+1] per chunk: expert, first slot, tokens (prefill path)
     size_t total;
     int ksplit;
     int nchunk;
@@ -86,9 +87,10 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.hbuf = take(T * k * I * 2);
     const bool small = T <= 64;
     L.ybuf = take(small ? T * k * H * 4 : 0);
-    L.xperm = take(small ? 0 : T * H * 2);
+    L.xperm = take(small ? 0 : T * k * H * 2);
     L.out_acc = take(small ? 0 : T * H * 4);
     L.chunk_base = take((E + 1) * 4);
+    L.chunk_info = take(small ? 0 : (T * k / 128 + E + 1) * 16);
     L.total = o;
     return L;
 }
@@ -162,6 +164,23 @@ __device__ inline void tma_load_2d(void *dst, const void *tmap, int c0, int c1, 
         : "memory");
 }
 
+// Same as tma_load_2d, with an L2 eviction-priority policy (from l2_evict_first()).
+__device__ inline void tma_load_2d_hint(void *dst, const void *tmap, int c0, int c1, uint64_t *bar,
+                                        uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once (streamed weights): evict it before other lines.
+__device__ inline uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ inline uint32_t ld_acquire_u32(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -225,6 +244,6 @@ __device__ inline uint32_t int4_pair(uint32_t w, int j) { return bf16x2_sub136(i
 
 __device__ inline float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-__device__ inline float silu(float g) { return g / (1.0f + __expf(-g)); }
+__device__ inline float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace moe

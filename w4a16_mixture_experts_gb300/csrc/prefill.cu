@@ -21,9 +21,11 @@
 //     threads' 16-byte shared loads over the banks (consecutive rows of one
 //     box are conflict-free; gate_up's paired lanes read two boxes and meet
 //     2-way);
-//   * 128 producer threads gather the stage's activation rows (128 bf16 per
-//     token, sixteen lanes per row) with cp.async into two 128-byte-swizzled
-//     K-major blocks, the layout the MMA's shared-memory descriptor reads;
+//   * warp 13 lane 0 loads the stage's activation rows (128 bf16 per slot)
+//     with 2-D TMA copies in the 128-byte swizzle, as two K-major blocks: the
+//     layout the MMA's shared-memory descriptor reads. The activations are in
+//     slot order in global memory (x is gathered per slot before gate_up; h
+//     is written per slot by it), so every tile's rows are contiguous;
 //   * 128 dequant threads (one per weight row; two groups take alternate
 //     stages) turn 128 nibbles into bf16 q*scale in registers and write them
 //     straight into tensor memory as the A operand (tcgen05.st);
@@ -38,8 +40,8 @@
 // Weights enter A as W = bf16(q * scale) (one rounding per weight). Nibble
 // pairs (j, j+4) of each word fill one 32-bit TMEM column, so the
 // activations are kept in the matching order within each 8-element chunk
-// (0,4,1,5,2,6,3,7): x is rewritten into that order once per call, and the
-// gate_up epilogue stores h in it directly.
+// (0,4,1,5,2,6,3,7): x is written in that order when it is gathered per
+// slot, and the gate_up epilogue stores h in it directly.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -52,12 +54,11 @@ constexpr int kKS = 128;             // K per pipeline stage: one quantisation g
 constexpr int kRR = 8;               // packed-INT4 stages (HBM stream)
 constexpr int kRS = 4;               // A slots in TMEM = activation stages in smem (freed together)
 constexpr int kPN = 128;             // max tokens per tile (columns of one TMEM accumulator)
-constexpr int kWEpi = 8, kWRaw = 12, kWProd = 13, kWMma = 17;
-constexpr int kNProdW = kWMma - kWProd;   // activation producer warps
-constexpr int kNProd = 32 * kNProdW;      // activation producer threads
-constexpr int kPThreads = 18 * 32;   // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
-                                     // 13-16 activation producers, 17 MMA
-constexpr int kLag = 2;              // stages a producer keeps in flight before publishing
+constexpr int kWEpi = 8, kWRaw = 12, kWAct = 13, kWMma = 14;
+constexpr int kPThreads = 15 * 32;   // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
+                                     // 13 activation TMA, 14 MMA
+constexpr int kNBoxMaps = 4;         // activation TMA boxes of 16, 32, 64 and 128 token rows
+static_assert((16 << (kNBoxMaps - 1)) == 128, "box sizes cover any multiple of 16 up to 128 rows");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAStage0 = 2 * kPN;          // TMEM columns: 2 accumulators, then the A slots
 constexpr uint32_t kACols = kKS / 2;            // 64 columns (bf16 pairs) per A slot
@@ -65,12 +66,12 @@ constexpr uint32_t kBKBlock = kPN * 128;        // 128 token rows x 64 bf16: one
 constexpr uint32_t kBBytes = 2 * kBKBlock;      // one activation stage: two K blocks
 constexpr uint32_t kRawHalf = 64 * 64;          // 64 weight rows x 16 words
 constexpr uint32_t kRawBytes = 2 * kRawHalf;    // one packed-INT4 stage
+constexpr uint32_t kStgBytes = 16 * 128 * 4;    // one down-epilogue transpose buffer
 constexpr uint32_t kPrefillSmemMax = 232448 - 1024;   // dynamic; the static part is a few bytes
 static_assert(kAStage0 + kRS * kACols <= kTmemCols, "tensor memory budget");
-static_assert(kLag < kRS, "a producer must not wait on a stage it has not published");
 
 struct PrefillLayout {   // shared-memory offsets from the 1024-aligned base; scales sized by K
-    uint32_t b, raw, sc, sc_bytes, cols, bars, tmem_slot, total;
+    uint32_t b, raw, sc, sc_bytes, stg, cols, bars, tmem_slot, total;
 };
 constexpr int kNBars = 2 * kRR + 3 * kRS + 8;
 
@@ -80,25 +81,28 @@ __host__ __device__ inline PrefillLayout prefill_layout(int G) {
     L.raw = L.b + kRS * kBBytes;
     L.sc = L.raw + kRR * kRawBytes;
     L.sc_bytes = (uint32_t)(128 * G * 2 + 127) / 128 * 128;
-    L.cols = L.sc + 2 * L.sc_bytes;           // per token column: f32 weight, i32 token, i32 source row
-    L.bars = L.cols + 3 * 4 * kPN;
+    L.stg = L.sc + 2 * L.sc_bytes;            // down epilogue: two [16 tokens][128 rows] f32 buffers
+    L.cols = L.stg + 2 * kStgBytes;           // per token column: f32 weight, i32 token
+    L.bars = L.cols + 2 * 4 * kPN;
     L.tmem_slot = L.bars + kNBars * 8;
     L.total = L.tmem_slot + 16 + 1024;   // + alignment slack
     return L;
 }
 
 struct PrefillParams {
-    CUtensorMap tm_w;          // int32 [rows][K/8], box (16 words, 64 rows), 64-byte swizzle
-    const uint16_t *b_src;     // gate_up: x in fragment order [T][H]; down: h [T*k][I]
+    CUtensorMap tm_w;          // int32 [rows][K/8], box (16 words, 64 rows; 128 for down), 64-byte swizzle
+    CUtensorMap tm_b[4];       // bf16 [T*k][K] activations per slot, boxes (64, 16 << i rows), 128-byte swizzle
     const uint16_t *scales;    // bf16 [rows][K/128]
     const int32_t *offsets;    // [E+1] slot offsets per expert
     const int32_t *active;     // active experts, increasing
     const int32_t *chunk_base; // [n_active+1] first 128-token chunk of each active expert
+    const int4 *chunk_info;    // per 128-token chunk: expert, first slot, tokens
     const int32_t *perm;       // slot -> assignment t*k+j
     const float *topk_w;
     const Ctrl *ctrl;
     Ctrl *ctrl_rw;
     uint16_t *hbuf;            // gate_up output, bf16 [T*k][I] fragment order
+    const uint16_t *xs;        // gate_up input, bf16 [T*k][H] fragment order
     float *out_acc;            // down output, f32 [T][H]
     int T, H, E, k, I;
     int K;                     // reduction length: H (gate_up) or I (down)
@@ -111,35 +115,22 @@ struct Tile {
     int e, s0, nv, n16, m;
 };
 
-// tile t -> (expert, token chunk, row block); chunks of each expert are
+// Tile t = (chunk t / mb, row block t % mb): chunks of each expert are
 // consecutive, and the row blocks of one chunk are consecutive tiles.
-__device__ inline Tile decode_tile(const PrefillParams &p, int nact, int t) {
-    const int c = t / p.mb;
+__device__ inline int4 chunk_of(const PrefillParams &p, int t) { return __ldg(p.chunk_info + t / p.mb); }
+
+__device__ inline Tile make_tile(int4 ci, int m) {
     Tile r;
-    r.m = t - c * p.mb;
-    int lo = 0, hi = nact;   // largest a with chunk_base[a] <= c
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.chunk_base[mid] <= c) lo = mid;
-        else hi = mid;
-    }
-    const int a = lo;
-    const int e = p.active[a];
-    const int chunk = c - p.chunk_base[a];
-    const int cnt = p.offsets[e + 1] - p.offsets[e];
-    r.e = e;
-    r.s0 = p.offsets[e] + chunk * kPN;
-    r.nv = min(kPN, cnt - chunk * kPN);
+    r.e = ci.x;
+    r.s0 = ci.y;
+    r.nv = ci.z;
     r.n16 = (r.nv + 15) & ~15;
+    r.m = m;
     return r;
 }
 
 __device__ inline void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ inline void cp_async_16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
 // One lane of the (converged) warp returns true.
@@ -200,7 +191,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *raw_full = bars;              // [kRR] INT4 TMA (+tx)
     uint64_t *raw_empty = raw_full + kRR;   // [kRR] the 128 dequant threads of the stage's group
-    uint64_t *b_full = raw_empty + kRR;     // [kRS] activation producers (copies landed and fenced)
+    uint64_t *b_full = raw_empty + kRR;     // [kRS] activation TMA (+tx)
     uint64_t *a_full = b_full + kRS;        // [kRS] 128 dequant threads (tcgen05.st done)
     uint64_t *ab_empty = a_full + kRS;      // [kRS] MMA commit: A slot and activation stage are free
     uint64_t *acc_full = ab_empty + kRS;    // [2] MMA commit
@@ -210,7 +201,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
     float *col_w = reinterpret_cast<float *>(smem + L.cols);     // epilogue (down): routing weight
     int *col_tok = reinterpret_cast<int *>(col_w + kPN);          // epilogue (down): token
-    int *row_idx = col_tok + kPN;                                 // producers: source row
     __shared__ int abort_s;
     volatile int *abort_flag = &abort_s;
 
@@ -222,7 +212,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             mbar_init(&raw_empty[i], 128);
         }
         for (int i = 0; i < kRS; ++i) {
-            mbar_init(&b_full[i], kNProd);
+            mbar_init(&b_full[i], 1);
             mbar_init(&a_full[i], 128);
             mbar_init(&ab_empty[i], 1);
         }
@@ -234,6 +224,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         }
         fence_mbar_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w) : "memory");
+        for (int i = 0; i < kNBoxMaps; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_b[i]) : "memory");
     }
     if (warp == kWMma) {
         tc::alloc(tmem_slot, kTmemCols);
@@ -305,9 +296,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         // gate_up: this lane pair's intermediate row and its fragment-order position
         const int il = et >> 1;
         const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
-        int lt = 0;
+        float *sStg = reinterpret_cast<float *>(smem + L.stg);
+        int lt = 0, nstg = 0;
+        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            const Tile T = decode_tile(p, nact, t);
+            const Tile T = make_tile(ci, t % p.mb);
+            if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);   // lands during this tile
             const int b = lt & 1;
             // the 128 epilogue threads share named barrier 1: they give up together
             if (!bar_and_128(pwait(&acc_full[b], (lt >> 1) & 1, abort_flag))) { fail(p, abort_flag); break; }
@@ -322,15 +316,25 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     col_tok[et] = a / p.k;
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                float *orow = p.out_acc + T.m * 128 + et;
-                for (int c0 = 0; c0 < T.nv; c0 += 16) {
+                float *ocol = p.out_acc + T.m * 128;
+                for (int c0 = 0; c0 < T.nv; c0 += 16, ++nstg) {
                     float v[16];
                     tc::ld_32x32b_x16(dbase + c0, v);
                     tc::wait_ld();
+                    // weighted rows into [token][row] order, then four 16-byte reductions per
+                    // thread; the two buffers alternate, so one barrier per chunk suffices
+                    float *st = sStg + (nstg & 1) * (kStgBytes / 4);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) st[u * 128 + et] = col_w[c0 + u] * v[u];
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
                     const int nu = min(16, T.nv - c0);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (u < nu) atomicAdd(orow + (size_t)col_tok[c0 + u] * p.H, col_w[c0 + u] * v[u]);
+                    for (int j = 0; j < 4; ++j) {
+                        const int f = et + 128 * j, u = f >> 5, r4 = (f & 31) * 4;
+                        if (u < nu)
+                            atomicAdd(reinterpret_cast<float4 *>(ocol + (size_t)col_tok[c0 + u] * p.H + r4),
+                                      *reinterpret_cast<const float4 *>(st + u * 128 + r4));
+                    }
                 }
             } else {
                 uint16_t *hrow = p.hbuf + (size_t)T.s0 * p.I + T.m * 64 + pl;
@@ -339,11 +343,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     tc::ld_32x32b_x16(dbase + c0, v);
                     tc::wait_ld();
                     const int nu = min(16, T.nv - c0);
+                    // the gate lane finishes columns 0-7 of the chunk, the up lane columns 8-15
+                    const bool odd = et & 1;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float up = __shfl_xor_sync(0xffffffffu, v[u], 1);
-                        if (!(et & 1) && u < nu) {
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(v[u]) * up);
+                    for (int j = 0; j < 8; ++j) {
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 8], 1);
+                        const float gv = odd ? recv : v[j], uv = odd ? v[j + 8] : recv;
+                        const int u = odd ? j + 8 : j;
+                        if (u < nu) {
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(gv) * uv);
                             hrow[(size_t)(c0 + u) * p.I] = *reinterpret_cast<const uint16_t *>(&hb);
                         }
                     }
@@ -354,11 +362,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         }
     } else if (warp == kWRaw) {
         // ------------------------------------------------ INT4 stages and scales: one TMA thread
+        // (the weights are read once: they go through L2 at evict-first priority, so that
+        // the activations, which every row block of a chunk re-reads, stay resident)
         if (lane == 0) {
+            const uint64_t wpol = l2_evict_first();
             uint32_t g = 0;
             int lt = 0;
+            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-                const Tile T = decode_tile(p, nact, t);
+                const Tile T = make_tile(ci, t % p.mb);
+                if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);
                 const int tb = lt & 1;
                 if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
                 // weight rows of TMEM lanes 0-63 and 64-127
@@ -374,8 +387,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     if (!pwait(&raw_empty[sr], ((g / kRR) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&raw_full[sr], kRawBytes);
                     uint8_t *rdst = sRaw + sr * kRawBytes;
-                    tma_load_2d(rdst, &p.tm_w, ks * 16, row_a, &raw_full[sr]);
-                    tma_load_2d(rdst + kRawHalf, &p.tm_w, ks * 16, row_b, &raw_full[sr]);
+                    // down's 128 rows are consecutive: one box (gate_up: gate and up boxes)
+                    tma_load_2d_hint(rdst, &p.tm_w, ks * 16, row_a, &raw_full[sr], wpol);
+                    if (!p.down) tma_load_2d_hint(rdst + kRawHalf, &p.tm_w, ks * 16, row_b, &raw_full[sr], wpol);
                 }
                 if (!ok) { fail(p, abort_flag); break; }
             }
@@ -385,68 +399,57 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 for (uint32_t gg = g > (uint32_t)kRR ? g - kRR : 0; gg < g; ++gg)
                     mbar_wait(&raw_full[gg % kRR], (gg / kRR) & 1);
         }
-    } else if (warp < kWMma) {
-        // ------------------------------------------------ activation rows (cp.async, 128-byte swizzle)
-        // Sixteen lanes copy one token row's 256 bytes of the stage, so each warp
-        // instruction reads two contiguous 256-byte runs. Each stage is one cp.async
-        // group. The tensor core reads through the async proxy, so a stage is
-        // published only after this thread's copies into it have landed and been
-        // fenced: kLag stages after they were issued.
-        const int wp = warp - kWProd;
-        const int row0 = 2 * wp + (lane >> 4);
-        const int kb = (lane >> 3) & 1, cc = lane & 7;   // K block and 16-byte chunk of this lane
-        uint32_t g = 0;
-        int lt = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
-            const Tile T = decode_tile(p, nact, t);
-            // source row of each token column this warp copies: lane l fills rows
-            // 2*kNProdW*l + 2*wp and the next one, which only this warp reads
-            __syncwarp();
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int r = 2 * kNProdW * lane + 2 * wp + s2;
-                if (r < T.n16) {
-                    const int rr = r < T.nv ? r : 0;   // padding columns repeat a valid row
-                    row_idx[r] = p.down ? T.s0 + rr : p.perm[T.s0 + rr] / p.k;
+    } else if (warp == kWAct) {
+        // ------------------------------------------------ activation stages: one TMA thread
+        if (lane == 0) {
+            uint32_t g = 0;
+            const int grid = (int)gridDim.x;
+            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
+            int4 ci2 = blockIdx.x + grid < ntiles ? chunk_of(p, blockIdx.x + grid) : make_int4(0, 0, 0, 0);
+            for (int t = blockIdx.x; t < ntiles; t += grid) {
+                const Tile T = make_tile(ci, t % p.mb);
+                ci = ci2;
+                const int t2 = t + 2 * grid;   // the tile after next
+                if (t2 < ntiles) ci2 = chunk_of(p, t2);
+                bool ok = true;
+                for (int ks = 0; ks < G; ++ks, ++g) {
+                    const int sb = g % kRS;
+                    if (!pwait(&ab_empty[sb], ((g / kRS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&b_full[sb], 2u * T.n16 * 128u);
+                    // n16 rows as few, large boxes (TMA moves big boxes much faster); rows past
+                    // the tile's tokens belong to other slots (or lie past the tensor and read as
+                    // zero): they only feed columns the epilogue skips
+                    for (int kb = 0; kb < 2; ++kb)
+                        for (int i = kNBoxMaps - 1, r0 = 0; i >= 0; --i)
+                            if (T.n16 & (16 << i)) {
+                                tma_load_2d(sB + sb * kBBytes + kb * kBKBlock + r0 * 128, &p.tm_b[i],
+                                            ks * kKS + kb * 64, T.s0 + r0, &b_full[sb]);
+                                r0 += 16 << i;
+                            }
                 }
+                if (!ok) { fail(p, abort_flag); break; }
+                // gate_up's x rows of a chunk are first read from HBM by the chunk's row-block
+                // tiles all at once; the CTA that will start a chunk pulls its rows into L2
+                // about one tile ahead
+                if (!p.down && t2 < ntiles && t2 % p.mb == 0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.xs + (size_t)ci2.y * p.H),
+                                 "r"((uint32_t)ci2.z * (uint32_t)p.H * 2u)
+                                 : "memory");
             }
-            __syncwarp();
-            const uint16_t *src_k = p.b_src + kb * 64 + 8 * cc;
-            const size_t row_len = p.down ? (size_t)p.I : (size_t)p.H;
-            uint8_t *dst_k = sB + kb * kBKBlock;
-            for (int ks = 0; ks < G; ++ks, ++g) {
-                const int sb = g % kRS;
-                // every wait gives up the same way in all lanes, so the warp never splits
-                if (!__all_sync(0xffffffffu, pwait(&ab_empty[sb], ((g / kRS) & 1) ^ 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *dst_s = dst_k + sb * kBBytes;
-                for (int r = row0; r < T.n16; r += 2 * kNProdW)
-                    // chunk cc of row r goes to chunk cc ^ (r % 8) of its 128-byte line
-                    cp_async_16(dst_s + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4),
-                                src_k + (size_t)row_idx[r] * row_len + ks * kKS);
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                if (g >= (uint32_t)kLag) {
-                    asm volatile("cp.async.wait_group %0;" ::"n"(kLag) : "memory");
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_arrive(&b_full[(g - kLag) % kRS]);
-                }
-            }
+            // after an abort, give the stages still in flight a bounded wait before the CTA exits
+            if (*abort_flag)
+                for (uint32_t gg = g > (uint32_t)kRS ? g - kRS : 0; gg < g; ++gg)
+                    mbar_wait(&b_full[gg % kRS], (gg / kRS) & 1);
         }
-        if (!ok) fail(p, abort_flag);
-        // publish the last stages
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (uint32_t gg = g > (uint32_t)kLag ? g - kLag : 0; gg < g; ++gg) mbar_arrive(&b_full[gg % kRS]);
     } else {
         // ------------------------------------------------ MMA issuer: the whole warp waits, one
         // elected lane issues the stage's 8 MMAs and the commit
         uint32_t g = 0;
         int lt = 0;
+        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            const Tile T = decode_tile(p, nact, t);
+            const Tile T = make_tile(ci, t % p.mb);
+            if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);
             const int b = lt & 1;
             if (!__all_sync(0xffffffffu, pwait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, abort_flag))) {
                 fail(p, abort_flag);
@@ -491,14 +494,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     if (warp == kWMma) tc::dealloc(tmem, kTmemCols);
 }
 // ---------------------------------------------------------------------------
-// x -> fragment order within each 8-element chunk: (0,4,1,5,2,6,3,7).
-__global__ void xperm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int64_t nchunks) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= nchunks) return;
-    const uint4 c = ld_nc_v4(x + 8 * i);
-    *reinterpret_cast<uint4 *>(xp + 8 * i) =
-        make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632), __byte_perm(c.y, c.w, 0x5410),
-                   __byte_perm(c.y, c.w, 0x7632));
+// xs[slot] = x[token of slot] in fragment order within each 8-element chunk
+// (0,4,1,5,2,6,3,7), for the offsets[E] slots that hold a valid assignment.
+__global__ void xgather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
+                               const int32_t *__restrict__ offsets, int E, int H, int k, uint16_t *__restrict__ xs) {
+    const int nslots = offsets[E];
+    const int cpr = H / 8;   // 16-byte chunks per row
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)nslots * cpr;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int slot = (int)(i / cpr), c = (int)(i - (int64_t)slot * cpr);
+        const int tok = perm[slot] / k;
+        const uint4 v = ld_nc_v4(x + (size_t)tok * H + 8 * c);
+        *reinterpret_cast<uint4 *>(xs + (size_t)slot * H + 8 * c) =
+            make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
+                       __byte_perm(v.y, v.w, 0x7632));
+    }
 }
 
 // One CTA: first 128-token chunk of each active expert (exclusive scan over
@@ -544,6 +554,25 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int32_t *__restr
     const int base_a = wa[w] + ia - act;
     if (act) chunk_base[base_a] = base_c;
     if (e == E - 1) chunk_base[base_a + act] = base_c + c;
+}
+
+// chunk_info[c] = (expert, first slot, tokens) of 128-token chunk c.
+__global__ void __launch_bounds__(256) chunk_info_kernel(const int32_t *__restrict__ chunk_base,
+                                                         const int32_t *__restrict__ active,
+                                                         const int32_t *__restrict__ offsets, const Ctrl *ctrl,
+                                                         int4 *__restrict__ chunk_info) {
+    const int nact = (int)ctrl->n_active;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (nact == 0 || c >= chunk_base[nact]) return;
+    int lo = 0, hi = nact;   // largest a with chunk_base[a] <= c
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (chunk_base[mid] <= c) lo = mid;
+        else hi = mid;
+    }
+    const int e = active[lo], j = c - chunk_base[lo];
+    const int cnt = offsets[e + 1] - offsets[e];
+    chunk_info[c] = make_int4(e, offsets[e] + j * kPN, min(kPN, cnt - j * kPN), 0);
 }
 
 // out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue), then out_acc = 0.
@@ -600,15 +629,21 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
-    const int64_t nch = (int64_t)d.T * d.H / 8;
-    xperm_kernel<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(a.x, xperm, nch);
+    xgather_kernel<<<(unsigned)(4 * sm_count()), 256, 0, s>>>(a.x, ws_at<int32_t>(ws, W.perm),
+                                                            ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm);
     chunk_scan_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), d.E, chunk_base);
+    int4 *chunk_info = ws_at<int4>(ws, W.chunk_info);
+    const int max_chunks = (int)((int64_t)d.T * d.k / kPN) + d.E + 1;
+    chunk_info_kernel<<<(max_chunks + 255) / 256, 256, 0, s>>>(chunk_base, ws_at<int32_t>(ws, W.active),
+                                                              ws_at<int32_t>(ws, W.offsets), ws_at<Ctrl>(ws, W.ctrl),
+                                                              chunk_info);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     PrefillParams p;
     p.offsets = ws_at<int32_t>(ws, W.offsets);
     p.active = ws_at<int32_t>(ws, W.active);
     p.chunk_base = chunk_base;
+    p.chunk_info = chunk_info;
     p.perm = ws_at<int32_t>(ws, W.perm);
     p.topk_w = a.topk_w;
     p.ctrl = ws_at<Ctrl>(ws, W.ctrl);
@@ -627,7 +662,11 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
                          (uint64_t)d.H / 2, 16u, 64u, CU_TENSOR_MAP_SWIZZLE_64B);
     if (err != cudaSuccess) return err;
     if ((err = record_profile_event(ev_before, s)) != cudaSuccess) return err;
-    p.b_src = xperm;
+    p.xs = xperm;
+    for (int i = 0; i < kNBoxMaps && err == cudaSuccess; ++i)
+        err = encode_tmap_2d(&p.tm_b[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xperm, (uint64_t)d.H,
+                             (uint64_t)d.T * d.k, (uint64_t)d.H * 2, 64u, 16u << i, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
     p.scales = a.w1s;
     p.K = d.H;
     p.mb = d.I / 64;
@@ -638,9 +677,12 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
 
     // down: K = I, 128 output rows per tile
     err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w2p, (uint64_t)d.I / 8, (uint64_t)d.E * d.H,
-                         (uint64_t)d.I / 2, 16u, 64u, CU_TENSOR_MAP_SWIZZLE_64B);
+                         (uint64_t)d.I / 2, 16u, 128u, CU_TENSOR_MAP_SWIZZLE_64B);
     if (err != cudaSuccess) return err;
-    p.b_src = p.hbuf;
+    for (int i = 0; i < kNBoxMaps && err == cudaSuccess; ++i)
+        err = encode_tmap_2d(&p.tm_b[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.hbuf, (uint64_t)d.I,
+                             (uint64_t)d.T * d.k, (uint64_t)d.I * 2, 64u, 16u << i, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
     p.scales = a.w2s;
     p.K = d.I;
     p.mb = d.H / 128;
