@@ -10,10 +10,11 @@
 //   gate_up: tile = (expert, 64 intermediate rows i0.., up to 128 tokens).
 //            A = 128 weight rows: gate row i0+i in TMEM lane 2i, the
 //            matching up row in lane 2i+1; K = H.
-//            Epilogue: h = SiLU(g) * u (lane pairs meet by one shuffle),
-//            rounded to bf16 and stored per slot.
+//            Epilogue: h = topk_w * SiLU(g) * u (lane pairs meet by one
+//            shuffle), rounded to bf16 and stored per slot. The routing weight
+//            is applied here because the down projection is linear in h.
 //   down:    tile = (expert, 128 output rows, up to 128 tokens), K = I.
-//            Epilogue: out_acc[t] += topk_w * y (fp32 reductions in L2).
+//            Epilogue: out_acc[t] += y (fp32 reductions in L2).
 //
 // One pipeline stage is one quantisation group (128 of K):
 //   * warp 12 lane 0 loads the stage's packed INT4 (128 rows x 64 bytes) with
@@ -35,7 +36,7 @@
 // Issuing the MMAs from a tight, unrolled, warp-uniform sequence matters: a
 // 128x128x16 MMA takes about 64 SM cycles, so per-instruction issue overhead
 // of the same order halves the tensor rate. The accumulator is double-buffered
-// in TMEM so 128 epilogue threads drain one tile while the next accumulates.
+// in TMEM so 256 epilogue threads drain one tile while the next accumulates.
 //
 // Weights enter A as W = bf16(q * scale) (one rounding per weight). Nibble
 // pairs (j, j+4) of each word fill one 32-bit TMEM column, so the
@@ -54,9 +55,10 @@ constexpr int kKS = 128;             // K per pipeline stage: one quantisation g
 constexpr int kRR = 8;               // packed-INT4 stages (HBM stream)
 constexpr int kRS = 4;               // A slots in TMEM = activation stages in smem (freed together)
 constexpr int kPN = 128;             // max tokens per tile (columns of one TMEM accumulator)
-constexpr int kWEpi = 8, kWRaw = 12, kWAct = 13, kWMma = 14;
-constexpr int kPThreads = 15 * 32;   // warps 0-7 dequant (two groups), 8-11 epilogue, 12 INT4 TMA,
+constexpr int kWEpi = 8, kWRaw = 12, kWAct = 13, kWMma = 14, kWEpi2 = 15;
+constexpr int kPThreads = 19 * 32;   // warps 0-7 dequant (two groups), 8-11 and 15-18 epilogue, 12 INT4 TMA,
                                      // 13 activation TMA, 14 MMA
+constexpr int kNEpi = 256;           // epilogue threads: two per accumulator row
 constexpr int kNBoxMaps = 4;         // activation TMA boxes of 16, 32, 64 and 128 token rows
 static_assert((16 << (kNBoxMaps - 1)) == 128, "box sizes cover any multiple of 16 up to 128 rows");
 constexpr uint32_t kTmemCols = 512;
@@ -66,12 +68,11 @@ constexpr uint32_t kBKBlock = kPN * 128;        // 128 token rows x 64 bf16: one
 constexpr uint32_t kBBytes = 2 * kBKBlock;      // one activation stage: two K blocks
 constexpr uint32_t kRawHalf = 64 * 64;          // 64 weight rows x 16 words
 constexpr uint32_t kRawBytes = 2 * kRawHalf;    // one packed-INT4 stage
-constexpr uint32_t kStgBytes = 16 * 128 * 4;    // one down-epilogue transpose buffer
 constexpr uint32_t kPrefillSmemMax = 232448 - 1024;   // dynamic; the static part is a few bytes
 static_assert(kAStage0 + kRS * kACols <= kTmemCols, "tensor memory budget");
 
 struct PrefillLayout {   // shared-memory offsets from the 1024-aligned base; scales sized by K
-    uint32_t b, raw, sc, sc_bytes, stg, cols, bars, tmem_slot, total;
+    uint32_t b, raw, sc, sc_bytes, cols, bars, tmem_slot, total;
 };
 constexpr int kNBars = 2 * kRR + 3 * kRS + 8;
 
@@ -81,8 +82,7 @@ __host__ __device__ inline PrefillLayout prefill_layout(int G) {
     L.raw = L.b + kRS * kBBytes;
     L.sc = L.raw + kRR * kRawBytes;
     L.sc_bytes = (uint32_t)(128 * G * 2 + 127) / 128 * 128;
-    L.stg = L.sc + 2 * L.sc_bytes;            // down epilogue: two [16 tokens][128 rows] f32 buffers
-    L.cols = L.stg + 2 * kStgBytes;           // per token column: f32 weight, i32 token
+    L.cols = L.sc + 2 * L.sc_bytes;           // per token column: f32 weight, i32 token
     L.bars = L.cols + 2 * 4 * kPN;
     L.tmem_slot = L.bars + kNBars * 8;
     L.total = L.tmem_slot + 16 + 1024;   // + alignment slack
@@ -149,14 +149,14 @@ __device__ inline bool pwait(uint64_t *bar, uint32_t parity, volatile int *abort
     return false;
 }
 
-// Named barrier 1 over the 128 epilogue threads, returning the AND of `v`.
-__device__ inline bool bar_and_128(bool v) {
+// Named barrier 1 over the epilogue threads, returning the AND of `v`.
+__device__ inline bool bar_and_epi(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "barrier.cta.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(kNEpi)
         : "memory");
     return r != 0;
 }
@@ -195,12 +195,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint64_t *a_full = b_full + kRS;        // [kRS] 128 dequant threads (tcgen05.st done)
     uint64_t *ab_empty = a_full + kRS;      // [kRS] MMA commit: A slot and activation stage are free
     uint64_t *acc_full = ab_empty + kRS;    // [2] MMA commit
-    uint64_t *acc_empty = acc_full + 2;     // [2] 128 epilogue threads
+    uint64_t *acc_empty = acc_full + 2;     // [2] the epilogue threads
     uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
-    uint64_t *sc_empty = sc_full + 2;       // [2] 256 dequant threads
+    uint64_t *sc_empty = sc_full + 2;       // [2] the 256 dequant threads
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
-    float *col_w = reinterpret_cast<float *>(smem + L.cols);     // epilogue (down): routing weight
-    int *col_tok = reinterpret_cast<int *>(col_w + kPN);          // epilogue (down): token
+    float *col_w = reinterpret_cast<float *>(smem + L.cols);     // epilogue (gate_up): routing weight
+    uint32_t *col_off = reinterpret_cast<uint32_t *>(col_w + kPN);   // epilogue (down): token * H (< 2^32)
     __shared__ int abort_s;
     volatile int *abort_flag = &abort_s;
 
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 128);
+            mbar_init(&acc_empty[b], kNEpi);
             mbar_init(&sc_full[b], 1);
             mbar_init(&sc_empty[b], 256);
         }
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         // 0 (warps 0-3) takes the even stages, group 1 (warps 4-7) the odd ones
         const int grp = warp >> 2;
         const int r = threadIdx.x & 127;   // tile row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;   // the warp's TMEM lane quarter
         // TMA box (half of the stage) and row within it: gate_up puts gate row i in lane 2i and
         // up row i in lane 2i+1, so the epilogue pairs them with one shuffle; down is in order
         const int half = p.down ? r >> 6 : r & 1;
@@ -288,57 +288,50 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             if (!ok) { fail(p, abort_flag); break; }
             mbar_arrive(&sc_empty[tb]);
         }
-    } else if (warp < kWRaw) {
-        // ------------------------------------------------ epilogue: one accumulator row per thread,
-        // written straight to global memory (h as bf16 stores, down as fp32 reductions in L2)
-        const int q = warp - kWEpi;
-        const int et = threadIdx.x - 32 * kWEpi;   // 0..127 = TMEM lane = tile row
+    } else if (warp < kWRaw || warp >= kWEpi2) {
+        // ------------------------------------------------ epilogue: two threads per accumulator row
+        // (one in warps 8-11, one in warps 15-18) taking alternate column chunks, written
+        // straight to global memory (h as bf16 stores, down as fp32 reductions in L2)
+        const int q = warp & 3;                    // TMEM lane quarter this warp may access
+        const int eh = warp >= kWEpi2;             // which of the row's two threads
+        const int et = 32 * q + lane;              // 0..127 = TMEM lane = tile row
         // gate_up: this lane pair's intermediate row and its fragment-order position
         const int il = et >> 1;
         const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
-        float *sStg = reinterpret_cast<float *>(smem + L.stg);
-        int lt = 0, nstg = 0;
+        int lt = 0;
         int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = make_tile(ci, t % p.mb);
             if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);   // lands during this tile
             const int b = lt & 1;
-            // the 128 epilogue threads share named barrier 1: they give up together
-            if (!bar_and_128(pwait(&acc_full[b], (lt >> 1) & 1, abort_flag))) { fail(p, abort_flag); break; }
+            // the epilogue threads share named barrier 1: they give up together
+            if (!bar_and_epi(pwait(&acc_full[b], (lt >> 1) & 1, abort_flag))) { fail(p, abort_flag); break; }
             tc::fence_after();
             const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + b * kPN;
+            // per column of the tile: gate_up needs the slot's routing weight, down the
+            // token's output row (the previous tile's readers passed the barrier above)
+            if (!eh && et < T.nv) {
+                const int a = p.perm[T.s0 + et];
+                if (p.down) col_off[et] = (uint32_t)(a / p.k) * (uint32_t)p.H;
+                else col_w[et] = p.topk_w[a];
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kNEpi) : "memory");
             if (p.down) {
-                // routing weight and token of every column of the tile (the previous tile's
-                // readers passed the barrier above before these are rewritten)
-                if (et < T.nv) {
-                    const int a = p.perm[T.s0 + et];
-                    col_w[et] = p.topk_w[a];
-                    col_tok[et] = a / p.k;
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                float *ocol = p.out_acc + T.m * 128;
-                for (int c0 = 0; c0 < T.nv; c0 += 16, ++nstg) {
-                    float v[16];
-                    tc::ld_32x32b_x16(dbase + c0, v);
+                // one reduction per (row, token): the 32 lanes of a warp cover 128 consecutive
+                // bytes of the token's output row; the routing weight is already in h
+                float *orow = p.out_acc + T.m * 128 + et;
+                for (int c0 = 32 * eh; c0 < T.nv; c0 += 64) {
+                    float v[32];
+                    tc::ld_32x32b_x32(dbase + c0, v);
                     tc::wait_ld();
-                    // weighted rows into [token][row] order, then four 16-byte reductions per
-                    // thread; the two buffers alternate, so one barrier per chunk suffices
-                    float *st = sStg + (nstg & 1) * (kStgBytes / 4);
+                    const int nu = min(32, T.nv - c0);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) st[u * 128 + et] = col_w[c0 + u] * v[u];
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    const int nu = min(16, T.nv - c0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int f = et + 128 * j, u = f >> 5, r4 = (f & 31) * 4;
-                        if (u < nu)
-                            atomicAdd(reinterpret_cast<float4 *>(ocol + (size_t)col_tok[c0 + u] * p.H + r4),
-                                      *reinterpret_cast<const float4 *>(st + u * 128 + r4));
-                    }
+                    for (int u = 0; u < 32; ++u)
+                        if (u < nu) atomicAdd(orow + (size_t)col_off[c0 + u], v[u]);
                 }
             } else {
                 uint16_t *hrow = p.hbuf + (size_t)T.s0 * p.I + T.m * 64 + pl;
-                for (int c0 = 0; c0 < T.nv; c0 += 16) {
+                for (int c0 = 16 * eh; c0 < T.nv; c0 += 32) {
                     float v[16];
                     tc::ld_32x32b_x16(dbase + c0, v);
                     tc::wait_ld();
@@ -351,7 +344,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                         const float gv = odd ? recv : v[j], uv = odd ? v[j + 8] : recv;
                         const int u = odd ? j + 8 : j;
                         if (u < nu) {
-                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(gv) * uv);
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(silu(gv) * uv * col_w[c0 + u]);
                             hrow[(size_t)(c0 + u) * p.I] = *reinterpret_cast<const uint16_t *>(&hb);
                         }
                     }
