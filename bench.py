@@ -143,10 +143,12 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest v over the ranks (NCCL on the GPUs, or gloo on the host)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -424,9 +426,10 @@ def run_ours(args, rank, world, local):
 
 def main():
     args = parse()
-    rank, world, local = dist_setup(args)
     wl = synth.WORKLOADS[args.config]
     if args.impl == "reference":
+        # the oracle on the host cores: rank 0 alone runs it, the other ranks leave at once
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
         if rank == 0:
             cb = cpu_baseline(wl, args.seed, args.cpu_seconds)
             line = {"impl": "reference", "metric": "MoE layer tok/s (%s)" % wl.name, "value": cb["value"],
@@ -438,6 +441,7 @@ def main():
                             "d2h_bytes_per_step": 0}}
             print(json.dumps(line), flush=True)
         return
+    rank, world, local = dist_setup(args)
     res = run_ours(args, rank, world, local)
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)

@@ -23,7 +23,7 @@
  *  - Every tensor is row-major and contiguous; every pointer is 16-byte
  *    aligned.
  *  - Supported shapes: T >= 0, H and I multiples of 128, 1 <= k <= 32,
- *    k <= E <= 1024, H <= 8192, I <= 4096. Others return
+ *    k <= E <= 1024, H <= 8064, I <= 4096. Others return
  *    MOE_ERR_UNSUPPORTED before anything is enqueued.
  *  - Argument errors are returned synchronously and enqueue nothing. A
  *    launch failure returns MOE_ERR_CUDA. Errors seen by a kernel (an expert
