@@ -21,7 +21,9 @@ struct Ctrl {
     uint32_t error;          // first MOE_ERR_DEVICE / MOE_ERR_TIMEOUT seen
     uint32_t pad0;
     uint32_t n_active;       // experts with at least one assignment
-    uint32_t pad1[61];
+    uint32_t bar_arrive;     // grid barrier of the decode stack step: CTAs arrived
+    uint32_t bar_depart;     // ... and CTAs done with the rows after it (the last resets both)
+    uint32_t pad1[59];
 };
 static_assert(sizeof(Ctrl) == 256, "control block");
 
@@ -34,7 +36,7 @@ struct WsLayout {
     size_t done1;        // u32 [E]        per expert: finished gate_up tasks
     size_t done2;        // u32 [E]        per expert: finished down tasks
     size_t ticket;       // u32 [T][H/32]  per output block: finished slots
-    size_t rowdone;      // u32 [T]        per token: finished output blocks
+    size_t rowss;        // f32 [T]        per token: sum of r^2 (stack epilogue, decode path)
     size_t rbuf;         // f32 [T][H]     residual sums (stack epilogue)
     size_t chunk;        // i32 [nchunk][E] per-chunk counts -> per-chunk bases
     size_t perm;         // i32 [T*k]      slot -> assignment
@@ -79,7 +81,7 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.done1 = take(E * 4);
     L.done2 = take(E * 4);
     L.ticket = take(T * (H / 32) * 4);
-    L.rowdone = take(T * 4);
+    L.rowss = take(T * 4);
     L.rbuf = take(T <= 64 ? T * H * 4 : 0);
     L.chunk = take((size_t)(L.nchunk > 0 ? L.nchunk : 1) * E * 4);
     L.perm = take(T * k * 4);

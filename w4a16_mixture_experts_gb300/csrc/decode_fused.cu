@@ -64,7 +64,7 @@ struct FusedParams {
     uint32_t *done1;     // [E] finished gate_up tasks
     uint32_t *done2;     // [E] finished down tasks
     uint32_t *ticket;    // [T][H/32] finished slots per output block
-    uint32_t *rowdone;   // [T] finished output blocks (stack variant)
+    float *rowss;        // [T] sum of r^2 per token (stack variant)
     uint16_t *hbuf;      // bf16 [T*k][I], fragment order
     float *ybuf;         // f32 [T*k][H]
     float *rbuf;         // f32 [T][H] residual sums (stack variant)
@@ -520,22 +520,58 @@ __device__ __noinline__ void f_combine_block(const FusedParams &p, const Pro &v,
         const __nv_bfloat16 b = __float2bfloat16_rn(s);
         p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
     } else {
-        p.rbuf[(size_t)t * p.H + n] = s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]);
+        // stack step: keep r = x + moe(x) and add this block's share of sum(r^2)
+        const float r = s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]);
+        p.rbuf[(size_t)t * p.H + n] = r;
+        float ss = r * r;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) atomicAdd(&p.rowss[t], ss);
     }
 }
 
-__device__ __noinline__ void f_rms_row(const FusedParams &p, int t, int lane) {
-    float ss = 0.f;
-    for (int n = lane; n < p.H; n += 32) {
-        const float r = __ldcg(p.rbuf + (size_t)t * p.H + n);
-        ss += r * r;
+// Stack step, after every CTA has combined its blocks (a grid barrier on two
+// self-resetting counters; the launch is cooperative, so every CTA is resident
+// and the bounded wait ends): one CTA per token scales its row by
+// 1/sqrt(mean(r^2) + eps) with 16-byte loads.
+__device__ __noinline__ void f_stack_rows(const FusedParams &p) {
+    __shared__ float s_scale;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_add_u32(&p.ctrl->bar_arrive, 1u);
+        uint32_t i = 0;
+        while (ld_acquire_u32(&p.ctrl->bar_arrive) < gridDim.x)
+            if (++i > kSpinLimit) {
+                set_error(p.ctrl, MOE_ERR_TIMEOUT);
+                break;
+            }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float scale = rsqrtf(ss / (float)p.H + p.eps);
-    for (int n = lane; n < p.H; n += 32) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(__ldcg(p.rbuf + (size_t)t * p.H + n) * scale);
-        p.next[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
+    __syncthreads();
+    for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+        if (threadIdx.x == 0) {
+            const float ss = __ldcg(&p.rowss[t]);
+            p.rowss[t] = 0.f;
+            s_scale = rsqrtf(ss / (float)p.H + p.eps);
+        }
+        __syncthreads();
+        const float sc = s_scale;
+        const float *row = p.rbuf + (size_t)t * p.H;
+        uint16_t *nrow = p.next + (size_t)t * p.H;
+        for (int n = 4 * threadIdx.x; n < p.H; n += 4 * blockDim.x) {
+            const float4 r = __ldcg(reinterpret_cast<const float4 *>(row + n));
+            __nv_bfloat162 lo = __floats2bfloat162_rn(r.x * sc, r.y * sc), hi = __floats2bfloat162_rn(r.z * sc, r.w * sc);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(nrow + n) = u;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0 && atomicAdd(&p.ctrl->bar_depart, 1u) + 1 == gridDim.x) {
+        // every CTA has passed the barrier and finished its rows
+        p.ctrl->bar_arrive = 0;
+        p.ctrl->bar_depart = 0;
     }
 }
 
@@ -642,20 +678,6 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
             m &= m - 1;
             const int tt = __shfl_sync(0xffffffffu, t, src);
             f_combine_block(p, v, tt, c, lane);
-            if (!p.out) {
-                __threadfence();
-                __syncwarp();
-                uint32_t last = 0;
-                if (lane == 0) {
-                    last = atomicAdd(&p.rowdone[tt], 1u) + 1 == (uint32_t)tp2;
-                    if (last) p.rowdone[tt] = 0;
-                }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    __threadfence();
-                    f_rms_row(p, tt, lane);
-                }
-            }
         }
     }
     // the last down task of expert e resets the expert's counters
@@ -718,7 +740,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
             // copy one more bounded wait, and stop
             if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
             mbar_wait(&bar[st ^ 1], phase[st ^ 1]);
-            return;
+            break;
         }
         phase[st] ^= 1u;
         if (tk < n1) {
@@ -741,6 +763,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         }
         L.advance(cur);
     }
+    if (!p.out) f_stack_rows(p);
 }
 
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
@@ -766,7 +789,7 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.done1 = ws_at<uint32_t>(ws, W.done1);
     p.done2 = ws_at<uint32_t>(ws, W.done2);
     p.ticket = ws_at<uint32_t>(ws, W.ticket);
-    p.rowdone = ws_at<uint32_t>(ws, W.rowdone);
+    p.rowss = ws_at<float>(ws, W.rowss);
     p.hbuf = ws_at<uint16_t>(ws, W.hbuf);
     p.ybuf = ws_at<float>(ws, W.ybuf);
     p.rbuf = ws_at<float>(ws, W.rbuf);
