@@ -58,7 +58,17 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Router K split: small batches split K across CTAs so that enough SMs pull
 // the router weight; each split must be a whole number of 32-wide K blocks.
+// Large batches (the tensor-core router, E a multiple of 128) split K until
+// the 128x128 tiles times the splits fill about one wave of 148 CTAs, keeping
+// at least four 64-wide K steps per split.
+inline bool router_tc(const moe_dims &d) { return d.T > 64 && d.E % 128 == 0; }
 inline int router_ksplit(const moe_dims &d) {
+    if (router_tc(d)) {
+        const int tiles = (d.E / 128) * ((d.T + 127) / 128);
+        int s = 1;
+        while (s < 8 && tiles * s * 2 <= 148 && d.H / 64 / (s * 2) >= 4) s *= 2;
+        return s;
+    }
     if (d.T > 64) return 1;
     for (int s = 16; s > 1; s >>= 1)
         if (d.H % (32 * s) == 0 && s <= d.H / 128) return s;

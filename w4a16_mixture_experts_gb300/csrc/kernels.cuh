@@ -25,6 +25,11 @@ cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s);
 cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
                          int32_t *ids, float *w, void *ws, cudaStream_t s);
 
+// Router logits on the tensor core for T > 64 and E a multiple of 128:
+// partial [ksplit][T][E] f32 (summed by the top-k kernel).
+cudaError_t launch_route_logits_tc(const uint16_t *x, const uint16_t *wr, const moe_dims &d, float *partial,
+                                   int ksplit, struct Ctrl *ctrl, cudaStream_t s);
+
 cudaError_t launch_permute(const int32_t *ids, const moe_dims &d, void *ws, cudaStream_t s);
 
 struct ExpertArgs {

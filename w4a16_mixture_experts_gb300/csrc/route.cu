@@ -171,6 +171,12 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     const WsLayout L = ws_layout(d);
     float *partial = ws_at<float>(ws, L.partial);
     const int ksplit = L.ksplit;
+    if (router_tc(d)) {
+        cudaError_t err = launch_route_logits_tc(x, wr, d, partial, ksplit, ws_at<Ctrl>(ws, L.ctrl), s);
+        if (err != cudaSuccess) return err;
+        route_topk_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+        return cudaGetLastError();
+    }
     const int tt = d.T <= 64 ? d.T : 64;
     int nt = 1;
     while (8 * nt < tt) nt <<= 1;

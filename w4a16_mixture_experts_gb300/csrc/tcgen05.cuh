@@ -34,6 +34,16 @@ __device__ inline void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f16, both operands by shared-memory descriptor.
+__device__ inline void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` when all tcgen05.mma issued so far by this thread have completed.
 __device__ inline void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
