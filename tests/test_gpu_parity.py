@@ -323,6 +323,8 @@ def test_forward_rms_stack_step():
     (129, 128, 1, 1, 128),      # one expert: a full 128-token chunk and a 1-token chunk
     (300, 384, 4, 2, 256),      # hot experts spanning three chunks, odd group count
     (200, 512, 64, 8, 384),     # many small experts, ragged N tiles
+    (4, 256, 16, 2, 1408),      # small batch the fused decode kernel cannot take (I > 1280)
+    (33, 384, 8, 3, 1536),      # likewise, ragged token count
 ])
 def test_prefill_forward_parity(T, H, E, k, I):
     seed = T * 7 + E

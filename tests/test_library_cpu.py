@@ -106,3 +106,14 @@ def test_argument_errors_are_synchronous(L):
     e = moe.moe_dims(0, 256, 16, 2, 128)
     assert L.moe_w4a16_forward(None, None, None, *[ctypes.c_void_p(p) for p in good[:4]], None, e,
                                ctypes.c_void_p(good[5]), need, None) == 0
+
+
+def test_workspace_holds_the_regions_of_the_path_taken():
+    """A small batch the fused decode kernel cannot take (I > 1280) runs the
+    prefill pipeline, so its workspace must hold the per-slot activations and
+    the fp32 accumulator; a decode-sized batch of the same kind does not."""
+    T, H, E, k = 4, 256, 16, 2
+    big = moe.moe_workspace_size(T, H, E, k, 1408)
+    small = moe.moe_workspace_size(T, H, E, k, 128)
+    assert big >= T * k * H * 2 + T * H * 4 + T * k * 1408 * 2
+    assert small < T * k * H * 2 + T * H * 4 + T * k * 128 * 2 + 64 * 1024

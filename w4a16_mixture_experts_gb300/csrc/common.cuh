@@ -75,6 +75,11 @@ inline int router_ksplit(const moe_dims &d) {
     return 1;
 }
 
+// True when the forward calls take the fused decode kernel (T <= 7 and its
+// shared-memory layout fits); otherwise they take the prefill pipeline. The
+// workspace holds the regions of the path that will run.
+bool fused_supported(const moe_dims &d);
+
 inline WsLayout ws_layout(const moe_dims &d) {
     WsLayout L{};
     size_t o = 0;
@@ -92,12 +97,12 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.done2 = take(E * 4);
     L.ticket = take(T * (H / 32) * 4);
     L.rowss = take(T * 4);
-    L.rbuf = take(T <= 64 ? T * H * 4 : 0);
+    const bool small = fused_supported(d);
+    L.rbuf = take(small ? T * H * 4 : 0);
     L.chunk = take((size_t)(L.nchunk > 0 ? L.nchunk : 1) * E * 4);
     L.perm = take(T * k * 4);
     L.inv = take(T * k * 4);
     L.hbuf = take(T * k * I * 2);
-    const bool small = T <= 64;
     L.ybuf = take(small ? T * k * H * 4 : 0);
     L.xperm = take(small ? 0 : T * k * H * 2);
     L.out_acc = take(small ? 0 : T * H * 4);

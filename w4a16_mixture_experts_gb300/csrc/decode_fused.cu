@@ -2,7 +2,7 @@
 //
 // Computes the fused Marlin MoE of "Running 125B MoE on Three 3090s - vLLM
 // Optimization Edition", section 3.3 "MoE block" (moe_align_block_size,
-// gate_up, SiluAndMul, down, moe_sum) for small batches (T <= 64), on
+// gate_up, SiluAndMul, down, moe_sum) for decode batches (T <= 7), on
 // symmetric INT4 group-128 weights (model card, "What is quantized", group A).
 // At decode the layer streams ~2.5 MB of packed weights per active expert
 // and does a few FLOPs per byte, so everything here serves the byte stream:
@@ -43,9 +43,12 @@ namespace moe {
 constexpr int kFW = 8;               // warps per CTA
 constexpr int kGC = 10;              // quantisation groups per gate_up chunk
 constexpr int kP2Rows = 32;          // output rows per down task
-constexpr int kMaxNT = 8;            // token tiles of 8 per expert (T <= 64)
+// Batches of up to 7 tokens. From 8 tokens on, the tensor-core grouped GEMM
+// (prefill.cu) is as fast on GB300 and grows faster (measured: T = 8 at 114
+// us either way, T = 64 at 378 us there against 662 us here).
+constexpr int kDecodeMaxT = 7;
+constexpr int kMaxNT = (kDecodeMaxT + 7) / 8;   // token tiles of 8 per expert
 constexpr int kFastN = 256;          // assignments ranked by comparison
-constexpr int kFusedMaxT = 64;
 constexpr int kFusedMaxN = 2048;     // T * k
 constexpr int kFusedSmem = 232448 - 512;   // per-block opt-in limit, less static shared memory
 
@@ -105,7 +108,7 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     L.total = L.xs_off ? base + xs_bytes : base;
     // scratch of the prologue lives in the stage area
     const uint32_t scratch = kFW * d.E * 2 + 2 * d.E * 4 + 3 * kFastN * 4;
-    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= 2 * kFW * L.stage_bytes && d.T <= kFusedMaxT &&
+    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= 2 * kFW * L.stage_bytes && d.T <= kDecodeMaxT &&
            d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
     return L;
 }

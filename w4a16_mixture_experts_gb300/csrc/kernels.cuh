@@ -49,7 +49,7 @@ bool prefill_supported(const moe_dims &d);
 cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
                            cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t s);
 
-// Fused decode forward (T <= 64): permute, experts and combine in one launch.
+// Fused decode forward (T <= 7): permute, experts and combine in one launch.
 bool fused_supported(const moe_dims &d);
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
                                 float eps, cudaStream_t s);

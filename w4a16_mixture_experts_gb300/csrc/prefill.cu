@@ -1,4 +1,5 @@
-// Prefill expert path (T > 64): W4A16 grouped GEMMs on the tcgen05 tensor core.
+// Expert path for batches of 8 tokens and more: W4A16 grouped GEMMs on the
+// tcgen05 tensor core.
 //
 // Same computation as the fused Marlin MoE of "Running 125B MoE on Three
 // 3090s - vLLM Optimization Edition", section 3.3 "MoE block" (gate_up,
