@@ -62,7 +62,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // the 128x128 tiles times the splits fill about one wave of 148 CTAs, keeping
 // at least four 64-wide K steps per split.
 inline bool router_tc(const moe_dims &d) { return d.T > 64 && d.E % 128 == 0; }
-inline int router_ksplit(const moe_dims &d) {
+inline int router_ksplit(const moe_dims &d) {   // at most 16
     if (router_tc(d)) {
         const int tiles = (d.E / 128) * ((d.T + 127) / 128);
         int s = 1;
@@ -216,25 +216,26 @@ __device__ inline uint4 ld_cg_v4(const void *p) {
     return v;
 }
 
+// Read-only (for the whole kernel) global load through the non-coherent path:
+// not volatile, so the compiler may hoist and batch these loads.
 __device__ inline uint4 ld_nc_v4(const void *p) {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
 }
 
-__device__ inline uint4 lds_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_u32(p)));
-    return v;
-}
+// 16-byte shared-memory load. A plain C++ load, so that the compiler may
+// schedule it around arithmetic (and software-pipeline loops), while it still
+// stays after the mbarrier waits, whose asm carries a memory clobber.
+__device__ inline uint4 lds_v4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 // D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulate.
+// A pure register operation: not volatile, so loads of the next step can be
+// scheduled ahead of it.
 __device__ inline void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -102,7 +102,8 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
     L.pro_off = 2 * kFW * L.stage_bytes;
-    const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2;
+    // staged activations, then their sum over each 128-wide group (f32 [T][H/128])
+    const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2 + (uint32_t)align_up((size_t)d.T * G1 * 4, 16);
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
     L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
     L.total = L.xs_off ? base + xs_bytes : base;
@@ -184,12 +185,29 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
     int id_reg = -1;
     if (fast && tid < n) id_reg = p.ids[tid];
     if (p.xs_off) {
+        // x in fragment order, and per token the sum of each 128-wide group (the
+        // gate_up MMAs run on the biased nibbles 128 + n, see f_gate_up_chunk).
+        // A row holds H/8 chunks, a multiple of 16, so the 16 chunks of a group
+        // sit in 16 consecutive lanes; every lane runs every pass (the count is
+        // rounded up to whole warps) so that the shuffles see the full warp.
         uint4 *xs = reinterpret_cast<uint4 *>(smem + p.xs_off);
+        float *xsum = reinterpret_cast<float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
         const int nch = p.T * p.H / 8;
-        for (int i = tid; i < nch; i += nthr) {
-            const uint4 c = ld_nc_v4(p.x + (size_t)i * 8);
-            xs[i] = make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632),
-                               __byte_perm(c.y, c.w, 0x5410), __byte_perm(c.y, c.w, 0x7632));
+        const int nch32 = (nch + 31) & ~31;
+        for (int i = tid; i < nch32; i += nthr) {
+            float sum = 0.f;
+            if (i < nch) {
+                const uint4 c = ld_nc_v4(p.x + (size_t)i * 8);
+                xs[i] = make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632),
+                                   __byte_perm(c.y, c.w, 0x5410), __byte_perm(c.y, c.w, 0x7632));
+                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    sum += __uint_as_float(w[m] << 16) + __uint_as_float(w[m] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (i < nch && (lane & 15) == 0) xsum[i / 16] = sum;   // i / 16 = token * (H/128) + group
         }
     }
     bool bad = false;
@@ -437,18 +455,27 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
 #pragma unroll
         for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     }
+    // staged x: the MMAs take the biased nibble values 128 + n (exact in bf16, no
+    // subtraction per weight) and each group's sum is corrected by 136 * sum(x)
+    // over the group: sum (n - 8) x = sum (128 + n) x - 136 sum x, in fp32
+    const float *xsum = reinterpret_cast<const float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
     for (int nt = 0; nt < nt_n; ++nt) {
         // activation row of the token in column g of this N tile
         const int j = 8 * nt + g;
         const bool vx = j < ne;
         const int tok = vx ? v.perm[s0 + j] / p.k : 0;
+        // group sums of the tokens of the output columns 2tig and 2tig+1 (0 past ne)
+        const int j0 = 8 * nt + 2 * tig, j1 = j0 + 1;
+        const float *xs0 = j0 < ne ? xsum + (size_t)(v.perm[s0 + j0] / p.k) * G1 : nullptr;
+        const float *xs1 = j1 < ne ? xsum + (size_t)(v.perm[s0 + j1] / p.k) * G1 : nullptr;
         const uint4 *xb;
         if (kStaged)
             xb = reinterpret_cast<const uint4 *>(smem + p.xs_off) + (size_t)tok * (p.H / 8) + 4 * tig;
         else
             xb = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.H + 32 * tig);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 1
+        // two groups per pass: their load -> dequant -> mma chains overlap
+#pragma unroll 2
         for (int qq = 0; qq < qn; ++qq) {
             const int q = q0 + qq;
             const uint4 wg = lds_v4(rg + 64 * qq), wu = lds_v4(ru + 64 * qq);
@@ -467,16 +494,29 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const uint32_t xg = fw_word(wg, m), xu = fw_word(wu, m);
-                const uint32_t f0[4] = {int4_pair(xg, 0), int4_pair(xu, 0), int4_pair(xg, 1), int4_pair(xu, 1)};
-                const uint32_t f1[4] = {int4_pair(xg, 2), int4_pair(xu, 2), int4_pair(xg, 3), int4_pair(xu, 3)};
+                uint32_t f0[4], f1[4];
+                if (kStaged) {
+                    f0[0] = int4_pair_bias(xg, 0), f0[1] = int4_pair_bias(xu, 0);
+                    f0[2] = int4_pair_bias(xg, 1), f0[3] = int4_pair_bias(xu, 1);
+                    f1[0] = int4_pair_bias(xg, 2), f1[1] = int4_pair_bias(xu, 2);
+                    f1[2] = int4_pair_bias(xg, 3), f1[3] = int4_pair_bias(xu, 3);
+                } else {
+                    f0[0] = int4_pair(xg, 0), f0[1] = int4_pair(xu, 0), f0[2] = int4_pair(xg, 1), f0[3] = int4_pair(xu, 1);
+                    f1[0] = int4_pair(xg, 2), f1[1] = int4_pair(xu, 2), f1[2] = int4_pair(xg, 3), f1[3] = int4_pair(xu, 3);
+                }
                 c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
                 mma_bf16_16816(c[m], f0, X[m].x, X[m].y);
                 mma_bf16_16816(c[m], f1, X[m].z, X[m].w);
             }
-            a0 += sg * ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0]));
-            a1 += sg * ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1]));
-            a2 += su * ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2]));
-            a3 += su * ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+            float b0 = 0.f, b1 = 0.f;
+            if (kStaged) {
+                b0 = xs0 ? 136.f * xs0[q] : 0.f;
+                b1 = xs1 ? 136.f * xs1[q] : 0.f;
+            }
+            a0 += sg * (((c[0][0] + c[1][0]) + (c[2][0] + c[3][0])) - b0);
+            a1 += sg * (((c[0][1] + c[1][1]) + (c[2][1] + c[3][1])) - b1);
+            a2 += su * (((c[0][2] + c[1][2]) + (c[2][2] + c[3][2])) - b0);
+            a3 += su * (((c[0][3] + c[1][3]) + (c[2][3] + c[3][3])) - b1);
         }
 #pragma unroll
         for (int i = 0; i < kMaxNT; ++i)

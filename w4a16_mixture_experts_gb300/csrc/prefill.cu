@@ -494,14 +494,27 @@ __global__ void xgather_kernel(const uint16_t *__restrict__ x, const int32_t *__
                                const int32_t *__restrict__ offsets, int E, int H, int k, uint16_t *__restrict__ xs) {
     const int nslots = offsets[E];
     const int cpr = H / 8;   // 16-byte chunks per row
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)nslots * cpr;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int slot = (int)(i / cpr), c = (int)(i - (int64_t)slot * cpr);
-        const int tok = perm[slot] / k;
-        const uint4 v = ld_nc_v4(x + (size_t)tok * H + 8 * c);
-        *reinterpret_cast<uint4 *>(xs + (size_t)slot * H + 8 * c) =
-            make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
-                       __byte_perm(v.y, v.w, 0x7632));
+    const int64_t n = (int64_t)nslots * cpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // four independent chunks per pass, so that four loads are in flight per thread
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int slot = (int)(i / cpr), c = (int)(i - (int64_t)slot * cpr);
+                v[u] = ld_nc_v4(x + (size_t)(perm[slot] / k) * H + 8 * c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n)
+                *reinterpret_cast<uint4 *>(xs + (size_t)i * 8) =
+                    make_uint4(__byte_perm(v[u].x, v[u].z, 0x5410), __byte_perm(v[u].x, v[u].z, 0x7632),
+                               __byte_perm(v[u].y, v[u].w, 0x5410), __byte_perm(v[u].y, v[u].w, 0x7632));
+        }
     }
 }
 
@@ -570,28 +583,50 @@ __global__ void __launch_bounds__(256) chunk_info_kernel(const int32_t *__restri
 }
 
 // out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue), then out_acc = 0.
-__global__ void __launch_bounds__(256) acc_convert_kernel(float *__restrict__ acc, const uint16_t *__restrict__ x,
-                                                          int H, float eps, uint16_t *__restrict__ out,
-                                                          uint16_t *__restrict__ next) {
-    __shared__ float red[8];
+// One CTA per token, 16-byte accesses; the stack variant keeps the token's
+// row in registers between the sum of squares and the rescale.
+constexpr int kConvThreads = 256;
+constexpr int kConvPer = 8192 / 4 / kConvThreads;   // float4s of a row per thread (H <= 8192)
+
+__device__ inline uint2 bf16x4(float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&lo);
+    u.y = *reinterpret_cast<uint32_t *>(&hi);
+    return u;
+}
+
+__global__ void __launch_bounds__(kConvThreads) acc_convert_kernel(float *__restrict__ acc, const uint16_t *__restrict__ x,
+                                                                   int H, float eps, uint16_t *__restrict__ out,
+                                                                   uint16_t *__restrict__ next) {
+    __shared__ float red[kConvThreads / 32];
     const int t = blockIdx.x;
-    float *row = acc + (size_t)t * H;
+    float4 *row = reinterpret_cast<float4 *>(acc + (size_t)t * H);
+    const int n4 = H / 4;
     if (!next) {
-        for (int n = 4 * threadIdx.x; n < H; n += 1024) {
-            const float4 v = *reinterpret_cast<const float4 *>(row + n);
-            *reinterpret_cast<float4 *>(row + n) = make_float4(0.f, 0.f, 0.f, 0.f);
-            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-            uint2 u;
-            u.x = *reinterpret_cast<uint32_t *>(&lo);
-            u.y = *reinterpret_cast<uint32_t *>(&hi);
-            *reinterpret_cast<uint2 *>(out + (size_t)t * H + n) = u;
+        uint2 *o = reinterpret_cast<uint2 *>(out + (size_t)t * H);
+        for (int i = threadIdx.x; i < n4; i += kConvThreads) {
+            const float4 v = row[i];
+            row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            o[i] = bf16x4(v.x, v.y, v.z, v.w);
         }
         return;
     }
+    const uint2 *xr = reinterpret_cast<const uint2 *>(x + (size_t)t * H);
+    float4 r[kConvPer];
     float ss = 0.f;
-    for (int n = threadIdx.x; n < H; n += 256) {
-        const float r = row[n] + bf16_bits_to_f32(x[(size_t)t * H + n]);
-        ss += r * r;
+#pragma unroll
+    for (int j = 0; j < kConvPer; ++j) {
+        const int i = threadIdx.x + kConvThreads * j;
+        r[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4) {
+            const float4 v = row[i];
+            const uint2 xv = xr[i];
+            r[j] = make_float4(v.x + __uint_as_float(xv.x << 16), v.y + __uint_as_float(xv.x & 0xffff0000u),
+                               v.z + __uint_as_float(xv.y << 16), v.w + __uint_as_float(xv.y & 0xffff0000u));
+            row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += r[j].x * r[j].x + r[j].y * r[j].y + r[j].z * r[j].z + r[j].w * r[j].w;
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -599,13 +634,13 @@ __global__ void __launch_bounds__(256) acc_convert_kernel(float *__restrict__ ac
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
+    for (int w = 0; w < kConvThreads / 32; ++w) tot += red[w];
     const float scale = rsqrtf(tot / (float)H + eps);
-    for (int n = threadIdx.x; n < H; n += 256) {
-        const float r = row[n] + bf16_bits_to_f32(x[(size_t)t * H + n]);
-        row[n] = 0.f;
-        const __nv_bfloat16 b = __float2bfloat16_rn(r * scale);
-        next[(size_t)t * H + n] = *reinterpret_cast<const uint16_t *>(&b);
+    uint2 *o = reinterpret_cast<uint2 *>(next + (size_t)t * H);
+#pragma unroll
+    for (int j = 0; j < kConvPer; ++j) {
+        const int i = threadIdx.x + kConvThreads * j;
+        if (i < n4) o[i] = bf16x4(r[j].x * scale, r[j].y * scale, r[j].z * scale, r[j].w * scale);
     }
 }
 
@@ -686,7 +721,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = record_profile_event(ev_after, s)) != cudaSuccess) return err;
 
-    acc_convert_kernel<<<d.T, 256, 0, s>>>(out_acc, a.x, d.H, eps, next ? nullptr : out, next);
+    acc_convert_kernel<<<d.T, kConvThreads, 0, s>>>(out_acc, a.x, d.H, eps, next ? nullptr : out, next);
     return cudaGetLastError();
 }
 

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__res
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
     const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 2
+#pragma unroll 4
     for (int kk = 0; kk < kpart; kk += 32) {
         const uint4 A0 = va ? ld_nc_v4(pa + kk) : zero;
         const uint4 A1 = vb ? ld_nc_v4(pb + kk) : zero;
@@ -93,16 +93,15 @@ __device__ inline float f32_from_order_key(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------
-// Top-k: one CTA of 256 threads per token. Thread i sums the K-split partial
-// logits of experts i, i+256, ... and forms their 64-bit keys (order key of
-// the fp32 logit << 32 | 0xffffffff - id). Each warp extracts its own k
-// largest keys (k rounds of a two-step warp max with redux.sync: first the
-// logit half, then the id half among the lanes holding that logit); warp 0
-// then takes the k largest of the 8 warps' candidates. Keys are unique, so
-// every maximum has exactly one holder. Weights: softmax over the selected
-// logits in fp32.
-constexpr int kTopkThreads = 256;
-constexpr int kTopkPer = kMaxE / kTopkThreads;
+// Top-k for large batches: one warp per token. Lane l sums the K-split partial logits of experts
+// l, l+32, ... and forms their 64-bit keys (order key of the fp32 logit << 32
+// | 0xffffffff - id); k rounds of a two-step warp max with redux.sync (first
+// the logit half, then the id half among the lanes holding that logit) take
+// the k largest. Keys are unique, so every maximum has exactly one holder.
+// Weights: softmax over the selected logits in fp32.
+constexpr int kTopkWarps = 8;
+constexpr int kMaxKsplit = 16;   // router_ksplit() never returns more
+constexpr int kTopkPer = kMaxE / 32;
 
 __device__ inline uint64_t warp_max_key(uint64_t m) {
     const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
@@ -110,16 +109,69 @@ __device__ inline uint64_t warp_max_key(uint64_t m) {
     return ((uint64_t)hi << 32) | lo;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ partial, int ksplit,
+__global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float *__restrict__ partial, int ksplit,
+                                                                     const float *__restrict__ bias, int T, int E,
+                                                                     int k, int32_t *__restrict__ ids,
+                                                                     float *__restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    uint64_t key[kTopkPer];
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i) {
+        key[i] = 0;
+        const int e = lane + 32 * i;
+        if (e < E) {
+            // the split partials are independent loads: unrolled, they are all in flight at once
+            float l = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxKsplit; ++s)
+                if (s < ksplit) l += partial[((size_t)s * T + t) * E + e];
+            if (bias) l += bias[e];
+            key[i] = ((uint64_t)f32_order_key(l) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+        }
+    }
+    const int nper = (E + 31) / 32;   // keys a lane may hold
+    uint64_t mine = 0;
+    for (int j = 0; j < k; ++j) {
+        uint64_t m = 0;
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i)
+            if (i < nper) m = key[i] > m ? key[i] : m;
+        m = warp_max_key(m);
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+        if (lane == j) mine = m;
+    }
+    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
+    const float l = f32_from_order_key((uint32_t)(mine >> 32));
+    const float p = lane < k ? expf(l - lmax) : 0.f;
+    float z = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+        w[(size_t)t * k + lane] = p / z;
+    }
+}
+
+// Small batches: one CTA of 256 threads per token, so that the K-split partial
+// sums of a token's experts are spread over many threads. Thread i forms the
+// keys of experts i, i+256, ...; each warp extracts its own k largest keys,
+// then warp 0 takes the k largest of the 8 warps' candidates.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkCtaPer = kMaxE / kTopkThreads;
+
+__global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const float *__restrict__ partial, int ksplit,
                                                                   const float *__restrict__ bias, int T, int E,
                                                                   int k, int32_t *__restrict__ ids,
                                                                   float *__restrict__ w) {
     __shared__ uint64_t cand[kTopkThreads / 32][kMaxK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x;
-    uint64_t key[kTopkPer];
+    uint64_t key[kTopkCtaPer];
 #pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
+    for (int i = 0; i < kTopkCtaPer; ++i) {
         key[i] = 0;
         const int e = threadIdx.x + kTopkThreads * i;
         if (e < E) {
@@ -132,10 +184,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     for (int j = 0; j < k; ++j) {
         uint64_t m = 0;
 #pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) m = key[i] > m ? key[i] : m;
+        for (int i = 0; i < kTopkCtaPer; ++i) m = key[i] > m ? key[i] : m;
         m = warp_max_key(m);
 #pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+        for (int i = 0; i < kTopkCtaPer; ++i) key[i] = key[i] == m ? 0 : key[i];
         if (lane == 0) cand[warp][j] = m;
     }
     __syncthreads();
@@ -174,7 +226,13 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     if (router_tc(d)) {
         cudaError_t err = launch_route_logits_tc(x, wr, d, partial, ksplit, ws_at<Ctrl>(ws, L.ctrl), s);
         if (err != cudaSuccess) return err;
-        route_topk_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+        // a warp per token once there are enough tokens to fill the GPU with warps
+        // (and few K splits to sum); a CTA per token below that
+        if (d.T >= 2048)
+            route_topk_kernel<<<(d.T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias,
+                                                                                         d.T, d.E, d.k, ids, w);
+        else
+            route_topk_cta_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
         return cudaGetLastError();
     }
     const int tt = d.T <= 64 ? d.T : 64;
@@ -189,7 +247,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_topk_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+    route_topk_cta_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
     return cudaGetLastError();
 }
 
