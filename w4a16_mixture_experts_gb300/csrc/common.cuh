@@ -17,13 +17,18 @@ constexpr uint32_t kSpinLimit = 1u << 22;   // polls before a wait gives up (~0.
 // ---- workspace layout -------------------------------------------------------
 // A fixed control block followed by 256-byte aligned regions; offsets depend
 // only on the dims, so host and device agree without storing them.
+// Per-expert completion counters sit one 128-byte line apart, so that the
+// pollers and the increments of different experts do not share a line.
+constexpr int kCtrStride = 32;
+
 struct Ctrl {
     uint32_t error;          // first MOE_ERR_DEVICE / MOE_ERR_TIMEOUT seen
-    uint32_t pad0;
+    uint32_t route_ticket;   // router CTAs done with their logits (small batches; the last resets it)
     uint32_t n_active;       // experts with at least one assignment
     uint32_t bar_arrive;     // grid barrier of the decode stack step: CTAs arrived
     uint32_t bar_depart;     // ... and CTAs done with the rows after it (the last resets both)
-    uint32_t pad1[59];
+    uint32_t exit_count;     // decode CTAs finished (the last resets the per-expert counters)
+    uint32_t pad1[58];
 };
 static_assert(sizeof(Ctrl) == 256, "control block");
 
@@ -33,9 +38,9 @@ struct WsLayout {
     size_t counts;       // i32 [E]        per-expert assignment counts
     size_t offsets;      // i32 [E+1]
     size_t active;       // i32 [E]        active expert ids, increasing
-    size_t done1;        // u32 [E]        per expert: finished gate_up tasks
-    size_t done2;        // u32 [E]        per expert: finished down tasks
-    size_t ticket;       // u32 [T][H/32]  per output block: finished slots
+    size_t done1;        // u32 [E][kCtrStride] per expert (one 128-byte line each): finished gate_up tasks
+    size_t done2;        // unused, kept empty
+    size_t ticket;       // u32 [T][H/16]  per 16-row output block: finished slots
     size_t rowss;        // f32 [T]        per token: sum of r^2 (stack epilogue, decode path)
     size_t rbuf;         // f32 [T][H]     residual sums (stack epilogue)
     size_t chunk;        // i32 [nchunk][E] per-chunk counts -> per-chunk bases
@@ -93,9 +98,9 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);
-    L.done1 = take(E * 4);
-    L.done2 = take(E * 4);
-    L.ticket = take(T * (H / 32) * 4);
+    L.done1 = take((size_t)E * kCtrStride * 4);
+    L.done2 = take(0);
+    L.ticket = take(T * (H / 16) * 4);
     L.rowss = take(T * 4);
     const bool small = fused_supported(d);
     L.rbuf = take(small ? T * H * 4 : 0);
@@ -208,6 +213,12 @@ __device__ inline void red_release_add_u32(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ inline uint32_t atom_acq_rel_add_u32(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ inline uint4 ld_cg_v4(const void *p) {
     uint4 v;
     asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -247,8 +258,14 @@ __device__ inline void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uin
 // (n_j, n_{j+4}) as bf16x2 with n_j in the low half, converted to q exactly:
 // OR-ing a nibble into the mantissa of 128.0 (0x4300) gives 128 + n, and
 // subtracting 136 leaves n - 8, both exact in bf16.
+// The mask and the bias go into one lop3 ((a & b) | c, table 0xEA) with the
+// bias in a register: written as plain C the pair costs a third instruction,
+// and the dequantisation loops are bound by the integer pipe.
 __device__ inline uint32_t int4_pair_bias(uint32_t w, int j) {
-    return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t s = w >> (4 * j);
+    uint32_t d;
+    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(s), "r"(0x43004300u));
+    return d;
 }
 
 __device__ inline uint32_t bf16x2_sub136(uint32_t v) {

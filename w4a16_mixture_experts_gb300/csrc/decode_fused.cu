@@ -7,32 +7,37 @@
 // At decode the layer streams ~2.5 MB of packed weights per active expert
 // and does a few FLOPs per byte, so everything here serves the byte stream:
 //
-//  * One persistent CTA per SM, 8 warps. Each CTA first derives the whole
+//  * One persistent CTA per SM, 16 warps. Each CTA first derives the whole
 //    token-to-expert permutation from topk_ids in shared memory (every CTA
 //    computes the same result), so no separate permute launch sits on the
 //    critical path. Small batches rank each assignment by comparison
 //    (slot = #assignments with a lower expert + #earlier ones with the same
 //    expert); larger ones use a histogram and prefix sum over the experts.
-//  * Work is a list of tasks: gate_up tasks (8 gate rows and the matching 8
-//    up rows of one expert, all of K) then down tasks (32 output rows of one
-//    expert, all of K = I). Each CTA takes a contiguous range of each list and
-//    deals the concatenation round-robin to its warps, so every warp runs its
-//    gate_up tasks before its down tasks.
-//  * A task is streamed as ~10 KB chunks (gate_up: K in pieces of 10 groups,
-//    loaded as two 2-D TMA boxes; down: one 1-D bulk copy) through a 2-stage
-//    shared-memory ring per warp completed on mbarriers, so a warp always has
-//    its next chunk in flight, including the first chunk of its next task.
+//    The first weight copies are issued right after it; the activations are
+//    staged while they fly.
+//  * Work: gate_up tasks (8 gate rows and the matching 8 up rows of one
+//    expert) and down items (16 output rows of one expert, all of K = I).
+//    Each CTA takes a contiguous range of each list. A gate_up task belongs
+//    to one group of 4 warps, which splits its K: warp i of the group takes
+//    chunks i, i+4, ... (a chunk is 5 quantisation groups). The warp that
+//    finishes its part of a task last sums the 4 partial results in shared
+//    memory in a fixed order (deterministic) and publishes h. Down items are
+//    dealt to all 16 warps; every warp runs its gate_up work first.
+//  * Every chunk (~5.5 KB: two 2-D TMA boxes for gate_up, one 1-D bulk copy
+//    for down, plus scales) goes through a 2-stage shared-memory ring per
+//    warp completed on mbarriers, so a warp always has its next chunk in
+//    flight, including the first chunk of its next task or item.
 //  * Weights are dequantised in registers into mma.sync m16n8k16 A fragments
 //    (bf16 holds q in [-8, 7] exactly); each group's fp32 partial sum is
 //    scaled by its bf16 scale, so W = q * scale is never rounded. Tokens are
 //    the N = 8 side. Activations for small T are staged once per CTA in
 //    shared memory, already in fragment order.
-//  * A down task of expert e waits (bounded, acquire) until all gate_up tasks
+//  * A down item of expert e waits (bounded, acquire) until all gate_up tasks
 //    of e have published SiLU(g)*u (bf16, stored in fragment order), then
 //    loads it from L2 into registers.
-//  * The combine is fused: after writing its fp32 down outputs, a down task
-//    counts, per (token, 32-row block), how many of the token's slots are
-//    done; the task that completes a block sums the slots in slot order and
+//  * The combine is fused: after writing its fp32 down outputs, a down item
+//    counts, per (token, 16-row block), how many of the token's slots are
+//    done; the item that completes a block sums the slots in slot order and
 //    writes the bf16 output (in the stack variant: residual + RMS rescale
 //    once the token's last block is done). All counters reset themselves.
 #include "common.cuh"
@@ -40,14 +45,17 @@
 
 namespace moe {
 
-constexpr int kFW = 8;               // warps per CTA
-constexpr int kGC = 10;              // quantisation groups per gate_up chunk
-constexpr int kP2Rows = 32;          // output rows per down task
+constexpr int kFW = 16;              // warps per CTA
+constexpr int kGrp = 4;              // warps that split one gate_up task over K
+constexpr int kNGrp = kFW / kGrp;    // gate_up groups per CTA
+constexpr int kGC = 5;               // quantisation groups per gate_up chunk
+constexpr int kP2Rows = 16;          // output rows per down item
 // Batches of up to 7 tokens. From 8 tokens on, the tensor-core grouped GEMM
 // (prefill.cu) is as fast on GB300 and grows faster (measured: T = 8 at 114
 // us either way, T = 64 at 378 us there against 662 us here).
 constexpr int kDecodeMaxT = 7;
 constexpr int kMaxNT = (kDecodeMaxT + 7) / 8;   // token tiles of 8 per expert
+static_assert(kMaxNT == 1, "the gate_up reduction slots hold one token tile");
 constexpr int kFastN = 256;          // assignments ranked by comparison
 constexpr int kFusedMaxN = 2048;     // T * k
 constexpr int kFusedSmem = 232448 - 512;   // per-block opt-in limit, less static shared memory
@@ -64,9 +72,8 @@ struct FusedParams {
     uint16_t *next;      // bf16 [T][H] stack variant output
     float eps;
     Ctrl *ctrl;
-    uint32_t *done1;     // [E] finished gate_up tasks
-    uint32_t *done2;     // [E] finished down tasks
-    uint32_t *ticket;    // [T][H/32] finished slots per output block
+    uint32_t *done1;     // [E][kCtrStride] finished gate_up tasks (reset by the last CTA to exit)
+    uint32_t *ticket;    // [T][H/16] finished slots per output block
     float *rowss;        // [T] sum of r^2 per token (stack variant)
     uint16_t *hbuf;      // bf16 [T*k][I], fragment order
     float *ybuf;         // f32 [T*k][H]
@@ -75,12 +82,13 @@ struct FusedParams {
     int gcw;             // words per gate_up chunk row (groups per chunk * 16)
     int nkc;             // chunks per gate_up task
     uint32_t stage_bytes;
+    uint32_t red_off;    // offset of the gate_up reduction slots and counters
     uint32_t pro_off;    // offset of the permutation arrays
     uint32_t xs_off;     // offset of the staged activations (0: not staged)
 };
 
 struct FusedLayout {
-    uint32_t stage_bytes, pro_off, xs_off, total;
+    uint32_t stage_bytes, red_off, pro_off, xs_off, total;
     int gcw, nkc;
     bool ok;
 };
@@ -91,7 +99,12 @@ inline uint32_t fused_pro_bytes(const moe_dims &d) {
                       align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
 }
 
-// Shared memory: 2 stages per warp | permutation arrays | staged activations (if they fit).
+// Gate_up partial results: [group][warp of the group][lane][4] f32, then per
+// group a count of finished parts and the number of finalised tasks.
+constexpr uint32_t kRedBytes = kNGrp * kGrp * 32 * 16 + 2 * kNGrp * 4;
+
+// Shared memory: 2 stages per warp | reduction slots | permutation arrays |
+// staged activations (if they fit).
 inline FusedLayout fused_layout(const moe_dims &d) {
     FusedLayout L{};
     const int G1 = d.H / 128, G2 = d.I / 128;
@@ -101,7 +114,8 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
     const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
-    L.pro_off = 2 * kFW * L.stage_bytes;
+    L.red_off = 2 * kFW * L.stage_bytes;
+    L.pro_off = L.red_off + (uint32_t)align_up(kRedBytes, 128);
     // staged activations, then their sum over each 128-wide group (f32 [T][H/128])
     const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2 + (uint32_t)align_up((size_t)d.T * G1 * 4, 16);
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
@@ -181,35 +195,8 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
     const int n = p.T * p.k, E = p.E;
     const bool fast = n <= kFastN && n <= nthr;
 
-    // issue the id loads first, then stage the activations while they fly
     int id_reg = -1;
     if (fast && tid < n) id_reg = p.ids[tid];
-    if (p.xs_off) {
-        // x in fragment order, and per token the sum of each 128-wide group (the
-        // gate_up MMAs run on the biased nibbles 128 + n, see f_gate_up_chunk).
-        // A row holds H/8 chunks, a multiple of 16, so the 16 chunks of a group
-        // sit in 16 consecutive lanes; every lane runs every pass (the count is
-        // rounded up to whole warps) so that the shuffles see the full warp.
-        uint4 *xs = reinterpret_cast<uint4 *>(smem + p.xs_off);
-        float *xsum = reinterpret_cast<float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
-        const int nch = p.T * p.H / 8;
-        const int nch32 = (nch + 31) & ~31;
-        for (int i = tid; i < nch32; i += nthr) {
-            float sum = 0.f;
-            if (i < nch) {
-                const uint4 c = ld_nc_v4(p.x + (size_t)i * 8);
-                xs[i] = make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632),
-                                   __byte_perm(c.y, c.w, 0x5410), __byte_perm(c.y, c.w, 0x7632));
-                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    sum += __uint_as_float(w[m] << 16) + __uint_as_float(w[m] & 0xffff0000u);
-            }
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (i < nch && (lane & 15) == 0) xsum[i / 16] = sum;   // i / 16 = token * (H/128) + group
-        }
-    }
     bool bad = false;
     if (fast) {
         if (tid < n) {
@@ -348,6 +335,50 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
         }
     }
     __syncthreads();
+    if (tid < kNGrp) {
+        reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[tid] = 0;           // parts done
+        reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[kNGrp + tid] = 0;   // tasks finalised
+    }
+    // weight copies will land in the scratch written above (the stage area)
+    fence_proxy_async_smem();
+    __syncthreads();
+}
+
+// After the first weight copies are in flight: the activations in fragment
+// order and their per-group sums (if staged), and the outputs of tokens with
+// no valid slot.
+__device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, const Pro &v) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    if (p.xs_off) {
+        // x arrived row-major (a bulk copy issued at kernel entry); each 16-byte
+        // chunk is rewritten in place in fragment order, and per token the sum
+        // of each 128-wide group is formed (the gate_up MMAs run on the biased
+        // nibbles 128 + n, see f_gate_up_chunk). A row holds H/8 chunks, a
+        // multiple of 16, so the 16 chunks of a group sit in 16 consecutive
+        // lanes; every lane runs every pass (the count is rounded up to whole
+        // warps) so that the shuffles see the full warp.
+        if (!mbar_wait(v.bar + 2 * kFW, 0) && tid == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+        uint4 *xs = reinterpret_cast<uint4 *>(smem + p.xs_off);
+        float *xsum = reinterpret_cast<float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
+        const int nch = p.T * p.H / 8;
+        const int nch32 = (nch + 31) & ~31;
+        for (int i = tid; i < nch32; i += nthr) {
+            float sum = 0.f;
+            if (i < nch) {
+                const uint4 c = xs[i];
+                xs[i] = make_uint4(__byte_perm(c.x, c.z, 0x5410), __byte_perm(c.x, c.z, 0x7632),
+                                   __byte_perm(c.y, c.w, 0x5410), __byte_perm(c.y, c.w, 0x7632));
+                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    sum += __uint_as_float(w[m] << 16) + __uint_as_float(w[m] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (i < nch && (lane & 15) == 0) xsum[i / 16] = sum;   // i / 16 = token * (H/128) + group
+        }
+    }
     // tokens with no valid slot still get an output: zero, or the rescaled residual
     if (blockIdx.x == 0 && warp == 0)
         for (int t = 0; t < p.T; ++t)
@@ -378,25 +409,41 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
 }
 
 // ---- the warp's chunk sequence ------------------------------------------------
-struct Seq {       // position in the warp's list of tasks, and chunk within the task
-    int pos, chunk;
+// A warp's list: its group's gate_up tasks (b1 + grp, b1 + grp + 4, ... within
+// the CTA's range), of each of which it takes the chunks part, part + 4, ...,
+// then its down items (b2 + warp, b2 + warp + 16, ...). Task ids: gate_up
+// tasks 0..n1-1, then down items n1, n1 + 1, ...
+struct Seq {       // position in the warp's list, and chunk (of this warp's share) within it
+    int pos, ci;
 };
 
 struct WarpList {
-    int b1, m1, b2, m2, warp, n1, nkc;
-    // task at list position `pos` of this warp, or -1 past the end
+    int b1, b2, warp, grp, part, n1;
+    int ng;        // gate_up tasks of this warp (0 if it takes no chunk of any)
+    int ncw;       // chunks of each gate_up task that this warp takes
+    int nd;        // down items of this warp
+    __device__ void init(int b1_, int m1, int b2_, int m2, int warp_, int n1_, int nkc) {
+        b1 = b1_;
+        b2 = b2_;
+        warp = warp_;
+        grp = warp_ / kGrp;
+        part = warp_ % kGrp;
+        n1 = n1_;
+        ncw = part < nkc ? (nkc - part + kGrp - 1) / kGrp : 0;
+        ng = (ncw > 0 && grp < m1) ? (m1 - grp + kNGrp - 1) / kNGrp : 0;
+        nd = warp < m2 ? (m2 - warp + kFW - 1) / kFW : 0;
+    }
+    // task at list position `pos`, or -1 past the end
     __device__ int task(int pos) const {
-        const int i = warp + pos * kFW;
-        if (i < m1) return b1 + i;
-        if (i < m1 + m2) return n1 + b2 + (i - m1);
+        if (pos < ng) return b1 + grp + kNGrp * pos;
+        if (pos < ng + nd) return n1 + b2 + warp + kFW * (pos - ng);
         return -1;
     }
+    __device__ int chunk(const Seq &s) const { return part + kGrp * s.ci; }
     __device__ void advance(Seq &s) const {
-        const int tk = task(s.pos);
-        if (++s.chunk >= (tk < n1 ? nkc : 1)) {
-            s.chunk = 0;
-            ++s.pos;
-        }
+        if (s.pos < ng && ++s.ci < ncw) return;
+        s.ci = 0;
+        ++s.pos;
     }
 };
 
@@ -435,8 +482,9 @@ __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int tas
 // (2h+1, 2h+5) for the high ones, so the B fragment of token g is the
 // activation chunk base..base+7 in the order (0,4),(1,5),(2,6),(3,7).
 template <bool kStaged>
-__device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int task, int chunk, const uint8_t *stage,
-                                       const uint8_t *smem, int lane, float (&acc)[kMaxNT][4]) {
+__device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int task, int chunk, bool first,
+                                       const uint8_t *stage, const uint8_t *smem, int lane,
+                                       float (&acc)[kMaxNT][4]) {
     const int tp1 = p.I / 8;
     const int a = task / tp1;
     const int s0 = v.aoff[a], ne = v.acnt[a];
@@ -451,7 +499,7 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
     const uint8_t *ru = stage + 8 * rowb + g * rowb + 16 * tig;
     const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + 16 * rowb);
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    if (chunk == 0) {
+    if (first) {
 #pragma unroll
         for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     }
@@ -460,10 +508,10 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
     // over the group: sum (n - 8) x = sum (128 + n) x - 136 sum x, in fp32
     const float *xsum = reinterpret_cast<const float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
     for (int nt = 0; nt < nt_n; ++nt) {
-        // activation row of the token in column g of this N tile
+        // activation row of the token in column g of this N tile; columns past
+        // ne read the first column's token (always valid) and are never stored
         const int j = 8 * nt + g;
-        const bool vx = j < ne;
-        const int tok = vx ? v.perm[s0 + j] / p.k : 0;
+        const int tok = v.perm[s0 + (j < ne ? j : 8 * nt)] / p.k;
         // group sums of the tokens of the output columns 2tig and 2tig+1 (0 past ne)
         const int j0 = 8 * nt + 2 * tig, j1 = j0 + 1;
         const float *xs0 = j0 < ne ? xsum + (size_t)(v.perm[s0 + j0] / p.k) * G1 : nullptr;
@@ -484,7 +532,7 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
             uint4 X[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                X[m] = vx ? (kStaged ? xb[16 * q + m] : ld_nc_v4(xb + 16 * q + m)) : zero;
+                X[m] = kStaged ? xb[16 * q + m] : ld_nc_v4(xb + 16 * q + m);
                 if (!kStaged)
                     X[m] = make_uint4(__byte_perm(X[m].x, X[m].z, 0x5410), __byte_perm(X[m].x, X[m].z, 0x7632),
                                       __byte_perm(X[m].y, X[m].w, 0x5410), __byte_perm(X[m].y, X[m].w, 0x7632));
@@ -550,23 +598,87 @@ __device__ inline void f_gate_up_store(const FusedParams &p, const Pro &v, int t
         }
 }
 
+// The warp has finished its share of gate_up task `task`, the `n`-th task of
+// its group. Its partial sums go to its slot; the warp that completes the
+// count of the task's nparts parts adds the slots in part order, publishes h
+// and releases the expert's done1 counter. A warp writes its slot for task n
+// only once task n-1 of the group is finalised (its slots read), a bounded
+// wait on the group's count of finalised tasks. Returns false if it gave up.
+__device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *smem, int task, int n, int grp,
+                                   int part, int nparts, int lane, const float (&acc)[kMaxNT][4]) {
+    float4 *slots = reinterpret_cast<float4 *>(smem + p.red_off) + grp * kGrp * 32;
+    int *cnt = reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16) + grp;
+    volatile int *gen = cnt + kNGrp;
+    uint32_t ok = 1;
+    if (lane == 0) {
+        uint32_t i = 0;
+        while (*gen < n)
+            if (++i > kSpinLimit) {
+                ok = 0;
+                set_error(p.ctrl, MOE_ERR_TIMEOUT);
+                break;
+            }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    __threadfence_block();
+    slots[part * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(cnt, 1) + 1 == nparts;
+        if (last) *cnt = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return true;
+    __threadfence_block();
+    float sum[kMaxNT][4];
+    float4 a = slots[lane];
+    sum[0][0] = a.x, sum[0][1] = a.y, sum[0][2] = a.z, sum[0][3] = a.w;
+    for (int q = 1; q < nparts; ++q) {
+        a = slots[q * 32 + lane];
+        sum[0][0] += a.x, sum[0][1] += a.y, sum[0][2] += a.z, sum[0][3] += a.w;
+    }
+    f_gate_up_store(p, v, task, lane, sum);
+    // the warp's h stores are ordered before lane 0's release by the warp barrier
+    __syncwarp();
+    if (lane == 0) {
+        red_release_add_u32(&p.done1[(size_t)v.act[task / (p.I / 8)] * kCtrStride], 1u);
+        __threadfence_block();
+        *gen = n + 1;
+    }
+    return true;
+}
+
 // ---- down + fused combine ----------------------------------------------------
+// Lanes 0..15 own the block's rows.
 __device__ __noinline__ void f_combine_block(const FusedParams &p, const Pro &v, int t, int c, int lane) {
-    const int n = kP2Rows * c + lane;
+    const bool own = lane < kP2Rows;
+    const int n = kP2Rows * c + (own ? lane : 0);
+    // the loads of 8 slots are issued together, then summed in slot order
+    // (an invalid slot adds w * y = 0 * 0, which leaves the sum unchanged)
     float s = 0.f;
-    for (int j = 0; j < p.k; ++j) {
-        const int slot = v.inv[t * p.k + j];
-        if (slot < 0) continue;
-        s += p.topk_w[(size_t)t * p.k + j] * __ldcg(p.ybuf + (size_t)slot * p.H + n);
+    for (int j0 = 0; j0 < p.k; j0 += 8) {
+        float wv[8], yv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            const int slot = j < p.k ? v.inv[t * p.k + j] : -1;
+            wv[u] = slot >= 0 ? p.topk_w[(size_t)t * p.k + j] : 0.f;
+            yv[u] = slot >= 0 ? __ldcg(p.ybuf + (size_t)slot * p.H + n) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += wv[u] * yv[u];
     }
     if (p.out) {
         const __nv_bfloat16 b = __float2bfloat16_rn(s);
-        p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
+        if (own) p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
     } else {
         // stack step: keep r = x + moe(x) and add this block's share of sum(r^2)
         const float r = s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]);
-        p.rbuf[(size_t)t * p.H + n] = r;
-        float ss = r * r;
+        if (own) p.rbuf[(size_t)t * p.H + n] = r;
+        float ss = own ? r * r : 0.f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (lane == 0) atomicAdd(&p.rowss[t], ss);
@@ -628,17 +740,20 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
     const uint32_t rb = p.I / 2;
     const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + kP2Rows * rb);
 
-    // wait until every gate_up task of expert e has published its h
+    // wait until every gate_up task of expert e has published its h (polls
+    // back off from 64 to 512 ns, so that the pollers of an expert leave its
+    // counter's L2 line to the increments)
     uint32_t ok = 1;
     if (lane == 0) {
-        uint32_t i = 0;
-        while (ld_acquire_u32(&p.done1[e]) < (uint32_t)tp1) {
+        uint32_t i = 0, ns = 64;
+        while (ld_acquire_u32(&p.done1[(size_t)e * kCtrStride]) < (uint32_t)tp1) {
             if (++i > kSpinLimit) {
                 ok = 0;
                 set_error(p.ctrl, MOE_ERR_TIMEOUT);
                 break;
             }
-            __nanosleep(32);
+            __nanosleep(ns);
+            if (ns < 512) ns *= 2;
         }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -650,23 +765,14 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
         const int j = np + g;
         const bool valid = j < ne;
         const uint4 *hb = reinterpret_cast<const uint4 *>(p.hbuf + (size_t)(s0 + (valid ? j : 0)) * p.I) + 4 * tig;
-        float acc[2][4];
+        constexpr int kSub = kP2Rows / 16;
+        float acc[kSub][4];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
-        uint4 Yn[4];
+        for (int s = 0; s < kSub; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+        // one group of K: dequantise the rows' words, 8 MMAs against h, scale
+        auto group = [&](int q, const uint4 (&Y)[4]) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) Yn[m] = valid ? ld_cg_v4(hb + m) : zero;
-#pragma unroll 1
-        for (int q = 0; q < G2; ++q) {
-            uint4 Y[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) Y[m] = Yn[m];
-            if (q + 1 < G2) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) Yn[m] = valid ? ld_cg_v4(hb + 16 * (q + 1) + m) : zero;
-            }
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < kSub; ++s) {
                 const int R = 16 * s + g;
                 const uint4 w0 = lds_v4(stage + R * rb + 64 * q + 16 * tig);
                 const uint4 w1 = lds_v4(stage + (R + 8) * rb + 64 * q + 16 * tig);
@@ -687,9 +793,34 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
                 acc[s][2] += s1v * ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2]));
                 acc[s][3] += s1v * ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
             }
+        };
+        // h comes from L2: a ring of 4 groups in registers, the first 4 loaded
+        // before the first MMA and each slot refilled with the group 4 ahead
+        // once it has been used, so the latencies overlap
+        constexpr int kRing = 4, kUnrolled = 8;   // groups handled by the unrolled loop (I <= 1024)
+        uint4 Yr[kRing][4];
+#pragma unroll
+        for (int q = 0; q < kRing; ++q)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) Yr[q][m] = q < G2 ? ld_cg_v4(hb + 16 * q + m) : zero;
+#pragma unroll
+        for (int q = 0; q < kUnrolled; ++q)
+            if (q < G2) {
+                group(q, Yr[q % kRing]);
+                if (q + kRing < kUnrolled && q + kRing < G2) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) Yr[q % kRing][m] = ld_cg_v4(hb + 16 * (q + kRing) + m);
+                }
+            }
+#pragma unroll 1
+        for (int q = kUnrolled; q < G2; ++q) {
+            uint4 Y[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) Y[m] = ld_cg_v4(hb + 16 * q + m);
+            group(q, Y);
         }
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < kSub; ++s)
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const int jj = np + 2 * tig + b;
@@ -701,8 +832,11 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
             }
     }
 
-    // fused combine: count this task's slots per (token, block); complete blocks
-    __threadfence();
+    // fused combine: count this item's slots per (token, block); complete blocks.
+    // The warp barrier orders every lane's y stores before the counting lanes'
+    // acq_rel atomics; the lane that completes a block acquires the other
+    // items' stores, and the warp barrier after the ballot extends that to the
+    // lanes that read them.
     __syncwarp();
     for (int j0 = 0; j0 < ne; j0 += 32) {
         const int j = j0 + lane;
@@ -710,12 +844,12 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
         bool fin = false;
         if (j < ne) {
             t = v.perm[s0 + j] / p.k;
-            const uint32_t old = atomicAdd(&p.ticket[(size_t)t * tp2 + c], 1u);
+            const uint32_t old = atom_acq_rel_add_u32(&p.ticket[(size_t)t * tp2 + c], 1u);
             fin = old + 1 == (uint32_t)v.kv[t];
             if (fin) p.ticket[(size_t)t * tp2 + c] = 0;
         }
         unsigned m = __ballot_sync(0xffffffffu, fin);
-        if (m) __threadfence();
+        __syncwarp();
         while (m) {
             const int src = __ffs(m) - 1;
             m &= m - 1;
@@ -723,15 +857,21 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
             f_combine_block(p, v, tt, c, lane);
         }
     }
-    // the last down task of expert e resets the expert's counters
-    if (lane == 0) {
-        __threadfence();
-        if (atomicAdd(&p.done2[e], 1u) + 1 == (uint32_t)tp2) {
-            p.done1[e] = 0;
-            p.done2[e] = 0;
-        }
-    }
     return true;
+}
+
+// The CTA that exits last (every other CTA has counted itself after all its
+// work) sets the active experts' gate_up counters back to zero for the next
+// call, and the exit count itself.
+__device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atom_acq_rel_add_u32(&p.ctrl->exit_count, 1u) + 1 == gridDim.x;
+    __syncthreads();
+    if (!s_last) return;
+    const int nact = *v.nact;
+    for (int a = threadIdx.x; a < nact; a += blockDim.x) p.done1[(size_t)v.act[a] * kCtrStride] = 0;
+    if (threadIdx.x == 0) p.ctrl->exit_count = 0;
 }
 
 // ---- kernel -----------------------------------------------------------------
@@ -741,20 +881,26 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w1) : "memory");
     const Pro v = pro_views(smem, p);
+    if (p.xs_off && threadIdx.x == 0) {
+        uint64_t *xbar = v.bar + 2 * kFW;
+        // the activations start moving now, behind the permutation
+        const uint32_t xb = (uint32_t)p.T * p.H * 2;
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(xbar, xb);
+        bulk_g2s(smem + p.xs_off, p.x, xb, xbar);
+    }
     fused_prologue(p, smem, v);
 
     const int nact = *v.nact;
     const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
     const int n1 = nact * tp1, n2 = nact * tp2;
     const int C = gridDim.x, cb = blockIdx.x;
+    const int b1 = (int)((long long)n1 * cb / C), m1 = (int)((long long)n1 * (cb + 1) / C) - b1;
+    const int b2 = (int)((long long)n2 * cb / C), m2 = (int)((long long)n2 * (cb + 1) / C) - b2;
     WarpList L;
-    L.b1 = (int)((long long)n1 * cb / C);
-    L.m1 = (int)((long long)n1 * (cb + 1) / C) - L.b1;
-    L.b2 = (int)((long long)n2 * cb / C);
-    L.m2 = (int)((long long)n2 * (cb + 1) / C) - L.b2;
-    L.warp = warp;
-    L.n1 = n1;
-    L.nkc = p.nkc;
+    L.init(b1, m1, b2, m2, warp, n1, p.nkc);
+    const int nparts = p.nkc < kGrp ? p.nkc : kGrp;
     uint8_t *stages = smem + (size_t)warp * 2 * p.stage_bytes;
     uint64_t *bar = v.bar + 2 * warp;
     if (lane == 0) {
@@ -762,15 +908,22 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_init(&bar[1], 1);
     }
     fence_mbar_init();
+    // the stage area served as the prologue's scratch: order those generic
+    // writes before the copies that land there
+    fence_proxy_async_smem();
     __syncwarp();
 
     Seq ahead{0, 0};
+    bool inflight[2] = {false, false};
     for (int s = 0; s < 2; ++s) {
         const int tk = L.task(ahead.pos);
         if (tk < 0) break;
-        f_issue(p, v, tk, ahead.chunk, n1, stages + s * p.stage_bytes, &bar[s], lane);
+        f_issue(p, v, tk, L.chunk(ahead), n1, stages + s * p.stage_bytes, &bar[s], lane);
+        inflight[s] = true;
         L.advance(ahead);
     }
+    fused_stage(p, smem, v);
+
     float acc[kMaxNT][4];
     uint32_t phase[2] = {0u, 0u};
     Seq cur{0, 0};
@@ -778,22 +931,16 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         const int tk = L.task(cur.pos);
         if (tk < 0) break;
         uint8_t *stage = stages + st * p.stage_bytes;
+        inflight[st] = false;
         if (!mbar_wait(&bar[st], phase[st])) {
-            // a copy did not land in time: record it, give the other stage's
-            // copy one more bounded wait, and stop
             if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
-            mbar_wait(&bar[st ^ 1], phase[st ^ 1]);
             break;
         }
         phase[st] ^= 1u;
         if (tk < n1) {
-            f_gate_up_chunk<kStaged>(p, v, tk, cur.chunk, stage, smem, lane, acc);
-            if (cur.chunk == p.nkc - 1) {
-                f_gate_up_store(p, v, tk, lane, acc);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) red_release_add_u32(&p.done1[v.act[tk / tp1]], 1u);
-            }
+            f_gate_up_chunk<kStaged>(p, v, tk, L.chunk(cur), cur.ci == 0, stage, smem, lane, acc);
+            if (cur.ci == L.ncw - 1 && !f_gu_reduce(p, v, smem, tk, cur.pos, L.grp, L.part, nparts, lane, acc))
+                break;
         } else {
             f_down(p, v, tk - n1, stage, lane);
         }
@@ -801,12 +948,19 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         const int nx = L.task(ahead.pos);
         if (nx >= 0) {
             fence_proxy_async_smem();
-            f_issue(p, v, nx, ahead.chunk, n1, stage, &bar[st], lane);
+            f_issue(p, v, nx, L.chunk(ahead), n1, stage, &bar[st], lane);
+            inflight[st] = true;
             L.advance(ahead);
         }
         L.advance(cur);
     }
+    // after an abort: let the copies still in flight land (bounded) before the CTA exits
+    for (int s = 0; s < 2; ++s)
+        if (inflight[s]) mbar_wait(&bar[s], phase[s]);
+    if (p.xs_off && threadIdx.x == 0)   // complete already, unless its wait gave up
+        mbar_wait(pro_views(smem, p).bar + 2 * kFW, 0);
     if (!p.out) f_stack_rows(p);
+    f_exit(p, v);
 }
 
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
@@ -830,7 +984,6 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.eps = eps;
     p.ctrl = ws_at<Ctrl>(ws, W.ctrl);
     p.done1 = ws_at<uint32_t>(ws, W.done1);
-    p.done2 = ws_at<uint32_t>(ws, W.done2);
     p.ticket = ws_at<uint32_t>(ws, W.ticket);
     p.rowss = ws_at<float>(ws, W.rowss);
     p.hbuf = ws_at<uint16_t>(ws, W.hbuf);
@@ -844,6 +997,7 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.gcw = L.gcw;
     p.nkc = L.nkc;
     p.stage_bytes = L.stage_bytes;
+    p.red_off = L.red_off;
     p.pro_off = L.pro_off;
     p.xs_off = L.xs_off;
 
@@ -853,8 +1007,10 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     err = set_smem_once(fn, kFusedSmem);
     if (err != cudaSuccess) return err;
     const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
-    const long long max_tasks = max_active * (d.I / 8 + d.H / kP2Rows);
-    long long grid = (max_tasks + kFW - 1) / kFW;
+    // enough CTAs that every group has a gate_up task and every warp a down item
+    const long long g1 = (max_active * (d.I / 8) + kNGrp - 1) / kNGrp;
+    const long long g2 = (max_active * (d.H / kP2Rows) + kFW - 1) / kFW;
+    long long grid = g1 > g2 ? g1 : g2;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};

@@ -95,7 +95,7 @@ extern "C" int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *
     cudaError_t err = static_scratch(&ws);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // done1, done2, ticket and rowss are adjacent in the layout; rbuf follows.
+    // done1, ticket and rowss are adjacent in the layout; rbuf follows.
     const WsLayout W = ws_layout(d);
     err = cudaMemsetAsync(ws_at<char>(ws, W.done1), 0, W.rbuf - W.done1, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t *__restrict_
         offsets[e] = off;
         for (int c = 0; c < nchunk; ++c) chunk[(size_t)c * E + e] += off;
         if (total > 0) active[act] = e;
-        done1[e] = 0;
+        done1[(size_t)e * kCtrStride] = 0;
     }
     __syncthreads();
     if (e == 0) {

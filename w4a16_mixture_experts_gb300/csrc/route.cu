@@ -23,10 +23,8 @@ namespace moe {
 // second), the same physical-K assignment being used for A and B, so the dot
 // product is unchanged. Grid: (ceil(E/64), ksplit, ceil(T/(8*NT))), 4 warps.
 template <int NT>
-__global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__restrict__ x,
-                                                           const uint16_t *__restrict__ wr,
-                                                           float *__restrict__ partial, int T, int H,
-                                                           int E) {
+__device__ __forceinline__ void route_logits_tile(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
+                                                  float *__restrict__ partial, int T, int H, int E) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
     const int ksplit = gridDim.y, kb = blockIdx.y;
@@ -82,6 +80,13 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__res
     }
 }
 
+template <int NT>
+__global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__restrict__ x,
+                                                           const uint16_t *__restrict__ wr,
+                                                           float *__restrict__ partial, int T, int H, int E) {
+    route_logits_tile<NT>(x, wr, partial, T, H, E);
+}
+
 // Order-preserving map of an fp32 value onto uint32.
 __device__ inline uint32_t f32_order_key(float v) {
     const uint32_t u = __float_as_uint(v);
@@ -109,6 +114,37 @@ __device__ inline uint64_t warp_max_key(uint64_t m) {
     return ((uint64_t)hi << 32) | lo;
 }
 
+// k rounds of warp max over the keys the lanes hold; lane j < k ends with the
+// j-th largest. Writes ids and the softmax over the selected logits.
+__device__ inline void warp_topk_write(uint64_t (&key)[kTopkPer], int nper, int k, int lane, int32_t *ids_row,
+                                       float *w_row) {
+    uint64_t mine = 0;
+    for (int j = 0; j < k; ++j) {
+        uint64_t m = 0;
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i)
+            if (i < nper) m = key[i] > m ? key[i] : m;
+        m = warp_max_key(m);
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+        if (lane == j) mine = m;
+    }
+    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
+    const float l = f32_from_order_key((uint32_t)(mine >> 32));
+    const float p = lane < k ? expf(l - lmax) : 0.f;
+    float z = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane < k) {
+        ids_row[lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+        w_row[lane] = p / z;
+    }
+}
+
+__device__ inline uint64_t topk_key(float logit, int e) {
+    return ((uint64_t)f32_order_key(logit) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+}
+
 __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float *__restrict__ partial, int ksplit,
                                                                      const float *__restrict__ bias, int T, int E,
                                                                      int k, int32_t *__restrict__ ids,
@@ -128,31 +164,10 @@ __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float
             for (int s = 0; s < kMaxKsplit; ++s)
                 if (s < ksplit) l += partial[((size_t)s * T + t) * E + e];
             if (bias) l += bias[e];
-            key[i] = ((uint64_t)f32_order_key(l) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+            key[i] = topk_key(l, e);
         }
     }
-    const int nper = (E + 31) / 32;   // keys a lane may hold
-    uint64_t mine = 0;
-    for (int j = 0; j < k; ++j) {
-        uint64_t m = 0;
-#pragma unroll
-        for (int i = 0; i < kTopkPer; ++i)
-            if (i < nper) m = key[i] > m ? key[i] : m;
-        m = warp_max_key(m);
-#pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
-        if (lane == j) mine = m;
-    }
-    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
-    const float l = f32_from_order_key((uint32_t)(mine >> 32));
-    const float p = lane < k ? expf(l - lmax) : 0.f;
-    float z = p;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane < k) {
-        ids[(size_t)t * k + lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
-        w[(size_t)t * k + lane] = p / z;
-    }
+    warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
 }
 
 // Small batches: one CTA of 256 threads per token, so that the K-split partial
@@ -176,9 +191,11 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const floa
         const int e = threadIdx.x + kTopkThreads * i;
         if (e < E) {
             float l = 0.f;
-            for (int s = 0; s < ksplit; ++s) l += partial[((size_t)s * T + t) * E + e];
+#pragma unroll
+            for (int s = 0; s < kMaxKsplit; ++s)
+                if (s < ksplit) l += partial[((size_t)s * T + t) * E + e];
             if (bias) l += bias[e];
-            key[i] = ((uint64_t)f32_order_key(l) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+            key[i] = topk_key(l, e);
         }
     }
     for (int j = 0; j < k; ++j) {
@@ -218,6 +235,59 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const floa
     }
 }
 
+// Small batches: logits and top-k in one launch. Every CTA writes its partial
+// logits as route_logits_kernel does, fences them and counts itself on the
+// control block's ticket. The CTA that completes the count sees every other
+// CTA's writes; it sums the K splits of all T x E logits into shared memory
+// (its 128 threads, split loads unrolled so they are in flight together),
+// then warp w selects for tokens w, w + 4, ... and the ticket is reset for
+// the next launch.
+constexpr int kRouteInlineMaxT = 8;
+
+template <int NT>
+__global__ void __launch_bounds__(128) route_small_kernel(const uint16_t *__restrict__ x,
+                                                          const uint16_t *__restrict__ wr,
+                                                          float *__restrict__ partial, int T, int H, int E,
+                                                          const float *__restrict__ bias, int k,
+                                                          int32_t *__restrict__ ids, float *__restrict__ w,
+                                                          Ctrl *ctrl) {
+    extern __shared__ float s_logit[];   // [T][E]
+    __shared__ bool s_last;
+    route_logits_tile<NT>(x, wr, partial, T, H, E);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(&ctrl->route_ticket, 1u) + 1 == gridDim.x * gridDim.y * gridDim.z;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int ksplit = gridDim.y;
+    const size_t plane = (size_t)T * E;
+    for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
+        float part[kMaxKsplit];
+#pragma unroll
+        for (int s = 0; s < kMaxKsplit; ++s) part[s] = s < ksplit ? __ldcg(partial + s * plane + i) : 0.f;
+        float l = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxKsplit; ++s)
+            if (s < ksplit) l += part[s];
+        if (bias) l += bias[i % E];
+        s_logit[i] = l;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < T; t += blockDim.x / 32) {
+        uint64_t key[kTopkPer];
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i) {
+            const int e = lane + 32 * i;
+            key[i] = e < E ? topk_key(s_logit[t * E + e], e) : 0;
+        }
+        warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+    }
+    if (threadIdx.x == 0) ctrl->route_ticket = 0;
+}
+
 cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
                          int32_t *ids, float *w, void *ws, cudaStream_t s) {
     const WsLayout L = ws_layout(d);
@@ -239,6 +309,12 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     int nt = 1;
     while (8 * nt < tt) nt <<= 1;
     dim3 grid((d.E + 63) / 64, ksplit, (d.T + 8 * nt - 1) / (8 * nt));
+    if (d.T <= kRouteInlineMaxT) {
+        const size_t smem = (size_t)d.T * d.E * sizeof(float);
+        route_small_kernel<1><<<grid, 128, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k, ids, w,
+                                                      ws_at<Ctrl>(ws, L.ctrl));
+        return cudaGetLastError();
+    }
     switch (nt) {
         case 1: route_logits_kernel<1><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
         case 2: route_logits_kernel<2><<<grid, 128, 0, s>>>(x, wr, partial, d.T, d.H, d.E); break;
