@@ -13,13 +13,16 @@ Prints one JSON line. Workloads (shapes from "Running 125B MoE on Three
 decode64, prefill512 (Zipf-skewed routing), stack_prefill4096 and
 stack_decode4 (48 layers).
 
-Timing: inputs resident in HBM; each step is a CUDA-graph replay; steps
-rotate over independent weight sets so that no step finds its experts in L2
-(their total exceeds the 129 MB L2); CUDA events on the launching stream;
->= 3 warm-up steps. The expert kernel's own time is taken from events that
-the library records around it inside the same graphs. `e2e` repeats the
-timing through the same public calls with the step's tokens copied in from
-pinned host memory and its output copied back, inside the timed region.
+Timing: inputs resident in HBM; steps rotate over independent weight sets so
+that no step finds its experts in L2 (their total exceeds the 129 MB L2); a
+CUDA graph holds one pass over the sets (consecutive steps, as consecutive
+layers of a model run), and K steps are whole replays plus one graph of the
+remainder; CUDA events on the launching stream; >= 3 warm-up steps. The
+expert kernel's own time is taken from events that the library records
+around it in separate one-step graphs, replayed after the timed region.
+`e2e` repeats the timing through the same public calls with every step's
+tokens copied in from pinned host memory and its output copied back, inside
+the timed region.
 The CPU baseline is the fp64 oracle on a bounded sample of the workload.
 Multi-GPU: independent replicas (the layer has no exchange step).
 """
@@ -305,29 +308,66 @@ def run_ours(args, rank, world, local):
                 x = act[l % 2]
         assert moe.moe_check_device_error(ws, stream) == 0
 
-        graphs = []
+        # Timed graphs hold consecutive steps over the weight sets (like consecutive
+        # layers of a model) with no profiling nodes; K steps = full replays plus one
+        # graph of the remainder. Separate one-step graphs with the library's events
+        # around the expert kernel give its duration. The e2e graphs add, to every
+        # step, the copy of its tokens from pinned host memory and of its output back.
+        n_in = 1 if stack else nsets
+        h_in = [(x0 if stack else sets[i]["hidden"]).cpu().pin_memory() for i in range(n_in)]
+        h_out = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(n_in)]
+        dst_in = [x0 if stack else sets[i]["hidden"] for i in range(n_in)]
+        final = act[(wl.layers - 1) % 2] if stack else out
+
+        def enqueue(seq, profile=False, e2e=False):
+            for i in seq:
+                if e2e:
+                    dst_in[i].copy_(h_in[i], non_blocking=True)
+                step(i, profile=profile)
+                if e2e:
+                    h_out[i].copy_(final, non_blocking=True)
+            if profile:
+                moe.moe_profile_events(None, None)
+
         use_graph = not args.no_graph
+        per = n_in                      # steps per full graph
+        rem = args.steps % per
+        G = {}
         if use_graph:
             try:
-                for i in range(1 if stack else nsets):
+                for key, seq, prof, e2e in [("all", range(per), False, False), ("rem", range(rem), False, False),
+                                            ("e2e_all", range(per), False, True), ("e2e_rem", range(rem), False, True)] + \
+                                           [("prof%d" % i, [i], True, False) for i in range(per)]:
+                    if len(seq) == 0:
+                        continue
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=stream):
-                        step(i, profile=True)
-                    graphs.append(g)
-                moe.moe_profile_events(None, None)
-            except Exception as exc:  # capture not possible: time eagerly
+                        enqueue(seq, profile=prof, e2e=e2e)
+                    G[key] = g
+            except Exception as exc:  # capture not possible: time eager launches
                 moe.moe_profile_events(None, None)
                 print("graph capture failed (%s); timing eager launches" % exc, file=sys.stderr)
-                graphs, use_graph = [], False
+                G, use_graph = {}, False
 
-        def replay(i):
+        def run_steps(nsteps, e2e=False):
+            """Exactly nsteps steps, set i % per for step i."""
             if use_graph:
-                graphs[0 if stack else i % nsets].replay()
+                pre = "e2e_" if e2e else ""
+                for _ in range(nsteps // per):
+                    G[pre + "all"].replay()
+                if nsteps % per:
+                    assert nsteps % per == rem
+                    G[pre + "rem"].replay()
             else:
-                step(i % nsets, profile=True)
+                for i in range(nsteps):
+                    enqueue([i % per], e2e=e2e)
 
-        for i in range(args.warmup):
-            replay(i)
+        # warm-up: at least W untimed steps, in whole graphs
+        for _ in range(-(-max(args.warmup, 1) // per)):
+            if use_graph:
+                G["all"].replay()
+            else:
+                enqueue(range(per))
         stream.synchronize()
         barrier(world)
 
@@ -336,56 +376,46 @@ def run_ours(args, rank, world, local):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for i in range(args.steps):
-            replay(i)
+        run_steps(args.steps)
         t1.record(stream)
         stream.synchronize()
         ms = t0.elapsed_time(t1)
         clk = clocks.stop()
-        moe.moe_profile_events(None, None)
         assert moe.moe_check_device_error(ws, stream) == 0
 
-        # expert kernel durations of the last replay of each graph
+        # expert kernel durations: each set's profiled step once, in rotation
+        # (so no set finds its experts in L2), after the timed region
+        for i in range(per):
+            if use_graph:
+                G["prof%d" % i].replay()
+            else:
+                enqueue([i], profile=True)
+        stream.synchronize()
         if stack:
             durs = [ev_b[l].elapsed_time(ev_a[l]) for l in range(wl.layers)]
             bytes_l = [u * EXPERT_BYTES for u in unique]
         else:
-            m = min(args.steps, nsets)
-            last = [(args.steps - 1 - j) % nsets for j in range(m)]
-            durs = [ev_b[i].elapsed_time(ev_a[i]) for i in last]
-            bytes_l = [unique[i] * EXPERT_BYTES for i in last]
+            durs = [ev_b[i].elapsed_time(ev_a[i]) for i in range(per)]
+            bytes_l = [unique[i] * EXPERT_BYTES for i in range(per)]
 
-        # end to end: tokens in from pinned host memory, output back, every step
-        h_in = [sets[i % nsets]["hidden"].cpu().pin_memory() if not stack else x0.cpu().pin_memory()
-                for i in range(1 if stack else nsets)]
-        h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-        dst_in = [x0 if stack else sets[i]["hidden"] for i in range(1 if stack else nsets)]
-        final = act[(wl.layers - 1) % 2] if stack else out
+        # end to end through the same calls, with the host copies inside the timed region
+        run_steps(per, e2e=True)
+        stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        for i in range(3):
-            j = 0 if stack else i % nsets
-            dst_in[j].copy_(h_in[j], non_blocking=True)
-            replay(i)
-            h_out.copy_(final, non_blocking=True)
-        stream.synchronize()
         e0.record(stream)
-        for i in range(args.steps):
-            j = 0 if stack else i % nsets
-            dst_in[j].copy_(h_in[j], non_blocking=True)
-            replay(i)
-            h_out.copy_(final, non_blocking=True)
+        run_steps(args.steps, e2e=True)
         e1.record(stream)
         stream.synchronize()
         ms_e2e = e0.elapsed_time(e1)
 
     ms = max_over_ranks(ms, world)
     ms_e2e = max_over_ranks(ms_e2e, world)
-    # route: logits + top-k; forward: one fused kernel (the library's decode path,
-    # T <= 7) or permute 3 + x gather + chunk scan + chunk table + gate_up + down +
-    # convert
+    # route: one kernel for T <= 8 (logits, then top-k in the last CTA), else logits +
+    # top-k; forward: one fused kernel (the library's decode path, T <= 7) or permute 3
+    # + x gather + chunk scan + chunk table + gate_up + down + convert
     fused = T <= FUSED_MAX_T
-    launches_per_layer = 2 + (1 if fused else 9)
+    launches_per_layer = (1 if T <= 8 else 2) + (1 if fused else 9)
     pk, pk_src = peaks()
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
     flops_launch = 2.0 * 3 * H * I * T * k           # algorithmic: gate, up and down over all slots
@@ -422,7 +452,8 @@ def run_ours(args, rank, world, local):
                    "zipf": wl.zipf, "weight_sets": nsets,
                    "l2": "rotating %d independent weight sets (> L2) between steps" % nsets
                    if not stack else "48 layers x 1.3 GB of weights per step (> L2)",
-                   "graph": use_graph, "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "graph": use_graph, "steps_per_graph": per if use_graph else 1,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": world * T * args.steps / (ms_e2e * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},

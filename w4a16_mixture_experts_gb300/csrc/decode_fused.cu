@@ -95,7 +95,8 @@ struct FusedLayout {
 
 inline uint32_t fused_pro_bytes(const moe_dims &d) {
     const size_t n = (size_t)d.T * d.k;
-    return (uint32_t)(align_up(n * 2, 16) * 3 + align_up(d.E * 4, 16) + align_up((d.E + 1) * 2, 16) +
+    return (uint32_t)(align_up(n * 2, 16) * 3 + align_up((d.E > kFastN ? d.E : kFastN) * 4, 16) +
+                      align_up((d.E + 1) * 2, 16) +
                       align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
 }
 
@@ -132,7 +133,7 @@ bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
 
 struct Pro {   // permutation arrays in shared memory
     int16_t *ids, *perm, *inv;
-    int32_t *cnt;
+    int32_t *cnt;   // per-expert counts (large batches) or per-assignment lead flags (small)
     int16_t *offs, *act, *aoff, *acnt, *kv;
     uint64_t *bar;
     int *nact;
@@ -146,7 +147,7 @@ __device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
     v.ids = reinterpret_cast<int16_t *>(take(n * 2));
     v.perm = reinterpret_cast<int16_t *>(take(n * 2));
     v.inv = reinterpret_cast<int16_t *>(take(n * 2));
-    v.cnt = reinterpret_cast<int32_t *>(take(p.E * 4));
+    v.cnt = reinterpret_cast<int32_t *>(take((p.E > kFastN ? p.E : kFastN) * 4));
     v.offs = reinterpret_cast<int16_t *>(take((p.E + 1) * 2));
     v.act = reinterpret_cast<int16_t *>(take(p.E * 2));
     v.aoff = reinterpret_cast<int16_t *>(take(p.E * 2));
@@ -187,7 +188,8 @@ __device__ inline int cta_exclusive_scan(int v, int *warp_sums, int *total) {
 
 // The stable permutation, in every CTA: the slot of assignment a is
 // #{valid a' with a lower expert} + #{a' < a with the same expert}.
-__device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v) {
+// Small batches: id_reg is thread a's id, already loaded by the caller.
+__device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v, int id_reg) {
     __shared__ int warp_sums[kFW];
     __shared__ int total, nact_s;
     const int tid = threadIdx.x, nthr = blockDim.x;
@@ -195,8 +197,6 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
     const int n = p.T * p.k, E = p.E;
     const bool fast = n <= kFastN && n <= nthr;
 
-    int id_reg = -1;
-    if (fast && tid < n) id_reg = p.ids[tid];
     bool bad = false;
     if (fast) {
         if (tid < n) {
@@ -226,7 +226,7 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
     }
 
     if (fast) {
-        int32_t *is_lead = reinterpret_cast<int32_t *>(smem);   // scratch in the stage area
+        int32_t *is_lead = v.cnt;
         const int a = tid;
         int e = -1, cl = 0, rk = 0, ct = 0;
         if (a < n) {
@@ -339,14 +339,13 @@ __device__ __noinline__ void fused_prologue(const FusedParams &p, uint8_t *smem,
         reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[tid] = 0;           // parts done
         reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[kNGrp + tid] = 0;   // tasks finalised
     }
-    // weight copies will land in the scratch written above (the stage area)
-    fence_proxy_async_smem();
+    // large batches used the stage area as scratch, where weight copies will land
+    if (!fast) fence_proxy_async_smem();
     __syncthreads();
 }
 
-// After the first weight copies are in flight: the activations in fragment
-// order and their per-group sums (if staged), and the outputs of tokens with
-// no valid slot.
+// After the permutation: the activations in fragment order and their
+// per-group sums (if staged), and the outputs of tokens with no valid slot.
 __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, const Pro &v) {
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -880,6 +879,9 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w1) : "memory");
+    // the ids are the first thing every path needs
+    int id_reg = -1;
+    if (p.T * p.k <= kFastN && (int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
     const Pro v = pro_views(smem, p);
     if (p.xs_off && threadIdx.x == 0) {
         uint64_t *xbar = v.bar + 2 * kFW;
@@ -890,7 +892,9 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_arrive_expect_tx(xbar, xb);
         bulk_g2s(smem + p.xs_off, p.x, xb, xbar);
     }
-    fused_prologue(p, smem, v);
+    fused_prologue(p, smem, v, id_reg);
+    // the activations, converted while no warp is held by its copies yet
+    fused_stage(p, smem, v);
 
     const int nact = *v.nact;
     const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
@@ -908,9 +912,6 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_init(&bar[1], 1);
     }
     fence_mbar_init();
-    // the stage area served as the prologue's scratch: order those generic
-    // writes before the copies that land there
-    fence_proxy_async_smem();
     __syncwarp();
 
     Seq ahead{0, 0};
@@ -922,7 +923,6 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         inflight[s] = true;
         L.advance(ahead);
     }
-    fused_stage(p, smem, v);
 
     float acc[kMaxNT][4];
     uint32_t phase[2] = {0u, 0u};

@@ -114,19 +114,47 @@ __device__ inline uint64_t warp_max_key(uint64_t m) {
     return ((uint64_t)hi << 32) | lo;
 }
 
-// k rounds of warp max over the keys the lanes hold; lane j < k ends with the
-// j-th largest. Writes ids and the softmax over the selected logits.
+// Sorts the first N keys of a lane in descending order (bitonic network; all
+// indices are compile-time, so the keys stay in registers).
+template <int N>
+__device__ inline void sort_desc(uint64_t (&key)[kTopkPer]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size / 2; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int l = i ^ stride;
+                if (l > i) {
+                    const bool up = (i & size) != 0;   // this pair ends ascending
+                    const uint64_t a = key[i], b = key[l];
+                    if (up ? a > b : a < b) {
+                        key[i] = b;
+                        key[l] = a;
+                    }
+                }
+            }
+}
+
+// The k largest keys over the warp: every lane sorts its keys, then each round
+// takes the warp maximum of the lanes' heads and the lane that held it moves
+// to its next key; lane j < k ends with the j-th largest. Writes ids and the
+// softmax over the selected logits.
 __device__ inline void warp_topk_write(uint64_t (&key)[kTopkPer], int nper, int k, int lane, int32_t *ids_row,
                                        float *w_row) {
+    constexpr int kHalf = kTopkPer / 2;
+    if (nper <= kHalf)
+        sort_desc<kHalf>(key);
+    else
+        sort_desc<kTopkPer>(key);
     uint64_t mine = 0;
     for (int j = 0; j < k; ++j) {
-        uint64_t m = 0;
+        const uint64_t m = warp_max_key(key[0]);
+        if (key[0] == m) {   // keys are unique: one lane
 #pragma unroll
-        for (int i = 0; i < kTopkPer; ++i)
-            if (i < nper) m = key[i] > m ? key[i] : m;
-        m = warp_max_key(m);
-#pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) key[i] = key[i] == m ? 0 : key[i];
+            for (int i = 0; i + 1 < kTopkPer; ++i) key[i] = key[i + 1];
+            key[kTopkPer - 1] = 0;
+        }
         if (lane == j) mine = m;
     }
     const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
@@ -235,53 +263,100 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const floa
     }
 }
 
-// Small batches: logits and top-k in one launch. Every CTA writes its partial
-// logits as route_logits_kernel does, fences them and counts itself on the
-// control block's ticket. The CTA that completes the count sees every other
-// CTA's writes; it sums the K splits of all T x E logits into shared memory
-// (its 128 threads, split loads unrolled so they are in flight together),
-// then warp w selects for tokens w, w + 4, ... and the ticket is reset for
-// the next launch.
+// Small batches (T <= 8): logits and top-k in one launch, no K split. Warp w
+// of CTA b computes the logits of expert 4b + w for every token: each lane
+// issues all of its 16-byte loads of the router row (8 columns per load, 256
+// columns per pass of the warp, kRouteLoads passes at once) before any
+// arithmetic, then runs fp32 FMAs against each token's activations and the
+// warp sums its lanes. Logits (with the bias) go to partial[0]. Each CTA then
+// counts itself on the control block's ticket (release); the CTA that
+// completes the count acquires every other CTA's logits, loads all T x E of
+// them at once into shared memory, and warp w selects for tokens w, w + 4, ...
+// The ticket is reset for the next launch.
 constexpr int kRouteInlineMaxT = 8;
+constexpr int kRouteLoads = 10;   // 16-byte loads per lane in flight (H <= 2560 in one pass)
 
-template <int NT>
 __global__ void __launch_bounds__(128) route_small_kernel(const uint16_t *__restrict__ x,
                                                           const uint16_t *__restrict__ wr,
-                                                          float *__restrict__ partial, int T, int H, int E,
+                                                          float *__restrict__ logits, int T, int H, int E,
                                                           const float *__restrict__ bias, int k,
                                                           int32_t *__restrict__ ids, float *__restrict__ w,
                                                           Ctrl *ctrl) {
     extern __shared__ float s_logit[];   // [T][E]
-    __shared__ bool s_last;
-    route_logits_tile<NT>(x, wr, partial, T, H, E);
-    __threadfence();
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 4 + warp;
+    if (e < E) {
+        float acc[kRouteInlineMaxT];
+#pragma unroll
+        for (int t = 0; t < kRouteInlineMaxT; ++t) acc[t] = 0.f;
+        const uint16_t *row = wr + (size_t)e * H;
+        for (int c0 = 0; c0 < H; c0 += 256 * kRouteLoads) {
+            uint4 wv[kRouteLoads];
+#pragma unroll
+            for (int i = 0; i < kRouteLoads; ++i) {
+                const int c = c0 + 256 * i + 8 * lane;
+                wv[i] = c < H ? ld_nc_v4(row + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int t = 0; t < kRouteInlineMaxT; ++t) {
+                if (t >= T) break;
+                const uint16_t *xr = x + (size_t)t * H;
+                // the token's loads are all issued before its FMAs
+                uint4 xv[kRouteLoads];
+#pragma unroll
+                for (int i = 0; i < kRouteLoads; ++i) {
+                    const int c = c0 + 256 * i + 8 * lane;
+                    xv[i] = c < H ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int i = 0; i < kRouteLoads; ++i) {
+                    const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+                    const uint32_t xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[t] = fmaf(__uint_as_float(ww[j] << 16), __uint_as_float(xx[j] << 16), acc[t]);
+                        acc[t] = fmaf(__uint_as_float(ww[j] & 0xffff0000u), __uint_as_float(xx[j] & 0xffff0000u), acc[t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouteInlineMaxT; ++t) {
+            if (t >= T) break;
+            float v = acc[t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) logits[(size_t)t * E + e] = bias ? v + bias[e] : v;
+        }
+    }
+    // the CTA barrier orders every warp's logit stores before thread 0's release
     __syncthreads();
-    if (threadIdx.x == 0)
-        s_last = atomicAdd(&ctrl->route_ticket, 1u) + 1 == gridDim.x * gridDim.y * gridDim.z;
+    if (threadIdx.x == 0) s_last = atom_acq_rel_add_u32(&ctrl->route_ticket, 1u) + 1 == gridDim.x;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    const int ksplit = gridDim.y;
-    const size_t plane = (size_t)T * E;
-    for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
-        float part[kMaxKsplit];
+    // the last CTA: all logits at once (8 loads per thread in flight), then top-k
+    const int n = T * E;
+    for (int i0 = 0; i0 < n; i0 += 8 * blockDim.x) {
+        float lv[8];
 #pragma unroll
-        for (int s = 0; s < kMaxKsplit; ++s) part[s] = s < ksplit ? __ldcg(partial + s * plane + i) : 0.f;
-        float l = 0.f;
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x + threadIdx.x;
+            lv[u] = i < n ? __ldcg(logits + i) : 0.f;
+        }
 #pragma unroll
-        for (int s = 0; s < kMaxKsplit; ++s)
-            if (s < ksplit) l += part[s];
-        if (bias) l += bias[i % E];
-        s_logit[i] = l;
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x + threadIdx.x;
+            if (i < n) s_logit[i] = lv[u];
+        }
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = warp; t < T; t += blockDim.x / 32) {
         uint64_t key[kTopkPer];
 #pragma unroll
         for (int i = 0; i < kTopkPer; ++i) {
-            const int e = lane + 32 * i;
-            key[i] = e < E ? topk_key(s_logit[t * E + e], e) : 0;
+            const int ee = lane + 32 * i;
+            key[i] = ee < E ? topk_key(s_logit[t * E + ee], ee) : 0;
         }
         warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
     }
@@ -311,8 +386,8 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     dim3 grid((d.E + 63) / 64, ksplit, (d.T + 8 * nt - 1) / (8 * nt));
     if (d.T <= kRouteInlineMaxT) {
         const size_t smem = (size_t)d.T * d.E * sizeof(float);
-        route_small_kernel<1><<<grid, 128, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k, ids, w,
-                                                      ws_at<Ctrl>(ws, L.ctrl));
+        route_small_kernel<<<(d.E + 3) / 4, 128, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k, ids, w,
+                                                             ws_at<Ctrl>(ws, L.ctrl));
         return cudaGetLastError();
     }
     switch (nt) {
