@@ -249,14 +249,19 @@ def test_forward_layer_end_to_end_decode():
     (17, 256, 8, 8, 128),       # every expert active, k == E
     (3, 1024, 1024, 32, 128),   # E and k at their maxima
     (40, 256, 4, 2, 384),       # many tokens on few experts (several N passes)
+    (7, 3072, 64, 8, 256),      # decode: gate_up chunks split unevenly over a group, several tasks each
+    (2, 8064, 16, 4, 128),      # decode: H at its maximum (16 chunks per gate_up task)
 ])
 def test_forward_edge_shapes(T, H, E, k, I):
     seed = T + H + E
     x = synth.hidden(T, H, seed=seed)
     wts = synth.expert_weights(E, H, I, seed=seed)
     ids, w = synth.random_topk(T, E, k, seed=seed)
+    ws = moe.workspace(T, H, E, k, I)
     out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *(wts[n].cuda() for n in
-                                ("w1_packed", "w1_scales", "w2_packed", "w2_scales")))
+                                ("w1_packed", "w1_scales", "w2_packed", "w2_scales")), ws=ws)
+    # no bounded wait may have given up, and no id was out of range
+    assert moe.moe_check_device_error(ws) == 0
     ref = oracle.expert_forward(x, ids, w, wts["w1_packed"], wts["w1_scales"], wts["w2_packed"],
                                 wts["w2_scales"], E, I)
     assert_close(out.float().cpu().numpy(), ref, "T=%d H=%d E=%d k=%d I=%d" % (T, H, E, k, I))

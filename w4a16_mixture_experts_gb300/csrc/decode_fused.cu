@@ -45,10 +45,13 @@
 
 namespace moe {
 
-constexpr int kFW = 16;              // warps per CTA
-constexpr int kGrp = 4;              // warps that split one gate_up task over K
-constexpr int kNGrp = kFW / kGrp;    // gate_up groups per CTA
-constexpr int kGC = 5;               // quantisation groups per gate_up chunk
+constexpr int kFW = 16;              // warps per CTA: kCons consumers, then the producer
+constexpr int kCons = 15;            // warps that compute
+constexpr int kProd = kCons;         // the warp that issues every weight copy
+constexpr int kGrp = 5;              // consumers that split one gate_up task over K
+constexpr int kNGrp = kCons / kGrp;  // gate_up groups per CTA
+constexpr int kGC = 4;               // quantisation groups per gate_up chunk
+constexpr int kStages = 2;           // ring stages per consumer
 constexpr int kP2Rows = 16;          // output rows per down item
 // Batches of up to 7 tokens. From 8 tokens on, the tensor-core grouped GEMM
 // (prefill.cu) is as fast on GB300 and grows faster (measured: T = 8 at 114
@@ -100,12 +103,14 @@ inline uint32_t fused_pro_bytes(const moe_dims &d) {
                       align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
 }
 
-// Gate_up partial results: [group][warp of the group][lane][4] f32, then per
-// group a count of finished parts and the number of finalised tasks.
-constexpr uint32_t kRedBytes = kNGrp * kGrp * 32 * 16 + 2 * kNGrp * 4;
+// Gate_up partial results: [group][task parity][warp of the group][lane][4]
+// f32, then per group and parity a count of finished parts and of finalised
+// tasks.
+constexpr uint32_t kRedSlotBytes = kNGrp * 2 * kGrp * 32 * 16;   // [group][task parity][part][lane] float4
+constexpr uint32_t kRedBytes = kRedSlotBytes + 4 * kNGrp * 4;       // + parts done, tasks finalised [group][parity]
 
-// Shared memory: 2 stages per warp | reduction slots | permutation arrays |
-// staged activations (if they fit).
+// Shared memory: kStages stages per consumer | reduction slots | permutation
+// arrays | staged activations (if they fit).
 inline FusedLayout fused_layout(const moe_dims &d) {
     FusedLayout L{};
     const int G1 = d.H / 128, G2 = d.I / 128;
@@ -115,7 +120,7 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
     const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
-    L.red_off = 2 * kFW * L.stage_bytes;
+    L.red_off = kStages * kCons * L.stage_bytes;
     L.pro_off = L.red_off + (uint32_t)align_up(kRedBytes, 128);
     // staged activations, then their sum over each 128-wide group (f32 [T][H/128])
     const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2 + (uint32_t)align_up((size_t)d.T * G1 * 4, 16);
@@ -124,7 +129,7 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     L.total = L.xs_off ? base + xs_bytes : base;
     // scratch of the prologue lives in the stage area
     const uint32_t scratch = kFW * d.E * 2 + 2 * d.E * 4 + 3 * kFastN * 4;
-    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= 2 * kFW * L.stage_bytes && d.T <= kDecodeMaxT &&
+    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= kStages * kCons * L.stage_bytes && d.T <= kDecodeMaxT &&
            d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
     return L;
 }
@@ -157,6 +162,14 @@ __device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
     v.nact = reinterpret_cast<int *>(take(16));
     return v;
 }
+
+// mbarriers in v.bar: for consumer c and stage s, "full" (the producer's copies
+// landed) and "empty" (the consumer is done with the stage); then the
+// activations' bulk copy.
+static_assert(2 * kCons * kStages + 1 <= 4 * kFW, "mbarrier slots");
+__device__ inline uint64_t *full_bar(const Pro &v, int c, int s) { return v.bar + c * kStages + s; }
+__device__ inline uint64_t *empty_bar(const Pro &v, int c, int s) { return v.bar + (kCons + c) * kStages + s; }
+__device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + 2 * kCons * kStages; }
 
 // Exclusive scan over the CTA (kFW warps) of one int per thread; *total gets the sum.
 __device__ inline int cta_exclusive_scan(int v, int *warp_sums, int *total) {
@@ -335,9 +348,12 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
         }
     }
     __syncthreads();
-    if (tid < kNGrp) {
-        reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[tid] = 0;           // parts done
-        reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16)[kNGrp + tid] = 0;   // tasks finalised
+    if (tid < 4 * kNGrp) reinterpret_cast<int *>(smem + p.red_off + kRedSlotBytes)[tid] = 0;   // parts done, finalised
+    // the ring's full and empty barriers (one arrival each: the producer's
+    // expect_tx, a consumer's release)
+    if (tid < 2 * kCons * kStages) {
+        mbar_init(v.bar + tid, 1);
+        fence_mbar_init();
     }
     // large batches used the stage area as scratch, where weight copies will land
     if (!fast) fence_proxy_async_smem();
@@ -346,8 +362,9 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
 
 // After the permutation: the activations in fragment order and their
 // per-group sums (if staged), and the outputs of tokens with no valid slot.
+// Run by the consumer warps only; ends on a named barrier among them.
 __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, const Pro &v) {
-    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int tid = threadIdx.x, nthr = kCons * 32;
     const int lane = tid & 31, warp = tid >> 5;
     if (p.xs_off) {
         // x arrived row-major (a bulk copy issued at kernel entry); each 16-byte
@@ -357,7 +374,7 @@ __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, co
         // multiple of 16, so the 16 chunks of a group sit in 16 consecutive
         // lanes; every lane runs every pass (the count is rounded up to whole
         // warps) so that the shuffles see the full warp.
-        if (!mbar_wait(v.bar + 2 * kFW, 0) && tid == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+        if (!mbar_wait(x_bar(v), 0) && tid == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
         uint4 *xs = reinterpret_cast<uint4 *>(smem + p.xs_off);
         float *xsum = reinterpret_cast<float *>(smem + p.xs_off + (size_t)p.T * p.H * 2);
         const int nch = p.T * p.H / 8;
@@ -400,27 +417,28 @@ __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, co
                     }
                 }
             }
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"n"(kCons * 32) : "memory");
 }
 
 __device__ inline uint32_t fw_word(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
-// ---- the warp's chunk sequence ------------------------------------------------
-// A warp's list: its group's gate_up tasks (b1 + grp, b1 + grp + 4, ... within
-// the CTA's range), of each of which it takes the chunks part, part + 4, ...,
-// then its down items (b2 + warp, b2 + warp + 16, ...). Task ids: gate_up
-// tasks 0..n1-1, then down items n1, n1 + 1, ...
-struct Seq {       // position in the warp's list, and chunk (of this warp's share) within it
-    int pos, ci;
+// ---- a consumer's chunk sequence ------------------------------------------------
+// Consumer c's list: its group's gate_up tasks (b1 + grp, b1 + grp + 3, ...
+// within the CTA's range), of each of which it takes the chunks part,
+// part + 5, ..., then its down items (b2 + c, b2 + c + 15, ...). Task ids:
+// gate_up tasks 0..n1-1, then down items n1, n1 + 1, ... The producer walks
+// every consumer's list with the same arithmetic.
+struct ChunkRef {
+    int task, chunk, ci, pos;   // task id, K chunk (gate_up), index of the chunk in this warp's share, list position
 };
 
 struct WarpList {
     int b1, b2, warp, grp, part, n1;
-    int ng;        // gate_up tasks of this warp (0 if it takes no chunk of any)
-    int ncw;       // chunks of each gate_up task that this warp takes
-    int nd;        // down items of this warp
+    int ng;        // gate_up tasks of this consumer (0 if it takes no chunk of any)
+    int ncw;       // chunks of each gate_up task that it takes
+    int nd;        // down items of this consumer
     __device__ void init(int b1_, int m1, int b2_, int m2, int warp_, int n1_, int nkc) {
         b1 = b1_;
         b2 = b2_;
@@ -430,19 +448,24 @@ struct WarpList {
         n1 = n1_;
         ncw = part < nkc ? (nkc - part + kGrp - 1) / kGrp : 0;
         ng = (ncw > 0 && grp < m1) ? (m1 - grp + kNGrp - 1) / kNGrp : 0;
-        nd = warp < m2 ? (m2 - warp + kFW - 1) / kFW : 0;
+        nd = warp < m2 ? (m2 - warp + kCons - 1) / kCons : 0;
     }
-    // task at list position `pos`, or -1 past the end
-    __device__ int task(int pos) const {
-        if (pos < ng) return b1 + grp + kNGrp * pos;
-        if (pos < ng + nd) return n1 + b2 + warp + kFW * (pos - ng);
-        return -1;
-    }
-    __device__ int chunk(const Seq &s) const { return part + kGrp * s.ci; }
-    __device__ void advance(Seq &s) const {
-        if (s.pos < ng && ++s.ci < ncw) return;
-        s.ci = 0;
-        ++s.pos;
+    __device__ int count() const { return ng * ncw + nd; }
+    // the j-th chunk of the list (0 <= j < count())
+    __device__ ChunkRef at(int j) const {
+        ChunkRef r;
+        if (j < ng * ncw) {
+            r.pos = j / ncw;
+            r.ci = j - r.pos * ncw;
+            r.task = b1 + grp + kNGrp * r.pos;
+            r.chunk = part + kGrp * r.ci;
+        } else {
+            r.pos = ng + (j - ng * ncw);
+            r.ci = 0;
+            r.chunk = 0;
+            r.task = n1 + b2 + warp + kCons * (r.pos - ng);
+        }
+        return r;
     }
 };
 
@@ -598,20 +621,23 @@ __device__ inline void f_gate_up_store(const FusedParams &p, const Pro &v, int t
 }
 
 // The warp has finished its share of gate_up task `task`, the `n`-th task of
-// its group. Its partial sums go to its slot; the warp that completes the
-// count of the task's nparts parts adds the slots in part order, publishes h
-// and releases the expert's done1 counter. A warp writes its slot for task n
-// only once task n-1 of the group is finalised (its slots read), a bounded
-// wait on the group's count of finalised tasks. Returns false if it gave up.
+// its group. Its partial sums go to its slot in the buffer of parity n & 1;
+// the warp that completes the count of the task's nparts parts adds the slots
+// in part order, publishes h and releases the expert's done1 counter. A warp
+// writes its slot for task n only once task n-2, the buffer's previous user,
+// is finalised (its slots read): a bounded wait on the count of the buffer's
+// finalised tasks, which task n-1's finalisation does not hold up. Returns
+// false if it gave up.
 __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *smem, int task, int n, int grp,
                                    int part, int nparts, int lane, const float (&acc)[kMaxNT][4]) {
-    float4 *slots = reinterpret_cast<float4 *>(smem + p.red_off) + grp * kGrp * 32;
-    int *cnt = reinterpret_cast<int *>(smem + p.red_off + kNGrp * kGrp * 32 * 16) + grp;
-    volatile int *gen = cnt + kNGrp;
+    const int par = n & 1;
+    float4 *slots = reinterpret_cast<float4 *>(smem + p.red_off) + (grp * 2 + par) * kGrp * 32;
+    int *cnt = reinterpret_cast<int *>(smem + p.red_off + kRedSlotBytes) + grp * 2 + par;
+    volatile int *fin = cnt + 2 * kNGrp;
     uint32_t ok = 1;
     if (lane == 0) {
         uint32_t i = 0;
-        while (*gen < n)
+        while (*fin < (n >> 1))
             if (++i > kSpinLimit) {
                 ok = 0;
                 set_error(p.ctrl, MOE_ERR_TIMEOUT);
@@ -645,7 +671,7 @@ __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *
     if (lane == 0) {
         red_release_add_u32(&p.done1[(size_t)v.act[task / (p.I / 8)] * kCtrStride], 1u);
         __threadfence_block();
-        *gen = n + 1;
+        *fin = (n >> 1) + 1;
     }
     return true;
 }
@@ -873,6 +899,51 @@ __device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
     if (threadIdx.x == 0) p.ctrl->exit_count = 0;
 }
 
+// The producer warp: lane c (c < kCons) keeps consumer c's stages full, in the
+// consumer's own order, refilling a stage once the consumer has released it.
+// The lanes poll their barriers without blocking, so the lanes issue side by
+// side and none waits on another lane's consumer. No cycle can form: a
+// consumer releases a gate_up stage as soon as its words are in registers;
+// its only other wait before its down items is for its group's previous task
+// to be finalised, which needs chunks of earlier tasks only (issued by the
+// other lanes on their own); a down item holds its stage until the expert's
+// gate_up tasks are done, in any CTA, and those depend on gate_up chunks only.
+// The loop is bounded. Before the warp leaves every lane waits (bounded) for
+// the copies it issued, so that none lands after the CTA has exited.
+__device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8_t *smem, int b1, int m1, int b2,
+                                       int m2, int n1) {
+    const int c = threadIdx.x & 31;
+    WarpList L;
+    L.init(b1, m1, b2, m2, c < kCons ? c : 0, n1, p.nkc);
+    const int cnt = c < kCons ? L.count() : 0;
+    int j = 0;
+    uint32_t polls = 0;
+    bool ok = true;
+    while (__any_sync(0xffffffffu, j < cnt)) {
+        if (j < cnt) {
+            const int s = j % kStages;
+            if (j < kStages || mbar_try_wait(empty_bar(v, c, s), (j / kStages - 1) & 1)) {
+                // (the consumer's reads of the stage completed before its release)
+                const ChunkRef r = L.at(j);
+                f_issue(p, v, r.task, r.chunk, n1, smem + (size_t)(c * kStages + s) * p.stage_bytes,
+                        full_bar(v, c, s), 0);
+                ++j;
+            }
+        }
+        if (++polls > 16u * kSpinLimit) {
+            ok = false;
+            break;
+        }
+    }
+    if (!ok && c == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+    for (int s = 0; s < kStages; ++s) {
+        const int t = j - 1;   // the last chunk this lane issued ...
+        if (t < 0) continue;
+        const int jl = t - ((t - s) % kStages + kStages) % kStages;   // ... into stage s
+        if (jl >= 0) mbar_wait(full_bar(v, c, s), (jl / kStages) & 1);
+    }
+}
+
 // ---- kernel -----------------------------------------------------------------
 template <bool kStaged>
 __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_constant__ FusedParams p) {
@@ -884,7 +955,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     if (p.T * p.k <= kFastN && (int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
     const Pro v = pro_views(smem, p);
     if (p.xs_off && threadIdx.x == 0) {
-        uint64_t *xbar = v.bar + 2 * kFW;
+        uint64_t *xbar = x_bar(v);
         // the activations start moving now, behind the permutation
         const uint32_t xb = (uint32_t)p.T * p.H * 2;
         mbar_init(xbar, 1);
@@ -893,8 +964,6 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         bulk_g2s(smem + p.xs_off, p.x, xb, xbar);
     }
     fused_prologue(p, smem, v, id_reg);
-    // the activations, converted while no warp is held by its copies yet
-    fused_stage(p, smem, v);
 
     const int nact = *v.nact;
     const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
@@ -902,63 +971,39 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     const int C = gridDim.x, cb = blockIdx.x;
     const int b1 = (int)((long long)n1 * cb / C), m1 = (int)((long long)n1 * (cb + 1) / C) - b1;
     const int b2 = (int)((long long)n2 * cb / C), m2 = (int)((long long)n2 * (cb + 1) / C) - b2;
-    WarpList L;
-    L.init(b1, m1, b2, m2, warp, n1, p.nkc);
-    const int nparts = p.nkc < kGrp ? p.nkc : kGrp;
-    uint8_t *stages = smem + (size_t)warp * 2 * p.stage_bytes;
-    uint64_t *bar = v.bar + 2 * warp;
-    if (lane == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-    }
-    fence_mbar_init();
-    __syncwarp();
-
-    Seq ahead{0, 0};
-    bool inflight[2] = {false, false};
-    for (int s = 0; s < 2; ++s) {
-        const int tk = L.task(ahead.pos);
-        if (tk < 0) break;
-        f_issue(p, v, tk, L.chunk(ahead), n1, stages + s * p.stage_bytes, &bar[s], lane);
-        inflight[s] = true;
-        L.advance(ahead);
-    }
-
-    float acc[kMaxNT][4];
-    uint32_t phase[2] = {0u, 0u};
-    Seq cur{0, 0};
-    for (int st = 0;; st ^= 1) {
-        const int tk = L.task(cur.pos);
-        if (tk < 0) break;
-        uint8_t *stage = stages + st * p.stage_bytes;
-        inflight[st] = false;
-        if (!mbar_wait(&bar[st], phase[st])) {
-            if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
-            break;
-        }
-        phase[st] ^= 1u;
-        if (tk < n1) {
-            f_gate_up_chunk<kStaged>(p, v, tk, L.chunk(cur), cur.ci == 0, stage, smem, lane, acc);
-            if (cur.ci == L.ncw - 1 && !f_gu_reduce(p, v, smem, tk, cur.pos, L.grp, L.part, nparts, lane, acc))
+    if (warp == kProd) {
+        f_produce(p, v, smem, b1, m1, b2, m2, n1);
+    } else {
+        // the activations, converted while the producer requests the first chunks
+        fused_stage(p, smem, v);
+        WarpList L;
+        L.init(b1, m1, b2, m2, warp, n1, p.nkc);
+        const int nparts = p.nkc < kGrp ? p.nkc : kGrp;
+        const int nch = L.count();
+        float acc[kMaxNT][4];
+        for (int j = 0; j < nch; ++j) {
+            const int s = j % kStages;
+            uint8_t *stage = smem + (size_t)(warp * kStages + s) * p.stage_bytes;
+            if (!mbar_wait(full_bar(v, warp, s), (j / kStages) & 1)) {
+                if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
                 break;
-        } else {
-            f_down(p, v, tk - n1, stage, lane);
+            }
+            const ChunkRef r = L.at(j);
+            if (r.task < n1) {
+                f_gate_up_chunk<kStaged>(p, v, r.task, r.chunk, r.ci == 0, stage, smem, lane, acc);
+                // the stage is free as soon as its words are in registers
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(v, warp, s));
+                if (r.ci == L.ncw - 1 && !f_gu_reduce(p, v, smem, r.task, r.pos, L.grp, L.part, nparts, lane, acc))
+                    break;
+            } else {
+                f_down(p, v, r.task - n1, stage, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(v, warp, s));
+            }
         }
-        __syncwarp();
-        const int nx = L.task(ahead.pos);
-        if (nx >= 0) {
-            fence_proxy_async_smem();
-            f_issue(p, v, nx, L.chunk(ahead), n1, stage, &bar[st], lane);
-            inflight[st] = true;
-            L.advance(ahead);
-        }
-        L.advance(cur);
+        if (p.xs_off && threadIdx.x == 0) mbar_wait(x_bar(v), 0);   // complete already, unless its wait gave up
     }
-    // after an abort: let the copies still in flight land (bounded) before the CTA exits
-    for (int s = 0; s < 2; ++s)
-        if (inflight[s]) mbar_wait(&bar[s], phase[s]);
-    if (p.xs_off && threadIdx.x == 0)   // complete already, unless its wait gave up
-        mbar_wait(pro_views(smem, p).bar + 2 * kFW, 0);
     if (!p.out) f_stack_rows(p);
     f_exit(p, v);
 }
@@ -1009,7 +1054,7 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
     // enough CTAs that every group has a gate_up task and every warp a down item
     const long long g1 = (max_active * (d.I / 8) + kNGrp - 1) / kNGrp;
-    const long long g2 = (max_active * (d.H / kP2Rows) + kFW - 1) / kFW;
+    const long long g2 = (max_active * (d.H / kP2Rows) + kCons - 1) / kCons;
     long long grid = g1 > g2 ? g1 : g2;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;

@@ -130,10 +130,6 @@ __device__ inline Tile make_tile(int4 ci, int m) {
     return r;
 }
 
-__device__ inline void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // One lane of the (converged) warp returns true.
 __device__ inline bool elect_one() {
     uint32_t pred;
