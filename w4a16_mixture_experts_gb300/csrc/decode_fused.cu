@@ -48,10 +48,10 @@ namespace moe {
 constexpr int kFW = 16;              // warps per CTA: kCons consumers, then the producer
 constexpr int kCons = 15;            // warps that compute
 constexpr int kProd = kCons;         // the warp that issues every weight copy
-constexpr int kGrp = 5;              // consumers that split one gate_up task over K
-constexpr int kNGrp = kCons / kGrp;  // gate_up groups per CTA
 constexpr int kGC = 4;               // quantisation groups per gate_up chunk
-constexpr int kStages = 2;           // ring stages per consumer
+constexpr int kNS = 30;              // stages of the CTA's chunk ring
+constexpr int kRedMax = 20480;       // bytes for the gate_up partial-sum buffers
+constexpr int kMaxNB = 8;            // partial-sum buffers (gate_up tasks in flight)
 constexpr int kP2Rows = 16;          // output rows per down item
 // Batches of up to 7 tokens. From 8 tokens on, the tensor-core grouped GEMM
 // (prefill.cu) is as fast on GB300 and grows faster (measured: T = 8 at 114
@@ -85,14 +85,15 @@ struct FusedParams {
     int gcw;             // words per gate_up chunk row (groups per chunk * 16)
     int nkc;             // chunks per gate_up task
     uint32_t stage_bytes;
-    uint32_t red_off;    // offset of the gate_up reduction slots and counters
+    uint32_t red_off;    // offset of the gate_up partial sums and counters
+    int nb;              // partial-sum buffers
     uint32_t pro_off;    // offset of the permutation arrays
     uint32_t xs_off;     // offset of the staged activations (0: not staged)
 };
 
 struct FusedLayout {
     uint32_t stage_bytes, red_off, pro_off, xs_off, total;
-    int gcw, nkc;
+    int gcw, nkc, nb;
     bool ok;
 };
 
@@ -103,13 +104,29 @@ inline uint32_t fused_pro_bytes(const moe_dims &d) {
                       align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
 }
 
-// Gate_up partial results: [group][task parity][warp of the group][lane][4]
-// f32, then per group and parity a count of finished parts and of finalised
-// tasks.
-constexpr uint32_t kRedSlotBytes = kNGrp * 2 * kGrp * 32 * 16;   // [group][task parity][part][lane] float4
-constexpr uint32_t kRedBytes = kRedSlotBytes + 4 * kNGrp * 4;       // + parts done, tasks finalised [group][parity]
+// Gate_up partial results: nb buffers of [chunk][lane][4] f32 (a task's
+// chunks each leave one), then per buffer a count of finished chunks and of
+// finalised tasks, the consumers' chunk ticket, and per ring stage the chunk
+// last issued into it and the chunk it may take next.
+inline uint32_t fused_red_bytes(int nb, int nkc) {
+    return (uint32_t)(nb * nkc * 32 * 16 + 2 * nb * 4 + 4 + 2 * kNS * 4);
+}
+struct RingWords {
+    int *cnt, *ticket;
+    volatile int *fin, *issued, *next;
+};
+__device__ inline RingWords ring_words(uint8_t *smem, const FusedParams &p) {
+    int *w = reinterpret_cast<int *>(smem + p.red_off + p.nb * p.nkc * 512);
+    RingWords r;
+    r.cnt = w;
+    r.fin = w + p.nb;
+    r.ticket = w + 2 * p.nb;
+    r.issued = w + 2 * p.nb + 1;
+    r.next = w + 2 * p.nb + 1 + kNS;
+    return r;
+}
 
-// Shared memory: kStages stages per consumer | reduction slots | permutation
+// Shared memory: the CTA's ring of kNS stages | partial sums | permutation
 // arrays | staged activations (if they fit).
 inline FusedLayout fused_layout(const moe_dims &d) {
     FusedLayout L{};
@@ -120,8 +137,10 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
     const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
-    L.red_off = kStages * kCons * L.stage_bytes;
-    L.pro_off = L.red_off + (uint32_t)align_up(kRedBytes, 128);
+    L.nb = kRedMax / (L.nkc * 512);
+    L.nb = L.nb < 1 ? 1 : L.nb > kMaxNB ? kMaxNB : L.nb;
+    L.red_off = kNS * L.stage_bytes;
+    L.pro_off = L.red_off + (uint32_t)align_up(fused_red_bytes(L.nb, L.nkc), 128);
     // staged activations, then their sum over each 128-wide group (f32 [T][H/128])
     const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2 + (uint32_t)align_up((size_t)d.T * G1 * 4, 16);
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
@@ -129,7 +148,7 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     L.total = L.xs_off ? base + xs_bytes : base;
     // scratch of the prologue lives in the stage area
     const uint32_t scratch = kFW * d.E * 2 + 2 * d.E * 4 + 3 * kFastN * 4;
-    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= kStages * kCons * L.stage_bytes && d.T <= kDecodeMaxT &&
+    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= kNS * L.stage_bytes && d.T <= kDecodeMaxT &&
            d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
     return L;
 }
@@ -163,13 +182,16 @@ __device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
     return v;
 }
 
-// mbarriers in v.bar: for consumer c and stage s, "full" (the producer's copies
-// landed) and "empty" (the consumer is done with the stage); then the
-// activations' bulk copy.
-static_assert(2 * kCons * kStages + 1 <= 4 * kFW, "mbarrier slots");
-__device__ inline uint64_t *full_bar(const Pro &v, int c, int s) { return v.bar + c * kStages + s; }
-__device__ inline uint64_t *empty_bar(const Pro &v, int c, int s) { return v.bar + (kCons + c) * kStages + s; }
-__device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + 2 * kCons * kStages; }
+// mbarriers in v.bar: per ring stage "full" (the producer's copies landed),
+// then the activations' bulk copy. A stage changes hands through two shared
+// words (RingWords): the producer writes issued[q] = i just before it copies
+// chunk i into stage q, which it may do only once next[q] == i; the consumer
+// of chunk i waits for issued[q] == i before it waits on the barrier, so the
+// barrier's phase is then exactly chunk i's (a parity alone cannot tell chunk
+// i from chunk i - 2 * kNS), and sets next[q] = i + kNS when done with it.
+static_assert(kNS + 1 <= 4 * kFW, "mbarrier slots");
+__device__ inline uint64_t *full_bar(const Pro &v, int q) { return v.bar + q; }
+__device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + kNS; }
 
 // Exclusive scan over the CTA (kFW warps) of one int per thread; *total gets the sum.
 __device__ inline int cta_exclusive_scan(int v, int *warp_sums, int *total) {
@@ -348,10 +370,16 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
         }
     }
     __syncthreads();
-    if (tid < 4 * kNGrp) reinterpret_cast<int *>(smem + p.red_off + kRedSlotBytes)[tid] = 0;   // parts done, finalised
-    // the ring's full and empty barriers (one arrival each: the producer's
-    // expect_tx, a consumer's release)
-    if (tid < 2 * kCons * kStages) {
+    {
+        const RingWords rw = ring_words(smem, p);
+        if (tid < 2 * p.nb + 1) rw.cnt[tid] = 0;   // chunks done, tasks finalised, the ticket
+        if (tid < kNS) {
+            rw.issued[tid] = -1;
+            rw.next[tid] = tid;
+        }
+    }
+    // the ring's full barriers (one arrival: the producer's expect_tx)
+    if (tid < kNS) {
         mbar_init(v.bar + tid, 1);
         fence_mbar_init();
     }
@@ -424,50 +452,27 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
-// ---- a consumer's chunk sequence ------------------------------------------------
-// Consumer c's list: its group's gate_up tasks (b1 + grp, b1 + grp + 3, ...
-// within the CTA's range), of each of which it takes the chunks part,
-// part + 5, ..., then its down items (b2 + c, b2 + c + 15, ...). Task ids:
-// gate_up tasks 0..n1-1, then down items n1, n1 + 1, ... The producer walks
-// every consumer's list with the same arithmetic.
+// ---- the CTA's chunk sequence -----------------------------------------------
+// Chunk i of the CTA: for i < m1 * nkc, K chunk i % nkc of gate_up task
+// b1 + i / nkc (tasks in order); after them the down items b2, b2 + 1, ...
+// Task ids: gate_up tasks 0..n1-1, down items n1, n1 + 1, ... The producer
+// issues the chunks in this order and the consumers take them in this order.
 struct ChunkRef {
-    int task, chunk, ci, pos;   // task id, K chunk (gate_up), index of the chunk in this warp's share, list position
+    int task, chunk;
 };
 
-struct WarpList {
-    int b1, b2, warp, grp, part, n1;
-    int ng;        // gate_up tasks of this consumer (0 if it takes no chunk of any)
-    int ncw;       // chunks of each gate_up task that it takes
-    int nd;        // down items of this consumer
-    __device__ void init(int b1_, int m1, int b2_, int m2, int warp_, int n1_, int nkc) {
-        b1 = b1_;
-        b2 = b2_;
-        warp = warp_;
-        grp = warp_ / kGrp;
-        part = warp_ % kGrp;
-        n1 = n1_;
-        ncw = part < nkc ? (nkc - part + kGrp - 1) / kGrp : 0;
-        ng = (ncw > 0 && grp < m1) ? (m1 - grp + kNGrp - 1) / kNGrp : 0;
-        nd = warp < m2 ? (m2 - warp + kCons - 1) / kCons : 0;
+__device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int nkc) {
+    ChunkRef r;
+    if (i < m1 * nkc) {
+        const int u = i / nkc;
+        r.task = b1 + u;
+        r.chunk = i - u * nkc;
+    } else {
+        r.task = n1 + b2 + (i - m1 * nkc);
+        r.chunk = 0;
     }
-    __device__ int count() const { return ng * ncw + nd; }
-    // the j-th chunk of the list (0 <= j < count())
-    __device__ ChunkRef at(int j) const {
-        ChunkRef r;
-        if (j < ng * ncw) {
-            r.pos = j / ncw;
-            r.ci = j - r.pos * ncw;
-            r.task = b1 + grp + kNGrp * r.pos;
-            r.chunk = part + kGrp * r.ci;
-        } else {
-            r.pos = ng + (j - ng * ncw);
-            r.ci = 0;
-            r.chunk = 0;
-            r.task = n1 + b2 + warp + kCons * (r.pos - ng);
-        }
-        return r;
-    }
-};
+    return r;
+}
 
 __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int task, int chunk, int n1, uint8_t *stage,
                                uint64_t *bar, int lane) {
@@ -620,24 +625,24 @@ __device__ inline void f_gate_up_store(const FusedParams &p, const Pro &v, int t
         }
 }
 
-// The warp has finished its share of gate_up task `task`, the `n`-th task of
-// its group. Its partial sums go to its slot in the buffer of parity n & 1;
-// the warp that completes the count of the task's nparts parts adds the slots
-// in part order, publishes h and releases the expert's done1 counter. A warp
-// writes its slot for task n only once task n-2, the buffer's previous user,
-// is finalised (its slots read): a bounded wait on the count of the buffer's
-// finalised tasks, which task n-1's finalisation does not hold up. Returns
+// The warp has computed K chunk c of gate_up task `task`, the CTA's u-th
+// task. Its partial sums go to slot c of buffer u % nb; the warp that
+// completes the count of the task's nkc chunks adds the slots in chunk order,
+// publishes h and releases the expert's done1 counter. A buffer is written for
+// task u only once task u - nb, its previous user, is finalised (its slots
+// read): a bounded wait on the buffer's count of finalised tasks. Returns
 // false if it gave up.
-__device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *smem, int task, int n, int grp,
-                                   int part, int nparts, int lane, const float (&acc)[kMaxNT][4]) {
-    const int par = n & 1;
-    float4 *slots = reinterpret_cast<float4 *>(smem + p.red_off) + (grp * 2 + par) * kGrp * 32;
-    int *cnt = reinterpret_cast<int *>(smem + p.red_off + kRedSlotBytes) + grp * 2 + par;
-    volatile int *fin = cnt + 2 * kNGrp;
+__device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *smem, int task, int u, int c,
+                                   int lane, const float (&acc)[kMaxNT][4]) {
+    const int b = u % p.nb;
+    float4 *slots = reinterpret_cast<float4 *>(smem + p.red_off) + b * p.nkc * 32;
+    const RingWords rw = ring_words(smem, p);
+    int *cnt = rw.cnt + b;
+    volatile int *fin = rw.fin + b;
     uint32_t ok = 1;
     if (lane == 0) {
         uint32_t i = 0;
-        while (*fin < (n >> 1))
+        while (*fin < u / p.nb)
             if (++i > kSpinLimit) {
                 ok = 0;
                 set_error(p.ctrl, MOE_ERR_TIMEOUT);
@@ -647,12 +652,12 @@ __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) return false;
     __threadfence_block();
-    slots[part * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    slots[c * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
     __syncwarp();
     int last = 0;
     if (lane == 0) {
         __threadfence_block();
-        last = atomicAdd(cnt, 1) + 1 == nparts;
+        last = atomicAdd(cnt, 1) + 1 == p.nkc;
         if (last) *cnt = 0;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
@@ -661,7 +666,7 @@ __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *
     float sum[kMaxNT][4];
     float4 a = slots[lane];
     sum[0][0] = a.x, sum[0][1] = a.y, sum[0][2] = a.z, sum[0][3] = a.w;
-    for (int q = 1; q < nparts; ++q) {
+    for (int q = 1; q < p.nkc; ++q) {
         a = slots[q * 32 + lane];
         sum[0][0] += a.x, sum[0][1] += a.y, sum[0][2] += a.z, sum[0][3] += a.w;
     }
@@ -671,7 +676,7 @@ __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *
     if (lane == 0) {
         red_release_add_u32(&p.done1[(size_t)v.act[task / (p.I / 8)] * kCtrStride], 1u);
         __threadfence_block();
-        *fin = (n >> 1) + 1;
+        *fin = u / p.nb + 1;
     }
     return true;
 }
@@ -899,35 +904,39 @@ __device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
     if (threadIdx.x == 0) p.ctrl->exit_count = 0;
 }
 
-// The producer warp: lane c (c < kCons) keeps consumer c's stages full, in the
-// consumer's own order, refilling a stage once the consumer has released it.
-// The lanes poll their barriers without blocking, so the lanes issue side by
-// side and none waits on another lane's consumer. No cycle can form: a
-// consumer releases a gate_up stage as soon as its words are in registers;
-// its only other wait before its down items is for its group's previous task
-// to be finalised, which needs chunks of earlier tasks only (issued by the
-// other lanes on their own); a down item holds its stage until the expert's
-// gate_up tasks are done, in any CTA, and those depend on gate_up chunks only.
-// The loop is bounded. Before the warp leaves every lane waits (bounded) for
-// the copies it issued, so that none lands after the CTA has exited.
+// The producer warp: lane l issues chunks l, l + 32, ... of the CTA's
+// sequence, chunk i into ring stage i % kNS once the stage has been handed
+// back for it (next[q] == i). The lanes poll without blocking, so they issue
+// side by side and the requests go out nearly in sequence order. No cycle can
+// form: consumers take chunks in sequence order (a ticket), gate_up chunks
+// first; a consumer hands a gate_up stage back as soon as its words are in
+// registers, and its one wait after that (for the previous user of its
+// partial-sum buffer, an earlier task) never holds up the oldest unfinished
+// task, whose chunks were all taken before; a down item holds its stage until
+// the expert's gate_up tasks are done, in any CTA, and those need gate_up
+// chunks only. The loop is bounded. Before the warp leaves, lane q waits
+// (bounded) for the last copy issued into stage q, so that none lands after
+// the CTA has exited.
 __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8_t *smem, int b1, int m1, int b2,
                                        int m2, int n1) {
-    const int c = threadIdx.x & 31;
-    WarpList L;
-    L.init(b1, m1, b2, m2, c < kCons ? c : 0, n1, p.nkc);
-    const int cnt = c < kCons ? L.count() : 0;
-    int j = 0;
+    const int l = threadIdx.x & 31;
+    const RingWords rw = ring_words(smem, p);
+    const int nc = m1 * p.nkc + m2;
+    int i = l;   // next chunk of this lane
     uint32_t polls = 0;
     bool ok = true;
-    while (__any_sync(0xffffffffu, j < cnt)) {
-        if (j < cnt) {
-            const int s = j % kStages;
-            if (j < kStages || mbar_try_wait(empty_bar(v, c, s), (j / kStages - 1) & 1)) {
-                // (the consumer's reads of the stage completed before its release)
-                const ChunkRef r = L.at(j);
-                f_issue(p, v, r.task, r.chunk, n1, smem + (size_t)(c * kStages + s) * p.stage_bytes,
-                        full_bar(v, c, s), 0);
-                ++j;
+    while (__any_sync(0xffffffffu, i < nc)) {
+        // the consumers' first chunks go out one pass ahead of the rest, so
+        // that they are not interleaved with later requests
+        if (i < nc && (polls > 0 || i < kCons)) {
+            const int q = i % kNS;
+            if (rw.next[q] == i) {
+                // (the previous consumer's reads of the stage completed before it
+                // handed the stage back)
+                rw.issued[q] = i;
+                const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
+                f_issue(p, v, r.task, r.chunk, n1, smem + (size_t)q * p.stage_bytes, full_bar(v, q), 0);
+                i += 32;
             }
         }
         if (++polls > 16u * kSpinLimit) {
@@ -935,12 +944,11 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
             break;
         }
     }
-    if (!ok && c == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
-    for (int s = 0; s < kStages; ++s) {
-        const int t = j - 1;   // the last chunk this lane issued ...
-        if (t < 0) continue;
-        const int jl = t - ((t - s) % kStages + kStages) % kStages;   // ... into stage s
-        if (jl >= 0) mbar_wait(full_bar(v, c, s), (jl / kStages) & 1);
+    if (!ok && l == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+    __syncwarp();
+    if (l < kNS) {
+        const int j = rw.issued[l];
+        if (j >= 0) mbar_wait(full_bar(v, l), (j / kNS) & 1);
     }
 }
 
@@ -976,30 +984,50 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     } else {
         // the activations, converted while the producer requests the first chunks
         fused_stage(p, smem, v);
-        WarpList L;
-        L.init(b1, m1, b2, m2, warp, n1, p.nkc);
-        const int nparts = p.nkc < kGrp ? p.nkc : kGrp;
-        const int nch = L.count();
+        const int ngu = m1 * p.nkc, nc = ngu + m2;
+        const RingWords rw = ring_words(smem, p);
         float acc[kMaxNT][4];
-        for (int j = 0; j < nch; ++j) {
-            const int s = j % kStages;
-            uint8_t *stage = smem + (size_t)(warp * kStages + s) * p.stage_bytes;
-            if (!mbar_wait(full_bar(v, warp, s), (j / kStages) & 1)) {
+        for (;;) {
+            // chunks are taken in sequence order
+            int i = 0;
+            if (lane == 0) i = atomicAdd(rw.ticket, 1);
+            i = __shfl_sync(0xffffffffu, i, 0);
+            if (i >= nc) break;
+            const int q = i % kNS;
+            uint8_t *stage = smem + (size_t)q * p.stage_bytes;
+            // chunk i's copy has been issued into stage q (then the barrier's
+            // pending phase is chunk i's), and has landed
+            uint32_t ok = 1;
+            if (lane == 0) {
+                uint32_t n = 0;
+                while (rw.issued[q] != i)
+                    if (++n > kSpinLimit) {
+                        ok = 0;
+                        break;
+                    }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || !mbar_wait(full_bar(v, q), (i / kNS) & 1)) {
                 if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
                 break;
             }
-            const ChunkRef r = L.at(j);
+            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
             if (r.task < n1) {
-                f_gate_up_chunk<kStaged>(p, v, r.task, r.chunk, r.ci == 0, stage, smem, lane, acc);
+                f_gate_up_chunk<kStaged>(p, v, r.task, r.chunk, true, stage, smem, lane, acc);
                 // the stage is free as soon as its words are in registers
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(v, warp, s));
-                if (r.ci == L.ncw - 1 && !f_gu_reduce(p, v, smem, r.task, r.pos, L.grp, L.part, nparts, lane, acc))
-                    break;
+                if (lane == 0) {
+                    __threadfence_block();
+                    rw.next[q] = i + kNS;
+                }
+                if (!f_gu_reduce(p, v, smem, r.task, r.task - b1, r.chunk, lane, acc)) break;
             } else {
                 f_down(p, v, r.task - n1, stage, lane);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(v, warp, s));
+                if (lane == 0) {
+                    __threadfence_block();
+                    rw.next[q] = i + kNS;
+                }
             }
         }
         if (p.xs_off && threadIdx.x == 0) mbar_wait(x_bar(v), 0);   // complete already, unless its wait gave up
@@ -1043,6 +1071,7 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.nkc = L.nkc;
     p.stage_bytes = L.stage_bytes;
     p.red_off = L.red_off;
+    p.nb = L.nb;
     p.pro_off = L.pro_off;
     p.xs_off = L.xs_off;
 
@@ -1052,10 +1081,9 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     err = set_smem_once(fn, kFusedSmem);
     if (err != cudaSuccess) return err;
     const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
-    // enough CTAs that every group has a gate_up task and every warp a down item
-    const long long g1 = (max_active * (d.I / 8) + kNGrp - 1) / kNGrp;
-    const long long g2 = (max_active * (d.H / kP2Rows) + kCons - 1) / kCons;
-    long long grid = g1 > g2 ? g1 : g2;
+    // enough CTAs that every consumer has a chunk
+    const long long chunks = max_active * ((long long)(d.I / 8) * L.nkc + d.H / kP2Rows);
+    long long grid = (chunks + kCons - 1) / kCons;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
