@@ -169,6 +169,58 @@ __device__ inline void warp_topk_write(uint64_t (&key)[kTopkPer], int nper, int 
     }
 }
 
+// Size-generic forms for lanes holding N keys each (N a power of two): sort,
+// k rounds of the heads' warp maximum (lane j < k ends with the j-th largest),
+// and the softmax over the selected logits with the writes.
+template <int N>
+__device__ inline void sort_desc_n(uint64_t (&key)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+        for (int stride = size / 2; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int l = i ^ stride;
+                if (l > i) {
+                    const bool up = (i & size) != 0;
+                    const uint64_t a = key[i], b = key[l];
+                    if (up ? a > b : a < b) {
+                        key[i] = b;
+                        key[l] = a;
+                    }
+                }
+            }
+}
+
+template <int N>
+__device__ inline uint64_t warp_topk_n(uint64_t (&key)[N], int k, int lane) {
+    sort_desc_n<N>(key);
+    uint64_t mine = 0;
+    for (int j = 0; j < k; ++j) {
+        const uint64_t m = warp_max_key(key[0]);
+        if (key[0] == m) {
+#pragma unroll
+            for (int i = 0; i + 1 < N; ++i) key[i] = key[i + 1];
+            key[N - 1] = 0;
+        }
+        if (lane == j) mine = m;
+    }
+    return mine;
+}
+
+__device__ inline void topk_finish(uint64_t mine, int k, int lane, int32_t *ids_row, float *w_row) {
+    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
+    const float l = f32_from_order_key((uint32_t)(mine >> 32));
+    const float p = lane < k ? expf(l - lmax) : 0.f;
+    float z = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane < k) {
+        ids_row[lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+        w_row[lane] = p / z;
+    }
+}
+
 __device__ inline uint64_t topk_key(float logit, int e) {
     return ((uint64_t)f32_order_key(logit) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
 }
@@ -271,8 +323,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const floa
 // warp sums its lanes. Logits (with the bias) go to partial[0]. Each CTA then
 // counts itself on the control block's ticket (release); the CTA that
 // completes the count acquires every other CTA's logits, loads all T x E of
-// them at once into shared memory, and warp w selects for tokens w, w + 4, ...
-// The ticket is reset for the next launch.
+// them at once into shared memory, and selects: for T < 4 each token's
+// experts are split over 4 / T warps whose candidates one warp then merges,
+// otherwise warp w takes tokens w, w + 4, ... The ticket is reset for the next
+// launch.
 constexpr int kRouteInlineMaxT = 8;
 constexpr int kRouteLoads = 10;   // 16-byte loads per lane in flight (H <= 2560 in one pass)
 
@@ -351,14 +405,61 @@ __global__ void __launch_bounds__(128) route_small_kernel(const uint16_t *__rest
         }
     }
     __syncthreads();
-    for (int t = warp; t < T; t += blockDim.x / 32) {
-        uint64_t key[kTopkPer];
+    const int nw = blockDim.x / 32;
+    const int wpt = T >= nw ? 1 : nw / T;   // warps per token
+    if (wpt == 1) {
+        for (int t = warp; t < T; t += nw) {
+            uint64_t key[kTopkPer];
 #pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) {
-            const int ee = lane + 32 * i;
-            key[i] = ee < E ? topk_key(s_logit[t * E + ee], ee) : 0;
+            for (int i = 0; i < kTopkPer; ++i) {
+                const int ee = lane + 32 * i;
+                key[i] = ee < E ? topk_key(s_logit[t * E + ee], ee) : 0;
+            }
+            warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
         }
-        warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+    } else {
+        // the token's experts split over wpt warps: each takes its part's k largest,
+        // then the part-0 warp takes the k largest of the wpt * k candidates
+        __shared__ uint64_t s_cand[4][32];
+        const int t = warp / wpt, part = warp % wpt;
+        const int ep = (E + wpt - 1) / wpt, lo = part * ep, hi = min(E, lo + ep);
+        uint64_t mine = 0;
+        if (t < T) {
+            if (ep <= 128) {
+                uint64_t key[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ee = lo + lane + 32 * i;
+                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                }
+                mine = warp_topk_n<4>(key, k, lane);
+            } else if (ep <= 256) {
+                uint64_t key[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int ee = lo + lane + 32 * i;
+                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                }
+                mine = warp_topk_n<8>(key, k, lane);
+            } else {
+                uint64_t key[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int ee = lo + lane + 32 * i;
+                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                }
+                mine = warp_topk_n<16>(key, k, lane);
+            }
+            s_cand[warp][lane] = lane < k ? mine : 0;
+        }
+        __syncthreads();
+        if (t < T && part == 0) {
+            uint64_t c[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) c[q] = q < wpt ? s_cand[warp + q][lane] : 0;
+            mine = warp_topk_n<4>(c, k, lane);
+            topk_finish(mine, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+        }
     }
     if (threadIdx.x == 0) ctrl->route_ticket = 0;
 }
