@@ -175,6 +175,21 @@ def test_route_repeated_calls_one_workspace(T):
     assert n_exact >= 0.6 * n_all
 
 
+@pytest.mark.parametrize("T", [1, 2, 3])
+@pytest.mark.parametrize("E", [1024, 777])
+def test_route_small_batch_many_experts(T, E):
+    # small batches split each token's experts over several warps of the last
+    # router CTA (up to 512 experts a warp, 16 keys a lane); E = 777 leaves
+    # ragged parts
+    H, k = 512, 32
+    x = synth.hidden(T, H, seed=40 + T)
+    wr = synth.router(E, H, seed=41)
+    ids, w = moe.moe_route(x.cuda(), wr.cuda(), k)
+    torch.cuda.synchronize()
+    # (a valid top-k within the gap for every token; ids exact where the gaps allow)
+    check_route(ids, w, oracle.router_logits(x, wr), k)
+
+
 def test_route_full_batch_sampled():
     # T = 4096 at full shape: route on the GPU, check a seeded sample of tokens
     wl = synth.WORKLOADS["stack_prefill4096"]
