@@ -39,7 +39,6 @@ struct WsLayout {
     size_t offsets;      // i32 [E+1]
     size_t active;       // i32 [E]        active expert ids, increasing
     size_t done1;        // u32 [E][kCtrStride] per expert (one 128-byte line each): finished gate_up tasks
-    size_t done2;        // unused, kept empty
     size_t ticket;       // u32 [T][H/16]  per 16-row output block: finished slots
     size_t rowss;        // f32 [T]        per token: sum of r^2 (stack epilogue, decode path)
     size_t rbuf;         // f32 [T][H]     residual sums (stack epilogue)
@@ -99,7 +98,6 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);
     L.done1 = take((size_t)E * kCtrStride * 4);
-    L.done2 = take(0);
     L.ticket = take(T * (H / 16) * 4);
     L.rowss = take(T * 4);
     const bool small = fused_supported(d);
