@@ -22,7 +22,8 @@ expert kernel's own time is taken from events that the library records
 around it in separate one-step graphs, replayed after the timed region.
 `e2e` repeats the timing through the same public calls with every step's
 tokens copied in from pinned host memory and its output copied back, inside
-the timed region.
+the timed region; the copies run on a second stream, so that a step's kernels
+overlap the copy-out of the step before it, as a serving loop would run them.
 The CPU baseline is the fp64 oracle on a bounded sample of the workload.
 Multi-GPU: independent replicas (the layer has no exchange step).
 """
@@ -255,7 +256,7 @@ def run_ours(args, rank, world, local):
     ws = moe.workspace(T, H, E, k, I, dev)
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     w = torch.empty(T, k, dtype=torch.float32, device=dev)
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    outs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(1 if stack else nsets)]
     act = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     stream = torch.cuda.Stream(device=dev)
     n_exp_launch = wl.layers
@@ -284,8 +285,8 @@ def run_ours(args, rank, world, local):
             moe.moe_profile_events(ev_b[i], ev_a[i])
         moe.moe_route(s["hidden"], s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
         moe.moe_w4a16_forward(s["hidden"], ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                              s["w2_scales"], out=out, ws=ws)
-        return out
+                              s["w2_scales"], out=outs[i], ws=ws)
+        return outs[i]
 
     with torch.cuda.stream(stream):
         # warm-up, and the unique experts each set touches
@@ -317,17 +318,38 @@ def run_ours(args, rank, world, local):
         h_in = [(x0 if stack else sets[i]["hidden"]).cpu().pin_memory() for i in range(n_in)]
         h_out = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(n_in)]
         dst_in = [x0 if stack else sets[i]["hidden"] for i in range(n_in)]
-        final = act[(wl.layers - 1) % 2] if stack else out
+        finals = [act[(wl.layers - 1) % 2]] if stack else outs
+        copy_stream = torch.cuda.Stream(device=dev)
+        ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+        ev_in = [torch.cuda.Event() for _ in range(n_in)]
+        ev_done = [torch.cuda.Event() for _ in range(n_in)]
 
         def enqueue(seq, profile=False, e2e=False):
-            for i in seq:
-                if e2e:
+            if not e2e:
+                for i in seq:
+                    step(i, profile=profile)
+                if profile:
+                    moe.moe_profile_events(None, None)
+                return
+            # every step copies its tokens in from pinned host memory and its output
+            # back, on a copy stream: the copy-in of later steps and the copy-out of
+            # earlier ones overlap a step's kernels, as a serving loop would
+            cur = torch.cuda.current_stream()
+            ev_fork.record(cur)
+            copy_stream.wait_event(ev_fork)
+            with torch.cuda.stream(copy_stream):
+                for i in seq:
                     dst_in[i].copy_(h_in[i], non_blocking=True)
-                step(i, profile=profile)
-                if e2e:
-                    h_out[i].copy_(final, non_blocking=True)
-            if profile:
-                moe.moe_profile_events(None, None)
+                    ev_in[i].record(copy_stream)
+            for i in seq:
+                cur.wait_event(ev_in[i])
+                step(i)
+                ev_done[i].record(cur)
+                copy_stream.wait_event(ev_done[i])
+                with torch.cuda.stream(copy_stream):
+                    h_out[i].copy_(finals[i], non_blocking=True)
+            ev_join.record(copy_stream)
+            cur.wait_event(ev_join)
 
         use_graph = not args.no_graph
         per = n_in                      # steps per full graph
@@ -456,7 +478,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": world * T * args.steps / (ms_e2e * 1e-3), "unit": "tok/s",
-                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+                "copies": "pinned host buffers, one copy in and one out per step, on a copy stream"},
         "gpu_launches": args.steps * wl.layers * launches_per_layer,
         "clocks": clk,
     }
