@@ -175,18 +175,30 @@ def test_route_repeated_calls_one_workspace(T):
     assert n_exact >= 0.6 * n_all
 
 
-@pytest.mark.parametrize("T", [1, 2, 3])
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
 @pytest.mark.parametrize("E", [1024, 777])
 def test_route_small_batch_many_experts(T, E):
     # small batches split each token's experts over several warps of the last
-    # router CTA (up to 512 experts a warp, 16 keys a lane); E = 777 leaves
-    # ragged parts
+    # router CTA (4 warps a token up to T = 4, then 2: up to 512 experts a
+    # warp, 16 keys a lane); E = 777 leaves ragged parts
     H, k = 512, 32
     x = synth.hidden(T, H, seed=40 + T)
     wr = synth.router(E, H, seed=41)
     ids, w = moe.moe_route(x.cuda(), wr.cuda(), k)
     torch.cuda.synchronize()
     # (a valid top-k within the gap for every token; ids exact where the gaps allow)
+    check_route(ids, w, oracle.router_logits(x, wr), k)
+
+
+@pytest.mark.parametrize("T,H,E,k", [(8, 8064, 64, 8), (5, 3072, 512, 10), (3, 6144, 16, 4), (7, 128, 5, 5)])
+def test_route_small_batch_wide_rows(T, H, E, k):
+    # the small-batch router stages the T x H activations in shared memory
+    # (126 KB at T = 8, H = 8064) and walks quarter rows in several passes
+    # once H > 3072; k == E leaves no choice
+    x = synth.hidden(T, H, seed=50 + T)
+    wr = synth.router(E, H, seed=51)
+    ids, w = moe.moe_route(x.cuda(), wr.cuda(), k)
+    torch.cuda.synchronize()
     check_route(ids, w, oracle.router_logits(x, wr), k)
 
 

@@ -221,6 +221,16 @@ __device__ inline uint32_t atom_acq_rel_add_u32(uint32_t *p, uint32_t v) {
     return old;
 }
 
+// Programmatic dependent launch. A kernel launched with the programmatic
+// stream-serialisation attribute may start while the kernel ahead of it in the
+// stream is still running; pdl_wait() returns once that kernel has completed
+// and its writes are visible (at once for a kernel launched without the
+// attribute). Nothing written by an earlier kernel may be read, and nothing an
+// earlier kernel reads may be written, before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream, if launched with the attribute, start
+// once every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ inline uint4 ld_cg_v4(const void *p) {
     uint4 v;
     asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -7,34 +7,37 @@
 // At decode the layer streams ~2.5 MB of packed weights per active expert
 // and does a few FLOPs per byte, so everything here serves the byte stream:
 //
-//  * One persistent CTA per SM, 16 warps. Each CTA first derives the whole
-//    token-to-expert permutation from topk_ids in shared memory (every CTA
-//    computes the same result), so no separate permute launch sits on the
-//    critical path. Small batches rank each assignment by comparison
-//    (slot = #assignments with a lower expert + #earlier ones with the same
-//    expert); larger ones use a histogram and prefix sum over the experts.
-//    The first weight copies are issued right after it; the activations are
-//    staged while they fly.
+//  * One persistent CTA per SM, launched programmatically behind the router,
+//    so that it takes its SM and sets up while the router finishes. Each CTA
+//    first derives the whole token-to-expert permutation from topk_ids in
+//    shared memory (every CTA computes the same result), so no separate
+//    permute launch sits on the critical path. Small batches rank each
+//    assignment by comparison (slot = #assignments with a lower expert +
+//    #earlier ones with the same expert); larger ones use a histogram and a
+//    prefix sum over the experts.
 //  * Work: gate_up tasks (8 gate rows and the matching 8 up rows of one
-//    expert) and down items (16 output rows of one expert, all of K = I).
-//    Each CTA takes a contiguous range of each list. A gate_up task belongs
-//    to one group of 4 warps, which splits its K: warp i of the group takes
-//    chunks i, i+4, ... (a chunk is 5 quantisation groups). The warp that
-//    finishes its part of a task last sums the 4 partial results in shared
-//    memory in a fixed order (deterministic) and publishes h. Down items are
-//    dealt to all 16 warps; every warp runs its gate_up work first.
-//  * Every chunk (~5.5 KB: two 2-D TMA boxes for gate_up, one 1-D bulk copy
-//    for down, plus scales) goes through a 2-stage shared-memory ring per
-//    warp completed on mbarriers, so a warp always has its next chunk in
-//    flight, including the first chunk of its next task or item.
+//    expert, all of K, in chunks of kGC quantisation groups) and down items
+//    (16 output rows of one expert, all of K = I). Each CTA takes a
+//    contiguous range of each list and runs them as one sequence of chunks:
+//    all its gate_up chunks first, then its down items.
+//  * One producer warp issues the copies of the sequence (two 2-D TMA boxes
+//    plus scales per gate_up chunk, a bulk copy plus scales per down item)
+//    into a ring of kNS shared-memory stages completed on mbarriers; its
+//    lanes issue side by side. The kCons consumer warps take chunks in
+//    sequence order by a shared ticket and hand each stage back as soon as
+//    they are done with it, so up to kNS copies are in flight per SM.
 //  * Weights are dequantised in registers into mma.sync m16n8k16 A fragments
-//    (bf16 holds q in [-8, 7] exactly); each group's fp32 partial sum is
-//    scaled by its bf16 scale, so W = q * scale is never rounded. Tokens are
-//    the N = 8 side. Activations for small T are staged once per CTA in
-//    shared memory, already in fragment order.
-//  * A down item of expert e waits (bounded, acquire) until all gate_up tasks
-//    of e have published SiLU(g)*u (bf16, stored in fragment order), then
-//    loads it from L2 into registers.
+//    (bf16 holds 128 + n exactly, and one lop3 makes a pair); each group's
+//    fp32 partial sum is corrected by 136 * sum(x) over the group and scaled
+//    by its bf16 scale, so W = q * scale is never rounded. Tokens are the
+//    N = 8 side. Activations for small T are staged once per CTA in shared
+//    memory, already in fragment order.
+//  * A gate_up chunk leaves its partial sums in a shared buffer of its task;
+//    the chunk that completes the task sums them in chunk order
+//    (deterministic), stores h = SiLU(g) * u (bf16, fragment order) and
+//    counts the task in its expert's counter (release).
+//  * A down item of expert e waits (bounded, acquire, with back-off) until
+//    all gate_up tasks of e are counted, then loads h from L2 into registers.
 //  * The combine is fused: after writing its fp32 down outputs, a down item
 //    counts, per (token, 16-row block), how many of the token's slots are
 //    done; the item that completes a block sums the slots in slot order and
@@ -716,8 +719,8 @@ __device__ __noinline__ void f_combine_block(const FusedParams &p, const Pro &v,
 }
 
 // Stack step, after every CTA has combined its blocks (a grid barrier on two
-// self-resetting counters; the launch is cooperative, so every CTA is resident
-// and the bounded wait ends): one CTA per token scales its row by
+// self-resetting counters; every CTA of the grid becomes resident, see the
+// launch, and the wait is bounded): one CTA per token scales its row by
 // 1/sqrt(mean(r^2) + eps) with 16-byte loads.
 __device__ __noinline__ void f_stack_rows(const FusedParams &p) {
     __shared__ float s_scale;
@@ -958,18 +961,22 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w1) : "memory");
+    const Pro v = pro_views(smem, p);
+    if (p.xs_off && threadIdx.x == 0) {
+        mbar_init(x_bar(v), 1);
+        fence_mbar_init();
+    }
+    // The launch is programmatic: the CTAs may start while the router still
+    // runs, and read its outputs (and the workspace) only once it has finished.
+    pdl_wait();
     // the ids are the first thing every path needs
     int id_reg = -1;
     if (p.T * p.k <= kFastN && (int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
-    const Pro v = pro_views(smem, p);
     if (p.xs_off && threadIdx.x == 0) {
-        uint64_t *xbar = x_bar(v);
         // the activations start moving now, behind the permutation
         const uint32_t xb = (uint32_t)p.T * p.H * 2;
-        mbar_init(xbar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(xbar, xb);
-        bulk_g2s(smem + p.xs_off, p.x, xb, xbar);
+        mbar_arrive_expect_tx(x_bar(v), xb);
+        bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
     }
     fused_prologue(p, smem, v, id_reg);
 
@@ -1091,9 +1098,15 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     cfg.blockDim = dim3(kFW * 32);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
+    // programmatic launch: the CTAs take their SMs and set up while the router
+    // finishes. The CTAs wait on one another; all of them become resident,
+    // since the grid is at most one CTA per SM and whatever else may hold an
+    // SM meanwhile (the router ahead) finishes without waiting on this grid,
+    // and a kernel behind it is launched only once every CTA has reached its
+    // exit. The waits are bounded all the same.
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, p);

@@ -315,81 +315,123 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const floa
     }
 }
 
-// Small batches (T <= 8): logits and top-k in one launch, no K split. Warp w
-// of CTA b computes the logits of expert 4b + w for every token: each lane
-// issues all of its 16-byte loads of the router row (8 columns per load, 256
-// columns per pass of the warp, kRouteLoads passes at once) before any
-// arithmetic, then runs fp32 FMAs against each token's activations and the
-// warp sums its lanes. Logits (with the bias) go to partial[0]. Each CTA then
-// counts itself on the control block's ticket (release); the CTA that
-// completes the count acquires every other CTA's logits, loads all T x E of
-// them at once into shared memory, and selects: for T < 4 each token's
-// experts are split over 4 / T warps whose candidates one warp then merges,
-// otherwise warp w takes tokens w, w + 4, ... The ticket is reset for the next
-// launch.
+// Small batches (T <= 8): logits and top-k in one launch, no K split over
+// CTAs. CTA b computes the logits of experts 4b .. 4b + 3 for every token;
+// the four warps of expert j (warps 4j .. 4j + 3) take a quarter of its router
+// row each. Every lane first issues its 16-byte loads of the row (8 columns
+// per load, 256 per pass of the warp, kRouteLoads passes at once); meanwhile
+// the CTA copies the T x H activations into shared memory, so that no token
+// costs a round trip of its own. Then fp32 FMAs, a warp sum, and the four
+// quarter sums added in order. Logits (with the bias) go to partial[0]. Each
+// CTA then counts itself on the control block's ticket (release); the CTA
+// that completes the count acquires every other CTA's logits, loads all
+// T x E of them into shared memory and selects: each token's experts are
+// split over wpt warps (4 for T <= 4, else 2), each takes the k largest of
+// its part, and one warp takes the k largest of their candidates. The ticket
+// is reset for the next launch.
 constexpr int kRouteInlineMaxT = 8;
-constexpr int kRouteLoads = 10;   // 16-byte loads per lane in flight (H <= 2560 in one pass)
+constexpr int kRouteWarps = 16;
+constexpr int kRouteLoads = 3;   // 16-byte loads per lane in flight (a quarter row of H <= 3072 in one pass)
+constexpr int kRouteMaxWpt = 4;
 
-__global__ void __launch_bounds__(128) route_small_kernel(const uint16_t *__restrict__ x,
-                                                          const uint16_t *__restrict__ wr,
-                                                          float *__restrict__ logits, int T, int H, int E,
-                                                          const float *__restrict__ bias, int k,
-                                                          int32_t *__restrict__ ids, float *__restrict__ w,
-                                                          Ctrl *ctrl) {
-    extern __shared__ float s_logit[];   // [T][E]
+inline size_t route_small_smem(const moe_dims &d) {
+    const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * 4;
+    return xb > lb ? xb : lb;
+}
+
+__global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uint16_t *__restrict__ x,
+                                                                       const uint16_t *__restrict__ wr,
+                                                                       float *__restrict__ logits, int T, int H,
+                                                                       int E, const float *__restrict__ bias, int k,
+                                                                       int32_t *__restrict__ ids,
+                                                                       float *__restrict__ w, Ctrl *ctrl) {
+    // the activations [T][H] bf16; in the last CTA, then, the logits [T][E] f32
+    extern __shared__ __align__(16) uint8_t s_raw[];
+    __shared__ float s_part[kRouteWarps][kRouteInlineMaxT];
+    __shared__ uint64_t s_cand[kRouteWarps][32];
     __shared__ int s_last;
+    // the expert kernel behind this one may be launched now (its CTAs wait
+    // for this grid's end themselves)
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 4 + warp;
-    if (e < E) {
-        float acc[kRouteInlineMaxT];
+    const int e = blockIdx.x * 4 + (warp >> 2);
+    const int q4 = H / 4, c_lo = (warp & 3) * q4, c_hi = c_lo + q4;
+    const uint16_t *row = wr + (size_t)(e < E ? e : 0) * H;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 wv[kRouteLoads];
 #pragma unroll
-        for (int t = 0; t < kRouteInlineMaxT; ++t) acc[t] = 0.f;
-        const uint16_t *row = wr + (size_t)e * H;
-        for (int c0 = 0; c0 < H; c0 += 256 * kRouteLoads) {
-            uint4 wv[kRouteLoads];
+    for (int i = 0; i < kRouteLoads; ++i) {
+        const int c = c_lo + 256 * i + 8 * lane;
+        wv[i] = e < E && c < c_hi ? ld_nc_v4(row + c) : zero;
+    }
+    uint4 *xs = reinterpret_cast<uint4 *>(s_raw);
+    const int nx = T * H / 8;
+    for (int i0 = threadIdx.x; i0 < nx; i0 += 4 * blockDim.x) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
+            v[u] = i < nx ? ld_nc_v4(x + 8 * (size_t)i) : zero;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < nx) xs[i] = v[u];
+        }
+    }
+    __syncthreads();
+    float acc[kRouteInlineMaxT];
+#pragma unroll
+    for (int t = 0; t < kRouteInlineMaxT; ++t) acc[t] = 0.f;
+    for (int c0 = c_lo; c0 < c_hi; c0 += 256 * kRouteLoads) {
+        if (c0 != c_lo) {
 #pragma unroll
             for (int i = 0; i < kRouteLoads; ++i) {
                 const int c = c0 + 256 * i + 8 * lane;
-                wv[i] = c < H ? ld_nc_v4(row + c) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int t = 0; t < kRouteInlineMaxT; ++t) {
-                if (t >= T) break;
-                const uint16_t *xr = x + (size_t)t * H;
-                // the token's loads are all issued before its FMAs
-                uint4 xv[kRouteLoads];
-#pragma unroll
-                for (int i = 0; i < kRouteLoads; ++i) {
-                    const int c = c0 + 256 * i + 8 * lane;
-                    xv[i] = c < H ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int i = 0; i < kRouteLoads; ++i) {
-                    const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-                    const uint32_t xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[t] = fmaf(__uint_as_float(ww[j] << 16), __uint_as_float(xx[j] << 16), acc[t]);
-                        acc[t] = fmaf(__uint_as_float(ww[j] & 0xffff0000u), __uint_as_float(xx[j] & 0xffff0000u), acc[t]);
-                    }
-                }
+                wv[i] = e < E && c < c_hi ? ld_nc_v4(row + c) : zero;
             }
         }
 #pragma unroll
         for (int t = 0; t < kRouteInlineMaxT; ++t) {
             if (t >= T) break;
-            float v = acc[t];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) logits[(size_t)t * E + e] = bias ? v + bias[e] : v;
+            for (int i = 0; i < kRouteLoads; ++i) {
+                const int c = c0 + 256 * i + 8 * lane;
+                const uint4 xv = c < c_hi ? xs[((size_t)t * H + c) / 8] : zero;
+                const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+                const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[t] = fmaf(__uint_as_float(ww[j] << 16), __uint_as_float(xx[j] << 16), acc[t]);
+                    acc[t] = fmaf(__uint_as_float(ww[j] & 0xffff0000u), __uint_as_float(xx[j] & 0xffff0000u), acc[t]);
+                }
+            }
         }
     }
-    // the CTA barrier orders every warp's logit stores before thread 0's release
+#pragma unroll
+    for (int t = 0; t < kRouteInlineMaxT; ++t) {
+        if (t >= T) break;
+        float v = acc[t];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) s_part[warp][t] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4 * kRouteInlineMaxT) {
+        const int jj = threadIdx.x / kRouteInlineMaxT, t = threadIdx.x % kRouteInlineMaxT;
+        const int ee = blockIdx.x * 4 + jj;
+        if (t < T && ee < E) {
+            const float v = ((s_part[4 * jj][t] + s_part[4 * jj + 1][t]) + s_part[4 * jj + 2][t]) + s_part[4 * jj + 3][t];
+            logits[(size_t)t * E + ee] = bias ? v + bias[ee] : v;
+        }
+    }
+    // the CTA barrier orders the logit stores before thread 0's release
     __syncthreads();
     if (threadIdx.x == 0) s_last = atom_acq_rel_add_u32(&ctrl->route_ticket, 1u) + 1 == gridDim.x;
     __syncthreads();
     if (!s_last) return;
     // the last CTA: all logits at once (8 loads per thread in flight), then top-k
+    float *s_logit = reinterpret_cast<float *>(s_raw);
     const int n = T * E;
     for (int i0 = 0; i0 < n; i0 += 8 * blockDim.x) {
         float lv[8];
@@ -405,61 +447,45 @@ __global__ void __launch_bounds__(128) route_small_kernel(const uint16_t *__rest
         }
     }
     __syncthreads();
-    const int nw = blockDim.x / 32;
-    const int wpt = T >= nw ? 1 : nw / T;   // warps per token
-    if (wpt == 1) {
-        for (int t = warp; t < T; t += nw) {
-            uint64_t key[kTopkPer];
+    const int wpt = T <= kRouteWarps / kRouteMaxWpt ? kRouteMaxWpt : kRouteWarps / kRouteInlineMaxT;
+    const int t = warp / wpt, part = warp % wpt;
+    const int ep = (E + wpt - 1) / wpt, lo = part * ep, hi = min(E, lo + ep);
+    if (t < T) {
+        uint64_t mine;
+        if (ep <= 128) {
+            uint64_t key[4];
 #pragma unroll
-            for (int i = 0; i < kTopkPer; ++i) {
-                const int ee = lane + 32 * i;
-                key[i] = ee < E ? topk_key(s_logit[t * E + ee], ee) : 0;
+            for (int i = 0; i < 4; ++i) {
+                const int ee = lo + lane + 32 * i;
+                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
             }
-            warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
-        }
-    } else {
-        // the token's experts split over wpt warps: each takes its part's k largest,
-        // then the part-0 warp takes the k largest of the wpt * k candidates
-        __shared__ uint64_t s_cand[4][32];
-        const int t = warp / wpt, part = warp % wpt;
-        const int ep = (E + wpt - 1) / wpt, lo = part * ep, hi = min(E, lo + ep);
-        uint64_t mine = 0;
-        if (t < T) {
-            if (ep <= 128) {
-                uint64_t key[4];
+            mine = warp_topk_n<4>(key, k, lane);
+        } else if (ep <= 256) {
+            uint64_t key[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int ee = lo + lane + 32 * i;
-                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
-                }
-                mine = warp_topk_n<4>(key, k, lane);
-            } else if (ep <= 256) {
-                uint64_t key[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int ee = lo + lane + 32 * i;
-                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
-                }
-                mine = warp_topk_n<8>(key, k, lane);
-            } else {
-                uint64_t key[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int ee = lo + lane + 32 * i;
-                    key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
-                }
-                mine = warp_topk_n<16>(key, k, lane);
+            for (int i = 0; i < 8; ++i) {
+                const int ee = lo + lane + 32 * i;
+                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
             }
-            s_cand[warp][lane] = lane < k ? mine : 0;
-        }
-        __syncthreads();
-        if (t < T && part == 0) {
-            uint64_t c[4];
+            mine = warp_topk_n<8>(key, k, lane);
+        } else {
+            uint64_t key[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) c[q] = q < wpt ? s_cand[warp + q][lane] : 0;
-            mine = warp_topk_n<4>(c, k, lane);
-            topk_finish(mine, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+            for (int i = 0; i < 16; ++i) {
+                const int ee = lo + lane + 32 * i;
+                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+            }
+            mine = warp_topk_n<16>(key, k, lane);
         }
+        s_cand[warp][lane] = lane < k ? mine : 0;
+    }
+    __syncthreads();
+    if (t < T && part == 0) {
+        uint64_t c[kRouteMaxWpt];
+#pragma unroll
+        for (int q = 0; q < kRouteMaxWpt; ++q) c[q] = q < wpt ? s_cand[warp + q][lane] : 0;
+        const uint64_t mine = warp_topk_n<kRouteMaxWpt>(c, k, lane);
+        topk_finish(mine, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
     }
     if (threadIdx.x == 0) ctrl->route_ticket = 0;
 }
@@ -486,9 +512,16 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     while (8 * nt < tt) nt <<= 1;
     dim3 grid((d.E + 63) / 64, ksplit, (d.T + 8 * nt - 1) / (8 * nt));
     if (d.T <= kRouteInlineMaxT) {
-        const size_t smem = (size_t)d.T * d.E * sizeof(float);
-        route_small_kernel<<<(d.E + 3) / 4, 128, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k, ids, w,
-                                                             ws_at<Ctrl>(ws, L.ctrl));
+        const size_t smem = route_small_smem(d);
+        if (smem > 48 * 1024) {
+            const cudaError_t err = set_smem_once(reinterpret_cast<const void *>(route_small_kernel),
+                                                  kRouteInlineMaxT * 8192 * 2);
+            if (err != cudaSuccess) return err;
+        }
+        // (a programmatic launch of this kernel behind the expert kernel was
+        // measured slower at T = 4: its CTAs then start on the first SMs freed)
+        route_small_kernel<<<(d.E + 3) / 4, 32 * kRouteWarps, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k,
+                                                                          ids, w, ws_at<Ctrl>(ws, L.ctrl));
         return cudaGetLastError();
     }
     switch (nt) {
