@@ -98,75 +98,16 @@ __device__ inline float f32_from_order_key(uint32_t k) {
 }
 
 // ---------------------------------------------------------------------------
-// Top-k for large batches: one warp per token. Lane l sums the K-split partial logits of experts
-// l, l+32, ... and forms their 64-bit keys (order key of the fp32 logit << 32
-// | 0xffffffff - id); k rounds of a two-step warp max with redux.sync (first
-// the logit half, then the id half among the lanes holding that logit) take
-// the k largest. Keys are unique, so every maximum has exactly one holder.
-// Weights: softmax over the selected logits in fp32.
-constexpr int kTopkWarps = 8;
-constexpr int kMaxKsplit = 16;   // router_ksplit() never returns more
-constexpr int kTopkPer = kMaxE / 32;
-
+// Top-k: keys pack an order key of the fp32 logit above 0xffffffff - id, so
+// keys are unique and one maximum gives value and id (ties to the lower id).
+// A warp's k largest: every lane sorts its keys, then k rounds of a two-step
+// warp max with redux.sync (first the logit half, then the id half among the
+// lanes holding that logit); the lane that held the maximum moves to its next
+// key. Weights: softmax over the selected logits in fp32.
 __device__ inline uint64_t warp_max_key(uint64_t m) {
     const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
     const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32) == hi ? (uint32_t)m : 0u);
     return ((uint64_t)hi << 32) | lo;
-}
-
-// Sorts the first N keys of a lane in descending order (bitonic network; all
-// indices are compile-time, so the keys stay in registers).
-template <int N>
-__device__ inline void sort_desc(uint64_t (&key)[kTopkPer]) {
-#pragma unroll
-    for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-        for (int stride = size / 2; stride > 0; stride >>= 1)
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int l = i ^ stride;
-                if (l > i) {
-                    const bool up = (i & size) != 0;   // this pair ends ascending
-                    const uint64_t a = key[i], b = key[l];
-                    if (up ? a > b : a < b) {
-                        key[i] = b;
-                        key[l] = a;
-                    }
-                }
-            }
-}
-
-// The k largest keys over the warp: every lane sorts its keys, then each round
-// takes the warp maximum of the lanes' heads and the lane that held it moves
-// to its next key; lane j < k ends with the j-th largest. Writes ids and the
-// softmax over the selected logits.
-__device__ inline void warp_topk_write(uint64_t (&key)[kTopkPer], int nper, int k, int lane, int32_t *ids_row,
-                                       float *w_row) {
-    constexpr int kHalf = kTopkPer / 2;
-    if (nper <= kHalf)
-        sort_desc<kHalf>(key);
-    else
-        sort_desc<kTopkPer>(key);
-    uint64_t mine = 0;
-    for (int j = 0; j < k; ++j) {
-        const uint64_t m = warp_max_key(key[0]);
-        if (key[0] == m) {   // keys are unique: one lane
-#pragma unroll
-            for (int i = 0; i + 1 < kTopkPer; ++i) key[i] = key[i + 1];
-            key[kTopkPer - 1] = 0;
-        }
-        if (lane == j) mine = m;
-    }
-    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
-    const float l = f32_from_order_key((uint32_t)(mine >> 32));
-    const float p = lane < k ? expf(l - lmax) : 0.f;
-    float z = p;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane < k) {
-        ids_row[lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
-        w_row[lane] = p / z;
-    }
 }
 
 // Size-generic forms for lanes holding N keys each (N a power of two): sort,
@@ -225,93 +166,63 @@ __device__ inline uint64_t topk_key(float logit, int e) {
     return ((uint64_t)f32_order_key(logit) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
 }
 
+// Top-k for T > 8 tokens: one CTA of four warps per token. Warp w takes the
+// experts [w * ep, (w + 1) * ep), ep = ceil(E / 4) <= 256: lane l sums the
+// K-split partial logits of experts lo + l, lo + l + 32, ... (all loads of a
+// split in flight at once), adds the bias and forms the keys; the warp takes
+// the k largest of its part, and warp 0 the k largest of the four parts'
+// candidates.
+constexpr int kTopkWarps = 4;
+
+template <int N>
+__device__ inline uint64_t part_topk(const float *__restrict__ row, size_t split_stride, int ksplit,
+                                     const float *__restrict__ bias, int lo, int hi, int k, int lane) {
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = 0.f;
+    for (int s = 0; s < ksplit; ++s) {
+        float u[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int e = lo + lane + 32 * i;
+            u[i] = e < hi ? __ldcg(row + s * split_stride + e) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] += u[i];
+    }
+    uint64_t key[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int e = lo + lane + 32 * i;
+        key[i] = e < hi ? topk_key(bias ? v[i] + bias[e] : v[i], e) : 0;
+    }
+    return warp_topk_n<N>(key, k, lane);
+}
+
 __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float *__restrict__ partial, int ksplit,
                                                                      const float *__restrict__ bias, int T, int E,
                                                                      int k, int32_t *__restrict__ ids,
                                                                      float *__restrict__ w) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
-    if (t >= T) return;
-    uint64_t key[kTopkPer];
-#pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
-        key[i] = 0;
-        const int e = lane + 32 * i;
-        if (e < E) {
-            // the split partials are independent loads: unrolled, they are all in flight at once
-            float l = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxKsplit; ++s)
-                if (s < ksplit) l += partial[((size_t)s * T + t) * E + e];
-            if (bias) l += bias[e];
-            key[i] = topk_key(l, e);
-        }
-    }
-    warp_topk_write(key, (E + 31) / 32, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
-}
-
-// Small batches: one CTA of 256 threads per token, so that the K-split partial
-// sums of a token's experts are spread over many threads. Thread i forms the
-// keys of experts i, i+256, ...; each warp extracts its own k largest keys,
-// then warp 0 takes the k largest of the 8 warps' candidates.
-constexpr int kTopkThreads = 256;
-constexpr int kTopkCtaPer = kMaxE / kTopkThreads;
-
-__global__ void __launch_bounds__(kTopkThreads) route_topk_cta_kernel(const float *__restrict__ partial, int ksplit,
-                                                                  const float *__restrict__ bias, int T, int E,
-                                                                  int k, int32_t *__restrict__ ids,
-                                                                  float *__restrict__ w) {
-    __shared__ uint64_t cand[kTopkThreads / 32][kMaxK];
+    __shared__ uint64_t s_cand[kTopkWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x;
-    uint64_t key[kTopkCtaPer];
-#pragma unroll
-    for (int i = 0; i < kTopkCtaPer; ++i) {
-        key[i] = 0;
-        const int e = threadIdx.x + kTopkThreads * i;
-        if (e < E) {
-            float l = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxKsplit; ++s)
-                if (s < ksplit) l += partial[((size_t)s * T + t) * E + e];
-            if (bias) l += bias[e];
-            key[i] = topk_key(l, e);
-        }
-    }
-    for (int j = 0; j < k; ++j) {
-        uint64_t m = 0;
-#pragma unroll
-        for (int i = 0; i < kTopkCtaPer; ++i) m = key[i] > m ? key[i] : m;
-        m = warp_max_key(m);
-#pragma unroll
-        for (int i = 0; i < kTopkCtaPer; ++i) key[i] = key[i] == m ? 0 : key[i];
-        if (lane == 0) cand[warp][j] = m;
-    }
+    const int ep = (E + kTopkWarps - 1) / kTopkWarps, lo = warp * ep, hi = min(E, lo + ep);
+    const float *row = partial + (size_t)t * E;
+    const size_t ss = (size_t)T * E;
+    uint64_t mine;
+    if (ep <= 64)
+        mine = part_topk<2>(row, ss, ksplit, bias, lo, hi, k, lane);
+    else if (ep <= 128)
+        mine = part_topk<4>(row, ss, ksplit, bias, lo, hi, k, lane);
+    else
+        mine = part_topk<8>(row, ss, ksplit, bias, lo, hi, k, lane);
+    s_cand[warp][lane] = lane < k ? mine : 0;
     __syncthreads();
-    if (warp != 0) return;
-    // lane l holds candidate slot l of every warp's list
-    uint64_t c[kTopkThreads / 32];
+    if (warp == 0) {
+        uint64_t c[kTopkWarps];
 #pragma unroll
-    for (int v = 0; v < kTopkThreads / 32; ++v) c[v] = lane < k ? cand[v][lane] : 0;
-    uint64_t mine = 0;
-    for (int j = 0; j < k; ++j) {
-        uint64_t m = 0;
-#pragma unroll
-        for (int v = 0; v < kTopkThreads / 32; ++v) m = c[v] > m ? c[v] : m;
-        m = warp_max_key(m);
-#pragma unroll
-        for (int v = 0; v < kTopkThreads / 32; ++v) c[v] = c[v] == m ? 0 : c[v];
-        if (lane == j) mine = m;
-    }
-    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
-    const float l = f32_from_order_key((uint32_t)(mine >> 32));
-    const float p = lane < k ? expf(l - lmax) : 0.f;
-    float z = p;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane < k) {
-        ids[(size_t)t * k + lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
-        w[(size_t)t * k + lane] = p / z;
+        for (int q = 0; q < kTopkWarps; ++q) c[q] = s_cand[q][lane];
+        topk_finish(warp_topk_n<kTopkWarps>(c, k, lane), k, lane, ids + (size_t)t * k, w + (size_t)t * k);
     }
 }
 
@@ -498,13 +409,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     if (router_tc(d)) {
         cudaError_t err = launch_route_logits_tc(x, wr, d, partial, ksplit, ws_at<Ctrl>(ws, L.ctrl), s);
         if (err != cudaSuccess) return err;
-        // a warp per token once there are enough tokens to fill the GPU with warps
-        // (and few K splits to sum); a CTA per token below that
-        if (d.T >= 2048)
-            route_topk_kernel<<<(d.T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias,
-                                                                                         d.T, d.E, d.k, ids, w);
-        else
-            route_topk_cta_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+        route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
         return cudaGetLastError();
     }
     const int tt = d.T <= 64 ? d.T : 64;
@@ -532,7 +437,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_topk_cta_kernel<<<d.T, kTopkThreads, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+    route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
     return cudaGetLastError();
 }
 

@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(128, 1) route_logits_tc_kernel(const __grid_co
                     mbar_wait(&full[j % kRtStages], (j / kRtStages) & 1);
             }
         }
+        // the other lanes wait here, not in the spin on the accumulator below:
+        // spinning beside the producing lane of their own warp held it back
+        __syncwarp();
     } else if (warp == 1) {
         const uint32_t idesc = tc::idesc_bf16(128, 128);
         for (int i = 0; i < nk; ++i) {
