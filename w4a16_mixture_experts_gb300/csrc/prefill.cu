@@ -486,31 +486,42 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 // xs[slot] = x[token of slot] in fragment order within each 8-element chunk
 // (0,4,1,5,2,6,3,7), for the offsets[E] slots that hold a valid assignment.
-__global__ void xgather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                               const int32_t *__restrict__ offsets, int E, int H, int k, uint16_t *__restrict__ xs) {
+// A warp copies whole rows: the row's token is read once (the next row's is
+// fetched while this one moves), then up to kXgLoads 16-byte chunks per lane
+// are in flight at once.
+constexpr int kXgThreads = 256;
+constexpr int kXgLoads = 10;   // a 2560-wide row in one pass
+
+__global__ void __launch_bounds__(kXgThreads) xgather_kernel(const uint16_t *__restrict__ x,
+                                                             const int32_t *__restrict__ perm,
+                                                             const int32_t *__restrict__ offsets, int E, int H, int k,
+                                                             uint16_t *__restrict__ xs) {
     const int nslots = offsets[E];
     const int cpr = H / 8;   // 16-byte chunks per row
-    const int64_t n = (int64_t)nslots * cpr;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    // four independent chunks per pass, so that four loads are in flight per thread
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
-        uint4 v[4];
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (kXgThreads / 32);
+    int slot = blockIdx.x * (kXgThreads / 32) + (threadIdx.x >> 5);
+    int tok = slot < nslots ? perm[slot] / k : 0;
+    for (; slot < nslots; slot += nw) {
+        const int nxt = slot + nw < nslots ? perm[slot + nw] / k : 0;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)slot * H);
+        for (int c0 = lane; c0 < cpr; c0 += 32 * kXgLoads) {
+            uint4 v[kXgLoads];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t i = i0 + u * stride;
-            if (i < n) {
-                const int slot = (int)(i / cpr), c = (int)(i - (int64_t)slot * cpr);
-                v[u] = ld_nc_v4(x + (size_t)(perm[slot] / k) * H + 8 * c);
+            for (int u = 0; u < kXgLoads; ++u) {
+                const int c = c0 + 32 * u;
+                v[u] = c < cpr ? ld_nc_v4(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kXgLoads; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < cpr)
+                    dst[c] = make_uint4(__byte_perm(v[u].x, v[u].z, 0x5410), __byte_perm(v[u].x, v[u].z, 0x7632),
+                                        __byte_perm(v[u].y, v[u].w, 0x5410), __byte_perm(v[u].y, v[u].w, 0x7632));
             }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t i = i0 + u * stride;
-            if (i < n)
-                *reinterpret_cast<uint4 *>(xs + (size_t)i * 8) =
-                    make_uint4(__byte_perm(v[u].x, v[u].z, 0x5410), __byte_perm(v[u].x, v[u].z, 0x7632),
-                               __byte_perm(v[u].y, v[u].w, 0x5410), __byte_perm(v[u].y, v[u].w, 0x7632));
-        }
+        tok = nxt;
     }
 }
 
@@ -599,30 +610,37 @@ __global__ void __launch_bounds__(kConvThreads) acc_convert_kernel(float *__rest
     const int t = blockIdx.x;
     float4 *row = reinterpret_cast<float4 *>(acc + (size_t)t * H);
     const int n4 = H / 4;
-    if (!next) {
-        uint2 *o = reinterpret_cast<uint2 *>(out + (size_t)t * H);
-        for (int i = threadIdx.x; i < n4; i += kConvThreads) {
-            const float4 v = row[i];
-            row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            o[i] = bf16x4(v.x, v.y, v.z, v.w);
-        }
-        return;
-    }
-    const uint2 *xr = reinterpret_cast<const uint2 *>(x + (size_t)t * H);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the whole row in flight at once (and, for the stack, the residual row)
     float4 r[kConvPer];
-    float ss = 0.f;
+    uint2 xv[kConvPer];
+    const uint2 *xr = reinterpret_cast<const uint2 *>(x + (size_t)t * H);
 #pragma unroll
     for (int j = 0; j < kConvPer; ++j) {
         const int i = threadIdx.x + kConvThreads * j;
-        r[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n4) {
-            const float4 v = row[i];
-            const uint2 xv = xr[i];
-            r[j] = make_float4(v.x + __uint_as_float(xv.x << 16), v.y + __uint_as_float(xv.x & 0xffff0000u),
-                               v.z + __uint_as_float(xv.y << 16), v.w + __uint_as_float(xv.y & 0xffff0000u));
-            row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            ss += r[j].x * r[j].x + r[j].y * r[j].y + r[j].z * r[j].z + r[j].w * r[j].w;
+        r[j] = i < n4 ? row[i] : zero;
+        xv[j] = next && i < n4 ? xr[i] : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kConvPer; ++j) {
+        const int i = threadIdx.x + kConvThreads * j;
+        if (i < n4) row[i] = zero;
+    }
+    if (!next) {
+        uint2 *o = reinterpret_cast<uint2 *>(out + (size_t)t * H);
+#pragma unroll
+        for (int j = 0; j < kConvPer; ++j) {
+            const int i = threadIdx.x + kConvThreads * j;
+            if (i < n4) o[i] = bf16x4(r[j].x, r[j].y, r[j].z, r[j].w);
         }
+        return;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kConvPer; ++j) {
+        r[j] = make_float4(r[j].x + __uint_as_float(xv[j].x << 16), r[j].y + __uint_as_float(xv[j].x & 0xffff0000u),
+                           r[j].z + __uint_as_float(xv[j].y << 16), r[j].w + __uint_as_float(xv[j].y & 0xffff0000u));
+        ss += r[j].x * r[j].x + r[j].y * r[j].y + r[j].z * r[j].z + r[j].w * r[j].w;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -654,8 +672,15 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
-    xgather_kernel<<<(unsigned)(4 * sm_count()), 256, 0, s>>>(a.x, ws_at<int32_t>(ws, W.perm),
-                                                            ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm);
+    {
+        // a warp per row, at most 8 CTAs of 8 warps per SM
+        const long long rows = (long long)d.T * d.k, per_cta = kXgThreads / 32;
+        long long grid = (rows + per_cta - 1) / per_cta;
+        if (grid > 8LL * sm_count()) grid = 8LL * sm_count();
+        if (grid < 1) grid = 1;
+        xgather_kernel<<<(unsigned)grid, kXgThreads, 0, s>>>(a.x, ws_at<int32_t>(ws, W.perm),
+                                                             ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm);
+    }
     chunk_scan_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), d.E, chunk_base);
     int4 *chunk_info = ws_at<int4>(ws, W.chunk_info);
     const int max_chunks = (int)((int64_t)d.T * d.k / kPN) + d.E + 1;
