@@ -442,10 +442,14 @@ def run_ours(args, rank, world, local):
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
     flops_launch = 2.0 * 3 * H * I * T * k           # algorithmic: gate, up and down over all slots
     expert_kernel = "decode_fused_kernel" if fused else "prefill_kernel (gate_up + down launches)"
-    if not wl.name.startswith(("decode", "stack_decode")):
-        tflops = flops_launch * len(durs) / (sum(durs) * 1e-3) / 1e12
-        peak_key = "bf16_tflops_sustained" if stack else "bf16_tflops"
-        roof = {"kernel": "prefill_kernel (gate_up + down launches)", "bound": "tensor", "achieved": tflops,
+    # the binding roofline: whichever of the unique weight bytes at the copy rate
+    # and the flops at the tensor rate takes longer
+    tflops = flops_launch * len(durs) / (sum(durs) * 1e-3) / 1e12
+    peak_key = "bf16_tflops_sustained" if stack else "bf16_tflops"
+    t_hbm = statistics.mean(bytes_l) / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops_launch / (pk[peak_key] * 1e12)
+    if t_tc > t_hbm:
+        roof = {"kernel": expert_kernel, "bound": "tensor", "achieved": tflops,
                 "peak": pk[peak_key], "peak_source": "%s %s (cuBLAS bf16)" % (pk_src, peak_key), "unit": "TFLOP/s",
                 "frac": tflops / pk[peak_key], "traffic": recorded_traffic(wl.name),
                 "algorithmic_flops_per_launch": flops_launch,
@@ -453,7 +457,8 @@ def run_ours(args, rank, world, local):
     else:
         roof = {"kernel": expert_kernel, "bound": "hbm", "achieved": hbm_gbs, "peak": pk["hbm_gbs"],
                 "peak_source": pk_src + " hbm_gbs (copy)", "unit": "GB/s", "frac": hbm_gbs / pk["hbm_gbs"],
-                "traffic": recorded_traffic(wl.name)}
+                "traffic": recorded_traffic(wl.name),
+                "tensor_achieved_tflops": tflops, "tensor_frac": tflops / pk[peak_key]}
     roof.update({"algorithmic_bytes_per_launch": statistics.mean(bytes_l),
                  "kernel_ms_per_launch": statistics.mean(durs), "launches_measured": len(durs),
                  "unique_experts_per_launch": statistics.mean(bytes_l) / EXPERT_BYTES})
