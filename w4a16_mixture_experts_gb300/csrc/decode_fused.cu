@@ -567,8 +567,9 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
                     X[m] = make_uint4(__byte_perm(X[m].x, X[m].z, 0x5410), __byte_perm(X[m].x, X[m].z, 0x7632),
                                       __byte_perm(X[m].y, X[m].w, 0x5410), __byte_perm(X[m].y, X[m].w, 0x7632));
             }
-            // one accumulator per word keeps the mma chains two deep
-            float c[4][4];
+            // the group's 8 MMAs accumulate in one fragment (fewer adds than a
+            // fragment per word; the two groups in flight keep the pipe busy)
+            float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const uint32_t xg = fw_word(wg, m), xu = fw_word(wu, m);
@@ -582,19 +583,18 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
                     f0[0] = int4_pair(xg, 0), f0[1] = int4_pair(xu, 0), f0[2] = int4_pair(xg, 1), f0[3] = int4_pair(xu, 1);
                     f1[0] = int4_pair(xg, 2), f1[1] = int4_pair(xu, 2), f1[2] = int4_pair(xg, 3), f1[3] = int4_pair(xu, 3);
                 }
-                c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
-                mma_bf16_16816(c[m], f0, X[m].x, X[m].y);
-                mma_bf16_16816(c[m], f1, X[m].z, X[m].w);
+                mma_bf16_16816(cc, f0, X[m].x, X[m].y);
+                mma_bf16_16816(cc, f1, X[m].z, X[m].w);
             }
             float b0 = 0.f, b1 = 0.f;
             if (kStaged) {
                 b0 = xs0 ? 136.f * xs0[q] : 0.f;
                 b1 = xs1 ? 136.f * xs1[q] : 0.f;
             }
-            a0 += sg * (((c[0][0] + c[1][0]) + (c[2][0] + c[3][0])) - b0);
-            a1 += sg * (((c[0][1] + c[1][1]) + (c[2][1] + c[3][1])) - b1);
-            a2 += su * (((c[0][2] + c[1][2]) + (c[2][2] + c[3][2])) - b0);
-            a3 += su * (((c[0][3] + c[1][3]) + (c[2][3] + c[3][3])) - b1);
+            a0 += sg * (cc[0] - b0);
+            a1 += sg * (cc[1] - b1);
+            a2 += su * (cc[2] - b0);
+            a3 += su * (cc[3] - b1);
         }
 #pragma unroll
         for (int i = 0; i < kMaxNT; ++i)
@@ -811,20 +811,19 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
                 const uint4 w1 = lds_v4(stage + (R + 8) * rb + 64 * q + 16 * tig);
                 const float s0v = bf16_bits_to_f32(sc[R * G2 + q]);
                 const float s1v = bf16_bits_to_f32(sc[(R + 8) * G2 + q]);
-                float c[4][4];
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const uint32_t x0 = fw_word(w0, m), x1 = fw_word(w1, m);
                     const uint32_t f0[4] = {int4_pair(x0, 0), int4_pair(x1, 0), int4_pair(x0, 1), int4_pair(x1, 1)};
                     const uint32_t f1[4] = {int4_pair(x0, 2), int4_pair(x1, 2), int4_pair(x0, 3), int4_pair(x1, 3)};
-                    c[m][0] = c[m][1] = c[m][2] = c[m][3] = 0.f;
-                    mma_bf16_16816(c[m], f0, Y[m].x, Y[m].y);
-                    mma_bf16_16816(c[m], f1, Y[m].z, Y[m].w);
+                    mma_bf16_16816(cc, f0, Y[m].x, Y[m].y);
+                    mma_bf16_16816(cc, f1, Y[m].z, Y[m].w);
                 }
-                acc[s][0] += s0v * ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0]));
-                acc[s][1] += s0v * ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1]));
-                acc[s][2] += s1v * ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2]));
-                acc[s][3] += s1v * ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+                acc[s][0] += s0v * cc[0];
+                acc[s][1] += s0v * cc[1];
+                acc[s][2] += s1v * cc[2];
+                acc[s][3] += s1v * cc[3];
             }
         };
         // h comes from L2: a ring of 4 groups in registers, the first 4 loaded
