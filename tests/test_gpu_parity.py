@@ -367,6 +367,47 @@ def test_forward_rms_stack_step():
     assert_close(nxt.float().cpu().numpy(), ref_next, "rms")
 
 
+def _stack_chain(name, n_layers, seed, rows=None):
+    """Layers of a stack chained on the GPU: route, experts, residual + RMS
+    rescale, the output feeding the next layer. Each layer is checked against
+    the oracle on the GPU's own input to it (so near ties cannot make the two
+    trajectories drift apart): the routing within the gap, then the layer's
+    output given the routing the GPU took (checked valid just before)."""
+    wl = synth.WORKLOADS[name]
+    T, H, E, k, I = wl.dims
+    x = synth.hidden(T, H, seed=seed).cuda()
+    ws = moe.workspace(T, H, E, k, I)
+    sel = np.arange(T) if rows is None else rows
+    for l in range(n_layers):
+        h = synth.layer_inputs(wl, seed=seed, layer=l)
+        W = [h[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
+        ids, w = moe.moe_route(x, h["router_w"].cuda(), k, ws=ws)
+        nxt = moe.moe_w4a16_forward_rms(x, ids, w, *W, eps=1e-6, ws=ws)
+        torch.cuda.synchronize()
+        assert moe.moe_check_device_error(ws) == 0
+        xh = x.cpu()[sel]
+        ids_h, w_h = ids.cpu()[sel], w.cpu()[sel]
+        check_route(ids_h, w_h, oracle.router_logits(xh, h["router_w"]), k)
+        ref_out = oracle.expert_forward(xh, ids_h, w_h, h["w1_packed"], h["w1_scales"], h["w2_packed"],
+                                        h["w2_scales"], E, I)
+        _, ref_next = oracle.residual_rms(xh, ref_out, eps=1e-6)
+        assert_close(nxt.float().cpu().numpy()[sel], ref_next, "%s layer %d" % (name, l))
+        x = nxt
+        del W, h
+
+
+def test_stack_decode_chained_layers():
+    # three full-shape layers of the 4-token decode stack (the fused decode kernel)
+    _stack_chain("stack_decode4", 3, seed=7)
+
+
+def test_stack_prefill_chained_layers_sampled():
+    # two full-shape layers of the 4096-token prefill stack (tensor-core path),
+    # 48 sampled rows checked per layer
+    rows = np.sort(np.random.default_rng(8).choice(4096, 48, replace=False))
+    _stack_chain("stack_prefill4096", 2, seed=8, rows=rows)
+
+
 # ------------------------------------------------------- prefill (tcgen05) ----
 
 @pytest.mark.parametrize("T,H,E,k,I", [
