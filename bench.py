@@ -435,9 +435,9 @@ def run_ours(args, rank, world, local):
     ms_e2e = max_over_ranks(ms_e2e, world)
     # route: one kernel for T <= 8 (logits, then top-k in the last CTA), else logits +
     # top-k; forward: one fused kernel (the library's decode path, T <= 7) or permute 3
-    # + x gather + chunk scan + chunk table + gate_up + down + convert
+    # + x gather + chunk table + gate_up + down + convert
     fused = T <= FUSED_MAX_T
-    launches_per_layer = (1 if T <= 8 else 2) + (1 if fused else 9)
+    launches_per_layer = (1 if T <= 8 else 2) + (1 if fused else 8)
     pk, pk_src = peaks()
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
     flops_launch = 2.0 * 3 * H * I * T * k           # algorithmic: gate, up and down over all slots

@@ -49,8 +49,8 @@ struct WsLayout {
     size_t ybuf;         // f32 [T*k][H]   down-projection output per slot (decode path)
     size_t xperm;        // bf16 [T*k][H]  activations per slot, fragment order (prefill path)
     size_t out_acc;      // f32 [T][H]     weighted output accumulator (prefill path)
-    size_t chunk_base;   // i32 [E+1]      first 128-token chunk per active expert (prefill path)
-    size_t chunk_info;   // i32x4 [T*k/128+E+1] per chunk: expert, first slot, tokens (prefill path)
+    size_t n_chunks;     // i32 [1]        chunks in chunk_info (prefill path)
+    size_t chunk_info;   // i32x4 [T*k/128+E+1] per chunk of at most 128 tokens: expert, first slot, tokens (prefill path)
     size_t total;
     int ksplit;
     int nchunk;
@@ -109,7 +109,7 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.ybuf = take(small ? T * k * H * 4 : 0);
     L.xperm = take(small ? 0 : T * k * H * 2);
     L.out_acc = take(small ? 0 : T * H * 4);
-    L.chunk_base = take((E + 1) * 4);
+    L.n_chunks = take(4);
     L.chunk_info = take(small ? 0 : (T * k / 128 + E + 1) * 16);
     L.total = o;
     return L;

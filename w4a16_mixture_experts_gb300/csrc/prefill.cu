@@ -96,8 +96,8 @@ struct PrefillParams {
     const uint16_t *scales;    // bf16 [rows][K/128]
     const int32_t *offsets;    // [E+1] slot offsets per expert
     const int32_t *active;     // active experts, increasing
-    const int32_t *chunk_base; // [n_active+1] first 128-token chunk of each active expert
-    const int4 *chunk_info;    // per 128-token chunk: expert, first slot, tokens
+    const int32_t *n_chunks;   // [1] chunks in chunk_info
+    const int4 *chunk_info;    // per chunk of at most 128 tokens: expert, first slot, tokens
     const int32_t *perm;       // slot -> assignment t*k+j
     const float *topk_w;
     const Ctrl *ctrl;
@@ -232,8 +232,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int nact = (int)p.ctrl->n_active;
-    const int ntiles = nact > 0 ? p.chunk_base[nact] * p.mb : 0;
+    const int ntiles = *p.n_chunks * p.mb;
     const int G = p.K / kKS;   // stages per tile
 
     if (warp < kWEpi) {
@@ -525,68 +524,67 @@ __global__ void __launch_bounds__(kXgThreads) xgather_kernel(const uint16_t *__r
     }
 }
 
-// One CTA: first 128-token chunk of each active expert (exclusive scan over
-// the active list, in expert order).
-__global__ void __launch_bounds__(1024) chunk_scan_kernel(const int32_t *__restrict__ counts, int E,
-                                                          int32_t *__restrict__ chunk_base) {
-    __shared__ int warp_sums[32];
+// The chunk table of the two persistent launches, in one CTA. Each active
+// expert's slots are split into c = ceil(count / 128) chunks of near-equal
+// size (the first count % c of them one token larger); the experts are
+// ordered by that size, largest first (by 16-token band, ties in expert
+// order), with each expert's chunks adjacent. The kernels deal tiles
+// round-robin in this order, so every CTA gets a tile of each size band and
+// the launch ends with the small ones, while an expert's chunks still run side
+// by side (its weights come from HBM once, the other chunks find them in L2).
+// chunk_info[i] = (expert, first slot, tokens); *n_chunks = their number.
+constexpr int kNBands = kPN / 16;
+
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *__restrict__ counts,
+                                                           const int32_t *__restrict__ offsets, int E,
+                                                           int32_t *__restrict__ n_chunks,
+                                                           int4 *__restrict__ chunk_info) {
+    __shared__ int s_warp[32][kNBands];   // chunks of each band in each warp, then the exclusive prefix
+    __shared__ int s_band[kNBands];       // first chunk of each band
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
-    const int c = e < E ? (counts[e] + kPN - 1) / kPN : 0;
-    const int act = e < E && counts[e] > 0;
-    // two inclusive scans at once: chunks and active flags
-    int ic = c, ia = act;
+    const int cnt = e < E ? counts[e] : 0;
+    const int c = (cnt + kPN - 1) / kPN;
+    const int band = c ? kNBands - ((cnt + c - 1) / c + 15) / 16 : -1;
+    int before = 0;   // chunks of e's band held by lower experts of this warp
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int oc = __shfl_up_sync(0xffffffffu, ic, off), oa = __shfl_up_sync(0xffffffffu, ia, off);
-        if (lane >= off) {
-            ic += oc;
-            ia += oa;
-        }
-    }
-    __shared__ int wa[32];
-    if (lane == 31) {
-        warp_sums[w] = ic;
-        wa[w] = ia;
-    }
-    __syncthreads();
-    if (w == 0) {
-        int sc = warp_sums[lane], sa = wa[lane];
-        int xc = sc, xa = sa;
+    for (int b = 0; b < kNBands; ++b) {
+        const int v = band == b ? c : 0;
+        int iv = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int oc = __shfl_up_sync(0xffffffffu, xc, off), oa = __shfl_up_sync(0xffffffffu, xa, off);
-            if (lane >= off) {
-                xc += oc;
-                xa += oa;
-            }
+            const int o = __shfl_up_sync(0xffffffffu, iv, off);
+            if (lane >= off) iv += o;
         }
-        warp_sums[lane] = xc - sc;
-        wa[lane] = xa - sa;
+        if (band == b) before = iv - v;
+        if (lane == 31) s_warp[w][b] = iv;
     }
     __syncthreads();
-    const int base_c = warp_sums[w] + ic - c;   // exclusive
-    const int base_a = wa[w] + ia - act;
-    if (act) chunk_base[base_a] = base_c;
-    if (e == E - 1) chunk_base[base_a + act] = base_c + c;
-}
-
-// chunk_info[c] = (expert, first slot, tokens) of 128-token chunk c.
-__global__ void __launch_bounds__(256) chunk_info_kernel(const int32_t *__restrict__ chunk_base,
-                                                         const int32_t *__restrict__ active,
-                                                         const int32_t *__restrict__ offsets, const Ctrl *ctrl,
-                                                         int4 *__restrict__ chunk_info) {
-    const int nact = (int)ctrl->n_active;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (nact == 0 || c >= chunk_base[nact]) return;
-    int lo = 0, hi = nact;   // largest a with chunk_base[a] <= c
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (chunk_base[mid] <= c) lo = mid;
-        else hi = mid;
+    if (e < kNBands) {   // exclusive prefix over the warps, band e
+        int run = 0;
+        for (int ww = 0; ww < 32; ++ww) {
+            const int v = s_warp[ww][e];
+            s_warp[ww][e] = run;
+            run += v;
+        }
+        s_band[e] = run;
     }
-    const int e = active[lo], j = c - chunk_base[lo];
-    const int cnt = offsets[e + 1] - offsets[e];
-    chunk_info[c] = make_int4(e, offsets[e] + j * kPN, min(kPN, cnt - j * kPN), 0);
+    __syncthreads();
+    if (e == 0) {
+        int run = 0;
+        for (int b = 0; b < kNBands; ++b) {
+            const int v = s_band[b];
+            s_band[b] = run;
+            run += v;
+        }
+        *n_chunks = run;
+    }
+    __syncthreads();
+    if (c > 0) {
+        const int first = s_band[band] + s_warp[w][band] + before;
+        const int base = cnt / c, rem = cnt % c;
+        for (int j = 0; j < c; ++j)
+            chunk_info[first + j] = make_int4(e, offsets[e] + j * base + min(j, rem), base + (j < rem), 0);
+    }
 }
 
 // out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue), then out_acc = 0.
@@ -668,7 +666,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     const WsLayout W = ws_layout(d);
     uint16_t *xperm = ws_at<uint16_t>(ws, W.xperm);
     float *out_acc = ws_at<float>(ws, W.out_acc);
-    int32_t *chunk_base = ws_at<int32_t>(ws, W.chunk_base);
+    int32_t *n_chunks = ws_at<int32_t>(ws, W.n_chunks);
     cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
@@ -681,18 +679,15 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
         xgather_kernel<<<(unsigned)grid, kXgThreads, 0, s>>>(a.x, ws_at<int32_t>(ws, W.perm),
                                                              ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm);
     }
-    chunk_scan_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), d.E, chunk_base);
     int4 *chunk_info = ws_at<int4>(ws, W.chunk_info);
-    const int max_chunks = (int)((int64_t)d.T * d.k / kPN) + d.E + 1;
-    chunk_info_kernel<<<(max_chunks + 255) / 256, 256, 0, s>>>(chunk_base, ws_at<int32_t>(ws, W.active),
-                                                              ws_at<int32_t>(ws, W.offsets), ws_at<Ctrl>(ws, W.ctrl),
-                                                              chunk_info);
+    chunk_table_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), ws_at<int32_t>(ws, W.offsets), d.E, n_chunks,
+                                          chunk_info);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     PrefillParams p;
     p.offsets = ws_at<int32_t>(ws, W.offsets);
     p.active = ws_at<int32_t>(ws, W.active);
-    p.chunk_base = chunk_base;
+    p.n_chunks = n_chunks;
     p.chunk_info = chunk_info;
     p.perm = ws_at<int32_t>(ws, W.perm);
     p.topk_w = a.topk_w;
