@@ -30,7 +30,7 @@ SRC = os.path.join(ROOT, "w4a16_mixture_experts_gb300", "csrc", "decode_fused.cu
 def _constants():
     src = open(SRC).read()
     c = {}
-    for name in ("kCons", "kGC", "kNS", "kRedMax", "kMaxNB", "kP2Rows"):
+    for name in ("kCons", "kGC", "kGCMin", "kNS", "kRedMax", "kMaxNB", "kP2Rows"):
         m = re.search(r"constexpr int %s = (\d+);" % name, src)
         assert m, name
         c[name] = int(m.group(1))
@@ -40,9 +40,9 @@ def _constants():
 C = _constants()
 
 
-def _launch(T, H, E, k, I, nact, sms=152):
+def _launch(T, H, E, k, I, nact, gc_max, sms=152):
     G1 = H // 128
-    gc = min(G1, C["kGC"])
+    gc = min(G1, gc_max)
     nkc = -(-G1 // gc)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
     tp1, tp2 = I // 8, H // C["kP2Rows"]
@@ -52,10 +52,10 @@ def _launch(T, H, E, k, I, nact, sms=152):
     return nkc, nb, tp1, tp2, n1, n2, grid
 
 
-def _simulate(T, H, E, k, I, nact, seed):
+def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
-    nkc, nb, tp1, tp2, n1, n2, grid = _launch(T, H, E, k, I, nact)
+    nkc, nb, tp1, tp2, n1, n2, grid = _launch(T, H, E, k, I, nact, gc_max)
     done1 = [0] * nact
     ctas = []
     for cb in range(grid):
@@ -120,12 +120,15 @@ def _simulate(T, H, E, k, I, nact, seed):
     (7, 2560, 512, 10, 640, 70),
     (3, 1024, 1024, 32, 128, 95),
     (4, 256, 16, 2, 128, 8),
-    (7, 3072, 64, 8, 256, 40),      # 6 K chunks per task
-    (2, 8064, 16, 4, 128, 8),       # 16 K chunks per task, 2 partial-sum buffers
+    (7, 3072, 64, 8, 256, 40),      # 5 or 6 K chunks per task, the last one shorter
+    (2, 8064, 16, 4, 128, 8),       # 13 or 16 K chunks per task, 2 or 3 partial-sum buffers
     (7, 8064, 1024, 32, 640, 224),
 ])
 def test_decode_schedule_completes(T, H, E, k, I, nact):
-    for seed in range(2):
-        stuck, done1 = _simulate(T, H, E, k, I, nact, seed)
-        assert not stuck, "CTAs with chunks that can never be processed: %s" % stuck[:4]
-        assert all(d == I // 8 for d in done1)
+    # either chunk size the launch may choose (the larger unless its stages
+    # leave no room for the activations)
+    for gc_max in (C["kGC"], C["kGCMin"]):
+        for seed in range(2):
+            stuck, done1 = _simulate(T, H, E, k, I, nact, seed, gc_max)
+            assert not stuck, "CTAs with chunks that can never be processed: %s" % stuck[:4]
+            assert all(d == I // 8 for d in done1)

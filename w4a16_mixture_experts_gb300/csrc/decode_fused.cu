@@ -51,8 +51,9 @@ namespace moe {
 constexpr int kFW = 16;              // warps per CTA: kCons consumers, then the producer
 constexpr int kCons = 15;            // warps that compute
 constexpr int kProd = kCons;         // the warp that issues every weight copy
-constexpr int kGC = 4;               // quantisation groups per gate_up chunk
-constexpr int kNS = 30;              // stages of the CTA's chunk ring
+constexpr int kGC = 5;               // quantisation groups per gate_up chunk
+constexpr int kGCMin = 4;            // ... where kGC's stages leave no room to stage the activations
+constexpr int kNS = 29;              // stages of the CTA's chunk ring
 constexpr int kRedMax = 20480;       // bytes for the gate_up partial-sum buffers
 constexpr int kMaxNB = 8;            // partial-sum buffers (gate_up tasks in flight)
 constexpr int kP2Rows = 16;          // output rows per down item
@@ -130,11 +131,11 @@ __device__ inline RingWords ring_words(uint8_t *smem, const FusedParams &p) {
 }
 
 // Shared memory: the CTA's ring of kNS stages | partial sums | permutation
-// arrays | staged activations (if they fit).
-inline FusedLayout fused_layout(const moe_dims &d) {
+// arrays | staged activations (if they fit). gc_max: groups per gate_up chunk.
+inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     FusedLayout L{};
     const int G1 = d.H / 128, G2 = d.I / 128;
-    const int gc = G1 < kGC ? G1 : kGC;
+    const int gc = G1 < gc_max ? G1 : gc_max;
     L.gcw = gc * 16;
     L.nkc = (G1 + gc - 1) / gc;
     const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
@@ -154,6 +155,16 @@ inline FusedLayout fused_layout(const moe_dims &d) {
     L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= kNS * L.stage_bytes && d.T <= kDecodeMaxT &&
            d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
     return L;
+}
+
+// kGC groups per chunk (fewer chunks, each task's partial sums in fewer
+// slots: measured faster at T = 1 and 4), unless its larger stages leave no
+// room to stage the activations or do not fit at all; then kGCMin.
+inline FusedLayout fused_layout(const moe_dims &d) {
+    const FusedLayout a = fused_layout_gc(d, kGC);
+    if (a.ok && a.xs_off) return a;
+    const FusedLayout b = fused_layout_gc(d, kGCMin);
+    return b.ok && (b.xs_off || !a.ok) ? b : a;
 }
 
 bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
