@@ -226,6 +226,12 @@ def recorded_traffic(config: str):
     return e.get("dram_bytes_per_launch")
 
 
+def binding_roofline(bytes_per_launch, flops_per_launch, hbm_gbs, tc_tflops):
+    """'tensor' if the flops at the tensor rate take longer than the bytes at
+    the copy rate, else 'hbm': the roofline that bounds the launch."""
+    return "tensor" if flops_per_launch / (tc_tflops * 1e12) > bytes_per_launch / (hbm_gbs * 1e9) else "hbm"
+
+
 def run_ours(args, rank, world, local):
     import w4a16_mixture_experts_gb300 as moe
     moe.build()
@@ -446,9 +452,7 @@ def run_ours(args, rank, world, local):
     # and the flops at the tensor rate takes longer
     tflops = flops_launch * len(durs) / (sum(durs) * 1e-3) / 1e12
     peak_key = "bf16_tflops_sustained" if stack else "bf16_tflops"
-    t_hbm = statistics.mean(bytes_l) / (pk["hbm_gbs"] * 1e9)
-    t_tc = flops_launch / (pk[peak_key] * 1e12)
-    if t_tc > t_hbm:
+    if binding_roofline(statistics.mean(bytes_l), flops_launch, pk["hbm_gbs"], pk[peak_key]) == "tensor":
         roof = {"kernel": expert_kernel, "bound": "tensor", "achieved": tflops,
                 "peak": pk[peak_key], "peak_source": "%s %s (cuBLAS bf16)" % (pk_src, peak_key), "unit": "TFLOP/s",
                 "frac": tflops / pk[peak_key], "traffic": recorded_traffic(wl.name),

@@ -62,3 +62,17 @@ def test_reference_arm_prints_from_rank_zero_only():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_binding_roofline_picks_the_longer_time():
+    # full-shape layer: 2,534,400 B per unique expert, 2*3*H*I flops per assignment
+    sys.path.insert(0, ROOT)
+    import bench
+    per_assign = 2.0 * 3 * 2560 * 640
+    peaks = dict(hbm_gbs=6771.0, tc_tflops=1890.5)
+    # decode, one token: 10 experts' bytes against 10 assignments' flops
+    assert bench.binding_roofline(10 * 2534400, 10 * per_assign, **peaks) == "hbm"
+    # 512 Zipf-routed tokens on about 125 experts: still the bytes
+    assert bench.binding_roofline(125 * 2534400, 5120 * per_assign, **peaks) == "hbm"
+    # 4096 tokens on about 146 experts: the flops
+    assert bench.binding_roofline(146 * 2534400, 40960 * per_assign, **peaks) == "tensor"
