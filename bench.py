@@ -203,10 +203,19 @@ def cpu_baseline(wl, seed: int, target_s: float):
 
 # ------------------------------------------------------------- our arm -----
 
-def source_hash() -> str:
+# The sources that make up each captured kernel (its file and the headers it
+# includes): its recorded DRAM traffic holds while these are unchanged.
+KERNEL_SOURCES = {
+    "decode1": ["decode_fused.cu", "common.cuh", "kernels.cuh"],
+    "prefill512": ["prefill.cu", "common.cuh", "kernels.cuh", "tcgen05.cuh"],
+}
+
+
+def source_hash(names=None) -> str:
+    """Hash of the named csrc files (all of them by default)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_mixture_experts_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(names if names is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -221,7 +230,7 @@ def recorded_traffic(config: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(config)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or config not in KERNEL_SOURCES or e.get("source_hash") != source_hash(KERNEL_SOURCES[config]):
         return None
     return e.get("dram_bytes_per_launch")
 
