@@ -69,6 +69,11 @@ def parse():
     ap.add_argument("--sets", type=int, default=0, help="weight sets to rotate over (0: enough to exceed L2)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
+    ap.add_argument("--clock-ms", type=float, default=300.0,
+                    help="length of the load window, ending with the timed region, over which clocks are sampled")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="measure the headline workload only (by default a decode1 run also measures %s)"
+                    % ", ".join(("decode64", "stack_prefill4096")))
     return ap.parse_args()
 
 
@@ -241,11 +246,19 @@ def binding_roofline(bytes_per_launch, flops_per_launch, hbm_gbs, tc_tflops):
     return "tensor" if flops_per_launch / (tc_tflops * 1e12) > bytes_per_launch / (hbm_gbs * 1e9) else "hbm"
 
 
-def run_ours(args, rank, world, local):
+def launches_per_layer(T: int, E: int) -> int:
+    """Kernels one layer launches: route is one kernel for T <= 8 (logits, then
+    top-k in the last CTA), else logits + top-k; the forward is one fused kernel
+    (the library's decode path, T <= 7), or permute 3 + x gather + chunk table +
+    gate_up + down + conversion."""
+    return (1 if T <= 8 else 2) + (1 if T <= FUSED_MAX_T else 8)
+
+
+def measure(args, wl, steps, rank, world, local):
+    """Times `steps` steps of workload wl on this rank; returns the JSON fields."""
     import w4a16_mixture_experts_gb300 as moe
     moe.build()
     moe.lib()
-    wl = synth.WORKLOADS[args.config]
     T, H, E, k, I = wl.dims
     stack = wl.layers > 1
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -267,6 +280,7 @@ def run_ours(args, rank, world, local):
         sets.append({key: (v.to(dev) if v is not None else None) for key, v in d.items()})
         if stack and i > 0:
             sets[i]["hidden"] = None
+        del d
     x0 = sets[0]["hidden"]
     ws = moe.workspace(T, H, E, k, I, dev)
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
@@ -274,33 +288,35 @@ def run_ours(args, rank, world, local):
     outs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(1 if stack else nsets)]
     act = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     stream = torch.cuda.Stream(device=dev)
-    n_exp_launch = wl.layers
-    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nsets * (1 if not stack else 1))]
-    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ev_b))]
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nsets)]
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nsets)]
     unique = [0] * nsets
     for e in ev_b + ev_a:       # torch only lets recorded events be timed; the library re-records them
         e.record(stream)
 
-    def step(i, profile=False):
+    def layer_call(x, s, nxt=None, out=None):
+        moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
+        if nxt is not None:
+            moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
+                                      s["w2_scales"], eps=1e-6, next=nxt, ws=ws)
+        else:
+            moe.moe_w4a16_forward(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
+                                  s["w2_scales"], out=out, ws=ws)
+
+    def step(i, profile=False, x_in=None):
         """Enqueue one step (set i for single layers; all layers for the stack)."""
         if stack:
-            x = x0
+            x = x0 if x_in is None else x_in
             for l in range(wl.layers):
-                s = sets[l]
                 if profile:
                     moe.moe_profile_events(ev_b[l], ev_a[l])
-                moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
                 nxt = act[l % 2]
-                moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                                          s["w2_scales"], eps=1e-6, next=nxt, ws=ws)
+                layer_call(x, sets[l], nxt=nxt)
                 x = nxt
             return x
-        s = sets[i]
         if profile:
             moe.moe_profile_events(ev_b[i], ev_a[i])
-        moe.moe_route(s["hidden"], s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
-        moe.moe_w4a16_forward(s["hidden"], ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                              s["w2_scales"], out=outs[i], ws=ws)
+        layer_call(sets[i]["hidden"] if x_in is None else x_in, sets[i], out=outs[i])
         return outs[i]
 
     with torch.cuda.stream(stream):
@@ -315,10 +331,7 @@ def run_ours(args, rank, world, local):
             # unique experts per layer along the stack's own routing
             x = x0
             for l in range(wl.layers):
-                s = sets[l]
-                moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
-                moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                                          s["w2_scales"], eps=1e-6, next=act[l % 2], ws=ws)
+                layer_call(x, sets[l], nxt=act[l % 2])
                 stream.synchronize()
                 unique[l] = len(torch.unique(ids).tolist())
                 x = act[l % 2]
@@ -368,7 +381,7 @@ def run_ours(args, rank, world, local):
 
         use_graph = not args.no_graph
         per = n_in                      # steps per full graph
-        rem = args.steps % per
+        rem = steps % per
         G = {}
         if use_graph:
             try:
@@ -408,16 +421,30 @@ def run_ours(args, rank, world, local):
         stream.synchronize()
         barrier(world)
 
+        # The clock sampler runs over a window of back-to-back passes of the same
+        # graphs that ends with the timed region, at least args.clock_ms long, so
+        # that it sees the GPU under this load even when the timed region is short.
         clocks = Clocks(local)
         clocks.start()
+        w0 = time.perf_counter()
+        while (time.perf_counter() - w0) * 1e3 < args.clock_ms:
+            if use_graph:
+                G["all"].replay()
+            else:
+                enqueue(range(per))
+            stream.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        run_steps(args.steps)
+        run_steps(steps)
         t1.record(stream)
         stream.synchronize()
+        window_ms = (time.perf_counter() - w0) * 1e3
         ms = t0.elapsed_time(t1)
         clk = clocks.stop()
+        if clk is not None:
+            clk["window_ms"] = round(window_ms, 1)
+            clk["window"] = "back-to-back passes of the timed graphs, ending with the timed region"
         assert moe.moe_check_device_error(ws, stream) == 0
 
         # expert kernel durations: each set's profiled step once, in rotation
@@ -441,48 +468,70 @@ def run_ours(args, rank, world, local):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        run_steps(args.steps, e2e=True)
+        run_steps(steps, e2e=True)
         e1.record(stream)
         stream.synchronize()
         ms_e2e = e0.elapsed_time(e1)
 
+        # end to end, eager: every step is a copy of its tokens from pinned host
+        # memory, the layer's C-ABI calls launched from the host (no graph), and
+        # the copy of its output back, in order on one stream
+        def eager_step(i):
+            j = i % n_in
+            dst_in[j].copy_(h_in[j], non_blocking=True)
+            res = step(j, x_in=dst_in[j])
+            h_out[j].copy_(res, non_blocking=True)
+
+        for i in range(max(args.warmup, 1)):
+            eager_step(i)
+        stream.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(steps):
+            eager_step(i)
+        g1.record(stream)
+        stream.synchronize()
+        ms_eager = g0.elapsed_time(g1)
+        assert moe.moe_check_device_error(ws, stream) == 0
+
     ms = max_over_ranks(ms, world)
     ms_e2e = max_over_ranks(ms_e2e, world)
-    # route: one kernel for T <= 8 (logits, then top-k in the last CTA), else logits +
-    # top-k; forward: one fused kernel (the library's decode path, T <= 7) or permute 3
-    # + x gather + chunk table + gate_up + down + convert
+    ms_eager = max_over_ranks(ms_eager, world)
     fused = T <= FUSED_MAX_T
-    launches_per_layer = (1 if T <= 8 else 2) + (1 if fused else 8)
     pk, pk_src = peaks()
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
     flops_launch = 2.0 * 3 * H * I * T * k           # algorithmic: gate, up and down over all slots
     expert_kernel = "decode_fused_kernel" if fused else "prefill_kernel (gate_up + down launches)"
     # the binding roofline: whichever of the unique weight bytes at the copy rate
-    # and the flops at the tensor rate takes longer
+    # and the flops at the tensor rate takes longer. The tensor peak is the dense
+    # bf16 burst rate; a stack's fraction of the sustained rate is given beside it.
     tflops = flops_launch * len(durs) / (sum(durs) * 1e-3) / 1e12
-    peak_key = "bf16_tflops_sustained" if stack else "bf16_tflops"
-    if binding_roofline(statistics.mean(bytes_l), flops_launch, pk["hbm_gbs"], pk[peak_key]) == "tensor":
+    if binding_roofline(statistics.mean(bytes_l), flops_launch, pk["hbm_gbs"], pk["bf16_tflops"]) == "tensor":
         roof = {"kernel": expert_kernel, "bound": "tensor", "achieved": tflops,
-                "peak": pk[peak_key], "peak_source": "%s %s (cuBLAS bf16)" % (pk_src, peak_key), "unit": "TFLOP/s",
-                "frac": tflops / pk[peak_key], "traffic": recorded_traffic(wl.name),
+                "peak": pk["bf16_tflops"], "peak_source": "%s bf16_tflops (cuBLAS bf16 dense, burst)" % pk_src,
+                "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops"], "traffic": recorded_traffic(wl.name),
                 "algorithmic_flops_per_launch": flops_launch,
                 "hbm_achieved_gbs": hbm_gbs, "hbm_frac": hbm_gbs / pk["hbm_gbs"]}
+        if stack:
+            roof["frac_of_sustained"] = tflops / pk["bf16_tflops_sustained"]
     else:
         roof = {"kernel": expert_kernel, "bound": "hbm", "achieved": hbm_gbs, "peak": pk["hbm_gbs"],
                 "peak_source": pk_src + " hbm_gbs (copy)", "unit": "GB/s", "frac": hbm_gbs / pk["hbm_gbs"],
                 "traffic": recorded_traffic(wl.name),
-                "tensor_achieved_tflops": tflops, "tensor_frac": tflops / pk[peak_key]}
+                "tensor_achieved_tflops": tflops, "tensor_frac": tflops / pk["bf16_tflops"]}
     roof.update({"algorithmic_bytes_per_launch": statistics.mean(bytes_l),
                  "kernel_ms_per_launch": statistics.mean(durs), "launches_measured": len(durs),
                  "unique_experts_per_launch": statistics.mean(bytes_l) / EXPERT_BYTES})
-    res = {
+    nlaunch = steps * wl.layers * launches_per_layer(T, E)
+    return {
         "metric": "MoE layer tok/s (%s)" % wl.name,
-        "value": world * T * args.steps / (ms * 1e-3),
+        "value": world * T * steps / (ms * 1e-3),
         "unit": "tok/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
-        "ms_per_step": ms / args.steps,
+        "ms_per_step": ms / steps,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -495,12 +544,36 @@ def run_ours(args, rank, world, local):
                    "graph": use_graph, "steps_per_graph": per if use_graph else 1,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
-        "e2e": {"value": world * T * args.steps / (ms_e2e * 1e-3), "unit": "tok/s",
+        "e2e": {"value": world * T * steps / (ms_e2e * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
-                "copies": "pinned host buffers, one copy in and one out per step, on a copy stream"},
-        "gpu_launches": args.steps * wl.layers * launches_per_layer,
+                "copies": "pinned host buffers, one copy in and one out per step, on a copy stream; "
+                          "the steps replayed from CUDA graphs",
+                "eager": {"value": world * T * steps / (ms_eager * 1e-3), "unit": "tok/s",
+                          "ms_per_step": ms_eager / steps,
+                          "how": "per step: copy in from pinned host memory, moe_route + moe_w4a16_forward%s "
+                                 "called through the C ABI from the host (no graph), copy out; one stream"
+                                 % ("_rms x %d layers" % wl.layers if stack else "")}},
+        "gpu_launches": nlaunch,
         "clocks": clk,
     }
+
+
+# Workloads measured beside the headline one in a default run: the metric's other
+# two batch sizes (64 concurrent decode tokens; the 4096-token prefill on the
+# 48-layer stack).
+PER_CONFIG = ("decode64", "stack_prefill4096")
+
+
+def run_ours(args, rank, world, local):
+    wl = synth.WORKLOADS[args.config]
+    res = measure(args, wl, args.steps, rank, world, local)
+    if args.per_config and args.config == "decode1":
+        res["per_config"] = {}
+        for name in PER_CONFIG:
+            torch.cuda.empty_cache()
+            r = measure(args, synth.WORKLOADS[name], args.steps, rank, world, local)
+            res["per_config"][name] = r
+            torch.cuda.empty_cache()
     return res
 
 
@@ -525,6 +598,8 @@ def main():
     res = run_ours(args, rank, world, local)
     if rank == 0:
         res["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)
+        for name, r in res.get("per_config", {}).items():
+            r["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[name], args.seed, args.cpu_seconds / 2)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -23,8 +23,8 @@
  *  - Every tensor is row-major and contiguous; every pointer is 16-byte
  *    aligned.
  *  - Supported shapes: T >= 0, H and I multiples of 128, 1 <= k <= 32,
- *    k <= E <= 1024, H <= 8064, I <= 4096. Others return
- *    MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *    k <= E <= 1024, H <= 8064, I <= 4096, T <= 2^20 and T * H < 2^32.
+ *    Others return MOE_ERR_UNSUPPORTED before anything is enqueued.
  *  - Argument errors are returned synchronously and enqueue nothing. A
  *    launch failure returns MOE_ERR_CUDA. Errors seen by a kernel (an expert
  *    id outside [0, E), an internal wait that gave up) are recorded in the
@@ -32,7 +32,10 @@
  *  - Workspace: `ws` must hold at least moe_workspace_size() bytes and must
  *    be all zero before its first use (the library leaves the counters it
  *    uses at zero when a call completes). One workspace must not be used by
- *    two calls that may run concurrently.
+ *    two calls that may run concurrently. A call whose bounded wait gave up
+ *    (MOE_ERR_TIMEOUT) can leave counters non-zero: moe_check_device_error
+ *    then clears the whole workspace before it returns, and a caller that
+ *    does not call it must clear the workspace itself before reusing it.
  */
 #ifndef W4A16MOE_H
 #define W4A16MOE_H
@@ -161,7 +164,7 @@ MOE_API int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_id
  *  - Calls on the same device that may overlap in time (other streams, other
  *    host threads) race on the array and give wrong results.
  *  - Ids outside [0, E) contribute nothing; the error word the kernel sets
- *    stays inside the array and is not reported.
+ *    stays inside the array, where moe_noalloc_check_device_error reads it.
  */
 MOE_API int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
                               const int32_t *w1_packed, const uint16_t *w1_scales,
@@ -194,6 +197,17 @@ MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed
                   int32_t *bad_count, void *stream);
 
 /*
+ * Which kernels a forward call of dims `d` runs (a host-only query, no
+ * counterpart on the pages; for tests and tuning). Writes *plan = 0 for the
+ * tensor-core pipeline (permute, grouped gate_up and down GEMMs, conversion);
+ * otherwise the fused decode kernel runs and *plan = s + 16 * g, where s = 1
+ * if the activations are staged in shared memory and 2 if they are read from
+ * global memory, and g is the number of 128-wide groups per gate_up chunk.
+ * Returns the shape checks' status.
+ */
+MOE_API int moe_forward_plan(moe_dims d, int32_t *plan);
+
+/*
  * Profiling aid (no counterpart on the pages): from now on, every forward
  * call records `before_experts` on its stream just before it launches the
  * expert kernel and `after_experts` just after it, so that the caller can
@@ -207,9 +221,19 @@ MOE_API int moe_profile_events(void *before_experts, void *after_experts);
 /*
  * Synchronises `stream`, then reads and clears the workspace's error word.
  * Returns MOE_OK, MOE_ERR_DEVICE or MOE_ERR_TIMEOUT (or MOE_ERR_CUDA if the
- * synchronisation itself failed).
+ * synchronisation itself failed). On MOE_ERR_TIMEOUT it also sets all
+ * ws_bytes of the workspace to zero (and waits for that), so that the
+ * workspace is fit for the next call.
  */
 MOE_API int moe_check_device_error(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The same check for moe_w4a16_forward_noalloc (no counterpart on the pages):
+ * synchronises `stream`, then reads and clears the error word of the
+ * library's static scratch on the current device. Every no-alloc call clears
+ * the word before it starts, so this reports on the last call only.
+ */
+MOE_API int moe_noalloc_check_device_error(void *stream);
 
 #ifdef __cplusplus
 }

@@ -30,14 +30,57 @@ SRC = os.path.join(ROOT, "w4a16_mixture_experts_gb300", "csrc", "decode_fused.cu
 def _constants():
     src = open(SRC).read()
     c = {}
-    for name in ("kCons", "kGC", "kGCMin", "kNS", "kRedMax", "kMaxNB", "kP2Rows"):
+    for name in ("kFW", "kCons", "kGC", "kGCMin", "kNS", "kRedMax", "kMaxNB", "kP2Rows", "kDecodeMaxT",
+                 "kFastN"):
         m = re.search(r"constexpr int %s = (\d+);" % name, src)
         assert m, name
         c[name] = int(m.group(1))
+    m = re.search(r"constexpr int kFusedSmem = (\d+) - (\d+);", src)
+    assert m, "kFusedSmem"
+    c["kFusedSmem"] = int(m.group(1)) - int(m.group(2))
     return c
 
 
 C = _constants()
+
+
+def _al(v, a):
+    return (v + a - 1) // a * a
+
+
+def _layout_gc(T, H, E, k, I, gc_max):
+    """Mirror of fused_layout_gc: (fits, staged activations, gcw)."""
+    G1, G2 = H // 128, I // 128
+    gc = min(G1, gc_max)
+    gcw = gc * 16
+    nkc = -(-G1 // gc)
+    p1 = 2 * 8 * gcw * 4 + 2 * 8 * G1 * 2
+    p2 = C["kP2Rows"] * (I // 2) + C["kP2Rows"] * G2 * 2
+    stage = _al(max(p1, p2), 128)
+    nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
+    red_off = C["kNS"] * stage
+    red = nb * nkc * 32 * 16 + 2 * nb * 4 + 4 + 2 * C["kNS"] * 4
+    pro_off = red_off + _al(red, 128)
+    n = T * k
+    na = max(1, min(E, n))
+    pro = _al(n * 2, 16) * 3 + _al(C["kFastN"] * 4, 16) + _al(na * 2, 16) * 3 + _al(T * 2, 16) + 4 * C["kFW"] * 8 + 16
+    xs = T * H * 2 + _al(T * G1 * 4, 16)
+    base = pro_off + _al(pro, 128)
+    staged = base + xs <= C["kFusedSmem"]
+    total = base + xs if staged else base
+    ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256
+    return ok, staged, gcw
+
+
+def fused_plan(T, H, E, k, I):
+    """Mirror of fused_layout: None if the decode kernel cannot take the shape,
+    else (staged, groups per chunk): which instantiation of the kernel runs."""
+    a = _layout_gc(T, H, E, k, I, C["kGC"])
+    if a[0] and a[1]:
+        return a[1], a[2] // 16
+    b = _layout_gc(T, H, E, k, I, C["kGCMin"])
+    pick = b if b[0] and (b[1] or not a[0]) else a
+    return (pick[1], pick[2] // 16) if pick[0] else None
 
 
 def _launch(T, H, E, k, I, nact, gc_max, sms=152):
@@ -132,3 +175,54 @@ def test_decode_schedule_completes(T, H, E, k, I, nact):
             stuck, done1 = _simulate(T, H, E, k, I, nact, seed, gc_max)
             assert not stuck, "CTAs with chunks that can never be processed: %s" % stuck[:4]
             assert all(d == I // 8 for d in done1)
+
+
+# The shapes of the GPU parity tests that run the decode kernel, and the
+# instantiation each one reaches: decode_fused_kernel<true> stages the
+# activations in shared memory, <false> reads them from global memory.
+GPU_DECODE_SHAPES = {
+    (1, 2560, 512, 10, 640): True,     # decode1
+    (4, 2560, 512, 10, 640): True,     # decode4
+    (4, 256, 16, 2, 128): True,        # tiny
+    (7, 2560, 512, 10, 640): True,     # the largest decode batch at full shape
+    (1, 128, 1, 1, 128): True,
+    (5, 384, 24, 3, 256): True,
+    (3, 1024, 1024, 32, 128): True,
+    (7, 3072, 64, 8, 256): True,
+    (2, 8064, 16, 4, 128): True,
+    (3, 128, 1024, 32, 128): True,     # E and k at their maxima, the smallest H
+    (7, 8064, 64, 8, 128): False,      # x too large to stage next to the ring
+    (6, 6144, 32, 4, 256): False,
+}
+
+
+@pytest.mark.parametrize("shape,staged", sorted(GPU_DECODE_SHAPES.items()))
+def test_decode_instantiation_of_gpu_shapes(shape, staged):
+    plan = fused_plan(*shape)
+    assert plan is not None, "the decode kernel must take %s" % (shape,)
+    assert plan[0] == staged
+    # the library's own choice (a host-only query) agrees with this mirror
+    assert _library_plan(*shape) == plan
+
+
+def _library_plan(*dims):
+    import w4a16_mixture_experts_gb300 as moe
+    moe.build()
+    return moe.moe_forward_plan(*dims)
+
+
+def test_mirror_matches_library_plan_over_many_shapes():
+    import itertools
+    for T, H, E, k, I in itertools.product((1, 3, 7, 8), (128, 2560, 6144, 8064), (16, 512, 1024),
+                                           (1, 10, 32), (128, 640, 1280, 1408)):
+        if k > E:
+            continue
+        assert _library_plan(T, H, E, k, I) == fused_plan(T, H, E, k, I), (T, H, E, k, I)
+
+
+def test_decode_takes_every_batch_up_to_seven_tokens_at_full_shape():
+    for T in range(1, C["kDecodeMaxT"] + 1):
+        for k in (1, 10, 32):
+            for E in (k, 512, 1024):
+                assert fused_plan(T, 2560, E, k, 640) is not None, (T, E, k)
+    assert fused_plan(C["kDecodeMaxT"] + 1, 2560, 512, 10, 640) is None

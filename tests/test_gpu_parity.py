@@ -238,7 +238,7 @@ def test_forward_parity(name):
     assert_close(got, forward_ref(h, ids, w32, E, I), name)
 
 
-def test_forward_prefill512_zipf_sampled():
+def test_forward_prefill512_zipf_whole_output():
     wl, h, g = layer("prefill512")
     T, H, E, k, I = wl.dims
     ids_g, w_g = moe.moe_route(g["hidden"], g["router_w"], k, bias=g["bias"])
@@ -246,11 +246,14 @@ def test_forward_prefill512_zipf_sampled():
     out = moe.moe_w4a16_forward(g["hidden"], ids_g, w_g, g["w1_packed"], g["w1_scales"], g["w2_packed"],
                                 g["w2_scales"], ws=ws)
     assert moe.moe_check_device_error(ws) == 0
-    rows = np.sort(np.random.default_rng(1).choice(T, 24, replace=False))
-    ids, w = ids_g.cpu().numpy()[rows], w_g.cpu().numpy()[rows]
-    # the routing the GPU used is itself checked above; here it is an input
-    ref = forward_ref(h, ids, w, E, I, rows=rows)
-    assert_close(out.float().cpu().numpy()[rows], ref, "prefill512")
+    ids, w = ids_g.cpu().numpy(), w_g.cpu().numpy()
+    # every row; the routing the GPU used is itself checked above, here it is an input
+    ref = forward_ref(h, ids, w, E, I)
+    got = out.float().cpu().numpy()
+    assert_close(got, ref, "prefill512")
+    # and row by row, so that one wrong row block of one chunk cannot hide under the global bar
+    for t in range(T):
+        assert np.abs(got[t] - ref[t]).max() <= OUT_TOL * np.abs(ref).max(), "row %d" % t
     counts = np.bincount(ids_g.cpu().numpy().ravel(), minlength=E)
     assert counts.max() > 4 * counts[counts > 0].mean(), "the Zipf bias should make hot experts"
 
@@ -278,6 +281,9 @@ def test_forward_layer_end_to_end_decode():
     (40, 256, 4, 2, 384),       # many tokens on few experts (several N passes)
     (7, 3072, 64, 8, 256),      # decode: gate_up chunks split unevenly over a group, several tasks each
     (2, 8064, 16, 4, 128),      # decode: H at its maximum (16 chunks per gate_up task)
+    (3, 128, 1024, 32, 128),    # decode: E and k at their maxima with the smallest H
+    (7, 8064, 64, 8, 128),      # decode, activations read from global memory (too large to stage)
+    (6, 6144, 32, 4, 256),      # likewise, at another chunk split
 ])
 def test_forward_edge_shapes(T, H, E, k, I):
     seed = T + H + E
@@ -372,40 +378,57 @@ def _stack_chain(name, n_layers, seed, rows=None):
     rescale, the output feeding the next layer. Each layer is checked against
     the oracle on the GPU's own input to it (so near ties cannot make the two
     trajectories drift apart): the routing within the gap, then the layer's
-    output given the routing the GPU took (checked valid just before)."""
+    output given the routing the GPU took (checked valid just before).
+
+    Each layer's experts are drawn (from the same per-expert streams as the
+    full layer) only for the experts its routing selects, and written into
+    full-size device tensors: the kernels read no other expert, so the result
+    is that of the full layer while the host draws a few experts a layer."""
     wl = synth.WORKLOADS[name]
     T, H, E, k, I = wl.dims
     x = synth.hidden(T, H, seed=seed).cuda()
     ws = moe.workspace(T, H, E, k, I)
+    W = [torch.zeros(E, 2 * I, H // 8, dtype=torch.int32, device="cuda"),
+         torch.zeros(E, 2 * I, H // 128, dtype=torch.bfloat16, device="cuda"),
+         torch.zeros(E, H, I // 8, dtype=torch.int32, device="cuda"),
+         torch.zeros(E, H, I // 128, dtype=torch.bfloat16, device="cuda")]
+    names = ("w1_packed", "w1_scales", "w2_packed", "w2_scales")
     sel = np.arange(T) if rows is None else rows
     for l in range(n_layers):
-        h = synth.layer_inputs(wl, seed=seed, layer=l)
-        W = [h[n].cuda() for n in ("w1_packed", "w1_scales", "w2_packed", "w2_scales")]
-        ids, w = moe.moe_route(x, h["router_w"].cuda(), k, ws=ws)
+        wr = synth.router(E, H, seed=seed, layer=l)
+        ids, w = moe.moe_route(x, wr.cuda(), k, ws=ws)
+        torch.cuda.synchronize()
+        held = np.unique(ids.cpu().numpy())
+        part = synth.expert_weights(E, H, I, seed=seed, layer=l, experts=held)
+        idx = torch.from_numpy(held).long().cuda()
+        for dst, n in zip(W, names):
+            dst[idx] = part[n].cuda()
         nxt = moe.moe_w4a16_forward_rms(x, ids, w, *W, eps=1e-6, ws=ws)
         torch.cuda.synchronize()
         assert moe.moe_check_device_error(ws) == 0
         xh = x.cpu()[sel]
         ids_h, w_h = ids.cpu()[sel], w.cpu()[sel]
-        check_route(ids_h, w_h, oracle.router_logits(xh, h["router_w"]), k)
-        ref_out = oracle.expert_forward(xh, ids_h, w_h, h["w1_packed"], h["w1_scales"], h["w2_packed"],
-                                        h["w2_scales"], E, I)
+        check_route(ids_h, w_h, oracle.router_logits(xh, wr), k)
+        row = np.full(E, -1, np.int32)
+        row[held] = np.arange(len(held))
+        ref_out = oracle.expert_forward(xh, ids_h, w_h, part["w1_packed"], part["w1_scales"], part["w2_packed"],
+                                        part["w2_scales"], E, I, expert_row=row)
         _, ref_next = oracle.residual_rms(xh, ref_out, eps=1e-6)
         assert_close(nxt.float().cpu().numpy()[sel], ref_next, "%s layer %d" % (name, l))
         x = nxt
-        del W, h
+        del part
 
 
-def test_stack_decode_chained_layers():
-    # three full-shape layers of the 4-token decode stack (the fused decode kernel)
-    _stack_chain("stack_decode4", 3, seed=7)
+def test_stack_decode_all_layers():
+    # all 48 full-shape layers of the 4-token decode stack (the fused decode kernel)
+    _stack_chain("stack_decode4", 48, seed=7)
 
 
 def test_stack_prefill_chained_layers_sampled():
-    # two full-shape layers of the 4096-token prefill stack (tensor-core path),
-    # 48 sampled rows checked per layer
-    rows = np.sort(np.random.default_rng(8).choice(4096, 48, replace=False))
-    _stack_chain("stack_prefill4096", 2, seed=8, rows=rows)
+    # four full-shape layers of the 4096-token prefill stack (tensor-core path),
+    # 256 sampled rows checked per layer
+    rows = np.sort(np.random.default_rng(8).choice(4096, 256, replace=False))
+    _stack_chain("stack_prefill4096", 4, seed=8, rows=rows)
 
 
 # ------------------------------------------------------- prefill (tcgen05) ----
@@ -446,7 +469,7 @@ def test_prefill_full_shape_sampled():
     ws = moe.workspace(T, H, E, k, I)
     out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W, ws=ws).float().cpu().numpy()
     assert moe.moe_check_device_error(ws) == 0
-    rows = np.sort(np.random.default_rng(11).choice(T, 16, replace=False))
+    rows = np.sort(np.random.default_rng(11).choice(T, 256, replace=False))
     ref = oracle.expert_forward(x[rows], ids[rows], w[rows], wts["w1_packed"], wts["w1_scales"],
                                 wts["w2_packed"], wts["w2_scales"], E, I)
     assert_close(out[rows], ref, "T=4096 sampled")

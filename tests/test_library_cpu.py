@@ -70,6 +70,14 @@ def test_workspace_size_and_shape_rules(L):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_workspace_size(-1, 2560, 512, 10, 640)
     assert ei.value.status == 1
+    # the fp32 accumulator's token rows are addressed by 32-bit offsets: T * H < 2^32
+    assert moe.moe_workspace_size(500_000, 8064, 512, 10, 640) > 0
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_size(600_000, 8064, 512, 10, 640)
+    assert ei.value.status == 2
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_size((1 << 20) + 1, 128, 16, 2, 128)
+    assert ei.value.status == 2
 
 
 def _call_forward(L, dims, ptrs, ws_bytes):

@@ -92,9 +92,12 @@ def _pair(T, H, E, k, I, seed=11):
     ws = moe.workspace(T, H, E, k, I)
     ref = moe.moe_w4a16_forward(x, ids, tw, *W, ws=ws)
     a = moe.moe_w4a16_forward_noalloc(x, ids, tw, *W)
+    a_err = moe.moe_noalloc_check_device_error()
     b = moe.moe_w4a16_forward_noalloc(x, ids, tw, *W)
     torch.cuda.synchronize()
     assert moe.moe_check_device_error(ws) == 0
+    # neither call saw a bad id or gave up a wait inside the static scratch
+    assert a_err == 0 and moe.moe_noalloc_check_device_error() == 0
     return ref, a, b
 
 
@@ -117,6 +120,21 @@ def test_noalloc_shape_changes_between_calls(_built):
         ref, a, b = _pair(T, 2560, 512, k, 640, seed=5)
         _close(a, ref)
         _close(b, ref)
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_a_bad_id(_built):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    x, ids, tw, W = _inputs(3, 2560, 512, 10, 640, seed=13)
+    bad = ids.clone()
+    bad[1, 2] = 512 + 7
+    moe.moe_w4a16_forward_noalloc(x, bad, tw, *W)
+    assert moe.moe_noalloc_check_device_error() == 5     # MOE_ERR_DEVICE, then cleared
+    assert moe.moe_noalloc_check_device_error() == 0
+    # the next call starts clean and matches the workspace forward
+    ref, a, b = _pair(3, 2560, 512, 10, 640, seed=13)
+    _close(a, ref)
 
 
 @pytest.mark.gpu
@@ -144,6 +162,7 @@ ids, tw = synth.random_topk(T, E, k, seed=2)
 ids, tw = ids.cuda(), tw.cuda()
 a = moe.moe_w4a16_forward_noalloc(x, ids, tw, *W)      # first library call: set-up
 b = moe.moe_w4a16_forward_noalloc(x, ids, tw, *W)
+assert moe.moe_noalloc_check_device_error() == 0
 ref = moe.moe_w4a16_forward(x, ids, tw, *W, ws=moe.workspace(T, H, E, k, I))
 torch.cuda.synchronize()
 bound = 1e-2 * ref.float().abs().max().item()

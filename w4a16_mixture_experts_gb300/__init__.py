@@ -23,7 +23,8 @@ import torch
 __all__ = [
     "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
     "workspace", "moe_route", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
-    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc", "STATUS",
+    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
+    "moe_noalloc_check_device_error", "moe_forward_plan", "STATUS",
 ]
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
@@ -78,7 +79,9 @@ def lib() -> ctypes.CDLL:
         L.moe_permute.argtypes, L.moe_permute.restype = [P, D, P, P, P, Z, P], I
         L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
+        L.moe_noalloc_check_device_error.argtypes, L.moe_noalloc_check_device_error.restype = [P], I
         L.moe_profile_events.argtypes, L.moe_profile_events.restype = [P, P], I
+        L.moe_forward_plan.argtypes, L.moe_forward_plan.restype = [D, ctypes.POINTER(ctypes.c_int32)], I
         _lib = L
     return _lib
 
@@ -239,6 +242,16 @@ def moe_pack_int4(q, bad_count=None, stream=None):
     return packed
 
 
+def moe_forward_plan(T: int, H: int, E: int, k: int, I: int):
+    """None if a forward of these dims takes the tensor-core pipeline, else
+    (staged, groups_per_chunk) of the fused decode kernel it runs."""
+    v = ctypes.c_int32(-1)
+    _check(lib().moe_forward_plan(moe_dims(T, H, E, k, I), ctypes.byref(v)), "moe_forward_plan")
+    if v.value == 0:
+        return None
+    return (v.value & 15) == 1, v.value >> 4
+
+
 def moe_profile_events(before=None, after=None):
     """Record two torch.cuda.Events (enable_timing=True, external=True) around
     the expert kernel of every later forward call; (None, None) stops."""
@@ -250,3 +263,8 @@ def moe_profile_events(before=None, after=None):
 def moe_check_device_error(ws, stream=None) -> int:
     """Synchronise the stream; return (and clear) the workspace's device error status."""
     return lib().moe_check_device_error(_p(ws), ws.numel(), _stream(stream))
+
+
+def moe_noalloc_check_device_error(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the error status of the no-alloc scratch."""
+    return lib().moe_noalloc_check_device_error(_stream(stream))

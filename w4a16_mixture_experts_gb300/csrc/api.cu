@@ -82,6 +82,8 @@ int check_dims(const moe_dims &d) {
     if (d.H % kGroup || d.I % kGroup || d.H > 8192 || d.I > 4096) return MOE_ERR_UNSUPPORTED;
     if (d.k > kMaxK || d.k > d.E || d.E > kMaxE) return MOE_ERR_UNSUPPORTED;
     if (d.T > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+    // token rows of the fp32 accumulator are addressed by 32-bit offsets t * H
+    if ((int64_t)d.T * d.H >= ((int64_t)1 << 32)) return MOE_ERR_UNSUPPORTED;
     if (!prefill_supported(d)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
@@ -209,6 +211,14 @@ int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_
     return cuda_status(launch_pack_int4(q, N, K, packed, bad_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_forward_plan(moe_dims d, int32_t *plan) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    const int rc = check_dims(d);
+    if (rc) return rc;
+    *plan = fused_plan(d);
+    return MOE_OK;
+}
+
 int moe_profile_events(void *before_experts, void *after_experts) {
     if ((before_experts == nullptr) != (after_experts == nullptr)) return MOE_ERR_INVALID_ARG;
     g_ev_before = reinterpret_cast<cudaEvent_t>(before_experts);
@@ -224,7 +234,12 @@ int moe_check_device_error(void *ws, size_t ws_bytes, void *stream) {
         return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (err_word) {
-        if (cudaMemsetAsync(ws, 0, sizeof(err_word), s) != cudaSuccess) return MOE_ERR_CUDA;
+        // A wait that gave up may leave completion counters anywhere in the
+        // workspace non-zero; the whole workspace is cleared so that the next
+        // call starts from the all-zero state. A bad id leaves the counters
+        // consistent: only the error word is cleared.
+        const size_t clear = err_word == MOE_ERR_TIMEOUT ? ws_bytes : sizeof(err_word);
+        if (cudaMemsetAsync(ws, 0, clear, s) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
         return err_word == MOE_ERR_TIMEOUT ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
     }

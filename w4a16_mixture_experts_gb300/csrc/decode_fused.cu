@@ -11,10 +11,9 @@
 //    so that it takes its SM and sets up while the router finishes. Each CTA
 //    first derives the whole token-to-expert permutation from topk_ids in
 //    shared memory (every CTA computes the same result), so no separate
-//    permute launch sits on the critical path. Small batches rank each
-//    assignment by comparison (slot = #assignments with a lower expert +
-//    #earlier ones with the same expert); larger ones use a histogram and a
-//    prefix sum over the experts.
+//    permute launch sits on the critical path. Each assignment is ranked by
+//    comparison (slot = #assignments with a lower expert + #earlier ones with
+//    the same expert): a batch holds at most kDecodeMaxT * kMaxK of them.
 //  * Work: gate_up tasks (8 gate rows and the matching 8 up rows of one
 //    expert, all of K, in chunks of kGC quantisation groups) and down items
 //    (16 output rows of one expert, all of K = I). Each CTA takes a
@@ -63,8 +62,8 @@ constexpr int kP2Rows = 16;          // output rows per down item
 constexpr int kDecodeMaxT = 7;
 constexpr int kMaxNT = (kDecodeMaxT + 7) / 8;   // token tiles of 8 per expert
 static_assert(kMaxNT == 1, "the gate_up reduction slots hold one token tile");
-constexpr int kFastN = 256;          // assignments ranked by comparison
-constexpr int kFusedMaxN = 2048;     // T * k
+constexpr int kFastN = 256;          // assignments ranked by comparison: one thread each
+static_assert(kDecodeMaxT * kMaxK <= kFastN && kFastN <= kFW * 32, "every assignment has a thread");
 constexpr int kFusedSmem = 232448 - 512;   // per-block opt-in limit, less static shared memory
 
 struct FusedParams {
@@ -101,11 +100,14 @@ struct FusedLayout {
     bool ok;
 };
 
+// At most min(E, T*k) experts are active.
+inline int fused_max_active(const moe_dims &d) { return d.E < d.T * d.k ? d.E : d.T * d.k; }
+
 inline uint32_t fused_pro_bytes(const moe_dims &d) {
     const size_t n = (size_t)d.T * d.k;
-    return (uint32_t)(align_up(n * 2, 16) * 3 + align_up((d.E > kFastN ? d.E : kFastN) * 4, 16) +
-                      align_up((d.E + 1) * 2, 16) +
-                      align_up(d.E * 2, 16) * 3 + align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
+    const size_t na = (size_t)(fused_max_active(d) > 0 ? fused_max_active(d) : 1);
+    return (uint32_t)(align_up(n * 2, 16) * 3 + align_up(kFastN * 4, 16) + align_up(na * 2, 16) * 3 +
+                      align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
 }
 
 // Gate_up partial results: nb buffers of [chunk][lane][4] f32 (a task's
@@ -150,10 +152,7 @@ inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
     L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
     L.total = L.xs_off ? base + xs_bytes : base;
-    // scratch of the prologue lives in the stage area
-    const uint32_t scratch = kFW * d.E * 2 + 2 * d.E * 4 + 3 * kFastN * 4;
-    L.ok = L.total <= (uint32_t)kFusedSmem && scratch <= kNS * L.stage_bytes && d.T <= kDecodeMaxT &&
-           d.T * d.k <= kFusedMaxN && d.I <= 1280 && L.gcw <= 256;
+    L.ok = L.total <= (uint32_t)kFusedSmem && d.T <= kDecodeMaxT && d.k <= kMaxK && d.I <= 1280 && L.gcw <= 256;
     return L;
 }
 
@@ -169,10 +168,16 @@ inline FusedLayout fused_layout(const moe_dims &d) {
 
 bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
 
+int fused_plan(const moe_dims &d) {
+    const FusedLayout L = fused_layout(d);
+    if (!L.ok) return 0;
+    return (L.xs_off ? 1 : 2) | ((L.gcw / 16) << 4);
+}
+
 struct Pro {   // permutation arrays in shared memory
     int16_t *ids, *perm, *inv;
-    int32_t *cnt;   // per-expert counts (large batches) or per-assignment lead flags (small)
-    int16_t *offs, *act, *aoff, *acnt, *kv;
+    int32_t *cnt;   // per assignment: 1 if it is its expert's first
+    int16_t *act, *aoff, *acnt, *kv;
     uint64_t *bar;
     int *nact;
 };
@@ -185,11 +190,11 @@ __device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
     v.ids = reinterpret_cast<int16_t *>(take(n * 2));
     v.perm = reinterpret_cast<int16_t *>(take(n * 2));
     v.inv = reinterpret_cast<int16_t *>(take(n * 2));
-    v.cnt = reinterpret_cast<int32_t *>(take((p.E > kFastN ? p.E : kFastN) * 4));
-    v.offs = reinterpret_cast<int16_t *>(take((p.E + 1) * 2));
-    v.act = reinterpret_cast<int16_t *>(take(p.E * 2));
-    v.aoff = reinterpret_cast<int16_t *>(take(p.E * 2));
-    v.acnt = reinterpret_cast<int16_t *>(take(p.E * 2));
+    v.cnt = reinterpret_cast<int32_t *>(take(kFastN * 4));
+    const int na = p.E < n ? p.E : n;
+    v.act = reinterpret_cast<int16_t *>(take((na > 0 ? na : 1) * 2));
+    v.aoff = reinterpret_cast<int16_t *>(take((na > 0 ? na : 1) * 2));
+    v.acnt = reinterpret_cast<int16_t *>(take((na > 0 ? na : 1) * 2));
     v.kv = reinterpret_cast<int16_t *>(take(p.T * 2));
     v.bar = reinterpret_cast<uint64_t *>(take(4 * kFW * 8));
     v.nact = reinterpret_cast<int *>(take(16));
@@ -207,63 +212,22 @@ static_assert(kNS + 1 <= 4 * kFW, "mbarrier slots");
 __device__ inline uint64_t *full_bar(const Pro &v, int q) { return v.bar + q; }
 __device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + kNS; }
 
-// Exclusive scan over the CTA (kFW warps) of one int per thread; *total gets the sum.
-__device__ inline int cta_exclusive_scan(int v, int *warp_sums, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int s = lane < kFW ? warp_sums[lane] : 0;
-        int si = s;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, si, off);
-            if (lane >= off) si += o;
-        }
-        if (lane < kFW) warp_sums[lane] = si - s;
-        if (lane == kFW - 1) *total = si;
-    }
-    __syncthreads();
-    const int r = warp_sums[warp] + incl - v;
-    __syncthreads();
-    return r;
-}
-
 // The stable permutation, in every CTA: the slot of assignment a is
-// #{valid a' with a lower expert} + #{a' < a with the same expert}.
-// Small batches: id_reg is thread a's id, already loaded by the caller.
+// #{valid a' with a lower expert} + #{a' < a with the same expert}. Thread a
+// ranks assignment a (id_reg: its id, already loaded by the caller); the
+// first assignment of each expert also places the expert in the active list.
 __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v, int id_reg) {
-    __shared__ int warp_sums[kFW];
-    __shared__ int total, nact_s;
+    __shared__ int nact_s;
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5;
     const int n = p.T * p.k, E = p.E;
-    const bool fast = n <= kFastN && n <= nthr;
 
     bool bad = false;
-    if (fast) {
-        if (tid < n) {
-            if (id_reg < 0 || id_reg >= E) {
-                id_reg = -1;
-                bad = true;
-            }
-            v.ids[tid] = (int16_t)id_reg;
+    if (tid < n) {
+        if (id_reg < 0 || id_reg >= E) {
+            id_reg = -1;
+            bad = true;
         }
-    } else {
-        for (int a = tid; a < n; a += nthr) {
-            int e = p.ids[a];
-            if (e < 0 || e >= E) {
-                e = -1;
-                bad = true;
-            }
-            v.ids[a] = (int16_t)e;
-        }
+        v.ids[tid] = (int16_t)id_reg;
     }
     if (bad && blockIdx.x == 0) set_error(p.ctrl, MOE_ERR_DEVICE);
     if (tid == 0) nact_s = 0;
@@ -274,116 +238,39 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
         v.kv[t] = (int16_t)c;
     }
 
-    if (fast) {
-        int32_t *is_lead = v.cnt;
-        const int a = tid;
-        int e = -1, cl = 0, rk = 0, ct = 0;
-        if (a < n) {
-            e = v.ids[a];
-            is_lead[a] = 0;
-            if (e < 0) {
-                v.inv[a] = -1;
-            } else {
-                for (int a2 = 0; a2 < n; ++a2) {
-                    const int e2 = v.ids[a2];
-                    cl += (e2 >= 0) & (e2 < e);
-                    ct += e2 == e;
-                    rk += (e2 == e) & (a2 < a);
-                }
-                const int slot = cl + rk;
-                v.perm[slot] = (int16_t)a;
-                v.inv[a] = (int16_t)slot;
-                if (rk == 0) {
-                    is_lead[a] = 1;
-                    atomicAdd(&nact_s, 1);
-                }
+    int32_t *is_lead = v.cnt;
+    const int a = tid;
+    int e = -1, cl = 0, rk = 0, ct = 0;
+    if (a < n) {
+        e = v.ids[a];
+        is_lead[a] = 0;
+        if (e < 0) {
+            v.inv[a] = -1;
+        } else {
+            for (int a2 = 0; a2 < n; ++a2) {
+                const int e2 = v.ids[a2];
+                cl += (e2 >= 0) & (e2 < e);
+                ct += e2 == e;
+                rk += (e2 == e) & (a2 < a);
             }
-        }
-        __syncthreads();
-        if (a < n && e >= 0 && rk == 0) {
-            int ai = 0;
-            for (int a2 = 0; a2 < n; ++a2) ai += is_lead[a2] & (v.ids[a2] < e);
-            v.act[ai] = (int16_t)e;
-            v.aoff[ai] = (int16_t)cl;
-            v.acnt[ai] = (int16_t)ct;
-        }
-        if (tid == 0) *v.nact = nact_s;
-    } else {
-        for (int e = tid; e < E; e += nthr) v.cnt[e] = 0;
-        __syncthreads();
-        for (int a = tid; a < n; a += nthr)
-            if (v.ids[a] >= 0) atomicAdd(&v.cnt[v.ids[a]], 1);
-        __syncthreads();
-        // offsets and active list: each thread owns ceil(E/nthr) consecutive experts
-        const int per = (E + nthr - 1) / nthr;
-        const int e0 = tid * per;
-        int sum = 0, nz = 0;
-        for (int i = 0; i < per; ++i)
-            if (e0 + i < E) {
-                sum += v.cnt[e0 + i];
-                nz += v.cnt[e0 + i] > 0;
+            const int slot = cl + rk;
+            v.perm[slot] = (int16_t)a;
+            v.inv[a] = (int16_t)slot;
+            if (rk == 0) {
+                is_lead[a] = 1;
+                atomicAdd(&nact_s, 1);
             }
-        const int off0 = cta_exclusive_scan(sum, warp_sums, &total);
-        const int all = total;
-        const int act0 = cta_exclusive_scan(nz, warp_sums, &total);
-        const int nact = total;
-        {
-            int o = off0, ai = act0;
-            for (int i = 0; i < per; ++i)
-                if (e0 + i < E) {
-                    const int c = v.cnt[e0 + i];
-                    v.offs[e0 + i] = (int16_t)o;
-                    if (c > 0) {
-                        v.act[ai] = (int16_t)(e0 + i);
-                        v.aoff[ai] = (int16_t)o;
-                        v.acnt[ai] = (int16_t)c;
-                        ++ai;
-                    }
-                    o += c;
-                }
-        }
-        if (tid == 0) {
-            v.offs[E] = (int16_t)all;
-            *v.nact = nact;
-        }
-        // stable scatter in chunks of nthr assignments; scratch in the stage area
-        uint16_t *wc = reinterpret_cast<uint16_t *>(smem);              // [kFW][E]
-        int32_t *run = reinterpret_cast<int32_t *>(smem + kFW * E * 2);  // [E]
-        int32_t *tot = run + E;                                          // [E]
-        for (int e = tid; e < E; e += nthr) run[e] = 0;
-        for (int base = 0; base < n; base += nthr) {
-            for (int i = tid; i < kFW * E; i += nthr) wc[i] = 0;
-            __syncthreads();
-            const int a = base + tid;
-            const int e = a < n ? v.ids[a] : -1;
-            const unsigned same = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(same & ((1u << lane) - 1u));
-            if (e >= 0 && rank == 0) wc[warp * E + e] = (uint16_t)__popc(same);
-            __syncthreads();
-            for (int x = tid; x < E; x += nthr) {
-                int r = 0;
-                for (int w = 0; w < kFW; ++w) {
-                    const int c = wc[w * E + x];
-                    wc[w * E + x] = (uint16_t)r;
-                    r += c;
-                }
-                tot[x] = r;
-            }
-            __syncthreads();
-            if (a < n) {
-                if (e >= 0) {
-                    const int slot = v.offs[e] + run[e] + wc[warp * E + e] + rank;
-                    v.perm[slot] = (int16_t)a;
-                    v.inv[a] = (int16_t)slot;
-                } else {
-                    v.inv[a] = -1;
-                }
-            }
-            __syncthreads();
-            for (int x = tid; x < E; x += nthr) run[x] += tot[x];
         }
     }
     __syncthreads();
+    if (a < n && e >= 0 && rk == 0) {
+        int ai = 0;
+        for (int a2 = 0; a2 < n; ++a2) ai += is_lead[a2] & (v.ids[a2] < e);
+        v.act[ai] = (int16_t)e;
+        v.aoff[ai] = (int16_t)cl;
+        v.acnt[ai] = (int16_t)ct;
+    }
+    if (tid == 0) *v.nact = nact_s;
     {
         const RingWords rw = ring_words(smem, p);
         if (tid < 2 * p.nb + 1) rw.cnt[tid] = 0;   // chunks done, tasks finalised, the ticket
@@ -397,8 +284,6 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
         mbar_init(v.bar + tid, 1);
         fence_mbar_init();
     }
-    // large batches used the stage area as scratch, where weight copies will land
-    if (!fast) fence_proxy_async_smem();
     __syncthreads();
 }
 
@@ -981,7 +866,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     pdl_wait();
     // the ids are the first thing every path needs
     int id_reg = -1;
-    if (p.T * p.k <= kFastN && (int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
+    if ((int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
     if (p.xs_off && threadIdx.x == 0) {
         // the activations start moving now, behind the permutation
         const uint32_t xb = (uint32_t)p.T * p.H * 2;
@@ -1108,17 +993,18 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     cfg.blockDim = dim3(kFW * 32);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
-    // programmatic launch: the CTAs take their SMs and set up while the router
-    // finishes. The CTAs wait on one another; all of them become resident,
-    // since the grid is at most one CTA per SM and whatever else may hold an
-    // SM meanwhile (the router ahead) finishes without waiting on this grid,
-    // and a kernel behind it is launched only once every CTA has reached its
-    // exit. The waits are bounded all the same.
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // The CTAs wait on one another, so the launch is cooperative: the runtime
+    // either makes every CTA co-resident or fails the launch (the grid is at
+    // most one CTA per SM), whatever other work shares the device. It is also
+    // programmatic: the CTAs take their SMs and set up while the router ahead
+    // finishes. The waits are bounded all the same.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, p);
     return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, p);
 }

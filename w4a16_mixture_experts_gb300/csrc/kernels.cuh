@@ -51,6 +51,10 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
 
 // Fused decode forward (T <= 7): permute, experts and combine in one launch.
 bool fused_supported(const moe_dims &d);
+// 0 if the forward takes the tensor-core pipeline; else 1 (activations staged
+// in shared memory) or 2 (read from global memory), plus 16 * quantisation
+// groups per gate_up chunk.
+int fused_plan(const moe_dims &d);
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
                                 float eps, cudaStream_t s);
 

@@ -22,13 +22,17 @@
 //    it and give wrong results.
 //  - The first call on a device does the set-up (the symbol lookup, which
 //    may load this module); make that first call outside any stream capture.
-//  - The fused kernel needs its completion counters at zero when it starts.
-//    Each call clears them itself with one small cudaMemsetAsync on its
-//    stream, so neither module-load zero fill nor what an earlier call (of any
-//    shape) left behind matters. Nothing else in the array must start at zero.
+//  - The fused kernel needs its completion counters and the control block
+//    (error word, exit and barrier counts) at zero when it starts. Each call
+//    clears both itself with two small cudaMemsetAsync on its stream, so
+//    neither the module-load zero fill nor what an earlier call (of any shape,
+//    finished or given up) left behind matters. Nothing else in the array must
+//    start at zero.
 //  - Errors seen by the kernel (an id outside [0, E), a bounded wait that
-//    gave up) are recorded in the array's error word, which this entry point
-//    does not expose; a bad id still contributes nothing to the output.
+//    gave up) are recorded in the array's error word; a bad id still
+//    contributes nothing to the output. moe_noalloc_check_device_error reads
+//    the word (it synchronises, so it is meant for tests and error paths).
+//    Since every call clears the word first, it reports the last call only.
 #include <stdint.h>
 
 #include <mutex>
@@ -95,11 +99,27 @@ extern "C" int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *
     cudaError_t err = static_scratch(&ws);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // done1, ticket and rowss are adjacent in the layout; rbuf follows.
+    // the control block, then done1, ticket and rowss, which are adjacent in
+    // the layout (rbuf follows them)
     const WsLayout W = ws_layout(d);
-    err = cudaMemsetAsync(ws_at<char>(ws, W.done1), 0, W.rbuf - W.done1, s);
+    err = cudaMemsetAsync(ws_at<char>(ws, W.ctrl), 0, sizeof(Ctrl), s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(ws_at<char>(ws, W.done1), 0, W.rbuf - W.done1, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     const ExpertArgs a{hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales};
     err = launch_decode_fused(a, d, ws, out, nullptr, 0.f, s);
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_noalloc_check_device_error(void *stream) {
+    void *ws = nullptr;
+    if (static_scratch(&ws) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t err_word = 0;
+    if (cudaMemcpyAsync(&err_word, ws, sizeof(err_word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!err_word) return MOE_OK;
+    if (cudaMemsetAsync(ws, 0, sizeof(err_word), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    return err_word == MOE_ERR_TIMEOUT ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
 }

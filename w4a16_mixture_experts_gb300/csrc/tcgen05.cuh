@@ -114,16 +114,5 @@ __device__ inline void ld_32x32b_x32(uint32_t taddr, float (&v)[32]) {
 }
 __device__ inline void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// ---- TMA ------------------------------------------------------------------------
-// Four rows (r0..r3) of a 2-D tensor whose box is one row high, starting at
-// column c0, into 4 consecutive box-sized slots of shared memory.
-__device__ inline void tma_gather4(void *dst, const void *tmap, int c0, int r0, int r1, int r2, int r3, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
-
 }  // namespace tc
 }  // namespace moe
