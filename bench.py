@@ -69,7 +69,7 @@ def parse():
     ap.add_argument("--sets", type=int, default=0, help="weight sets to rotate over (0: enough to exceed L2)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
-    ap.add_argument("--clock-ms", type=float, default=300.0,
+    ap.add_argument("--clock-ms", type=float, default=1000.0,
                     help="length of the load window, ending with the timed region, over which clocks are sampled")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="measure the headline workload only (by default a decode1 run also measures %s)"

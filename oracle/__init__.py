@@ -54,6 +54,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_residual_rms.argtypes = [P, P, I, I, ctypes.c_double, P, P]
         L.oracle_round_bf16.argtypes = [P, I64, P]
         L.oracle_max_threads.restype = I
+        L.oracle_shared_expert.argtypes = [P, P, P, P, P, P, I, I, I, P, P, I]
+        L.oracle_shared_combine.argtypes = [P, P, P, I, I, P]
+        L.oracle_quantize_int4.argtypes = [P, I64, I64, I, P, P, P, P]
+        L.oracle_quantize_int4.restype = I
         _lib = L
     return _lib
 
@@ -179,3 +183,49 @@ def round_bf16(v: np.ndarray) -> np.ndarray:
     bits = np.empty(a.shape, np.uint16)
     lib().oracle_round_bf16(_p(a), a.size, _p(bits))
     return bits
+
+
+def shared_expert(x, wg, w1_packed, w1_scales, w2_packed, w2_scales, I: int, nthreads: int = 0):
+    """(gate logits f64 [T], unweighted shared-expert output f64 [T, H]).
+
+    wg bf16 [H] is the router's extra row; the weights are one expert in the
+    routed experts' storage: w1 [2I, H/8] / [2I, H/128], w2 [H, I/8] / [H, I/128].
+    """
+    xs = _np(x, np.uint16)
+    T, H = xs.shape
+    g = _np(wg, np.uint16).reshape(-1)
+    p1, s1 = _np(w1_packed, np.int32), _np(w1_scales, np.uint16)
+    p2, s2 = _np(w2_packed, np.int32), _np(w2_scales, np.uint16)
+    gate = np.empty(T, np.float64)
+    y = np.empty((T, H), np.float64)
+    lib().oracle_shared_expert(_p(xs), _p(g), _p(p1), _p(s1), _p(p2), _p(s2), T, H, I, _p(gate), _p(y), nthreads)
+    return gate, y
+
+
+def shared_combine(routed: np.ndarray, gate: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """routed + sigmoid(gate) * y, f64 [T, H]."""
+    r = np.ascontiguousarray(routed, dtype=np.float64)
+    g = np.ascontiguousarray(gate, dtype=np.float64)
+    yy = np.ascontiguousarray(y, dtype=np.float64)
+    T, H = r.shape
+    out = np.empty((T, H), np.float64)
+    lib().oracle_shared_combine(_p(r), _p(g), _p(yy), T, H, _p(out))
+    return out
+
+
+def quantize_int4(w, nclip: int = 50):
+    """RTN INT4 g128 symmetric with a per-group clip search over nclip candidates.
+
+    w bf16 [N, K]. Returns (packed int32 [N, K/8], scales bf16 bits uint16 [N, K/128],
+    choice int32 [N, K/128] (the clip index j, c_j = (100 - j)/100), err f64 [N, K/128, nclip]).
+    """
+    ws = _np(w, np.uint16)
+    N, K = ws.shape
+    G = K // 128
+    packed = np.empty((N, K // 8), np.int32)
+    scales = np.empty((N, G), np.uint16)
+    choice = np.empty((N, G), np.int32)
+    err = np.empty((N, G, nclip), np.float64)
+    if lib().oracle_quantize_int4(_p(ws), N, K, nclip, _p(err), _p(packed), _p(scales), _p(choice)) != 0:
+        raise ValueError("K must be a multiple of 128 and 1 <= nclip <= 100")
+    return packed, scales, choice, err

@@ -30,6 +30,15 @@
  *              (section 3.3: fused Marlin MoE gate_up, SiluAndMul, down,
  *              moe_sum.)
  *   stack    - next layer input = bf16(r / sqrt(mean(r^2) + eps)), r = x + out.
+ *   shared   - the shared expert beside the routed ones: its gate logit
+ *              g = x . wg is one more row of the router GEMV, and the layer
+ *              output is routed + sigmoid(g) * SwiGLU_shared(x).
+ *              (section 3.3 "MoE block": the router and the shared expert gate
+ *              as one GEMV of 512 + 1 rows; the final combine, routed +
+ *              sigmoid(gate) x shared.)
+ *   quantise - round-to-nearest INT4, group size 128, symmetric, with a
+ *              per-group search for the clip that minimises the squared error.
+ *              (section 7 "Putting MTP on the GPU": make_mtp_int4.py.)
  *
  * Parity of the expert outputs themselves is pinned only by brute force,
  * closed forms and invariants in the tests; the pages print no worked example
@@ -317,4 +326,156 @@ void oracle_residual_rms(const uint16_t *x, const double *out, int T, int H, dou
 void oracle_round_bf16(const double *v, int64_t n, uint16_t *bits)
 {
     for (int64_t i = 0; i < n; ++i) bits[i] = f64_to_bf16(v[i]);
+}
+
+/* ---- shared expert ---------------------------------------------------------- */
+
+/*
+ * The shared expert of one layer, for every token:
+ *   gate[t] = sum_h x[t][h] * wg[h]                  (the router's extra row)
+ *   y[t]    = W2s (SiLU(W1s[0:I] x_t) * W1s[I:2I] x_t)   (unweighted)
+ * Weights in the routed experts' storage: w1p int32 [2I][H/8], w1s bf16
+ * [2I][H/128], w2p int32 [H][I/8], w2s bf16 [H][I/128].
+ */
+void oracle_shared_expert(const uint16_t *x, const uint16_t *wg, const int32_t *w1p, const uint16_t *w1s,
+                          const int32_t *w2p, const uint16_t *w2s, int T, int H, int I, double *gate,
+                          double *y, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic)
+        for (int t = 0; t < T; ++t) {
+            if (!xt || !h) continue;
+            double g0 = 0.0;
+            for (int c = 0; c < H; ++c) {
+                xt[c] = bf16_to_f64(x[(int64_t)t * H + c]);
+                g0 += xt[c] * bf16_to_f64(wg[c]);
+            }
+            gate[t] = g0;
+            for (int i = 0; i < I; ++i) {
+                double g = 0.0, u = 0.0;
+                for (int c = 0; c < H; ++c) {
+                    g += weight(w1p, w1s, H, i, c) * xt[c];
+                    u += weight(w1p, w1s, H, (int64_t)I + i, c) * xt[c];
+                }
+                h[i] = g / (1.0 + exp(-g)) * u;
+            }
+            for (int n = 0; n < H; ++n) {
+                double s = 0.0;
+                for (int i = 0; i < I; ++i) s += weight(w2p, w2s, I, n, i) * h[i];
+                y[(int64_t)t * H + n] = s;
+            }
+        }
+        free(xt);
+        free(h);
+    }
+}
+
+/* out[t][n] = routed[t][n] + sigmoid(gate[t]) * y[t][n]. */
+void oracle_shared_combine(const double *routed, const double *gate, const double *y, int T, int H,
+                           double *out)
+{
+    for (int t = 0; t < T; ++t) {
+        double sg = 1.0 / (1.0 + exp(-gate[t]));
+        for (int n = 0; n < H; ++n) out[(int64_t)t * H + n] = routed[(int64_t)t * H + n] + sg * y[(int64_t)t * H + n];
+    }
+}
+
+/* ---- INT4 quantiser ----------------------------------------------------------- */
+
+/*
+ * Round to nearest, symmetric, one scale per 128 consecutive values of a row.
+ * For a group with amax = max |w| and clip ratio c_j = (100 - j) / 100
+ * (j = 0 .. nclip-1; nclip = 1 is plain round-to-nearest):
+ *   s_j = bf16(c_j * amax / 7)            (the stored scale; fp32 arithmetic,
+ *                                          each step rounded to nearest)
+ *   q_i = clamp(rint(w_i / s_j), -8, 7)   (fp32 division; q = 0 if s_j = 0)
+ *   err_j = sum_i (w_i - q_i * s_j)^2     (fp64)
+ * The group takes the j with the smallest err_j, the lowest j on a tie.
+ * The rounding decisions are made in fp32, the precision of the kernel.
+ *
+ * w bf16 [N][K] (K a multiple of 128); err f64 [N][K/128][nclip] (may be
+ * NULL); packed int32 [N][K/8] and scales bf16 [N][K/128] (may be NULL: then
+ * only err is written); choice int32 [N][K/128] (may be NULL).
+ */
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint16_t f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float clip_scale(float amax, int j)
+{
+    volatile float c = (float)(100 - j) / 100.0f;   /* volatile: each step rounded to fp32 */
+    volatile float t = c * amax;
+    volatile float s = t / 7.0f;
+    return bf16_to_f32(f32_to_bf16(s));
+}
+
+static int quant_one(float w, float s)
+{
+    if (s == 0.0f) return 0;
+    volatile float r = w / s;
+    float q = rintf(r);
+    if (q < -8.0f) q = -8.0f;
+    if (q > 7.0f) q = 7.0f;
+    return (int)q;
+}
+
+int oracle_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nclip, double *err,
+                         int32_t *packed, uint16_t *scales, int32_t *choice)
+{
+    if (K % ORACLE_GROUP || nclip < 1 || nclip > 100) return -1;
+    const int64_t G = K / ORACLE_GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t rg = 0; rg < N * G; ++rg) {
+        const int64_t n = rg / G, g = rg % G;
+        const uint16_t *wv = w + n * K + g * ORACLE_GROUP;
+        float amax = 0.0f;
+        for (int i = 0; i < ORACLE_GROUP; ++i) {
+            float a = fabsf(bf16_to_f32(wv[i]));
+            if (a > amax) amax = a;
+        }
+        int best = 0;
+        double best_err = 0.0;
+        for (int j = 0; j < nclip; ++j) {
+            const float s = clip_scale(amax, j);
+            double e = 0.0;
+            for (int i = 0; i < ORACLE_GROUP; ++i) {
+                const double wi = (double)bf16_to_f32(wv[i]);
+                const double d = wi - (double)quant_one(bf16_to_f32(wv[i]), s) * (double)s;
+                e += d * d;
+            }
+            if (err) err[rg * nclip + j] = e;
+            if (j == 0 || e < best_err) {
+                best = j;
+                best_err = e;
+            }
+        }
+        if (choice) choice[rg] = best;
+        if (!packed || !scales) continue;
+        const float s = clip_scale(amax, best);
+        scales[rg] = f32_to_bf16(s);
+        for (int wd = 0; wd < ORACLE_GROUP / 8; ++wd) {
+            uint32_t word = 0;
+            for (int i = 0; i < 8; ++i)
+                word |= (uint32_t)(quant_one(bf16_to_f32(wv[8 * wd + i]), s) + 8) << (4 * i);
+            packed[n * (K / 8) + g * (ORACLE_GROUP / 8) + wd] = (int32_t)word;
+        }
+    }
+    return 0;
 }

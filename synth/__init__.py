@@ -36,7 +36,7 @@ import torch
 GROUP = 128  # quantisation group size along K
 
 # tensor ids inside a SeedSequence
-_T_HIDDEN, _T_ROUTER, _T_W1, _T_W1S, _T_W2, _T_W2S, _T_ZIPF, _T_TOPK = range(8)
+_T_HIDDEN, _T_ROUTER, _T_W1, _T_W1S, _T_W2, _T_W2S, _T_ZIPF, _T_TOPK, _T_QW = range(9)
 
 
 @dataclass(frozen=True)
@@ -156,6 +156,38 @@ def random_topk(T: int, E: int, k: int, seed: int = 0, layer: int = 0):
     ids = np.stack([g.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
     w = (np.float32(0.05) + np.float32(0.95) * g.random((T, k), dtype=np.float32))
     return torch.from_numpy(ids.reshape(T, k)), torch.from_numpy(w.reshape(T, k))
+
+
+def shared_layer_inputs(wl: Workload, seed: int = 0, layer: int = 0) -> dict:
+    """Inputs of one layer with a shared expert beside the E routed ones.
+
+    The router gets one more row (the shared expert's gate, drawn like the
+    others: the first E rows are those of router(E, H)), and the expert
+    tensors one more expert, the shared one, at index E (drawn from the
+    per-expert streams like a routed expert E would be).
+    """
+    T, H, E, k, I = wl.dims
+    d = {
+        "hidden": hidden(T, H, seed, 0),
+        "router_w": router(E + 1, H, seed, layer),
+        "bias": zipf_bias(E, wl.zipf, seed, layer) if wl.zipf else None,
+    }
+    d.update(expert_weights(E + 1, H, I, seed, layer))
+    return d
+
+
+def bf16_weights(N: int, K: int, seed: int = 0, layer: int = 0, outliers: float = 1.0 / 512) -> torch.Tensor:
+    """bf16 [N, K] weights to quantise: N(0, 0.02^2) with a few outliers.
+
+    A fraction `outliers` of the values is multiplied by a factor uniform on
+    [4, 12], so that some groups hold one large value: the groups where a
+    clipped scale beats the plain maximum.
+    """
+    g = _rng(seed, layer, _T_QW)
+    w = g.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    mask = g.random((N, K), dtype=np.float32) < np.float32(outliers)
+    w[mask] *= np.float32(4.0) + np.float32(8.0) * g.random(int(mask.sum()), dtype=np.float32)
+    return _bf16(w)
 
 
 def layer_inputs(wl: Workload, seed: int = 0, layer: int = 0, experts=None) -> dict:

@@ -293,3 +293,145 @@ def test_residual_rms_closed_form():
     r = _f64(xr) + o
     assert np.allclose(np.sqrt((nf ** 2).mean(1)), np.sqrt((r ** 2).mean(1) / ((r ** 2).mean(1) + 1e-6)),
                        atol=1e-14)
+
+
+# ---------------------------------------------------------- shared expert ----
+# "vLLM Optimization Edition" 3.3 "MoE block": the shared expert's gate is one
+# more row of the router GEMV, and the layer's output is routed + sigmoid(gate)
+# x shared.
+
+def _shared_tiny(seed=0):
+    wl = synth.WORKLOADS["tiny"]
+    T, H, E, k, I = wl.dims
+    d = synth.shared_layer_inputs(wl, seed=seed)
+    return wl, d
+
+
+def test_shared_gate_and_expert_equal_library_forms():
+    wl, d = _shared_tiny(seed=20)
+    T, H, E, k, I = wl.dims
+    wg = d["router_w"][E]
+    gate, y = oracle.shared_expert(d["hidden"], wg, d["w1_packed"][E], d["w1_scales"][E],
+                                   d["w2_packed"][E], d["w2_scales"][E], I)
+    x = _f64(d["hidden"])
+    assert np.allclose(gate, x @ _f64(wg), rtol=0, atol=1e-12)
+    W1 = _dense_numpy(d["w1_packed"][E], d["w1_scales"][E])
+    W2 = _dense_numpy(d["w2_packed"][E], d["w2_scales"][E])
+    g, u = x @ W1[:I].T, x @ W1[I:].T
+    ref = (g * expit(g) * u) @ W2.T
+    assert np.abs(y - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_shared_combine_closed_forms():
+    g = np.random.default_rng(21)
+    routed, y = g.standard_normal((3, 256)), g.standard_normal((3, 256))
+    # sigmoid(0) = 1/2 exactly
+    out = oracle.shared_combine(routed, np.zeros(3), y)
+    assert np.array_equal(out, routed + 0.5 * y)
+    # a gate far below zero leaves the routed output; far above, adds all of the shared one
+    assert np.allclose(oracle.shared_combine(routed, np.full(3, -800.0), y), routed, rtol=0, atol=0)
+    assert np.allclose(oracle.shared_combine(routed, np.full(3, 800.0), y), routed + y, rtol=0, atol=1e-15)
+    gate = np.array([-1.0, 0.3, 2.0])
+    ref = routed + y / (1.0 + np.exp(-gate))[:, None]
+    assert np.allclose(oracle.shared_combine(routed, gate, y), ref, rtol=0, atol=1e-14)
+
+
+def test_shared_expert_is_one_more_expert_with_weight_sigmoid_gate():
+    """routed + sigmoid(g) * shared equals the routed-expert sum over k + 1 slots
+    whose last slot is the shared expert (index E) with weight sigmoid(g)."""
+    wl, d = _shared_tiny(seed=22)
+    T, H, E, k, I = wl.dims
+    logits = oracle.router_logits(d["hidden"], d["router_w"][:E])
+    ids, w = oracle.topk_softmax(logits, k)
+    W = (d["w1_packed"], d["w1_scales"], d["w2_packed"], d["w2_scales"])
+    routed = oracle.expert_forward(d["hidden"], ids, w.astype(np.float32), *W, E + 1, I)
+    gate, y = oracle.shared_expert(d["hidden"], d["router_w"][E], *(t[E] for t in W), I)
+    layer = oracle.shared_combine(routed, gate, y)
+    sg = (1.0 / (1.0 + np.exp(-gate))).astype(np.float32)
+    ids1 = np.concatenate([ids, np.full((T, 1), E, np.int32)], axis=1)
+    w1 = np.concatenate([w.astype(np.float32), sg[:, None]], axis=1)
+    one = oracle.expert_forward(d["hidden"], ids1, w1, *W, E + 1, I)
+    # the only difference: the gate weight passes through float32 in the slot form
+    assert np.abs(one - layer).max() <= 1e-6 * np.abs(layer).max()
+    # the router's first E rows are those of the layer without a shared expert
+    assert torch.equal(d["router_w"][:E], synth.router(E, H, seed=22))
+
+
+# -------------------------------------------------------------- quantiser ----
+# "vLLM Optimization Edition" 7 "Putting MTP on the GPU": RTN, g128,
+# symmetric, with a per-group search for the clip that minimises squared error.
+
+def _bf16_tensor(v):
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16)
+
+
+def test_quantize_exactly_representable_group():
+    # w = q0 * 2^-6 with q0 in [-7, 7] reaching 7: the unclipped scale is 2^-6
+    # exactly, every value is hit, and no other candidate has zero error
+    g = np.random.default_rng(30)
+    q0 = g.integers(-7, 8, (3, 256))
+    q0[:, 5] = 7
+    q0[:, 133] = -7
+    w = _bf16_tensor(q0 * 2.0 ** -6)
+    packed, scales, choice, err = oracle.quantize_int4(w, 50)
+    assert (choice == 0).all() and (err[:, :, 0] == 0).all()
+    assert np.array_equal(_f64(torch.from_numpy(scales.view(np.int16)).view(torch.bfloat16)),
+                          np.full((3, 2), 2.0 ** -6))
+    assert np.array_equal(oracle.unpack_int4(packed, 3, 256), q0)
+
+
+def test_quantize_single_candidate_is_plain_round_to_nearest():
+    # nclip = 1 (no search): s = bf16(amax / 7), q = clip(round_half_even(w / s), -8, 7)
+    w = synth.bf16_weights(16, 512, seed=31)
+    packed, scales, choice, _ = oracle.quantize_int4(w, 1)
+    wf = w.float().numpy().reshape(16, 4, 128)
+    amax = np.abs(wf).max(axis=2)
+    s = torch.from_numpy((amax / np.float32(7.0)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    q = np.clip(np.round(wf / s[:, :, None]), -8, 7).astype(np.int64).reshape(16, 512)
+    assert np.array_equal(oracle.unpack_int4(packed, 16, 512), q)
+    assert np.array_equal(scales, _bits(torch.from_numpy(s).to(torch.bfloat16)))
+    assert (choice == 0).all()
+
+
+def test_quantize_choice_minimises_the_error_of_its_own_output():
+    w = synth.bf16_weights(32, 384, seed=32)
+    packed, scales, choice, err = oracle.quantize_int4(w, 50)
+    # the choice is the first minimum of the candidates' errors
+    assert np.array_equal(choice, err.argmin(axis=2))
+    # the packed output, dequantised by a separate routine, has exactly that error
+    W = oracle.dequant(packed, torch.from_numpy(scales.view(np.int16)).view(torch.bfloat16), 32, 384)
+    e = ((_f64(w) - W) ** 2).reshape(32, 3, 128).sum(axis=2)
+    assert np.allclose(e, err.min(axis=2), rtol=1e-12, atol=0)
+    # a search over more candidates never does worse than plain rounding
+    _, _, _, err1 = oracle.quantize_int4(w, 1)
+    assert (err.min(axis=2) <= err1[:, :, 0]).all()
+    assert (err.min(axis=2) < err1[:, :, 0]).mean() > 0.5
+
+
+def test_quantize_power_of_two_scaling_and_zero_groups():
+    w = synth.bf16_weights(8, 256, seed=33)
+    a = oracle.quantize_int4(w, 50)
+    b = oracle.quantize_int4((w.float() * 8.0).to(torch.bfloat16), 50)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+    sa = torch.from_numpy(a[1].view(np.int16)).view(torch.bfloat16).float()
+    sb = torch.from_numpy(b[1].view(np.int16)).view(torch.bfloat16).float()
+    assert torch.equal(sb, sa * 8.0)
+    # an all-zero group stores scale 0 and the nibble of q = 0 (8) everywhere
+    z = torch.zeros(2, 128, dtype=torch.bfloat16)
+    p, s, c, e = oracle.quantize_int4(z, 50)
+    assert (p.view(np.uint32) == 0x88888888).all() and (s == 0).all() and (e == 0).all()
+
+
+def test_quantize_single_outlier_closed_form():
+    # one value 7 * 2^-3 and 127 zeros: the unclipped scale 2^-3 gives q = 7 and zero error
+    v = np.zeros((1, 128), np.float32)
+    v[0, 77] = 7 * 2.0 ** -3
+    p, s, c, e = oracle.quantize_int4(_bf16_tensor(v), 50)
+    assert c[0, 0] == 0 and e[0, 0, 0] == 0
+    q = oracle.unpack_int4(p, 1, 128)
+    assert q[0, 77] == 7 and not np.delete(q[0], 77).any()
+    # the last candidate, c = 0.51: 0.51 * 0.875 / 7 = 0.06375 = 2^-4 * 1.02, and
+    # 1.02 * 128 = 130.56 rounds to 131, so the bf16 scale is 2^-4 * 131/128 =
+    # 0.06396484375; 0.875 / 0.06396484375 = 13.7 saturates q at 7, leaving
+    # (0.875 - 7 * 0.06396484375)^2 = 0.42724609375^2
+    assert e[0, 0, 49] == 0.42724609375 ** 2
