@@ -100,6 +100,30 @@ MOE_API int moe_route(const uint16_t *hidden, const uint16_t *router_w, const fl
               void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_route for a layer with a shared expert ("vLLM Optimization Edition",
+ * section 3.3 "MoE block (decode-05)": the router and the shared expert's gate
+ * are one GEMV of 512 + 1 rows, and the layer's output is routed +
+ * sigmoid(gate) x shared).
+ *
+ * router_w bf16 [E+1][H]: rows [0, E) route, row E is the shared expert's gate.
+ * d: the routed dims (E routed experts, k of them per token); k + 1 <= 32 and
+ * E + 1 <= 1024. bias f32 [E] or NULL applies to the routed logits only.
+ * topk_ids int32 [T][k+1], topk_w f32 [T][k+1] (outputs): slots [0, k) as
+ * moe_route; slot k = expert E with weight sigmoid(x . router_w[E]) (fp32).
+ * The workspace is sized by moe_workspace_size(d).
+ *
+ * The shared expert is then expert E of the weight tensors (stored as a
+ * routed expert, INT4 g128, intermediate I): moe_w4a16_forward with dims
+ * (T, H, E+1, k+1, I) and these ids and weights computes
+ *   out = sum_j topk_w[j] * expert_j(x) + sigmoid(gate) * shared(x)
+ * in one pass, with one rounding to bf16. Its workspace is sized by
+ * moe_workspace_size(T, H, E+1, k+1, I).
+ */
+MOE_API int moe_route_shared(const uint16_t *hidden, const uint16_t *router_w, const float *bias,
+                     moe_dims d, int32_t *topk_ids, float *topk_w,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Routed-expert forward ("vLLM Optimization Edition", section 3.3: the fused
  * Marlin MoE gate_up, SiluAndMul, down, and moe_sum; weights as in the model
  * card's group A):
@@ -195,6 +219,24 @@ MOE_API int moe_permute(const int32_t *topk_ids, moe_dims d, int32_t *offsets, i
  */
 MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed,
                   int32_t *bad_count, void *stream);
+
+/*
+ * INT4 quantiser of BF16 weights into the experts' storage ("vLLM
+ * Optimization Edition", section 7 "Putting MTP on the GPU", make_mtp_int4.py:
+ * round to nearest, group size 128, symmetric, per-group search for the clip
+ * that minimises the squared error). For each 128 consecutive values w of a
+ * row, with amax = max |w| and clip c_j = (100 - j) / 100, j in [0, nclip):
+ *   s_j = bf16(c_j * amax / 7)  (fp32 multiply and divide, bf16 round to nearest even)
+ *   q_i = clamp(rint(w_i / s_j), -8, 7)  (fp32 divide; q = 0 when s_j = 0)
+ * and the group keeps the j with the smallest sum_i (w_i - q_i s_j)^2 (summed
+ * in fp32; the lowest j on a tie). nclip = 1 is plain round to nearest.
+ *
+ * w bf16 [N][K], finite; K a multiple of 128; 1 <= nclip <= 100.
+ * packed int32 [N][K/8] (outputs; q + 8, lowest nibble first), scales bf16
+ * [N][K/128], choice int32 [N][K/128] (the chosen j; may be NULL).
+ */
+MOE_API int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t nclip, int32_t *packed,
+                      uint16_t *scales, int32_t *choice, void *stream);
 
 /*
  * Which kernels a forward call of dims `d` runs (a host-only query, no

@@ -108,6 +108,19 @@ def test_argument_errors_are_synchronous(L):
                        None) == 1
     # pack with K not a multiple of 8
     assert L.moe_pack_int4(ctypes.c_void_p(good[0]), 4, 12, ctypes.c_void_p(good[1]), None, None) == 1
+    # quantiser: K not a multiple of 128, nclip outside [1, 100]
+    assert L.moe_quantize_int4(ctypes.c_void_p(good[0]), 4, 200, 50, ctypes.c_void_p(good[1]),
+                               ctypes.c_void_p(good[2]), None, None) == 1
+    for nclip in (0, 101):
+        assert L.moe_quantize_int4(ctypes.c_void_p(good[0]), 4, 256, nclip, ctypes.c_void_p(good[1]),
+                                   ctypes.c_void_p(good[2]), None, None) == 1
+    # shared-expert routing: k + 1 must stay within 32 slots, E + 1 within 1024 experts
+    assert L.moe_route_shared(*[ctypes.c_void_p(p) for p in good[:3]], moe.moe_dims(4, 256, 64, 32, 128),
+                              ctypes.c_void_p(good[3]), ctypes.c_void_p(good[4]), ctypes.c_void_p(good[5]),
+                              1 << 30, None) == 2
+    assert L.moe_route_shared(*[ctypes.c_void_p(p) for p in good[:3]], moe.moe_dims(4, 256, 1024, 8, 128),
+                              ctypes.c_void_p(good[3]), ctypes.c_void_p(good[4]), ctypes.c_void_p(good[5]),
+                              1 << 30, None) == 2
     # device-error check with no workspace
     assert L.moe_check_device_error(None, 0, None) == 1
     # empty batch: nothing to do, no device access

@@ -22,8 +22,8 @@ import torch
 
 __all__ = [
     "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
-    "workspace", "moe_route", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
-    "moe_pack_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
+    "workspace", "moe_route", "moe_route_shared", "shared_workspace", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
+    "moe_pack_int4", "moe_quantize_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
     "moe_noalloc_check_device_error", "moe_forward_plan", "STATUS",
 ]
 
@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.moe_version.argtypes, L.moe_version.restype = [], I
         L.moe_workspace_size.argtypes, L.moe_workspace_size.restype = [D, ctypes.POINTER(Z)], I
         L.moe_route.argtypes, L.moe_route.restype = [P, P, P, D, P, P, P, Z, P], I
+        L.moe_route_shared.argtypes, L.moe_route_shared.restype = [P, P, P, D, P, P, P, Z, P], I
         L.moe_w4a16_forward.argtypes = [P, P, P, P, P, P, P, P, D, P, Z, P]
         L.moe_w4a16_forward.restype = I
         L.moe_w4a16_forward_rms.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, D, P, Z, P]
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.moe_w4a16_forward_noalloc.restype = I
         L.moe_permute.argtypes, L.moe_permute.restype = [P, D, P, P, P, Z, P], I
         L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
+        L.moe_quantize_int4.argtypes = [P, I64, I64, ctypes.c_int32, P, P, P, P]
+        L.moe_quantize_int4.restype = I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
         L.moe_noalloc_check_device_error.argtypes, L.moe_noalloc_check_device_error.restype = [P], I
         L.moe_profile_events.argtypes, L.moe_profile_events.restype = [P, P], I
@@ -155,6 +158,37 @@ def moe_route(hidden, router_w, k: int, bias=None, ws=None, topk_ids=None, topk_
         topk_w = torch.empty(T, k, dtype=torch.float32, device=hidden.device)
     _check(lib().moe_route(_p(hidden), _p(router_w), _p(bias), dims, _p(topk_ids), _p(topk_w), _p(ws),
                            ws.numel(), _stream(stream)), "moe_route")
+    return topk_ids, topk_w
+
+
+def shared_workspace(T: int, H: int, E: int, k: int, I: int, device=None) -> torch.Tensor:
+    """A zeroed workspace that serves moe_route_shared (routed dims E, k) and the
+    forward of the layer with its shared expert (E + 1 experts, k + 1 slots)."""
+    n = max(moe_workspace_size(T, H, E, k, I), moe_workspace_size(T, H, E + 1, k + 1, I))
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def moe_route_shared(hidden, router_w, k: int, bias=None, ws=None, topk_ids=None, topk_w=None, stream=None):
+    """Routing of a layer with a shared expert: router_w [E+1, H], row E the shared gate.
+
+    Returns (topk_ids int32 [T, k+1], topk_w f32 [T, k+1]); slot k is expert E with
+    weight sigmoid(gate). Pass them to moe_w4a16_forward with the E+1 experts' weights.
+    """
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(router_w, "router_w", torch.bfloat16, 2)
+    T, H = hidden.shape
+    E = router_w.shape[0] - 1
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+    dims = moe_dims(T, H, E, k, 128)
+    if ws is None:
+        ws = shared_workspace(T, H, E, k, 128, hidden.device)
+    if topk_ids is None:
+        topk_ids = torch.empty(T, k + 1, dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, k + 1, dtype=torch.float32, device=hidden.device)
+    _check(lib().moe_route_shared(_p(hidden), _p(router_w), _p(bias), dims, _p(topk_ids), _p(topk_w), _p(ws),
+                                  ws.numel(), _stream(stream)), "moe_route_shared")
     return topk_ids, topk_w
 
 
@@ -250,6 +284,22 @@ def moe_forward_plan(T: int, H: int, E: int, k: int, I: int):
     if v.value == 0:
         return None
     return (v.value & 15) == 1, v.value >> 4
+
+
+def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None):
+    """RTN INT4 g128 symmetric quantisation of bf16 w [N, K] with a per-group clip search.
+
+    Returns (packed int32 [N, K/8], scales bf16 [N, K/128]) and, with with_choice,
+    the chosen clip index int32 [N, K/128] (clip = (100 - j) / 100).
+    """
+    _need(w, "w", torch.bfloat16, 2)
+    N, K = w.shape
+    packed = torch.empty(N, K // 8, dtype=torch.int32, device=w.device)
+    scales = torch.empty(N, K // 128, dtype=torch.bfloat16, device=w.device)
+    choice = torch.empty(N, K // 128, dtype=torch.int32, device=w.device) if with_choice else None
+    _check(lib().moe_quantize_int4(_p(w), N, K, nclip, _p(packed), _p(scales), _p(choice), _stream(stream)),
+           "moe_quantize_int4")
+    return (packed, scales, choice) if with_choice else (packed, scales)
 
 
 def moe_profile_events(before=None, after=None):

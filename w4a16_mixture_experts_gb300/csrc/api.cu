@@ -167,6 +167,22 @@ int moe_route(const uint16_t *hidden, const uint16_t *router_w, const float *bia
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_route_shared(const uint16_t *hidden, const uint16_t *router_w, const float *bias, moe_dims d,
+                     int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    // the forward then runs with one more expert and one more slot per token
+    if (d.k + 1 > kMaxK || d.E + 1 > kMaxE) return MOE_ERR_UNSUPPORTED;
+    const bool empty = d.T == 0;
+    if (!ptr_ok(hidden, empty) || !ptr_ok(router_w, false) || !ptr_ok(topk_ids, empty) || !ptr_ok(topk_w, empty))
+        return MOE_ERR_INVALID_ARG;
+    if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+    if (empty) return MOE_OK;
+    return cuda_status(launch_route(hidden, router_w, bias, d, topk_ids, topk_w, ws,
+                                    reinterpret_cast<cudaStream_t>(stream), true));
+}
+
 int moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids, const float *topk_w,
                       const int32_t *w1_packed, const uint16_t *w1_scales, const int32_t *w2_packed,
                       const uint16_t *w2_scales, uint16_t *out, moe_dims d, void *ws, size_t ws_bytes,
@@ -217,6 +233,16 @@ int moe_forward_plan(moe_dims d, int32_t *plan) {
     if (rc) return rc;
     *plan = fused_plan(d);
     return MOE_OK;
+}
+
+int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t nclip, int32_t *packed, uint16_t *scales,
+                      int32_t *choice, void *stream) {
+    if (N < 0 || K < 0 || K % kGroup || nclip < 1 || nclip > 100) return MOE_ERR_INVALID_ARG;
+    const bool empty = N == 0 || K == 0;
+    if (!ptr_ok(w, empty) || !ptr_ok(packed, empty) || !ptr_ok(scales, empty)) return MOE_ERR_INVALID_ARG;
+    if (choice && !ptr_ok(choice, empty)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_quantize_int4(w, N, K, nclip, packed, scales, choice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_profile_events(void *before_experts, void *after_experts) {

@@ -34,7 +34,7 @@ static_assert(sizeof(Ctrl) == 256, "control block");
 
 struct WsLayout {
     size_t ctrl;         // Ctrl
-    size_t partial;      // f32 [ksplit][T][E] router partial logits
+    size_t partial;      // f32 [ksplit][T][E (+1)] router partial logits
     size_t counts;       // i32 [E]        per-expert assignment counts
     size_t offsets;      // i32 [E+1]
     size_t active;       // i32 [E]        active expert ids, increasing
@@ -93,7 +93,7 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.ksplit = router_ksplit(d);
     L.nchunk = (int)((T * k + kPermChunk - 1) / kPermChunk);
     L.ctrl = take(sizeof(Ctrl));
-    L.partial = take((size_t)L.ksplit * T * E * 4);
+    L.partial = take((size_t)L.ksplit * T * (E + 1) * 4);   // (+1: a shared expert's gate row)
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);

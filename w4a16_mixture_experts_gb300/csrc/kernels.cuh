@@ -22,8 +22,10 @@ int sm_count();
 // Records a caller's profiling event on `s` (nothing for a null event).
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t s);
 
+// gate: the router has E + 1 rows, the last being a shared expert's gate; ids
+// and w are then [T][k + 1] with slot k = (E, sigmoid(gate logit)).
 cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
-                         int32_t *ids, float *w, void *ws, cudaStream_t s);
+                         int32_t *ids, float *w, void *ws, cudaStream_t s, bool gate = false);
 
 // Router logits on the tensor core for T > 64 and E a multiple of 128:
 // partial [ksplit][T][E] f32 (summed by the top-k kernel).
@@ -57,6 +59,10 @@ bool fused_supported(const moe_dims &d);
 int fused_plan(const moe_dims &d);
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
                                 float eps, cudaStream_t s);
+
+// RTN INT4 g128 quantiser with the per-group clip search (quant.cu).
+cudaError_t launch_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nclip, int32_t *packed,
+                                 uint16_t *scales, int32_t *choice, cudaStream_t s);
 
 cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
                              cudaStream_t s);

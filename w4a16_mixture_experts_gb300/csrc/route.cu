@@ -199,13 +199,51 @@ __device__ inline uint64_t part_topk(const float *__restrict__ row, size_t split
     return warp_topk_n<N>(key, k, lane);
 }
 
+// With a shared expert (wg, the router's row E, not null) the CTA also forms the
+// token's gate logit x[t] . wg (fp32) and writes slot k of the token's row of
+// k + 1: expert E with weight sigmoid(gate).
+__device__ inline float gate_dot_cta(const uint16_t *__restrict__ xrow, const uint16_t *__restrict__ wg, int H,
+                                     float *s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc = 0.f;
+    for (int c = 8 * threadIdx.x; c < H; c += 8 * blockDim.x) {
+        const uint4 a = ld_nc_v4(xrow + c), b = ld_nc_v4(wg + c);
+        const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc = fmaf(__uint_as_float(aa[j] << 16), __uint_as_float(bb[j] << 16), acc);
+            acc = fmaf(__uint_as_float(aa[j] & 0xffff0000u), __uint_as_float(bb[j] & 0xffff0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) s_red[warp] = acc;
+    __syncthreads();
+    float g = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) g += s_red[i];
+    return g;
+}
+
+__device__ inline float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
+
 __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float *__restrict__ partial, int ksplit,
                                                                      const float *__restrict__ bias, int T, int E,
                                                                      int k, int32_t *__restrict__ ids,
-                                                                     float *__restrict__ w) {
+                                                                     float *__restrict__ w,
+                                                                     const uint16_t *__restrict__ x,
+                                                                     const uint16_t *__restrict__ wg, int H) {
     __shared__ uint64_t s_cand[kTopkWarps][32];
+    __shared__ float s_red[kTopkWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x;
+    const int ldk = wg ? k + 1 : k;
+    if (wg) {
+        const float g = gate_dot_cta(x + (size_t)t * H, wg, H, s_red);
+        if (threadIdx.x == 0) {
+            ids[(size_t)t * ldk + k] = E;
+            w[(size_t)t * ldk + k] = sigmoidf_(g);
+        }
+    }
     const int ep = (E + kTopkWarps - 1) / kTopkWarps, lo = warp * ep, hi = min(E, lo + ep);
     const float *row = partial + (size_t)t * E;
     const size_t ss = (size_t)T * E;
@@ -222,7 +260,7 @@ __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float
         uint64_t c[kTopkWarps];
 #pragma unroll
         for (int q = 0; q < kTopkWarps; ++q) c[q] = s_cand[q][lane];
-        topk_finish(warp_topk_n<kTopkWarps>(c, k, lane), k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+        topk_finish(warp_topk_n<kTopkWarps>(c, k, lane), k, lane, ids + (size_t)t * ldk, w + (size_t)t * ldk);
     }
 }
 
@@ -246,16 +284,20 @@ constexpr int kRouteLoads = 3;   // 16-byte loads per lane in flight (a quarter 
 constexpr int kRouteMaxWpt = 4;
 
 inline size_t route_small_smem(const moe_dims &d) {
-    const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * 4;
+    const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * (d.E + 1) * 4;
     return xb > lb ? xb : lb;
 }
 
+// With a shared expert (gate != 0) the router has E + 1 rows, the last being the
+// shared expert's gate: the CTAs compute all E + 1 logits (one GEMV, as on the
+// pages), the selection takes the k largest of the first E, and slot k of each
+// token's row of k + 1 is expert E with weight sigmoid(gate logit).
 __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uint16_t *__restrict__ x,
                                                                        const uint16_t *__restrict__ wr,
                                                                        float *__restrict__ logits, int T, int H,
                                                                        int E, const float *__restrict__ bias, int k,
                                                                        int32_t *__restrict__ ids,
-                                                                       float *__restrict__ w, Ctrl *ctrl) {
+                                                                       float *__restrict__ w, Ctrl *ctrl, int gate) {
     // the activations [T][H] bf16; in the last CTA, then, the logits [T][E] f32
     extern __shared__ __align__(16) uint8_t s_raw[];
     __shared__ float s_part[kRouteWarps][kRouteInlineMaxT];
@@ -265,15 +307,16 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
     // for this grid's end themselves)
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Eg = E + gate;   // router rows, and the row stride of the logits
     const int e = blockIdx.x * 4 + (warp >> 2);
     const int q4 = H / 4, c_lo = (warp & 3) * q4, c_hi = c_lo + q4;
-    const uint16_t *row = wr + (size_t)(e < E ? e : 0) * H;
+    const uint16_t *row = wr + (size_t)(e < Eg ? e : 0) * H;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint4 wv[kRouteLoads];
 #pragma unroll
     for (int i = 0; i < kRouteLoads; ++i) {
         const int c = c_lo + 256 * i + 8 * lane;
-        wv[i] = e < E && c < c_hi ? ld_nc_v4(row + c) : zero;
+        wv[i] = e < Eg && c < c_hi ? ld_nc_v4(row + c) : zero;
     }
     uint4 *xs = reinterpret_cast<uint4 *>(s_raw);
     const int nx = T * H / 8;
@@ -299,7 +342,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
 #pragma unroll
             for (int i = 0; i < kRouteLoads; ++i) {
                 const int c = c0 + 256 * i + 8 * lane;
-                wv[i] = e < E && c < c_hi ? ld_nc_v4(row + c) : zero;
+                wv[i] = e < Eg && c < c_hi ? ld_nc_v4(row + c) : zero;
             }
         }
 #pragma unroll
@@ -331,9 +374,9 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
     if (threadIdx.x < 4 * kRouteInlineMaxT) {
         const int jj = threadIdx.x / kRouteInlineMaxT, t = threadIdx.x % kRouteInlineMaxT;
         const int ee = blockIdx.x * 4 + jj;
-        if (t < T && ee < E) {
+        if (t < T && ee < Eg) {
             const float v = ((s_part[4 * jj][t] + s_part[4 * jj + 1][t]) + s_part[4 * jj + 2][t]) + s_part[4 * jj + 3][t];
-            logits[(size_t)t * E + ee] = bias ? v + bias[ee] : v;
+            logits[(size_t)t * Eg + ee] = bias && ee < E ? v + bias[ee] : v;
         }
     }
     // the CTA barrier orders the logit stores before thread 0's release
@@ -343,7 +386,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
     if (!s_last) return;
     // the last CTA: all logits at once (8 loads per thread in flight), then top-k
     float *s_logit = reinterpret_cast<float *>(s_raw);
-    const int n = T * E;
+    const int n = T * Eg;
     for (int i0 = 0; i0 < n; i0 += 8 * blockDim.x) {
         float lv[8];
 #pragma unroll
@@ -368,7 +411,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
             }
             mine = warp_topk_n<4>(key, k, lane);
         } else if (ep <= 256) {
@@ -376,7 +419,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
             }
             mine = warp_topk_n<8>(key, k, lane);
         } else {
@@ -384,7 +427,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * E + ee], ee) : 0;
+                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
             }
             mine = warp_topk_n<16>(key, k, lane);
         }
@@ -396,20 +439,27 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
 #pragma unroll
         for (int q = 0; q < kRouteMaxWpt; ++q) c[q] = q < wpt ? s_cand[warp + q][lane] : 0;
         const uint64_t mine = warp_topk_n<kRouteMaxWpt>(c, k, lane);
-        topk_finish(mine, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+        const int ldk = k + gate;
+        topk_finish(mine, k, lane, ids + (size_t)t * ldk, w + (size_t)t * ldk);
+        if (gate && lane == 0) {
+            ids[(size_t)t * ldk + k] = E;
+            w[(size_t)t * ldk + k] = sigmoidf_(s_logit[t * Eg + E]);
+        }
     }
     if (threadIdx.x == 0) ctrl->route_ticket = 0;
 }
 
 cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bias, const moe_dims &d,
-                         int32_t *ids, float *w, void *ws, cudaStream_t s) {
+                         int32_t *ids, float *w, void *ws, cudaStream_t s, bool gate) {
     const WsLayout L = ws_layout(d);
     float *partial = ws_at<float>(ws, L.partial);
     const int ksplit = L.ksplit;
+    // the shared expert's gate row follows the E router rows
+    const uint16_t *wg = gate ? wr + (size_t)d.E * d.H : nullptr;
     if (router_tc(d)) {
         cudaError_t err = launch_route_logits_tc(x, wr, d, partial, ksplit, ws_at<Ctrl>(ws, L.ctrl), s);
         if (err != cudaSuccess) return err;
-        route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+        route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w, x, wg, d.H);
         return cudaGetLastError();
     }
     const int tt = d.T <= 64 ? d.T : 64;
@@ -425,8 +475,10 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
         }
         // (a programmatic launch of this kernel behind the expert kernel was
         // measured slower at T = 4: its CTAs then start on the first SMs freed)
-        route_small_kernel<<<(d.E + 3) / 4, 32 * kRouteWarps, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k,
-                                                                          ids, w, ws_at<Ctrl>(ws, L.ctrl));
+        const int rows = d.E + (gate ? 1 : 0);
+        route_small_kernel<<<(rows + 3) / 4, 32 * kRouteWarps, smem, s>>>(x, wr, partial, d.T, d.H, d.E, bias, d.k,
+                                                                           ids, w, ws_at<Ctrl>(ws, L.ctrl),
+                                                                           gate ? 1 : 0);
         return cudaGetLastError();
     }
     switch (nt) {
@@ -437,7 +489,7 @@ cudaError_t launch_route(const uint16_t *x, const uint16_t *wr, const float *bia
     }
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w);
+    route_topk_kernel<<<d.T, 32 * kTopkWarps, 0, s>>>(partial, ksplit, bias, d.T, d.E, d.k, ids, w, x, wg, d.H);
     return cudaGetLastError();
 }
 
