@@ -228,8 +228,9 @@ MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed
  * row, with amax = max |w| and clip c_j = (100 - j) / 100, j in [0, nclip):
  *   s_j = bf16(c_j * amax / 7)  (fp32 multiply and divide, bf16 round to nearest even)
  *   q_i = clamp(rint(w_i / s_j), -8, 7)  (fp32 divide; q = 0 when s_j = 0)
- * and the group keeps the j with the smallest sum_i (w_i - q_i s_j)^2 (summed
- * in fp32; the lowest j on a tie). nclip = 1 is plain round to nearest.
+ * and the group keeps the j with the smallest sum_i (w_i - q_i s_j)^2 (the
+ * lowest j on a tie; the sums are formed in fp32, in units of max|w|^2 so that
+ * they neither underflow nor overflow). nclip = 1 is plain round to nearest.
  *
  * w bf16 [N][K], finite; K a multiple of 128; 1 <= nclip <= 100.
  * packed int32 [N][K/8] (outputs; q + 8, lowest nibble first), scales bf16

@@ -16,7 +16,9 @@
 // These scale and code decisions are exact fp32 operations, so any
 // implementation that performs them in fp32 reaches the same codes for a given
 // j; only the choice of j can differ between implementations, by the rounding
-// of the error sums (fp32 here).
+// of the error sums. Here the sums are formed in fp32 in units of amax^2:
+// err_j / amax^2 = (s_j / amax)^2 * sum_i (w_i / s_j - q_i)^2, the same ranking,
+// which neither underflows for tiny weights nor overflows for large ones.
 //
 // One warp per group: lane l holds values 4l .. 4l + 3 (one 8-byte load), the
 // warp forms amax, then for each candidate the lanes' partial errors are summed
@@ -64,10 +66,23 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_int4_kernel(const uint1
         for (int j = 0; j < nclip; ++j) {
             const float s = clip_scale_dev(amax, j);
             float e = 0.f;
+            if (s != 0.0f) {
+                // in units of s: d = w/s - q, then scaled by (s / amax)^2
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float d = v[i] - (float)quant_code(v[i], s) * s;
-                e = fmaf(d, d, e);
+                for (int i = 0; i < 4; ++i) {
+                    const float r = __fdiv_rn(v[i], s);
+                    const float d = r - fminf(fmaxf(rintf(r), -8.0f), 7.0f);
+                    e = fmaf(d, d, e);
+                }
+                const float ratio = __fdiv_rn(s, amax);
+                e *= ratio * ratio;
+            } else if (amax != 0.0f) {
+                // a scale that underflowed: every code is 0, the error is the group itself
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float d = __fdiv_rn(v[i], amax);
+                    e = fmaf(d, d, e);
+                }
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
