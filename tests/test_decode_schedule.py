@@ -2,14 +2,17 @@
 
 The decode kernel (csrc/decode_fused.cu) splits each CTA's work into a
 sequence of chunks: every gate_up task's K chunks in task order, then the
-down items. A producer warp's lane l issues chunks l, l + 32, ... into a ring
-of kNS stages, chunk i once chunk i - kNS has been handed back; consumer
-warps take chunks in sequence order by ticket. A gate_up chunk's stage is
-handed back as soon as its words are read; its partial sums then wait for the
+down chunks of the output blocks it owns (block by block, one chunk per active
+expert). A producer warp's lane l issues chunks l, l + 32, ... into a ring of
+kNS stages, chunk i once chunk i - kNS has been handed back; consumer warps
+take chunks in sequence order by ticket. A gate_up chunk's stage is handed
+back as soon as its words are read; its partial sums then wait for the
 previous user of their buffer (task u - nb) to be finalised; the last of a
 task's chunks finalises it and counts the expert's gate_up task done. A down
-item holds its stage until all gate_up tasks of its expert, in every CTA,
-are done.
+chunk holds its stage until all gate_up tasks of its expert, in every CTA,
+are done, until every gate_up task of its own CTA is finalised (its block
+buffer lives in the partial-sum area) and until the block that used its
+buffer before is combined; the chunk that completes a block combines it.
 
 This model plays that protocol for every CTA of a launch, in random order,
 until nothing can move, and requires that every chunk of every CTA was
@@ -31,7 +34,7 @@ def _constants():
     src = open(SRC).read()
     c = {}
     for name in ("kFW", "kCons", "kGC", "kGCMin", "kNS", "kRedMax", "kMaxNB", "kP2Rows", "kDecodeMaxT",
-                 "kFastN"):
+                 "kFastN", "kRingWordsExtra"):
         m = re.search(r"constexpr int %s = (\d+);" % name, src)
         assert m, name
         c[name] = int(m.group(1))
@@ -59,16 +62,20 @@ def _layout_gc(T, H, E, k, I, gc_max):
     stage = _al(max(p1, p2), 128)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
     red_off = C["kNS"] * stage
-    red = nb * nkc * 32 * 16 + 2 * nb * 4 + 4 + 2 * C["kNS"] * 4
+    yb = T * k * C["kP2Rows"] * 4
+    area = max(nb * nkc * 512, yb)
+    red = area + 2 * nb * 4 + 4 + 2 * C["kNS"] * 4 + 4 * C["kRingWordsExtra"]
+    nyb = min(2, area // yb)
     pro_off = red_off + _al(red, 128)
     n = T * k
     na = max(1, min(E, n))
-    pro = _al(n * 2, 16) * 3 + _al(C["kFastN"] * 4, 16) + _al(na * 2, 16) * 3 + _al(T * 2, 16) + 4 * C["kFW"] * 8 + 16
+    pro = (_al(n * 2, 16) * 3 + _al(C["kFastN"] * 4, 16) + _al(na * 2, 16) * 3 + _al(T * 2, 16) + 4 * C["kFW"] * 8
+           + 16 + _al(n * 4, 16))
     xs = T * H * 2 + _al(T * G1 * 4, 16)
     base = pro_off + _al(pro, 128)
     staged = base + xs <= C["kFusedSmem"]
     total = base + xs if staged else base
-    ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256
+    ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256 and nyb >= 1
     return ok, staged, gcw
 
 
@@ -88,26 +95,57 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
     gc = min(G1, gc_max)
     nkc = -(-G1 // gc)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
-    tp1, tp2 = I // 8, H // C["kP2Rows"]
-    n1, n2 = nact * tp1, nact * tp2
-    chunks = min(T * k, E) * (tp1 * nkc + tp2)
+    yb = T * k * C["kP2Rows"] * 4
+    nyb = min(2, max(nb * nkc * 512, yb) // yb)
+    tp1 = I // 8
+    n1 = nact * tp1
+    chunks = min(T * k, E) * (tp1 * nkc + H // C["kP2Rows"])
     grid = max(1, min(sms, -(-chunks // C["kCons"])))
-    return nkc, nb, tp1, tp2, n1, n2, grid
+    return nkc, nb, nyb, tp1, n1, grid
+
+
+def _split(H, I, nact, Cg, cb):
+    """Mirror of fused_split: (first gate_up task, tasks, first block, end block)."""
+    B = H // C["kP2Rows"]
+    n1 = nact * (I // 8)
+    cb0, cb1 = B * cb // Cg, B * (cb + 1) // Cg
+    task_bytes = 8 * H
+    block_bytes = nact * C["kP2Rows"] * (I // 2)
+    total = n1 * task_bytes + B * block_bytes
+    bmin = B // Cg
+    x0 = max(0, total - Cg * block_bytes * bmin)
+    x1 = max(0, total - Cg * block_bytes * (bmin + 1))
+
+    def cum(c):
+        nbig = B * c // Cg - bmin * c
+        return c * x0 + nbig * (x1 - x0)
+
+    a = cum(Cg)
+    if a > 0:
+        s0, s1 = n1 * cum(cb) // a, n1 * cum(cb + 1) // a
+    else:
+        s0, s1 = n1 * cb // Cg, n1 * (cb + 1) // Cg
+    return s0, s1 - s0, cb0, cb1
 
 
 def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
-    nkc, nb, tp1, tp2, n1, n2, grid = _launch(T, H, E, k, I, nact, gc_max)
+    nkc, nb, nyb, tp1, n1, grid = _launch(T, H, E, k, I, nact, gc_max)
     done1 = [0] * nact
     ctas = []
+    covered_tasks, covered_blocks = [], []
     for cb in range(grid):
-        b1 = n1 * cb // grid
-        m1 = n1 * (cb + 1) // grid - b1
-        b2 = n2 * cb // grid
-        m2 = n2 * (cb + 1) // grid - b2
-        seq = [("gu", b1 + u, u) for u in range(m1) for _ in range(nkc)] + [("dn", b2 + d, 0) for d in range(m2)]
-        ctas.append(dict(seq=seq, issued=set(), released=set(), ticket=0, held=[None] * kCons, cnt={}, fin=[0] * nb))
+        b1, m1, cb0, cb1 = _split(H, I, nact, grid, cb)
+        covered_tasks += list(range(b1, b1 + m1))
+        covered_blocks += list(range(cb0, cb1))
+        seq = [("gu", b1 + u, u) for u in range(m1) for _ in range(nkc)] + \
+              [("dn", a, c - cb0) for c in range(cb0, cb1) for a in range(nact)]
+        ctas.append(dict(seq=seq, issued=set(), released=set(), ticket=0, held=[None] * kCons, cnt={}, fin=[0] * nb,
+                         m1=m1, gu_done=0, dcnt=[0] * nyb, dfin=[0] * nyb))
+    # the split covers every gate_up task and every output block exactly once
+    assert sorted(covered_tasks) == list(range(n1))
+    assert sorted(covered_blocks) == list(range(H // C["kP2Rows"]))
     moved = True
     while moved:
         moved = False
@@ -133,8 +171,14 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
                     if i not in cta["issued"]:
                         continue
                     if kind == "dn":
-                        if done1[task // tp2] < tp1:
+                        a, lb = task, u
+                        buf = lb % nyb
+                        if done1[a] < tp1 or cta["gu_done"] < cta["m1"] or cta["dfin"][buf] < lb // nyb:
                             continue
+                        cta["dcnt"][buf] += 1
+                        if cta["dcnt"][buf] == nact:
+                            cta["dcnt"][buf] = 0
+                            cta["dfin"][buf] = lb // nyb + 1
                         cta["released"].add(i)
                         cta["held"][w] = None
                         moved = True
@@ -149,6 +193,7 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
                     cta["cnt"][u] = cta["cnt"].get(u, 0) + 1
                     if cta["cnt"][u] == nkc:
                         cta["fin"][b] = u // nb + 1
+                        cta["gu_done"] += 1
                         done1[task // tp1] += 1
                     cta["held"][w] = None
                     moved = True

@@ -39,14 +39,12 @@ struct WsLayout {
     size_t offsets;      // i32 [E+1]
     size_t active;       // i32 [E]        active expert ids, increasing
     size_t done1;        // u32 [E][kCtrStride] per expert (one 128-byte line each): finished gate_up tasks
-    size_t ticket;       // u32 [T][H/16]  per 16-row output block: finished slots
     size_t rowss;        // f32 [T]        per token: sum of r^2 (stack epilogue, decode path)
     size_t rbuf;         // f32 [T][H]     residual sums (stack epilogue)
     size_t chunk;        // i32 [nchunk][E] per-chunk counts -> per-chunk bases
     size_t perm;         // i32 [T*k]      slot -> assignment
     size_t inv;          // i32 [T*k]      assignment -> slot (-1: dropped)
     size_t hbuf;         // bf16 [T*k][I]  SiLU(g)*u per slot (fragment order)
-    size_t ybuf;         // f32 [T*k][H]   down-projection output per slot (decode path)
     size_t xperm;        // bf16 [T*k][H]  activations per slot, fragment order (prefill path)
     size_t out_acc;      // f32 [T][H]     weighted output accumulator (prefill path)
     size_t n_chunks;     // i32 [1]        chunks in chunk_info (prefill path)
@@ -98,7 +96,6 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);
     L.done1 = take((size_t)E * kCtrStride * 4);
-    L.ticket = take(T * (H / 16) * 4);
     L.rowss = take(T * 4);
     const bool small = fused_supported(d);
     L.rbuf = take(small ? T * H * 4 : 0);
@@ -106,7 +103,6 @@ inline WsLayout ws_layout(const moe_dims &d) {
     L.perm = take(T * k * 4);
     L.inv = take(T * k * 4);
     L.hbuf = take(T * k * I * 2);
-    L.ybuf = take(small ? T * k * H * 4 : 0);
     L.xperm = take(small ? 0 : T * k * H * 2);
     L.out_acc = take(small ? 0 : T * H * 4);
     L.n_chunks = take(4);

@@ -15,10 +15,14 @@
 //    comparison (slot = #assignments with a lower expert + #earlier ones with
 //    the same expert): a batch holds at most kDecodeMaxT * kMaxK of them.
 //  * Work: gate_up tasks (8 gate rows and the matching 8 up rows of one
-//    expert, all of K, in chunks of kGC quantisation groups) and down items
-//    (16 output rows of one expert, all of K = I). Each CTA takes a
-//    contiguous range of each list and runs them as one sequence of chunks:
-//    all its gate_up chunks first, then its down items.
+//    expert, all of K, in chunks of kGC quantisation groups) and output
+//    blocks (16 rows of H). A CTA owns whole output blocks: for each of them
+//    it runs one down chunk per active expert (the block's 16 rows of that
+//    expert's W2, all of K = I), so the sum over experts never leaves the
+//    CTA. The gate_up tasks are shared out so that every CTA streams about
+//    the same number of bytes. A CTA runs its work as one sequence of
+//    chunks: all its gate_up chunks first, then its down chunks, block by
+//    block.
 //  * One producer warp issues the copies of the sequence (two 2-D TMA boxes
 //    plus scales per gate_up chunk, a bulk copy plus scales per down item)
 //    into a ring of kNS shared-memory stages completed on mbarriers; its
@@ -35,13 +39,14 @@
 //    the chunk that completes the task sums them in chunk order
 //    (deterministic), stores h = SiLU(g) * u (bf16, fragment order) and
 //    counts the task in its expert's counter (release).
-//  * A down item of expert e waits (bounded, acquire, with back-off) until
+//  * A down chunk of expert e waits (bounded, acquire, with back-off) until
 //    all gate_up tasks of e are counted, then loads h from L2 into registers.
-//  * The combine is fused: after writing its fp32 down outputs, a down item
-//    counts, per (token, 16-row block), how many of the token's slots are
-//    done; the item that completes a block sums the slots in slot order and
-//    writes the bf16 output (in the stack variant: residual + RMS rescale
-//    once the token's last block is done). All counters reset themselves.
+//  * The combine is fused and stays in the CTA: a down chunk writes its fp32
+//    outputs per slot into a shared buffer of its block, and the chunk that
+//    completes the block's count sums each token's slots in slot order
+//    (deterministic) and writes the bf16 output (in the stack variant: the
+//    residual sum and its share of sum(r^2); the RMS rescale follows a grid
+//    barrier). All counters reset themselves.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -79,10 +84,8 @@ struct FusedParams {
     float eps;
     Ctrl *ctrl;
     uint32_t *done1;     // [E][kCtrStride] finished gate_up tasks (reset by the last CTA to exit)
-    uint32_t *ticket;    // [T][H/16] finished slots per output block
     float *rowss;        // [T] sum of r^2 per token (stack variant)
     uint16_t *hbuf;      // bf16 [T*k][I], fragment order
-    float *ybuf;         // f32 [T*k][H]
     float *rbuf;         // f32 [T][H] residual sums (stack variant)
     int T, H, E, k, I;
     int gcw;             // words per gate_up chunk row (groups per chunk * 16)
@@ -90,13 +93,15 @@ struct FusedParams {
     uint32_t stage_bytes;
     uint32_t red_off;    // offset of the gate_up partial sums and counters
     int nb;              // partial-sum buffers
+    int nyb;             // output-block buffers (in the partial-sum area, once gate_up is done)
+    uint32_t red_area;   // bytes of the partial-sum area: the larger of the partial sums and one block buffer
     uint32_t pro_off;    // offset of the permutation arrays
     uint32_t xs_off;     // offset of the staged activations (0: not staged)
 };
 
 struct FusedLayout {
-    uint32_t stage_bytes, red_off, pro_off, xs_off, total;
-    int gcw, nkc, nb;
+    uint32_t stage_bytes, red_off, red_area, pro_off, xs_off, total;
+    int gcw, nkc, nb, nyb;
     bool ok;
 };
 
@@ -107,28 +112,35 @@ inline uint32_t fused_pro_bytes(const moe_dims &d) {
     const size_t n = (size_t)d.T * d.k;
     const size_t na = (size_t)(fused_max_active(d) > 0 ? fused_max_active(d) : 1);
     return (uint32_t)(align_up(n * 2, 16) * 3 + align_up(kFastN * 4, 16) + align_up(na * 2, 16) * 3 +
-                      align_up(d.T * 2, 16) + 4 * kFW * 8 + 16);
+                      align_up(d.T * 2, 16) + 4 * kFW * 8 + 16 + align_up(n * 4, 16));
 }
 
 // Gate_up partial results: nb buffers of [chunk][lane][4] f32 (a task's
 // chunks each leave one), then per buffer a count of finished chunks and of
-// finalised tasks, the consumers' chunk ticket, and per ring stage the chunk
-// last issued into it and the chunk it may take next.
-inline uint32_t fused_red_bytes(int nb, int nkc) {
-    return (uint32_t)(nb * nkc * 32 * 16 + 2 * nb * 4 + 4 + 2 * kNS * 4);
+// finalised tasks, the consumers' chunk ticket, per ring stage the chunk last
+// issued into it and the chunk it may take next, the CTA's count of finalised
+// gate_up tasks, and per output-block buffer a count of finished down chunks
+// and of combined blocks. Once every gate_up task of the CTA is finalised, the
+// partial-sum area holds nyb output-block buffers of [T*k slots][16 rows] f32.
+constexpr int kRingWordsExtra = 5;
+inline uint32_t fused_red_bytes(uint32_t area, int nb) {
+    return area + (uint32_t)(2 * nb * 4 + 4 + 2 * kNS * 4 + 4 * kRingWordsExtra);
 }
 struct RingWords {
-    int *cnt, *ticket;
-    volatile int *fin, *issued, *next;
+    int *cnt, *ticket, *dcnt;
+    volatile int *fin, *issued, *next, *gu_done, *dfin;
 };
 __device__ inline RingWords ring_words(uint8_t *smem, const FusedParams &p) {
-    int *w = reinterpret_cast<int *>(smem + p.red_off + p.nb * p.nkc * 512);
+    int *w = reinterpret_cast<int *>(smem + p.red_off + p.red_area);
     RingWords r;
     r.cnt = w;
     r.fin = w + p.nb;
     r.ticket = w + 2 * p.nb;
     r.issued = w + 2 * p.nb + 1;
     r.next = w + 2 * p.nb + 1 + kNS;
+    r.gu_done = w + 2 * p.nb + 1 + 2 * kNS;
+    r.dcnt = w + 2 * p.nb + 2 + 2 * kNS;
+    r.dfin = w + 2 * p.nb + 4 + 2 * kNS;
     return r;
 }
 
@@ -145,14 +157,21 @@ inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
     L.nb = kRedMax / (L.nkc * 512);
     L.nb = L.nb < 1 ? 1 : L.nb > kMaxNB ? kMaxNB : L.nb;
+    // output-block buffers in the partial-sum area: one or two (the area holds at least one)
+    const uint32_t yb = (uint32_t)d.T * d.k * kP2Rows * 4;
+    const uint32_t pa = (uint32_t)(L.nb * L.nkc * 512);
+    L.red_area = pa > yb ? pa : yb;
+    L.nyb = yb ? (int)(L.red_area / yb) : 0;
+    L.nyb = L.nyb > 2 ? 2 : L.nyb;
     L.red_off = kNS * L.stage_bytes;
-    L.pro_off = L.red_off + (uint32_t)align_up(fused_red_bytes(L.nb, L.nkc), 128);
+    L.pro_off = L.red_off + (uint32_t)align_up(fused_red_bytes(L.red_area, L.nb), 128);
     // staged activations, then their sum over each 128-wide group (f32 [T][H/128])
     const uint32_t xs_bytes = (uint32_t)d.T * d.H * 2 + (uint32_t)align_up((size_t)d.T * G1 * 4, 16);
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
     L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
     L.total = L.xs_off ? base + xs_bytes : base;
-    L.ok = L.total <= (uint32_t)kFusedSmem && d.T <= kDecodeMaxT && d.k <= kMaxK && d.I <= 1280 && L.gcw <= 256;
+    L.ok = L.total <= (uint32_t)kFusedSmem && d.T <= kDecodeMaxT && d.k <= kMaxK && d.I <= 1280 && L.gcw <= 256 &&
+           L.nyb >= 1;
     return L;
 }
 
@@ -176,6 +195,7 @@ int fused_plan(const moe_dims &d) {
 
 struct Pro {   // permutation arrays in shared memory
     int16_t *ids, *perm, *inv;
+    float *wv;      // per assignment: its routing weight
     int32_t *cnt;   // per assignment: 1 if it is its expert's first
     int16_t *act, *aoff, *acnt, *kv;
     uint64_t *bar;
@@ -198,6 +218,7 @@ __device__ inline Pro pro_views(uint8_t *smem, const FusedParams &p) {
     v.kv = reinterpret_cast<int16_t *>(take(p.T * 2));
     v.bar = reinterpret_cast<uint64_t *>(take(4 * kFW * 8));
     v.nact = reinterpret_cast<int *>(take(16));
+    v.wv = reinterpret_cast<float *>(take(n * 4));
     return v;
 }
 
@@ -216,7 +237,8 @@ __device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + kNS; }
 // #{valid a' with a lower expert} + #{a' < a with the same expert}. Thread a
 // ranks assignment a (id_reg: its id, already loaded by the caller); the
 // first assignment of each expert also places the expert in the active list.
-__device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v, int id_reg) {
+__device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *smem, const Pro &v, int id_reg,
+                                               float w_reg) {
     __shared__ int nact_s;
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int n = p.T * p.k, E = p.E;
@@ -228,6 +250,7 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
             bad = true;
         }
         v.ids[tid] = (int16_t)id_reg;
+        v.wv[tid] = w_reg;
     }
     if (bad && blockIdx.x == 0) set_error(p.ctrl, MOE_ERR_DEVICE);
     if (tid == 0) nact_s = 0;
@@ -274,6 +297,7 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
     {
         const RingWords rw = ring_words(smem, p);
         if (tid < 2 * p.nb + 1) rw.cnt[tid] = 0;   // chunks done, tasks finalised, the ticket
+        if (tid < kRingWordsExtra) rw.gu_done[tid] = 0;   // tasks finalised, block counts
         if (tid < kNS) {
             rw.issued[tid] = -1;
             rw.next[tid] = tid;
@@ -288,11 +312,11 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
 }
 
 // After the permutation: the activations in fragment order and their
-// per-group sums (if staged), and the outputs of tokens with no valid slot.
-// Run by the consumer warps only; ends on a named barrier among them.
+// per-group sums (if staged). Run by the consumer warps only; ends on a named
+// barrier among them.
 __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, const Pro &v) {
     const int tid = threadIdx.x, nthr = kCons * 32;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = tid & 31;
     if (p.xs_off) {
         // x arrived row-major (a bulk copy issued at kernel entry); each 16-byte
         // chunk is rewritten in place in fragment order, and per token the sum
@@ -322,28 +346,6 @@ __device__ __noinline__ void fused_stage(const FusedParams &p, uint8_t *smem, co
             if (i < nch && (lane & 15) == 0) xsum[i / 16] = sum;   // i / 16 = token * (H/128) + group
         }
     }
-    // tokens with no valid slot still get an output: zero, or the rescaled residual
-    if (blockIdx.x == 0 && warp == 0)
-        for (int t = 0; t < p.T; ++t)
-            if (v.kv[t] == 0) {
-                if (p.out) {
-                    for (int c = lane; c < p.H; c += 32) p.out[(size_t)t * p.H + c] = 0;
-                } else {
-                    float ss = 0.f;
-                    for (int c = lane; c < p.H; c += 32) {
-                        const float r = bf16_bits_to_f32(p.x[(size_t)t * p.H + c]);
-                        ss += r * r;
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                    const float scale = rsqrtf(ss / (float)p.H + p.eps);
-                    for (int c = lane; c < p.H; c += 32) {
-                        const __nv_bfloat16 b =
-                            __float2bfloat16_rn(bf16_bits_to_f32(p.x[(size_t)t * p.H + c]) * scale);
-                        p.next[(size_t)t * p.H + c] = *reinterpret_cast<const uint16_t *>(&b);
-                    }
-                }
-            }
     asm volatile("bar.sync 1, %0;" ::"n"(kCons * 32) : "memory");
 }
 
@@ -353,9 +355,11 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
 
 // ---- the CTA's chunk sequence -----------------------------------------------
 // Chunk i of the CTA: for i < m1 * nkc, K chunk i % nkc of gate_up task
-// b1 + i / nkc (tasks in order); after them the down items b2, b2 + 1, ...
-// Task ids: gate_up tasks 0..n1-1, down items n1, n1 + 1, ... The producer
-// issues the chunks in this order and the consumers take them in this order.
+// b1 + i / nkc (tasks in order); after them the down chunks b2, b2 + 1, ...
+// Task ids: gate_up tasks 0..n1-1, down chunks n1, n1 + 1, ...; down chunk d
+// is (output block d / nact, active expert d % nact), and a CTA's down chunks
+// cover whole blocks. The producer issues the chunks in this order and the
+// consumers take them in this order.
 struct ChunkRef {
     int task, chunk;
 };
@@ -376,7 +380,7 @@ __device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int n
 __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int task, int chunk, int n1, uint8_t *stage,
                                uint64_t *bar, int lane) {
     if (lane != 0) return;
-    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
+    const int tp1 = p.I / 8;
     if (task < n1) {
         const int a = task / tp1, r = task - a * tp1;
         const int e = v.act[a];
@@ -389,8 +393,8 @@ __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int tas
         bulk_g2s(stage + 2 * box, p.w1s + (size_t)row * G1, 16 * G1, bar);
         bulk_g2s(stage + 2 * box + 16 * G1, p.w1s + (size_t)(row + p.I) * G1, 16 * G1, bar);
     } else {
-        const int t2 = task - n1;
-        const int a = t2 / tp2, c = t2 - a * tp2;
+        const int t2 = task - n1, nact = *v.nact;
+        const int c = t2 / nact, a = t2 - c * nact;   // output block c, active expert a
         const int e = v.act[a];
         const int G2 = p.I / 128;
         const uint32_t rb = p.I / 2;
@@ -576,41 +580,43 @@ __device__ inline bool f_gu_reduce(const FusedParams &p, const Pro &v, uint8_t *
         red_release_add_u32(&p.done1[(size_t)v.act[task / (p.I / 8)] * kCtrStride], 1u);
         __threadfence_block();
         *fin = u / p.nb + 1;
+        atomicAdd(const_cast<int *>(rw.gu_done), 1);   // after the slots' last reads (fence above)
     }
     return true;
 }
 
 // ---- down + fused combine ----------------------------------------------------
-// Lanes 0..15 own the block's rows.
-__device__ __noinline__ void f_combine_block(const FusedParams &p, const Pro &v, int t, int c, int lane) {
-    const bool own = lane < kP2Rows;
-    const int n = kP2Rows * c + (own ? lane : 0);
-    // the loads of 8 slots are issued together, then summed in slot order
-    // (an invalid slot adds w * y = 0 * 0, which leaves the sum unchanged)
-    float s = 0.f;
-    for (int j0 = 0; j0 < p.k; j0 += 8) {
-        float wv[8], yv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = j0 + u;
-            const int slot = j < p.k ? v.inv[t * p.k + j] : -1;
-            wv[u] = slot >= 0 ? p.topk_w[(size_t)t * p.k + j] : 0.f;
-            yv[u] = slot >= 0 ? __ldcg(p.ybuf + (size_t)slot * p.H + n) : 0.f;
+// Output block c (rows 16c .. 16c + 15) of every token, from the block's slot
+// buffer ys [T*k slots][16 rows] f32 in shared memory: out[t][n] = sum over
+// j < k, in slot order, of w[t][j] * y[slot of (t, j)][n]; a slot whose id was
+// invalid adds nothing (and a token with no valid slot gets 0). Lane l takes
+// row l % 16 of tokens l / 16, l / 16 + 2, ... The stack variant keeps
+// r = x + out and adds the block's share of sum(r^2) to the token's row sum.
+__device__ __noinline__ void f_block_combine(const FusedParams &p, const Pro &v, const float *ys, int c, int lane) {
+    const int r = lane & 15;
+    const int n = kP2Rows * c + r;
+    for (int t0 = 0; t0 < p.T; t0 += 2) {
+        const int t = t0 + (lane >> 4);
+        const bool on = t < p.T;
+        float s = 0.f;
+        if (on) {
+            for (int j = 0; j < p.k; ++j) {
+                const int slot = v.inv[t * p.k + j];
+                if (slot >= 0) s += v.wv[t * p.k + j] * ys[slot * kP2Rows + r];
+            }
         }
+        if (p.out) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(s);
+            if (on) p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
+        } else {
+            // stack step: keep r = x + moe(x) and add this block's share of sum(r^2)
+            const float rr = on ? s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]) : 0.f;
+            if (on) p.rbuf[(size_t)t * p.H + n] = rr;
+            float ss = rr * rr;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) s += wv[u] * yv[u];
-    }
-    if (p.out) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(s);
-        if (own) p.out[(size_t)t * p.H + n] = *reinterpret_cast<const uint16_t *>(&b);
-    } else {
-        // stack step: keep r = x + moe(x) and add this block's share of sum(r^2)
-        const float r = s + bf16_bits_to_f32(p.x[(size_t)t * p.H + n]);
-        if (own) p.rbuf[(size_t)t * p.H + n] = r;
-        float ss = own ? r * r : 0.f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) atomicAdd(&p.rowss[t], ss);
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (on && r == 0) atomicAdd(&p.rowss[t], ss);
+        }
     }
 }
 
@@ -659,9 +665,15 @@ __device__ __noinline__ void f_stack_rows(const FusedParams &p) {
     }
 }
 
-__device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const uint8_t *stage, int lane) {
-    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
-    const int a = t2 / tp2, c = t2 - a * tp2;
+// Down chunk t2 = (output block c, active expert a): y of the expert's slots for
+// the block's 16 rows, into the block's slot buffer; the chunk that completes
+// the block's count combines it. cb0: the CTA's first block (its blocks use
+// the nyb buffers in turn).
+__device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem, int t2, int cb0, int m1,
+                              const uint8_t *stage, int lane) {
+    const int tp1 = p.I / 8;
+    const int nact = *v.nact;
+    const int c = t2 / nact, a = t2 - c * nact;
     const int e = v.act[a];
     const int s0 = v.aoff[a], ne = v.acnt[a];
     const int g = lane >> 2, tig = lane & 3;
@@ -685,9 +697,25 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
             if (ns < 512) ns *= 2;
         }
     }
+    // the block's slot buffer lies in the gate_up partial-sum area: it is free
+    // once every gate_up task of this CTA is finalised, and once the block that
+    // used it before (nyb blocks earlier) is combined
+    const RingWords rw = ring_words(smem, p);
+    const int lb = c - cb0, buf = lb % p.nyb;
+    if (lane == 0 && ok) {
+        uint32_t i = 0;
+        while (*rw.gu_done < m1 || rw.dfin[buf] < lb / p.nyb)
+            if (++i > kSpinLimit) {
+                ok = 0;
+                set_error(p.ctrl, MOE_ERR_TIMEOUT);
+                break;
+            }
+    }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     if (!ok) return false;
+    __threadfence_block();
+    float *ys = reinterpret_cast<float *>(smem + p.red_off) + (size_t)buf * p.T * p.k * kP2Rows;
 
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int np = 0; np < ne; np += 8) {
@@ -753,36 +781,31 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, int t2, const 
             for (int b = 0; b < 2; ++b) {
                 const int jj = np + 2 * tig + b;
                 if (jj < ne) {
-                    float *yr = p.ybuf + (size_t)(s0 + jj) * p.H + kP2Rows * c + 16 * s + g;
+                    float *yr = ys + (s0 + jj) * kP2Rows + 16 * s + g;
                     yr[0] = acc[s][b];
                     yr[8] = acc[s][2 + b];
                 }
             }
     }
 
-    // fused combine: count this item's slots per (token, block); complete blocks.
-    // The warp barrier orders every lane's y stores before the counting lanes'
-    // acq_rel atomics; the lane that completes a block acquires the other
-    // items' stores, and the warp barrier after the ballot extends that to the
-    // lanes that read them.
+    // count the chunk in its block; the chunk that completes the block combines
+    // it (the warp barrier and fence order every lane's stores before the count,
+    // and the count's reader sees them after its own fence)
     __syncwarp();
-    for (int j0 = 0; j0 < ne; j0 += 32) {
-        const int j = j0 + lane;
-        int t = -1;
-        bool fin = false;
-        if (j < ne) {
-            t = v.perm[s0 + j] / p.k;
-            const uint32_t old = atom_acq_rel_add_u32(&p.ticket[(size_t)t * tp2 + c], 1u);
-            fin = old + 1 == (uint32_t)v.kv[t];
-            if (fin) p.ticket[(size_t)t * tp2 + c] = 0;
-        }
-        unsigned m = __ballot_sync(0xffffffffu, fin);
+    int last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(rw.dcnt + buf, 1) + 1 == nact;
+        if (last) rw.dcnt[buf] = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence_block();
+        f_block_combine(p, v, ys, c, lane);
         __syncwarp();
-        while (m) {
-            const int src = __ffs(m) - 1;
-            m &= m - 1;
-            const int tt = __shfl_sync(0xffffffffu, t, src);
-            f_combine_block(p, v, tt, c, lane);
+        if (lane == 0) {
+            __threadfence_block();
+            rw.dfin[buf] = lb / p.nyb + 1;
         }
     }
     return true;
@@ -850,6 +873,43 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
     }
 }
 
+// ---- work split ---------------------------------------------------------------
+// CTA cb of C owns output blocks [cb0, cb1) = [B cb / C, B (cb + 1) / C), B = H/16.
+// The gate_up tasks are shared out in proportion to each CTA's capacity: an
+// equal share of all the bytes (gate_up tasks and down chunks) minus the bytes
+// of its own blocks' down chunks (at least 0). CTAs own B / C or B / C + 1
+// blocks, so the capacities take two values and their prefix sums have a
+// closed form; every CTA computes the same split.
+__device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int &b1, int &m1, int &cb0,
+                                   int &cb1) {
+    const int B = p.H / kP2Rows;
+    const long long n1 = (long long)nact * (p.I / 8);
+    cb0 = (int)((long long)B * cb / C);
+    cb1 = (int)((long long)B * (cb + 1) / C);
+    const long long task_bytes = 8LL * p.H;                              // 16 rows of H/2 bytes
+    const long long block_bytes = (long long)nact * kP2Rows * (p.I / 2);  // one block, all active experts
+    const long long total = n1 * task_bytes + (long long)B * block_bytes;
+    const int bmin = B / C;
+    // C times the capacity of a CTA with bmin, bmin + 1 blocks
+    const long long x0 = max(0LL, total - (long long)C * block_bytes * bmin);
+    const long long x1 = max(0LL, total - (long long)C * block_bytes * (bmin + 1));
+    auto cum = [&](int c) {   // C times the capacity of CTAs [0, c)
+        const long long nbig = (long long)B * c / C - (long long)bmin * c;
+        return (long long)c * x0 + nbig * (x1 - x0);
+    };
+    const long long all = cum(C);
+    long long s0, s1;
+    if (all > 0) {
+        s0 = n1 * cum(cb) / all;
+        s1 = n1 * cum(cb + 1) / all;
+    } else {
+        s0 = n1 * cb / C;
+        s1 = n1 * (cb + 1) / C;
+    }
+    b1 = (int)s0;
+    m1 = (int)(s1 - s0);
+}
+
 // ---- kernel -----------------------------------------------------------------
 template <bool kStaged>
 __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_constant__ FusedParams p) {
@@ -866,21 +926,24 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     pdl_wait();
     // the ids are the first thing every path needs
     int id_reg = -1;
-    if ((int)threadIdx.x < p.T * p.k) id_reg = p.ids[threadIdx.x];
+    float w_reg = 0.f;
+    if ((int)threadIdx.x < p.T * p.k) {
+        id_reg = p.ids[threadIdx.x];
+        w_reg = p.topk_w[threadIdx.x];
+    }
     if (p.xs_off && threadIdx.x == 0) {
         // the activations start moving now, behind the permutation
         const uint32_t xb = (uint32_t)p.T * p.H * 2;
         mbar_arrive_expect_tx(x_bar(v), xb);
         bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
     }
-    fused_prologue(p, smem, v, id_reg);
+    fused_prologue(p, smem, v, id_reg, w_reg);
 
     const int nact = *v.nact;
-    const int tp1 = p.I / 8, tp2 = p.H / kP2Rows;
-    const int n1 = nact * tp1, n2 = nact * tp2;
-    const int C = gridDim.x, cb = blockIdx.x;
-    const int b1 = (int)((long long)n1 * cb / C), m1 = (int)((long long)n1 * (cb + 1) / C) - b1;
-    const int b2 = (int)((long long)n2 * cb / C), m2 = (int)((long long)n2 * (cb + 1) / C) - b2;
+    const int n1 = nact * (p.I / 8);
+    int b1, m1, cb0, cb1;
+    fused_split(p, nact, gridDim.x, blockIdx.x, b1, m1, cb0, cb1);
+    const int b2 = cb0 * nact, m2 = (cb1 - cb0) * nact;   // down chunks of whole blocks
     if (warp == kProd) {
         f_produce(p, v, smem, b1, m1, b2, m2, n1);
     } else {
@@ -888,6 +951,10 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         fused_stage(p, smem, v);
         const int ngu = m1 * p.nkc, nc = ngu + m2;
         const RingWords rw = ring_words(smem, p);
+        // no valid assignment at all: the blocks still get their output (0, or x
+        // in the stack variant) from a combine over no slots
+        if (nact == 0)
+            for (int c = cb0 + warp; c < cb1; c += kCons) f_block_combine(p, v, nullptr, c, lane);
         float acc[kMaxNT][4];
         for (;;) {
             // chunks are taken in sequence order
@@ -924,7 +991,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
                 }
                 if (!f_gu_reduce(p, v, smem, r.task, r.task - b1, r.chunk, lane, acc)) break;
             } else {
-                f_down(p, v, r.task - n1, stage, lane);
+                f_down(p, v, smem, r.task - n1, cb0, m1, stage, lane);
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence_block();
@@ -959,10 +1026,8 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.eps = eps;
     p.ctrl = ws_at<Ctrl>(ws, W.ctrl);
     p.done1 = ws_at<uint32_t>(ws, W.done1);
-    p.ticket = ws_at<uint32_t>(ws, W.ticket);
     p.rowss = ws_at<float>(ws, W.rowss);
     p.hbuf = ws_at<uint16_t>(ws, W.hbuf);
-    p.ybuf = ws_at<float>(ws, W.ybuf);
     p.rbuf = ws_at<float>(ws, W.rbuf);
     p.T = d.T;
     p.H = d.H;
@@ -974,6 +1039,8 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.stage_bytes = L.stage_bytes;
     p.red_off = L.red_off;
     p.nb = L.nb;
+    p.nyb = L.nyb;
+    p.red_area = L.red_area;
     p.pro_off = L.pro_off;
     p.xs_off = L.xs_off;
 

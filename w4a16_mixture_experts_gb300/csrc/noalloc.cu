@@ -99,7 +99,7 @@ extern "C" int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *
     cudaError_t err = static_scratch(&ws);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the control block, then done1, ticket and rowss, which are adjacent in
+    // the control block, then done1 and rowss, which are adjacent in
     // the layout (rbuf follows them)
     const WsLayout W = ws_layout(d);
     err = cudaMemsetAsync(ws_at<char>(ws, W.ctrl), 0, sizeof(Ctrl), s);
