@@ -65,7 +65,7 @@ def _layout_gc(T, H, E, k, I, gc_max):
     yb = T * k * C["kP2Rows"] * 4
     area = max(nb * nkc * 512, yb)
     red = area + 2 * nb * 4 + 4 + 2 * C["kNS"] * 4 + 4 * C["kRingWordsExtra"]
-    nyb = min(2, area // yb)
+    nyb = min(2, area // yb) if yb else 0
     pro_off = red_off + _al(red, 128)
     n = T * k
     na = max(1, min(E, n))
@@ -75,7 +75,8 @@ def _layout_gc(T, H, E, k, I, gc_max):
     base = pro_off + _al(pro, 128)
     staged = base + xs <= C["kFusedSmem"]
     total = base + xs if staged else base
-    ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256 and nyb >= 1
+    ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256 and \
+        (nyb >= 1 or T == 0)
     return ok, staged, gcw
 
 

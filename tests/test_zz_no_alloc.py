@@ -56,10 +56,11 @@ def _built():
 def test_noalloc_rejects_shapes_before_any_cuda_call(_built):
     # T beyond the decode path
     assert _call(8, 2560, 512, 10, 640) == 2                       # MOE_ERR_UNSUPPORTED
-    # a decode shape whose workspace exceeds the 2 MiB static scratch
-    need = moe.moe_workspace_size(7, 2560, 512, 32, 640)
-    assert need > (2 << 20)
-    assert _call(7, 2560, 512, 32, 640) == 3                       # MOE_ERR_WORKSPACE
+    # a decode shape whose workspace exceeds the 1 MiB static scratch
+    assert moe.moe_forward_plan(7, 6144, 1024, 32, 640) is not None
+    need = moe.moe_workspace_size(7, 6144, 1024, 32, 640)
+    assert need > (1 << 20)
+    assert _call(7, 6144, 1024, 32, 640) == 3                      # MOE_ERR_WORKSPACE
     # shapes every forward rejects
     assert _call(1, 200, 512, 10, 640) == 2
     assert _call(-1, 2560, 512, 10, 640) == 1
@@ -68,7 +69,7 @@ def test_noalloc_rejects_shapes_before_any_cuda_call(_built):
 
 
 def test_noalloc_capacity_covers_the_decode_path_at_full_shape():
-    assert moe.moe_workspace_size(7, 2560, 512, 10, 640) <= (2 << 20)
+    assert moe.moe_workspace_size(7, 2560, 512, 10, 640) <= (1 << 20)
 
 
 # ------------------------------------------------------------ GPU parity ----

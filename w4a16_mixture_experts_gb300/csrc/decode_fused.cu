@@ -171,7 +171,7 @@ inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
     L.total = L.xs_off ? base + xs_bytes : base;
     L.ok = L.total <= (uint32_t)kFusedSmem && d.T <= kDecodeMaxT && d.k <= kMaxK && d.I <= 1280 && L.gcw <= 256 &&
-           L.nyb >= 1;
+           (L.nyb >= 1 || d.T == 0);
     return L;
 }
 

@@ -14,7 +14,7 @@
 //
 // Limits and rules (also stated in w4a16moe.h):
 //  - Only the fused decode path (T <= 7) is served, and only when the
-//    workspace layout of the shape fits in kStaticScratchBytes (2 MiB);
+//    workspace layout of the shape fits in kStaticScratchBytes (1 MiB);
 //    larger shapes are rejected with MOE_ERR_WORKSPACE before anything is
 //    enqueued.
 //  - There is one scratch array per device per process: two calls on the same
@@ -44,7 +44,7 @@
 namespace moe {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(2) << 20;
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;
 constexpr int kMaxScratchDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
