@@ -106,16 +106,16 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
 
 
 def _split(H, I, nact, Cg, cb):
-    """Mirror of fused_split: (first gate_up task, tasks, first block, end block)."""
+    """Mirror of fused_split (exact integer arithmetic, as the kernel's result):
+    (first gate_up task, tasks, first block, end block)."""
     B = H // C["kP2Rows"]
     n1 = nact * (I // 8)
     cb0, cb1 = B * cb // Cg, B * (cb + 1) // Cg
-    task_bytes = 8 * H
-    block_bytes = nact * C["kP2Rows"] * (I // 2)
-    total = n1 * task_bytes + B * block_bytes
+    blk = nact * I
+    total = n1 * H + B * blk
     bmin = B // Cg
-    x0 = max(0, total - Cg * block_bytes * bmin)
-    x1 = max(0, total - Cg * block_bytes * (bmin + 1))
+    x0 = max(0, total - Cg * blk * bmin)
+    x1 = max(0, total - Cg * blk * (bmin + 1))
 
     def cum(c):
         nbig = B * c // Cg - bmin * c

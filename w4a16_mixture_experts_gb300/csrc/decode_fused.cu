@@ -879,35 +879,43 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
 // equal share of all the bytes (gate_up tasks and down chunks) minus the bytes
 // of its own blocks' down chunks (at least 0). CTAs own B / C or B / C + 1
 // blocks, so the capacities take two values and their prefix sums have a
-// closed form; every CTA computes the same split.
+// closed form, computed exactly in 64-bit integers (units of 8 bytes: a gate_up
+// task is H, a block's down chunks nact * I). CTA c's tasks start at
+// floor(n1 * cum(c) / cum(C)): non-decreasing in c, 0 at c = 0, n1 at c = C,
+// and the same value in every CTA that evaluates it. The split runs on the
+// critical path of every CTA, so the quotient is estimated in fp32 and made
+// exact with 64-bit multiplies (a 64-bit division is a long dependent chain).
+__device__ inline long long split_cum(int c, int C, int B, int bmin, long long x0, long long x1) {
+    const int nbig = B * c / C - bmin * c;   // CTAs among [0, c) with bmin + 1 blocks
+    return (long long)c * x0 + (long long)nbig * (x1 - x0);
+}
+
+__device__ inline int floor_ratio(long long num, long long den) {   // floor(num / den), 0 <= num / den < 2^24
+    int q = __float2int_rd(__fdiv_rn((float)num, (float)den));
+    while ((long long)(q + 1) * den <= num) ++q;
+    while (q > 0 && (long long)q * den > num) --q;
+    return q;
+}
+
 __device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int &b1, int &m1, int &cb0,
                                    int &cb1) {
     const int B = p.H / kP2Rows;
-    const long long n1 = (long long)nact * (p.I / 8);
-    cb0 = (int)((long long)B * cb / C);
-    cb1 = (int)((long long)B * (cb + 1) / C);
-    const long long task_bytes = 8LL * p.H;                              // 16 rows of H/2 bytes
-    const long long block_bytes = (long long)nact * kP2Rows * (p.I / 2);  // one block, all active experts
-    const long long total = n1 * task_bytes + (long long)B * block_bytes;
+    const int n1 = nact * (p.I / 8);
+    cb0 = B * cb / C;
+    cb1 = B * (cb + 1) / C;
+    const long long blk = (long long)nact * p.I;
+    const long long total = (long long)n1 * p.H + (long long)B * blk;
     const int bmin = B / C;
-    // C times the capacity of a CTA with bmin, bmin + 1 blocks
-    const long long x0 = max(0LL, total - (long long)C * block_bytes * bmin);
-    const long long x1 = max(0LL, total - (long long)C * block_bytes * (bmin + 1));
-    auto cum = [&](int c) {   // C times the capacity of CTAs [0, c)
-        const long long nbig = (long long)B * c / C - (long long)bmin * c;
-        return (long long)c * x0 + nbig * (x1 - x0);
-    };
-    const long long all = cum(C);
-    long long s0, s1;
+    const long long x0 = max(0LL, total - (long long)C * blk * bmin);
+    const long long x1 = max(0LL, total - (long long)C * blk * (bmin + 1));
+    const long long all = split_cum(C, C, B, bmin, x0, x1);
     if (all > 0) {
-        s0 = n1 * cum(cb) / all;
-        s1 = n1 * cum(cb + 1) / all;
+        b1 = floor_ratio((long long)n1 * split_cum(cb, C, B, bmin, x0, x1), all);
+        m1 = floor_ratio((long long)n1 * split_cum(cb + 1, C, B, bmin, x0, x1), all) - b1;
     } else {
-        s0 = n1 * cb / C;
-        s1 = n1 * (cb + 1) / C;
+        b1 = n1 * cb / C;
+        m1 = n1 * (cb + 1) / C - b1;
     }
-    b1 = (int)s0;
-    m1 = (int)(s1 - s0);
 }
 
 // ---- kernel -----------------------------------------------------------------
@@ -921,6 +929,15 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_init(x_bar(v), 1);
         fence_mbar_init();
     }
+    if (p.xs_off && threadIdx.x == 0) {
+        // The activations start moving at once: x is an input of the layer,
+        // complete before the router (the kernel ahead of this one) began, so
+        // it may be read before the wait below. Nothing of the router's
+        // output or the workspace is touched before it.
+        const uint32_t xb = (uint32_t)p.T * p.H * 2;
+        mbar_arrive_expect_tx(x_bar(v), xb);
+        bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
+    }
     // The launch is programmatic: the CTAs may start while the router still
     // runs, and read its outputs (and the workspace) only once it has finished.
     pdl_wait();
@@ -930,12 +947,6 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     if ((int)threadIdx.x < p.T * p.k) {
         id_reg = p.ids[threadIdx.x];
         w_reg = p.topk_w[threadIdx.x];
-    }
-    if (p.xs_off && threadIdx.x == 0) {
-        // the activations start moving now, behind the permutation
-        const uint32_t xb = (uint32_t)p.T * p.H * 2;
-        mbar_arrive_expect_tx(x_bar(v), xb);
-        bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
     }
     fused_prologue(p, smem, v, id_reg, w_reg);
 
