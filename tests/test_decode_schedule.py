@@ -57,8 +57,8 @@ def _layout_gc(T, H, E, k, I, gc_max):
     gc = min(G1, gc_max)
     gcw = gc * 16
     nkc = -(-G1 // gc)
-    p1 = 2 * 8 * gcw * 4 + 2 * 8 * G1 * 2
-    p2 = C["kP2Rows"] * (I // 2) + C["kP2Rows"] * G2 * 2
+    p1 = 2 * 8 * gcw * 4
+    p2 = C["kP2Rows"] * (I // 2)
     stage = _al(max(p1, p2), 128)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
     red_off = C["kNS"] * stage
@@ -238,7 +238,8 @@ GPU_DECODE_SHAPES = {
     (2, 8064, 16, 4, 128): True,
     (3, 128, 1024, 32, 128): True,     # E and k at their maxima, the smallest H
     (7, 8064, 64, 8, 128): False,      # x too large to stage next to the ring
-    (6, 6144, 32, 4, 256): False,
+    (7, 7168, 32, 4, 256): False,
+    (6, 6144, 32, 4, 256): True,       # staged with 4-group chunks
 }
 
 
@@ -247,6 +248,8 @@ def test_decode_instantiation_of_gpu_shapes(shape, staged):
     plan = fused_plan(*shape)
     assert plan is not None, "the decode kernel must take %s" % (shape,)
     assert plan[0] == staged
+    if shape == (6, 6144, 32, 4, 256):
+        assert plan[1] == C["kGCMin"]
     # the library's own choice (a host-only query) agrees with this mirror
     assert _library_plan(*shape) == plan
 

@@ -283,7 +283,8 @@ def test_forward_layer_end_to_end_decode():
     (2, 8064, 16, 4, 128),      # decode: H at its maximum (16 chunks per gate_up task)
     (3, 128, 1024, 32, 128),    # decode: E and k at their maxima with the smallest H
     (7, 8064, 64, 8, 128),      # decode, activations read from global memory (too large to stage)
-    (6, 6144, 32, 4, 256),      # likewise, at another chunk split
+    (7, 7168, 32, 4, 256),      # likewise, at another chunk split
+    (6, 6144, 32, 4, 256),      # decode, staged with chunks of 4 groups
 ])
 def test_forward_edge_shapes(T, H, E, k, I):
     seed = T + H + E

@@ -24,9 +24,12 @@
 //    chunks: all its gate_up chunks first, then its down chunks, block by
 //    block.
 //  * One producer warp issues the copies of the sequence (two 2-D TMA boxes
-//    plus scales per gate_up chunk, a bulk copy plus scales per down item)
-//    into a ring of kNS shared-memory stages completed on mbarriers; its
-//    lanes issue side by side. The kCons consumer warps take chunks in
+//    per gate_up chunk, one bulk copy per down chunk) into a ring of kNS
+//    shared-memory stages completed on mbarriers; its lanes issue side by
+//    side. The copy instructions themselves are the limit of this stream (a
+//    few tens of ns each per SM, measured), so the small scale rows do not
+//    take copies of their own: each consumer loads its chunk's scales with
+//    plain loads before it waits for the chunk's data. The kCons consumer warps take chunks in
 //    sequence order by a shared ticket and hand each stage back as soon as
 //    they are done with it, so up to kNS copies are in flight per SM.
 //  * Weights are dequantised in registers into mma.sync m16n8k16 A fragments
@@ -148,12 +151,12 @@ __device__ inline RingWords ring_words(uint8_t *smem, const FusedParams &p) {
 // arrays | staged activations (if they fit). gc_max: groups per gate_up chunk.
 inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     FusedLayout L{};
-    const int G1 = d.H / 128, G2 = d.I / 128;
+    const int G1 = d.H / 128;
     const int gc = G1 < gc_max ? G1 : gc_max;
     L.gcw = gc * 16;
     L.nkc = (G1 + gc - 1) / gc;
-    const uint32_t p1 = 2u * 8 * L.gcw * 4 + 2u * 8 * G1 * 2;
-    const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2) + (uint32_t)kP2Rows * G2 * 2;
+    const uint32_t p1 = 2u * 8 * L.gcw * 4;
+    const uint32_t p2 = (uint32_t)kP2Rows * (d.I / 2);
     L.stage_bytes = (uint32_t)align_up(p1 > p2 ? p1 : p2, 128);
     L.nb = kRedMax / (L.nkc * 512);
     L.nb = L.nb < 1 ? 1 : L.nb > kMaxNB ? kMaxNB : L.nb;
@@ -384,25 +387,70 @@ __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int tas
     if (task < n1) {
         const int a = task / tp1, r = task - a * tp1;
         const int e = v.act[a];
-        const int G1 = p.H / 128;
         const uint32_t box = 8u * p.gcw * 4;
         const int row = e * 2 * p.I + 8 * r;
-        mbar_arrive_expect_tx(bar, 2 * box + 32 * G1);
+        mbar_arrive_expect_tx(bar, 2 * box);
         tma_load_2d(stage, &p.tm_w1, chunk * p.gcw, row, bar);
         tma_load_2d(stage + box, &p.tm_w1, chunk * p.gcw, row + p.I, bar);
-        bulk_g2s(stage + 2 * box, p.w1s + (size_t)row * G1, 16 * G1, bar);
-        bulk_g2s(stage + 2 * box + 16 * G1, p.w1s + (size_t)(row + p.I) * G1, 16 * G1, bar);
     } else {
         const int t2 = task - n1, nact = *v.nact;
         const int c = t2 / nact, a = t2 - c * nact;   // output block c, active expert a
         const int e = v.act[a];
-        const int G2 = p.I / 128;
         const uint32_t rb = p.I / 2;
-        mbar_arrive_expect_tx(bar, kP2Rows * rb + kP2Rows * G2 * 2);
+        mbar_arrive_expect_tx(bar, kP2Rows * rb);
         bulk_g2s(stage, reinterpret_cast<const char *>(p.w2p) + ((size_t)e * p.H + kP2Rows * c) * rb, kP2Rows * rb,
                  bar);
-        bulk_g2s(stage + kP2Rows * rb, p.w2s + ((size_t)e * p.H + kP2Rows * c) * G2, kP2Rows * G2 * 2, bar);
     }
+}
+
+// ---- scales -------------------------------------------------------------------
+// A chunk's scales, loaded by its consumer from global memory (L2) before it
+// waits for the chunk's weights, held as bf16 pairs: sk[0..4] for the lane's
+// first row (gate row g of a gate_up chunk, row g of a down chunk), sk[5..9]
+// for its second row (up row g, row g + 8), group q in half q & 1 of word q / 2.
+// Indexed by runtime group numbers through selects, never through local memory.
+constexpr int kScW = 5;   // words per row: up to 10 groups (I <= 1280, kGC <= 10)
+static_assert(kGC <= 2 * kScW, "gate_up chunk scales fit");
+
+__device__ __forceinline__ float scale_of(const uint32_t (&sk)[2 * kScW], int half, int q) {
+    const int i = q >> 1;
+    uint32_t w = sk[half * kScW];
+#pragma unroll
+    for (int j = 1; j < kScW; ++j) w = i == j ? sk[half * kScW + j] : w;
+    return __uint_as_float((q & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// n consecutive scales from row pointer s (2-byte aligned) into half `half` of sk.
+__device__ __forceinline__ void load_scales(const uint16_t *s, int n, int half, uint32_t (&sk)[2 * kScW]) {
+#pragma unroll
+    for (int j = 0; j < kScW; ++j) {
+        const uint32_t lo = 2 * j < n ? (uint32_t)__ldg(s + 2 * j) : 0u;
+        const uint32_t hi = 2 * j + 1 < n ? (uint32_t)__ldg(s + 2 * j + 1) : 0u;
+        sk[half * kScW + j] = lo | (hi << 16);
+    }
+}
+
+// Scales of chunk `chunk` of gate_up task `task`: its groups q0 .. q0 + qn - 1
+// of gate row 8r + g and up row I + 8r + g of the task's expert.
+__device__ __forceinline__ void gate_up_scales(const FusedParams &p, const Pro &v, int task, int chunk, int lane,
+                                               uint32_t (&sk)[2 * kScW]) {
+    const int tp1 = p.I / 8, G1 = p.H / 128, gc = p.gcw / 16;
+    const int a = task / tp1, r = task - a * tp1;
+    const int q0 = chunk * gc, qn = G1 - q0 < gc ? G1 - q0 : gc;
+    const size_t row = (size_t)v.act[a] * 2 * p.I + 8 * r + (lane >> 2);
+    load_scales(p.w1s + row * G1 + q0, qn, 0, sk);
+    load_scales(p.w1s + (row + p.I) * G1 + q0, qn, 1, sk);
+}
+
+// Scales of down chunk t2 (output block c, active expert a): all groups of
+// rows 16c + g and 16c + g + 8 of the expert's W2.
+__device__ __forceinline__ void down_scales(const FusedParams &p, const Pro &v, int t2, int lane,
+                                            uint32_t (&sk)[2 * kScW]) {
+    const int nact = *v.nact, G2 = p.I / 128;
+    const int c = t2 / nact, a = t2 - c * nact;
+    const size_t row = (size_t)v.act[a] * p.H + kP2Rows * c + (lane >> 2);
+    load_scales(p.w2s + row * G2, G2, 0, sk);
+    load_scales(p.w2s + (row + 8) * G2, G2, 1, sk);
 }
 
 // ---- gate_up ----------------------------------------------------------------
@@ -414,7 +462,7 @@ __device__ __noinline__ void f_issue(const FusedParams &p, const Pro &v, int tas
 template <bool kStaged>
 __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int task, int chunk, bool first,
                                        const uint8_t *stage, const uint8_t *smem, int lane,
-                                       float (&acc)[kMaxNT][4]) {
+                                       const uint32_t (&sk)[2 * kScW], float (&acc)[kMaxNT][4]) {
     const int tp1 = p.I / 8;
     const int a = task / tp1;
     const int s0 = v.aoff[a], ne = v.acnt[a];
@@ -427,7 +475,6 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
     const uint32_t rowb = p.gcw * 4;
     const uint8_t *rg = stage + g * rowb + 16 * tig;
     const uint8_t *ru = stage + 8 * rowb + g * rowb + 16 * tig;
-    const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + 16 * rowb);
     const uint4 zero = make_uint4(0, 0, 0, 0);
     if (first) {
 #pragma unroll
@@ -457,8 +504,8 @@ __device__ inline void f_gate_up_chunk(const FusedParams &p, const Pro &v, int t
         for (int qq = 0; qq < qn; ++qq) {
             const int q = q0 + qq;
             const uint4 wg = lds_v4(rg + 64 * qq), wu = lds_v4(ru + 64 * qq);
-            const float sg = bf16_bits_to_f32(sc[g * G1 + q]);
-            const float su = bf16_bits_to_f32(sc[(8 + g) * G1 + q]);
+            const float sg = scale_of(sk, 0, qq);
+            const float su = scale_of(sk, 1, qq);
             uint4 X[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -670,7 +717,7 @@ __device__ __noinline__ void f_stack_rows(const FusedParams &p) {
 // the block's count combines it. cb0: the CTA's first block (its blocks use
 // the nyb buffers in turn).
 __device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem, int t2, int cb0, int m1,
-                              const uint8_t *stage, int lane) {
+                              const uint8_t *stage, int lane, const uint32_t (&sk)[2 * kScW]) {
     const int tp1 = p.I / 8;
     const int nact = *v.nact;
     const int c = t2 / nact, a = t2 - c * nact;
@@ -679,7 +726,6 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem,
     const int g = lane >> 2, tig = lane & 3;
     const int G2 = p.I / 128;
     const uint32_t rb = p.I / 2;
-    const uint16_t *sc = reinterpret_cast<const uint16_t *>(stage + kP2Rows * rb);
 
     // wait until every gate_up task of expert e has published its h (polls
     // back off from 64 to 512 ns, so that the pollers of an expert leave its
@@ -733,8 +779,8 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem,
                 const int R = 16 * s + g;
                 const uint4 w0 = lds_v4(stage + R * rb + 64 * q + 16 * tig);
                 const uint4 w1 = lds_v4(stage + (R + 8) * rb + 64 * q + 16 * tig);
-                const float s0v = bf16_bits_to_f32(sc[R * G2 + q]);
-                const float s1v = bf16_bits_to_f32(sc[(R + 8) * G2 + q]);
+                const float s0v = scale_of(sk, 0, q);
+                const float s1v = scale_of(sk, 1, q);
                 float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
@@ -975,6 +1021,11 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
             if (i >= nc) break;
             const int q = i % kNS;
             uint8_t *stage = smem + (size_t)q * p.stage_bytes;
+            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
+            // the chunk's scales travel while it waits for its weights
+            uint32_t sk[2 * kScW];
+            if (r.task < n1) gate_up_scales(p, v, r.task, r.chunk, lane, sk);
+            else down_scales(p, v, r.task - n1, lane, sk);
             // chunk i's copy has been issued into stage q (then the barrier's
             // pending phase is chunk i's), and has landed
             uint32_t ok = 1;
@@ -991,9 +1042,8 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
                 if (lane == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
                 break;
             }
-            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
             if (r.task < n1) {
-                f_gate_up_chunk<kStaged>(p, v, r.task, r.chunk, true, stage, smem, lane, acc);
+                f_gate_up_chunk<kStaged>(p, v, r.task, r.chunk, true, stage, smem, lane, sk, acc);
                 // the stage is free as soon as its words are in registers
                 __syncwarp();
                 if (lane == 0) {
@@ -1002,7 +1052,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
                 }
                 if (!f_gu_reduce(p, v, smem, r.task, r.task - b1, r.chunk, lane, acc)) break;
             } else {
-                f_down(p, v, smem, r.task - n1, cb0, m1, stage, lane);
+                f_down(p, v, smem, r.task - n1, cb0, m1, stage, lane, sk);
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence_block();
