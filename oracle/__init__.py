@@ -58,6 +58,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_shared_combine.argtypes = [P, P, P, I, I, P]
         L.oracle_quantize_int4.argtypes = [P, I64, I64, I, P, P, P, P]
         L.oracle_quantize_int4.restype = I
+        L.oracle_unpack_int8.argtypes = [P, I64, I64, P]
+        L.oracle_pack_int8.argtypes = [P, I64, I64, P]
+        L.oracle_pack_int8.restype = I
+        L.oracle_w8a16_linear.argtypes = [P, P, P, I, I, I64, I64, P, I]
+        L.oracle_w8a16_linear.restype = I
         _lib = L
     return _lib
 
@@ -229,3 +234,33 @@ def quantize_int4(w, nclip: int = 50):
     if lib().oracle_quantize_int4(_p(ws), N, K, nclip, _p(err), _p(packed), _p(scales), _p(choice)) != 0:
         raise ValueError("K must be a multiple of 128 and 1 <= nclip <= 100")
     return packed, scales, choice, err
+
+
+def unpack_int8(packed, N: int, K: int) -> np.ndarray:
+    """q int16 [N, K] in [-128, 127] from INT8 pack-quantized words int32 [N, K/4]."""
+    p = _np(packed, np.int32)
+    q = np.empty((N, K), np.int16)
+    lib().oracle_unpack_int8(_p(p), N, K, _p(q))
+    return q
+
+
+def pack_int8(q) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int16)
+    N, K = q.shape
+    out = np.empty((N, K // 4), np.int32)
+    if lib().oracle_pack_int8(_p(q), N, K, _p(out)) != 0:
+        raise ValueError("value outside [-128, 127]")
+    return out
+
+
+def w8a16_linear(x, packed, scales, gs: int, nthreads: int = 0) -> np.ndarray:
+    """fp64 y [T, N] = x . W^T for INT8 weights (q + 128, LSB first) with bf16 scales per gs of K."""
+    xs = _np(x, np.uint16)
+    T, K = xs.shape
+    p = _np(packed, np.int32)
+    N = p.shape[0]
+    s = _np(scales, np.uint16)
+    y = np.empty((T, N), np.float64)
+    if lib().oracle_w8a16_linear(_p(xs), _p(p), _p(s), gs, T, N, K, _p(y), nthreads) != 0:
+        raise ValueError("gs must be 64 or 128 and divide K")
+    return y

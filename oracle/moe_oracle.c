@@ -36,6 +36,11 @@
  *              (section 3.3 "MoE block": the router and the shared expert gate
  *              as one GEMV of 512 + 1 rows; the final combine, routed +
  *              sigmoid(gate) x shared.)
+ *   W8A16    - INT8 weights, four per int32 word, least significant byte
+ *              first, stored as q + 128, one bf16 scale per 64 or 128 values
+ *              of a row; y = x . W^T. (section 3.3 "Hyper-connection
+ *              (decode-04)": the INT8 GEMVs and the W8A16 GEMM; model card
+ *              "What is quantized", groups C and D.)
  *   quantise - round-to-nearest INT4, group size 128, symmetric, with a
  *              per-group search for the clip that minimises the squared error.
  *              (section 7 "Putting MTP on the GPU": make_mtp_int4.py.)
@@ -475,6 +480,67 @@ int oracle_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nclip, dou
             for (int i = 0; i < 8; ++i)
                 word |= (uint32_t)(quant_one(bf16_to_f32(wv[8 * wd + i]), s) + 8) << (4 * i);
             packed[n * (K / 8) + g * (ORACLE_GROUP / 8) + wd] = (int32_t)word;
+        }
+    }
+    return 0;
+}
+
+/* ---- INT8 weights (W8A16) --------------------------------------------------- */
+/*
+ * compressed-tensors INT8 pack-quantized ("vLLM Optimization Edition",
+ * section 3.3 "Hyper-connection (decode-04)"; model card "What is quantized",
+ * groups C and D): four values per int32 word, least significant byte first,
+ * each stored as q + 128, so q lies in [-128, 127]; one bf16 scale per row
+ * and group of gs (64 or 128) consecutive values along K.
+ */
+
+/* q[n][c] = byte c%4 of packed[n][c/4], minus 128. */
+void oracle_unpack_int8(const int32_t *packed, int64_t N, int64_t K, int16_t *q)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t c = 0; c < K; ++c) {
+            uint32_t word = (uint32_t)packed[n * (K / 4) + c / 4];
+            q[n * K + c] = (int16_t)((int)((word >> (8 * (c % 4))) & 0xFFu) - 128);
+        }
+}
+
+/* Inverse of oracle_unpack_int8. Returns -1 if some q lies outside [-128, 127]. */
+int oracle_pack_int8(const int16_t *q, int64_t N, int64_t K, int32_t *packed)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t w = 0; w < K / 4; ++w) {
+            uint32_t word = 0;
+            for (int i = 0; i < 4; ++i) {
+                int v = q[n * K + w * 4 + i];
+                if (v < -128 || v > 127) return -1;
+                word |= (uint32_t)(v + 128) << (8 * i);
+            }
+            packed[n * (K / 4) + w] = (int32_t)word;
+        }
+    return 0;
+}
+
+/*
+ * y[t][n] = sum_c x[t][c] * W[n][c], W[n][c] = q[n][c] * scale[n][c / gs]
+ * (fp64). x bf16 [T][K], packed int32 [N][K/4], scales bf16 [N][K/gs], y f64
+ * [T][N]. Returns -1 unless gs is 64 or 128 and divides K.
+ */
+int oracle_w8a16_linear(const uint16_t *x, const int32_t *packed, const uint16_t *scales, int gs, int T,
+                        int64_t N, int64_t K, double *y, int nthreads)
+{
+    if ((gs != 64 && gs != 128) || K % gs) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int t = 0; t < T; ++t) {
+            double s = 0.0;
+            for (int64_t c = 0; c < K; ++c) {
+                uint32_t word = (uint32_t)packed[n * (K / 4) + c / 4];
+                int q = (int)((word >> (8 * (c % 4))) & 0xFFu) - 128;
+                double w = (double)q * bf16_to_f64(scales[n * (K / gs) + c / gs]);
+                s += bf16_to_f64(x[(int64_t)t * K + c]) * w;
+            }
+            y[(int64_t)t * N + n] = s;
         }
     }
     return 0;

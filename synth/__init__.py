@@ -22,7 +22,9 @@ quantized" table, group A = INT4 gs128 symmetric pack-quantized experts):
 - per-group scales: bf16(0.002 + 0.018 * u), u = m / 2**24 with m uniform
   on [0, 2**24), evaluated in float32 as one multiply then one add;
 - skewed routing: a router bias of -s * ln(rank), rank = 1 + a seeded
-  random permutation of the experts (Zipf with exponent s = 1.1).
+  random permutation of the experts (Zipf with exponent s = 1.1);
+- INT8 linear layers (W8A16): uniform bytes q + 128, bf16 scales
+  0.0002 + 0.0018 u per group of 64 or 128 values.
 """
 from __future__ import annotations
 
@@ -36,7 +38,7 @@ import torch
 GROUP = 128  # quantisation group size along K
 
 # tensor ids inside a SeedSequence
-_T_HIDDEN, _T_ROUTER, _T_W1, _T_W1S, _T_W2, _T_W2S, _T_ZIPF, _T_TOPK, _T_QW = range(9)
+_T_HIDDEN, _T_ROUTER, _T_W1, _T_W1S, _T_W2, _T_W2S, _T_ZIPF, _T_TOPK, _T_QW, _T_W8, _T_W8S = range(11)
 
 
 @dataclass(frozen=True)
@@ -188,6 +190,31 @@ def bf16_weights(N: int, K: int, seed: int = 0, layer: int = 0, outliers: float 
     mask = g.random((N, K), dtype=np.float32) < np.float32(outliers)
     w[mask] *= np.float32(4.0) + np.float32(8.0) * g.random(int(mask.sum()), dtype=np.float32)
     return _bf16(w)
+
+
+def int8_weights(N: int, K: int, gs: int, seed: int = 0, layer: int = 0) -> dict:
+    """INT8 pack-quantized weights of an [N, K] linear layer, on the host.
+
+    Each int32 word is 32 uniform random bits: four bytes uniform on
+    [0, 255], the stored values q + 128 of int8 q uniform on [-128, 127]
+    (least significant byte first). Scales bf16 [N, K/gs] = 0.0002 + 0.0018 u
+    (u uniform on [0, 1), as for the INT4 scales, a tenth of their size since
+    |q| reaches 128). Rows are drawn in blocks of 4096 from their own streams,
+    so a large matrix is drawn in parallel.
+    """
+    words = np.empty((N, K // 4), np.int32)
+    sc = np.empty((N, K // gs), np.float32)
+    blocks = list(range(0, N, 4096))
+
+    def fill(b0: int) -> None:
+        b1 = min(N, b0 + 4096)
+        words[b0:b1] = _words((seed, layer, _T_W8, b0), (b1 - b0) * (K // 4)).reshape(b1 - b0, K // 4)
+        m = _rng(seed, layer, _T_W8S, b0).integers(0, 2**24, (b1 - b0) * (K // gs), dtype=np.int64).astype(np.float32)
+        sc[b0:b1] = (np.float32(0.0002) + np.float32(0.0018) * (m * np.float32(1.0 / 2**24))).reshape(b1 - b0, K // gs)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(fill, blocks))
+    return {"w_packed": torch.from_numpy(words), "scales": _bf16(sc)}
 
 
 def layer_inputs(wl: Workload, seed: int = 0, layer: int = 0, experts=None) -> dict:

@@ -435,3 +435,62 @@ def test_quantize_single_outlier_closed_form():
     # 0.06396484375; 0.875 / 0.06396484375 = 13.7 saturates q at 7, leaving
     # (0.875 - 7 * 0.06396484375)^2 = 0.42724609375^2
     assert e[0, 0, 49] == 0.42724609375 ** 2
+
+
+# ------------------------------------------------------------------- W8A16 ----
+# "vLLM Optimization Edition" 3.3 "Hyper-connection (decode-04)": INT8
+# pack-quantized puts four values in each int32 word, least significant byte
+# first, stored as value + 128, so the words viewed as bytes already are
+# q + 128 as [N, K]; model card "What is quantized", groups C (gs64) and D (gs128).
+
+def _golden_int8():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "int8_pack.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        lhs, rhs = line.split("->")
+        rows.append(([int(v) for v in lhs.split()], int(rhs, 16)))
+    return rows
+
+
+def test_int8_pack_matches_hand_worked_words():
+    for q, word in _golden_int8():
+        packed = oracle.pack_int8(np.array([q], np.int16))
+        assert int(packed.view(np.uint32)[0, 0]) == word
+        assert oracle.unpack_int8(packed, 1, 4).tolist() == [q]
+
+
+def test_int8_words_viewed_as_bytes_are_q_plus_128():
+    # the pages' observation: weight_packed.view(uint8) already is q + 128 as [N, K]
+    w = synth.int8_weights(7, 256, 64, seed=40)["w_packed"].numpy()
+    q = oracle.unpack_int8(w, 7, 256)
+    assert np.array_equal(w.view(np.uint8).reshape(7, 256).astype(np.int16) - 128, q)
+    assert np.array_equal(oracle.pack_int8(q), w)
+    with pytest.raises(ValueError):
+        oracle.pack_int8(np.full((1, 4), 128, np.int16))
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+def test_w8a16_linear_equals_library_matmul(gs):
+    T, N, K = 5, 24, 512
+    d = synth.int8_weights(N, K, gs, seed=41)
+    x = synth.hidden(T, K, seed=41)
+    y = oracle.w8a16_linear(x, d["w_packed"], d["scales"], gs)
+    q = d["w_packed"].numpy().view(np.uint8).reshape(N, K).astype(np.float64) - 128
+    W = q * np.repeat(_f64(d["scales"]), gs, axis=1)
+    assert np.allclose(y, _f64(x) @ W.T, rtol=0, atol=1e-12 * np.abs(y).max())
+
+
+def test_w8a16_group_index_and_closed_form():
+    # all bytes 0x81 (q = 1): y = x . (scale per group), so the group index c // gs shows
+    N, K = 2, 256
+    words = np.full((N, K // 4), 0x81818181, np.uint32).view(np.int32)
+    for gs in (64, 128):
+        sc = torch.tensor([[1.0, 2.0, 4.0, 8.0][: K // gs], [0.5, -1.0, 0.25, 3.0][: K // gs]], dtype=torch.bfloat16)
+        x = synth.hidden(3, K, seed=42)
+        y = oracle.w8a16_linear(x, words, sc, gs)
+        xg = _f64(x).reshape(3, K // gs, gs).sum(axis=2)
+        assert np.allclose(y, xg @ _f64(sc).T, rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.w8a16_linear(x, words, sc, 32)
