@@ -221,6 +221,23 @@ MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed
                   int32_t *bad_count, void *stream);
 
 /*
+ * W8A16 linear layer ("vLLM Optimization Edition", section 3.3
+ * "Hyper-connection (decode-04)": INT8 GEMVs on the pack-quantized words as
+ * stored, and a W8A16 GEMM for batches; model card "What is quantized",
+ * groups C (INT8 gs64: hyper-connection mixers) and D (INT8 gs128: lm_head)):
+ *   W[n][c] = (byte c%4 of w_packed[n][c/4] - 128) * scales[n][c/gs]
+ *   y[t][n] = sum_c x[t][c] * W[n][c]   (fp32 accumulation, rounded to bf16 once)
+ * x bf16 [T][K]; w_packed int32 [N][K/4] (four values per word, least
+ * significant byte first, stored q + 128); scales bf16 [N][K/gs]; y bf16
+ * [T][N] (output). gs is 64 or 128 and divides K (K a multiple of 64).
+ * No workspace. Supported: 1 <= T <= 8 with T * (K + 8) * 2 <= 196608 (the
+ * decode GEMV); other T return MOE_ERR_UNSUPPORTED. T = 0 or N = 0 return
+ * MOE_OK with nothing enqueued.
+ */
+MOE_API int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t *scales, int32_t gs,
+                     uint16_t *y, int32_t T, int32_t N, int32_t K, void *stream);
+
+/*
  * INT4 quantiser of BF16 weights into the experts' storage ("vLLM
  * Optimization Edition", section 7 "Putting MTP on the GPU", make_mtp_int4.py:
  * round to nearest, group size 128, symmetric, per-group search for the clip

@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
     "workspace", "moe_route", "moe_route_shared", "shared_workspace", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
-    "moe_pack_int4", "moe_quantize_int4", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
+    "moe_pack_int4", "moe_quantize_int4", "moe_w8a16_linear", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
     "moe_noalloc_check_device_error", "moe_forward_plan", "STATUS",
 ]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
         L.moe_quantize_int4.argtypes = [P, I64, I64, ctypes.c_int32, P, P, P, P]
         L.moe_quantize_int4.restype = I
+        L.moe_w8a16_linear.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+        L.moe_w8a16_linear.restype = I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
         L.moe_noalloc_check_device_error.argtypes, L.moe_noalloc_check_device_error.restype = [P], I
         L.moe_profile_events.argtypes, L.moe_profile_events.restype = [P, P], I
@@ -300,6 +302,23 @@ def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None
     _check(lib().moe_quantize_int4(_p(w), N, K, nclip, _p(packed), _p(scales), _p(choice), _stream(stream)),
            "moe_quantize_int4")
     return (packed, scales, choice) if with_choice else (packed, scales)
+
+
+def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, stream=None):
+    """bf16 y [T, N] = x . W^T for INT8 pack-quantized W (q + 128, four per int32 word, LSB first)
+    with bf16 scales per gs (64 or 128) values of K."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(w_packed, "w_packed", torch.int32, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    T, K = x.shape
+    N = w_packed.shape[0]
+    if w_packed.shape[1] * 4 != K or scales.shape != (N, K // gs):
+        raise ValueError("w_packed must be [N, K/4] and scales [N, K/gs]")
+    if y is None:
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_w8a16_linear(_p(x), _p(w_packed), _p(scales), gs, _p(y), T, N, K, _stream(stream)),
+           "moe_w8a16_linear")
+    return y
 
 
 def moe_profile_events(before=None, after=None):

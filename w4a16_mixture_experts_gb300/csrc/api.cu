@@ -245,6 +245,17 @@ int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t nclip, in
         launch_quantize_int4(w, N, K, nclip, packed, scales, choice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t *scales, int32_t gs, uint16_t *y,
+                     int32_t T, int32_t N, int32_t K, void *stream) {
+    if (T < 0 || N < 0 || K <= 0 || (gs != 64 && gs != 128) || K % gs) return MOE_ERR_INVALID_ARG;
+    const bool empty = T == 0 || N == 0;
+    if (!ptr_ok(x, T == 0) || !ptr_ok(w_packed, N == 0) || !ptr_ok(scales, N == 0) || !ptr_ok(y, empty))
+        return MOE_ERR_INVALID_ARG;
+    if (empty) return MOE_OK;
+    if (!w8a16_gemv_supported(T, K)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_w8a16(x, w_packed, scales, gs, y, T, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_profile_events(void *before_experts, void *after_experts) {
     if ((before_experts == nullptr) != (after_experts == nullptr)) return MOE_ERR_INVALID_ARG;
     g_ev_before = reinterpret_cast<cudaEvent_t>(before_experts);

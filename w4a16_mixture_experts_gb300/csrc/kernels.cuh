@@ -64,6 +64,11 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
 cudaError_t launch_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nclip, int32_t *packed,
                                  uint16_t *scales, int32_t *choice, cudaStream_t s);
 
+// W8A16 linear layer (w8a16.cu): the GEMV for T <= 8.
+bool w8a16_gemv_supported(int T, int K);
+cudaError_t launch_w8a16(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
+                         int K, cudaStream_t st);
+
 cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
                              cudaStream_t s);
 
