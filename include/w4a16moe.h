@@ -229,13 +229,17 @@ MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed
  *   y[t][n] = sum_c x[t][c] * W[n][c]   (fp32 accumulation, rounded to bf16 once)
  * x bf16 [T][K]; w_packed int32 [N][K/4] (four values per word, least
  * significant byte first, stored q + 128); scales bf16 [N][K/gs]; y bf16
- * [T][N] (output). gs is 64 or 128 and divides K (K a multiple of 64).
- * No workspace. Supported: 1 <= T <= 8 with T * (K + 8) * 2 <= 196608 (the
- * decode GEMV); other T return MOE_ERR_UNSUPPORTED. T = 0 or N = 0 return
- * MOE_OK with nothing enqueued.
+ * [T][N] (output). gs is 64 or 128 and divides K (K a multiple of 64, at most
+ * 65536); T <= 2^20.
+ *  - 1 <= T <= 8: the decode GEMV (weights streamed from HBM, mma.sync), when
+ *    T * (K + 8) * 2 <= 196608 (else MOE_ERR_UNSUPPORTED). ws may be NULL.
+ *  - T > 8: the tcgen05 GEMM (tiles of 128 rows x 128 tokens). ws: at least
+ *    256 bytes, 16-byte aligned, zero before its first use; it holds the error
+ *    word that moe_check_device_error reads (a bounded wait that gave up).
+ * T = 0 or N = 0 return MOE_OK with nothing enqueued.
  */
 MOE_API int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t *scales, int32_t gs,
-                     uint16_t *y, int32_t T, int32_t N, int32_t K, void *stream);
+                     uint16_t *y, int32_t T, int32_t N, int32_t K, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * INT4 quantiser of BF16 weights into the experts' storage ("vLLM

@@ -114,6 +114,15 @@ def test_argument_errors_are_synchronous(L):
     for nclip in (0, 101):
         assert L.moe_quantize_int4(ctypes.c_void_p(good[0]), 4, 256, nclip, ctypes.c_void_p(good[1]),
                                    ctypes.c_void_p(good[2]), None, None) == 1
+    # W8A16: gs other than 64/128, K not a multiple of gs, a batch without its workspace
+    assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 32,
+                              ctypes.c_void_p(good[3]), 4, 16, 256, None, 0, None) == 1
+    assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 128,
+                              ctypes.c_void_p(good[3]), 4, 16, 320, None, 0, None) == 1
+    assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 64,
+                              ctypes.c_void_p(good[3]), 64, 16, 256, None, 0, None) == 1
+    assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 64,
+                              ctypes.c_void_p(good[3]), 64, 16, 256, ctypes.c_void_p(good[4]), 128, None) == 3
     # shared-expert routing: k + 1 must stay within 32 slots, E + 1 within 1024 experts
     assert L.moe_route_shared(*[ctypes.c_void_p(p) for p in good[:3]], moe.moe_dims(4, 256, 64, 32, 128),
                               ctypes.c_void_p(good[3]), ctypes.c_void_p(good[4]), ctypes.c_void_p(good[5]),

@@ -81,7 +81,8 @@ def lib() -> ctypes.CDLL:
         L.moe_pack_int4.argtypes, L.moe_pack_int4.restype = [P, I64, I64, P, P, P], I
         L.moe_quantize_int4.argtypes = [P, I64, I64, ctypes.c_int32, P, P, P, P]
         L.moe_quantize_int4.restype = I
-        L.moe_w8a16_linear.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+        L.moe_w8a16_linear.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, Z,
+                                       P]
         L.moe_w8a16_linear.restype = I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
         L.moe_noalloc_check_device_error.argtypes, L.moe_noalloc_check_device_error.restype = [P], I
@@ -304,9 +305,11 @@ def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None
     return (packed, scales, choice) if with_choice else (packed, scales)
 
 
-def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, stream=None):
+def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, ws=None, stream=None):
     """bf16 y [T, N] = x . W^T for INT8 pack-quantized W (q + 128, four per int32 word, LSB first)
-    with bf16 scales per gs (64 or 128) values of K."""
+    with bf16 scales per gs (64 or 128) values of K. T <= 8: the decode GEMV; larger T: the
+    tensor-core GEMM, whose error word lives in ws (a zeroed uint8 tensor of >= 256 bytes;
+    allocated here when not given)."""
     _need(x, "x", torch.bfloat16, 2)
     _need(w_packed, "w_packed", torch.int32, 2)
     _need(scales, "scales", torch.bfloat16, 2)
@@ -316,8 +319,11 @@ def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, stream=None):
         raise ValueError("w_packed must be [N, K/4] and scales [N, K/gs]")
     if y is None:
         y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
-    _check(lib().moe_w8a16_linear(_p(x), _p(w_packed), _p(scales), gs, _p(y), T, N, K, _stream(stream)),
-           "moe_w8a16_linear")
+    if ws is None and T > 8:
+        ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+    nbytes = 0 if ws is None else ws.numel()
+    _check(lib().moe_w8a16_linear(_p(x), _p(w_packed), _p(scales), gs, _p(y), T, N, K, _p(ws), nbytes,
+                                  _stream(stream)), "moe_w8a16_linear")
     return y
 
 

@@ -246,14 +246,22 @@ int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t nclip, in
 }
 
 int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t *scales, int32_t gs, uint16_t *y,
-                     int32_t T, int32_t N, int32_t K, void *stream) {
+                     int32_t T, int32_t N, int32_t K, void *ws, size_t ws_bytes, void *stream) {
     if (T < 0 || N < 0 || K <= 0 || (gs != 64 && gs != 128) || K % gs) return MOE_ERR_INVALID_ARG;
+    if (T > (1 << 20) || K > 65536) return MOE_ERR_UNSUPPORTED;
     const bool empty = T == 0 || N == 0;
     if (!ptr_ok(x, T == 0) || !ptr_ok(w_packed, N == 0) || !ptr_ok(scales, N == 0) || !ptr_ok(y, empty))
         return MOE_ERR_INVALID_ARG;
     if (empty) return MOE_OK;
-    if (!w8a16_gemv_supported(T, K)) return MOE_ERR_UNSUPPORTED;
-    return cuda_status(launch_w8a16(x, w_packed, scales, gs, y, T, N, K, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T <= 8) {
+        if (!w8a16_gemv_supported(T, K)) return MOE_ERR_UNSUPPORTED;
+        return cuda_status(launch_w8a16(x, w_packed, scales, gs, y, T, N, K, s));
+    }
+    // the tensor-core GEMM records a wait that gave up in the workspace's error word
+    if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_w8a16_gemm(x, w_packed, scales, gs, y, T, N, K, reinterpret_cast<Ctrl *>(ws), s));
 }
 
 int moe_profile_events(void *before_experts, void *after_experts) {

@@ -68,6 +68,9 @@ cudaError_t launch_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nc
 bool w8a16_gemv_supported(int T, int K);
 cudaError_t launch_w8a16(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
                          int K, cudaStream_t st);
+// ... and the tensor-core GEMM for larger T (prefill.cu, the INT8 instantiation).
+cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
+                              int K, struct Ctrl *ctrl, cudaStream_t st);
 
 cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
                              cudaStream_t s);

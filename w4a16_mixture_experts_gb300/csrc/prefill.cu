@@ -39,6 +39,15 @@
 // of the same order halves the tensor rate. The accumulator is double-buffered
 // in TMEM so 256 epilogue threads drain one tile while the next accumulates.
 //
+// The same kernel, instantiated for INT8 (kW8), is the W8A16 linear layer for
+// batches ("vLLM Optimization Edition", section 3.3 "Hyper-connection": the
+// W8A16 GEMM over 4 tokens; model card groups C and D): one dense GEMM with the
+// weight rows as M and the tokens as N, tiles of (128 rows, up to 128 tokens).
+// The INT8 rows arrive by TMA (128 x 128 bytes a stage, 128-byte swizzle) and
+// are dequantised exactly into bf16 in natural K order, so the activation rows
+// are the caller's x as they are (no gather); each thread loads its row's
+// scale(s) for the stage itself; the epilogue stores bf16 y.
+//
 // Weights enter A as W = bf16(q * scale) (one rounding per weight). Nibble
 // pairs (j, j+4) of each word fill one 32-bit TMEM column, so the
 // activations are kept in the matching order within each 8-element chunk
@@ -69,6 +78,9 @@ constexpr uint32_t kBKBlock = kPN * 128;        // 128 token rows x 64 bf16: one
 constexpr uint32_t kBBytes = 2 * kBKBlock;      // one activation stage: two K blocks
 constexpr uint32_t kRawHalf = 64 * 64;          // 64 weight rows x 16 words
 constexpr uint32_t kRawBytes = 2 * kRawHalf;    // one packed-INT4 stage
+constexpr int kRR8 = 4;                         // INT8 stages: 128 rows x 128 bytes each
+constexpr uint32_t kRawBytes8 = 128 * 128;
+static_assert(kRR8 * kRawBytes8 == kRR * kRawBytes, "one raw ring size for both weight widths");
 constexpr uint32_t kPrefillSmemMax = 232448 - 1024;   // dynamic; the static part is a few bytes
 static_assert(kAStage0 + kRS * kACols <= kTmemCols, "tensor memory budget");
 
@@ -105,6 +117,8 @@ struct PrefillParams {
     uint16_t *hbuf;            // gate_up output, bf16 [T*k][I] fragment order
     const uint16_t *xs;        // gate_up input, bf16 [T*k][H] fragment order
     float *out_acc;            // down output, f32 [T][H]
+    uint16_t *y;               // W8A16 output, bf16 [T][N]
+    int N, gs, dense_chunks;   // W8A16: output features, scale group, token chunks of 128
     int T, H, E, k, I;
     int K;                     // reduction length: H (gate_up) or I (down)
     int mb;                    // row blocks per expert: I/64 (gate_up) or H/128 (down)
@@ -117,8 +131,17 @@ struct Tile {
 };
 
 // Tile t = (chunk t / mb, row block t % mb): chunks of each expert are
-// consecutive, and the row blocks of one chunk are consecutive tiles.
-__device__ inline int4 chunk_of(const PrefillParams &p, int t) { return __ldg(p.chunk_info + t / p.mb); }
+// consecutive, and the row blocks of one chunk are consecutive tiles. The
+// dense (W8A16) GEMM has one "expert" and chunks of 128 consecutive tokens.
+template <bool kW8>
+__device__ inline int4 chunk_of(const PrefillParams &p, int t) {
+    if constexpr (kW8) {
+        const int c = t / p.mb;
+        return make_int4(0, c * kPN, min(kPN, p.T - c * kPN), 0);
+    } else {
+        return __ldg(p.chunk_info + t / p.mb);
+    }
+}
 
 __device__ inline Tile make_tile(int4 ci, int m) {
     Tile r;
@@ -178,7 +201,38 @@ __device__ inline void dequant8(const uint4 &a, const uint4 &b, __nv_bfloat162 s
         }
 }
 
+// Bytes (b_lo, b_hi) of an INT8 pack-quantized word -> bf16x2 of (b - 128)
+// each, exactly: prmt places the bytes in the two halves; 128 + (b & 127)
+// and -256 (or -128 when b >= 128) are formed bitwise and added (sel 0x4140:
+// bytes 0, 1; 0x4342: bytes 2, 3).
+__device__ __forceinline__ uint32_t int8_pair(uint32_t w, uint32_t sel) {
+    const uint32_t v = __byte_perm(w, 0u, sel);
+    uint32_t lo, hi;
+    asm("lop3.b32 %0, %1, 0x007F007F, %2, 0xEA;" : "=r"(lo) : "r"(v), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, 0x00800080, %2, 0x6A;" : "=r"(hi) : "r"(v), "r"(0xC380C380u));
+    __nv_bfloat162 r = __hadd2(*reinterpret_cast<__nv_bfloat162 *>(&lo), *reinterpret_cast<__nv_bfloat162 *>(&hi));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// 16 words (64 INT8 values) of one weight row -> 32 TMEM columns in natural K
+// order (column j: values 2j, 2j + 1), times the scale.
+__device__ inline void dequant8_w8(const uint4 &a, const uint4 &b, const uint4 &c, const uint4 &d,
+                                   __nv_bfloat162 s2, uint32_t (&v)[32]) {
+    const uint32_t w[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        uint32_t lo = int8_pair(w[m], 0x4140), hi = int8_pair(w[m], 0x4342);
+        __nv_bfloat162 l2 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&lo), s2);
+        __nv_bfloat162 h2 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&hi), s2);
+        v[2 * m] = *reinterpret_cast<uint32_t *>(&l2);
+        v[2 * m + 1] = *reinterpret_cast<uint32_t *>(&h2);
+    }
+}
+
+template <bool kW8>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int kRing = kW8 ? kRR8 : kRR;                       // raw weight stages
+    constexpr uint32_t kStageBytes = kW8 ? kRawBytes8 : kRawBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const PrefillLayout &L = p.L;
@@ -204,7 +258,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         abort_s = 0;
-        for (int i = 0; i < kRR; ++i) {
+        for (int i = 0; i < kRing; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 128);
         }
@@ -232,10 +286,53 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int ntiles = *p.n_chunks * p.mb;
-    const int G = p.K / kKS;   // stages per tile
+    const int ntiles = kW8 ? p.dense_chunks * p.mb : *p.n_chunks * p.mb;
+    const int G = (p.K + kKS - 1) / kKS;   // stages per tile (the dense GEMM's last one may be half)
 
-    if (warp < kWEpi) {
+    if (kW8 && warp < kWEpi) {
+        // ------------------------------------------------ INT8 dequant: one weight row per thread
+        // (rows in order); group 0 takes the even stages, group 1 the odd ones. The row's scales
+        // for a stage (one per 128 values for gs 128, two for gs 64) come from global memory,
+        // requested before the stage's weights are waited for.
+        const int grp = warp >> 2;
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int sw = r & 7;              // 128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7)
+        const int nG = p.K / p.gs;          // scale groups per row
+        uint32_t g = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int n = (t % p.mb) * 128 + r;   // this thread's weight row (output feature)
+            const uint16_t *srow = p.scales + (size_t)(n < p.N ? n : 0) * nG;
+            bool ok = true;
+            for (int ks = 0; ks < G; ++ks, ++g) {
+                if ((int)(g & 1) != grp) continue;
+                const int sr = g % kRing, sa = g % kRS;
+                const int q0 = ks * kKS / p.gs, q1 = p.gs == kKS ? q0 : q0 + 1;
+                const uint32_t sb0 = n < p.N && q0 < nG ? (uint32_t)__ldg(srow + q0) : 0u;
+                const uint32_t sb1 = n < p.N && q1 < nG ? (uint32_t)__ldg(srow + q1) : 0u;
+                if (!pwait(&raw_full[sr], (g / kRing) & 1, abort_flag)) { ok = false; break; }
+                const uint8_t *rr = sRaw + sr * kStageBytes + r * 128;
+                uint4 c[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c[i] = lds_v4(rr + 16 * (i ^ sw));
+                const uint32_t s2a = sb0 | (sb0 << 16), s2b = sb1 | (sb1 << 16);
+                uint32_t v0[32], v1[32];
+                dequant8_w8(c[0], c[1], c[2], c[3], *reinterpret_cast<const __nv_bfloat162 *>(&s2a), v0);
+                dequant8_w8(c[4], c[5], c[6], c[7], *reinterpret_cast<const __nv_bfloat162 *>(&s2b), v1);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&raw_empty[sr]);
+                if (!pwait(&ab_empty[sa], ((g / kRS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t ta = tmem + lane_base + kAStage0 + sa * kACols;
+                tc::st_32x32b_x32(ta, v0);
+                tc::st_32x32b_x32(ta + 32, v1);
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(&a_full[sa]);
+            }
+            if (!ok) { fail(p, abort_flag); break; }
+        }
+    } else if (warp < kWEpi) {
         // ------------------------------------------------ dequant: one weight row per thread; group
         // 0 (warps 0-3) takes the even stages, group 1 (warps 4-7) the odd ones
         const int grp = warp >> 2;
@@ -295,10 +392,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         const int il = et >> 1;
         const int pl = 8 * (il >> 3) + 2 * (il & 3) + ((il >> 2) & 1);
         int lt = 0;
-        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
+        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of<kW8>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = make_tile(ci, t % p.mb);
-            if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);   // lands during this tile
+            if (t + (int)gridDim.x < ntiles) ci = chunk_of<kW8>(p, t + gridDim.x);   // lands during this tile
             const int b = lt & 1;
             // the epilogue threads share named barrier 1: they give up together
             if (!bar_and_epi(pwait(&acc_full[b], (lt >> 1) & 1, abort_flag))) { fail(p, abort_flag); break; }
@@ -306,13 +403,30 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const uint32_t dbase = tmem + ((uint32_t)(32 * q) << 16) + b * kPN;
             // per column of the tile: gate_up needs the slot's routing weight, down the
             // token's output row (the previous tile's readers passed the barrier above)
-            if (!eh && et < T.nv) {
+            if (!kW8 && !eh && et < T.nv) {
                 const int a = p.perm[T.s0 + et];
                 if (p.down) col_off[et] = (uint32_t)(a / p.k) * (uint32_t)p.H;
                 else col_w[et] = p.topk_w[a];
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kNEpi) : "memory");
-            if (p.down) {
+            if (kW8) {
+                // y[token][n]: for each column the 32 lanes of a warp store 32 consecutive n
+                const int n = T.m * 128 + et;
+                for (int c0 = 32 * eh; c0 < T.nv; c0 += 64) {
+                    float v[32];
+                    tc::ld_32x32b_x32(dbase + c0, v);
+                    tc::wait_ld();
+                    const int nu = min(32, T.nv - c0);
+                    if (n < p.N) {
+#pragma unroll
+                        for (int u = 0; u < 32; ++u)
+                            if (u < nu) {
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(v[u]);
+                                p.y[(size_t)(T.s0 + c0 + u) * p.N + n] = *reinterpret_cast<const uint16_t *>(&hb);
+                            }
+                    }
+                }
+            } else if (p.down) {
                 // one reduction per (row, token): the 32 lanes of a warp cover 128 consecutive
                 // bytes of the token's output row; the routing weight is already in h
                 float *orow = p.out_acc + T.m * 128 + et;
@@ -357,49 +471,56 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const uint64_t wpol = l2_evict_first();
             uint32_t g = 0;
             int lt = 0;
-            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
+            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of<kW8>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
                 const Tile T = make_tile(ci, t % p.mb);
-                if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);
+                if (t + (int)gridDim.x < ntiles) ci = chunk_of<kW8>(p, t + gridDim.x);
                 const int tb = lt & 1;
-                if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
                 // weight rows of TMEM lanes 0-63 and 64-127
-                const int row_a = p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
+                const int row_a = kW8 ? T.m * 128 : p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
                 const int row_b = row_a + (p.down ? 64 : p.I);
-                uint16_t *dst = sSc + tb * (L.sc_bytes / 2);
-                mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
-                bulk_g2s(dst, p.scales + (size_t)row_a * G, 64 * G * 2, &sc_full[tb]);
-                bulk_g2s(dst + 64 * G, p.scales + (size_t)row_b * G, 64 * G * 2, &sc_full[tb]);
+                if (!kW8) {
+                    if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+                    uint16_t *dst = sSc + tb * (L.sc_bytes / 2);
+                    mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
+                    bulk_g2s(dst, p.scales + (size_t)row_a * G, 64 * G * 2, &sc_full[tb]);
+                    bulk_g2s(dst + 64 * G, p.scales + (size_t)row_b * G, 64 * G * 2, &sc_full[tb]);
+                }
                 bool ok = true;
                 for (int ks = 0; ks < G; ++ks, ++g) {
-                    const int sr = g % kRR;
-                    if (!pwait(&raw_empty[sr], ((g / kRR) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&raw_full[sr], kRawBytes);
-                    uint8_t *rdst = sRaw + sr * kRawBytes;
-                    // down's 128 rows are consecutive: one box (gate_up: gate and up boxes)
-                    tma_load_2d_hint(rdst, &p.tm_w, ks * 16, row_a, &raw_full[sr], wpol);
-                    if (!p.down) tma_load_2d_hint(rdst + kRawHalf, &p.tm_w, ks * 16, row_b, &raw_full[sr], wpol);
+                    const int sr = g % kRing;
+                    if (!pwait(&raw_empty[sr], ((g / kRing) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&raw_full[sr], kStageBytes);
+                    uint8_t *rdst = sRaw + sr * kStageBytes;
+                    if (kW8) {
+                        // 128 INT8 rows x 128 values (32 words); rows past N and words past K read as zero
+                        tma_load_2d_hint(rdst, &p.tm_w, ks * 32, row_a, &raw_full[sr], wpol);
+                    } else {
+                        // down's 128 rows are consecutive: one box (gate_up: gate and up boxes)
+                        tma_load_2d_hint(rdst, &p.tm_w, ks * 16, row_a, &raw_full[sr], wpol);
+                        if (!p.down) tma_load_2d_hint(rdst + kRawHalf, &p.tm_w, ks * 16, row_b, &raw_full[sr], wpol);
+                    }
                 }
                 if (!ok) { fail(p, abort_flag); break; }
             }
-            // the consumers waited on every issued INT4 stage, except after an abort:
+            // the consumers waited on every issued weight stage, except after an abort:
             // then give the outstanding ones a bounded wait before the CTA exits
             if (*abort_flag)
-                for (uint32_t gg = g > (uint32_t)kRR ? g - kRR : 0; gg < g; ++gg)
-                    mbar_wait(&raw_full[gg % kRR], (gg / kRR) & 1);
+                for (uint32_t gg = g > (uint32_t)kRing ? g - kRing : 0; gg < g; ++gg)
+                    mbar_wait(&raw_full[gg % kRing], (gg / kRing) & 1);
         }
     } else if (warp == kWAct) {
         // ------------------------------------------------ activation stages: one TMA thread
         if (lane == 0) {
             uint32_t g = 0;
             const int grid = (int)gridDim.x;
-            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
-            int4 ci2 = blockIdx.x + grid < ntiles ? chunk_of(p, blockIdx.x + grid) : make_int4(0, 0, 0, 0);
+            int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of<kW8>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
+            int4 ci2 = blockIdx.x + grid < ntiles ? chunk_of<kW8>(p, blockIdx.x + grid) : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < ntiles; t += grid) {
                 const Tile T = make_tile(ci, t % p.mb);
                 ci = ci2;
                 const int t2 = t + 2 * grid;   // the tile after next
-                if (t2 < ntiles) ci2 = chunk_of(p, t2);
+                if (t2 < ntiles) ci2 = chunk_of<kW8>(p, t2);
                 bool ok = true;
                 for (int ks = 0; ks < G; ++ks, ++g) {
                     const int sb = g % kRS;
@@ -435,10 +556,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         // elected lane issues the stage's 8 MMAs and the commit
         uint32_t g = 0;
         int lt = 0;
-        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of(p, blockIdx.x) : make_int4(0, 0, 0, 0);
+        int4 ci = blockIdx.x < (unsigned)ntiles ? chunk_of<kW8>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
             const Tile T = make_tile(ci, t % p.mb);
-            if (t + (int)gridDim.x < ntiles) ci = chunk_of(p, t + gridDim.x);
+            if (t + (int)gridDim.x < ntiles) ci = chunk_of<kW8>(p, t + gridDim.x);
             const int b = lt & 1;
             if (!__all_sync(0xffffffffu, pwait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, abort_flag))) {
                 fail(p, abort_flag);
@@ -667,7 +788,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     uint16_t *xperm = ws_at<uint16_t>(ws, W.xperm);
     float *out_acc = ws_at<float>(ws, W.out_acc);
     int32_t *n_chunks = ws_at<int32_t>(ws, W.n_chunks);
-    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel), (int)kPrefillSmemMax);
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<false>), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
     {
@@ -717,7 +838,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.mb = d.I / 64;
     p.down = 0;
     p.L = prefill_layout(p.K / kKS);
-    prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
+    prefill_kernel<false><<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // down: K = I, 128 output rows per tile
@@ -733,11 +854,42 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.mb = d.H / 128;
     p.down = 1;
     p.L = prefill_layout(p.K / kKS);
-    prefill_kernel<<<grid, kPThreads, p.L.total, s>>>(p);
+    prefill_kernel<false><<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = record_profile_event(ev_after, s)) != cudaSuccess) return err;
 
     acc_convert_kernel<<<d.T, kConvThreads, 0, s>>>(out_acc, a.x, d.H, eps, next ? nullptr : out, next);
+    return cudaGetLastError();
+}
+
+// The W8A16 linear layer for batches: the dense INT8 instantiation, x and y the
+// caller's (token chunks of 128 consecutive tokens, row blocks of 128 weight rows).
+cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
+                              int K, Ctrl *ctrl, cudaStream_t st) {
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<true>), (int)kPrefillSmemMax);
+    if (err != cudaSuccess) return err;
+    PrefillParams p{};
+    err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, w, (uint64_t)K / 4, (uint64_t)N, (uint64_t)K, 32u,
+                         128u, CU_TENSOR_MAP_SWIZZLE_128B);
+    for (int i = 0; i < kNBoxMaps && err == cudaSuccess; ++i)
+        err = encode_tmap_2d(&p.tm_b[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, (uint64_t)K, (uint64_t)T,
+                             (uint64_t)K * 2, 64u, 16u << i, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    p.scales = s;
+    p.y = y;
+    p.N = N;
+    p.gs = gs;
+    p.T = T;
+    p.K = K;
+    p.mb = (N + 127) / 128;
+    p.dense_chunks = (T + kPN - 1) / kPN;
+    p.down = 1;
+    p.ctrl = ctrl;
+    p.ctrl_rw = ctrl;
+    p.L = prefill_layout(0);
+    const long long tiles = (long long)p.mb * p.dense_chunks;
+    const unsigned grid = (unsigned)(tiles < sm_count() ? tiles : sm_count());
+    prefill_kernel<true><<<grid, kPThreads, p.L.total, st>>>(p);
     return cudaGetLastError();
 }
 
