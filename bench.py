@@ -63,7 +63,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--config", default="decode1", choices=sorted(synth.WORKLOADS) + sorted(EXTRA))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--sets", type=int, default=0, help="weight sets to rotate over (0: enough to exceed L2)")
@@ -180,20 +180,25 @@ def cpu_baseline(wl, seed: int, target_s: float):
     T, H, E, k, I = wl.dims
     oracle.build()
     cores = oracle.max_threads()
-    wr = synth.router(E, H, seed=seed, layer=0)
+    wr = synth.router(E + 1 if wl.shared else E, H, seed=seed, layer=0)
     bias = synth.zipf_bias(E, wl.zipf, seed=seed) if wl.zipf else None
+    sh = synth.expert_weights(E + 1, H, I, seed=seed, layer=0, experts=[E]) if wl.shared else None
 
     def run(n):
         xs = synth.hidden(n, H, seed=seed, layer=101)
-        ids, w, _ = oracle.route(xs, wr, k, bias)
+        ids, w, _ = oracle.route(xs, wr[:E], k, bias)
         held = np.unique(ids)
         row = np.full(E, -1, np.int32)
         row[held] = np.arange(len(held))
         wts = synth.expert_weights(E, H, I, seed=seed, layer=0, experts=held)
         t0 = time.perf_counter()
-        oracle.route(xs, wr, k, bias)
-        oracle.expert_forward(xs, ids, w.astype(np.float32), wts["w1_packed"], wts["w1_scales"],
-                              wts["w2_packed"], wts["w2_scales"], E, I, expert_row=row)
+        oracle.route(xs, wr[:E], k, bias)
+        out = oracle.expert_forward(xs, ids, w.astype(np.float32), wts["w1_packed"], wts["w1_scales"],
+                                    wts["w2_packed"], wts["w2_scales"], E, I, expert_row=row)
+        if sh is not None:
+            gate, y = oracle.shared_expert(xs, wr[E], sh["w1_packed"][0], sh["w1_scales"][0], sh["w2_packed"][0],
+                                           sh["w2_scales"][0], I)
+            oracle.shared_combine(out, gate, y)
         return time.perf_counter() - t0
 
     n = cores
@@ -201,8 +206,9 @@ def cpu_baseline(wl, seed: int, target_s: float):
     n = max(cores, min(8192, int(n * target_s / max(t, 1e-3)) // cores * cores))
     t = run(n)
     return {"value": n / t / wl.layers, "unit": "tok/s", "cores": min(cores, n), "kind": "oracle",
-            "sample": "%d seeded tokens through one layer of workload %s (route + experts), fp64, %.1f s%s"
-                      % (n, wl.name, t, "; per-token rate divided by %d layers" % wl.layers
+            "sample": "%d seeded tokens through one layer of workload %s (route + experts%s), fp64, %.1f s%s"
+                      % (n, wl.name, " + shared expert" if wl.shared else "", t,
+                         "; per-token rate divided by %d layers" % wl.layers
                          if wl.layers > 1 else "")}
 
 
@@ -269,12 +275,14 @@ def measure(args, wl, steps, rank, world, local):
     elif args.sets:
         nsets = args.sets
     else:
-        touched = min(E, T * k) * EXPERT_BYTES
+        touched = (min(E, T * k) + (1 if wl.shared else 0)) * EXPERT_BYTES
         nsets = max(2, min(16, math.ceil(2.5 * L2_BYTES / touched)))
     seed = args.seed + 1000 * rank
+    # with a shared expert the forward runs over E + 1 experts and k + 1 slots
+    Ef, kf = (E + 1, k + 1) if wl.shared else (E, k)
     sets = []
     for i in range(nsets):
-        d = synth.layer_inputs(wl, seed=seed, layer=i)
+        d = synth.shared_layer_inputs(wl, seed=seed, layer=i) if wl.shared else synth.layer_inputs(wl, seed=seed, layer=i)
         if not stack:
             d["hidden"] = synth.hidden(T, H, seed=seed, layer=i)
         sets.append({key: (v.to(dev) if v is not None else None) for key, v in d.items()})
@@ -282,9 +290,9 @@ def measure(args, wl, steps, rank, world, local):
             sets[i]["hidden"] = None
         del d
     x0 = sets[0]["hidden"]
-    ws = moe.workspace(T, H, E, k, I, dev)
-    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
-    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    ws = moe.shared_workspace(T, H, E, k, I, dev) if wl.shared else moe.workspace(T, H, E, k, I, dev)
+    ids = torch.empty(T, kf, dtype=torch.int32, device=dev)
+    w = torch.empty(T, kf, dtype=torch.float32, device=dev)
     outs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(1 if stack else nsets)]
     act = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     stream = torch.cuda.Stream(device=dev)
@@ -294,8 +302,10 @@ def measure(args, wl, steps, rank, world, local):
     for e in ev_b + ev_a:       # torch only lets recorded events be timed; the library re-records them
         e.record(stream)
 
+    route = moe.moe_route_shared if wl.shared else moe.moe_route
+
     def layer_call(x, s, nxt=None, out=None):
-        moe.moe_route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
+        route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
         if nxt is not None:
             moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
                                       s["w2_scales"], eps=1e-6, next=nxt, ws=ws)
@@ -501,8 +511,10 @@ def measure(args, wl, steps, rank, world, local):
     fused = T <= FUSED_MAX_T
     pk, pk_src = peaks()
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
-    flops_launch = 2.0 * 3 * H * I * T * k           # algorithmic: gate, up and down over all slots
+    flops_launch = 2.0 * 3 * H * I * T * kf          # algorithmic: gate, up and down over all slots
     expert_kernel = "decode_fused_kernel" if fused else "prefill_kernel (gate_up + down launches)"
+    if wl.shared:
+        expert_kernel += ", shared expert as expert E"
     # the binding roofline: whichever of the unique weight bytes at the copy rate
     # and the flops at the tensor rate takes longer. The tensor peak is the dense
     # bf16 burst rate; a stack's fraction of the sustained rate is given beside it.
@@ -538,6 +550,7 @@ def measure(args, wl, steps, rank, world, local):
         "dtype": "bf16 activations x int4 weights, fp32 accumulate",
         "data": "synthetic (seeded; shapes and distributions of the pages' workload; random weights)",
         "config": {"workload": wl.name, "T": T, "H": H, "E": E, "k": k, "I": I, "layers": wl.layers,
+                   "shared_expert": wl.shared,
                    "zipf": wl.zipf, "weight_sets": nsets,
                    "l2": "rotating %d independent weight sets (> L2) between steps" % nsets
                    if not stack else "48 layers x 1.3 GB of weights per step (> L2)",
@@ -558,48 +571,311 @@ def measure(args, wl, steps, rank, world, local):
     }
 
 
+# ------------------------------------------------ W8A16 and quantiser workloads --
+# Outside the MoE layer proper, the pages' INT8 layers and the INT4 quantiser:
+#   w8a16_lm_head_decode1: lm_head [248320, 2560] INT8 gs128 at T = 1 (a GEMV, HBM-bound);
+#   w8a16_hc_prefill512:   a hyper-connection down + up pair ([320, 10240] and [10240, 320],
+#                          INT8 gs64) at T = 512, one weight pair per layer rotated over 48 layers;
+#   quantize_experts:      RTN INT4 g128 with a 50-candidate clip search over 32 experts' w1
+#                          rows ([40960, 2560] bf16), two sets rotated.
+EXTRA = {
+    "w8a16_lm_head_decode1": dict(kind="w8a16", T=1, layers=[(248320, 2560, 128)], sets=1),
+    "w8a16_hc_prefill512": dict(kind="w8a16", T=512, layers=[(320, 10240, 64), (10240, 320, 64)], sets=48),
+    "quantize_experts": dict(kind="quant", N=32 * 1280, K=2560, nclip=50, sets=2),
+}
+ISSUE_PER_SMSP = 1.0   # warp instructions issued per cycle per SM sub-partition (4 per SM)
+
+
+def recorded_counter(config: str, key: str):
+    """A per-launch counter of a committed ncu capture, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(config)
+    if not e or e.get("source_hash") != source_hash(e.get("sources", [])):
+        return None
+    return e.get(key)
+
+
+def graph_timing(args, stream, one_step, steps, local, world, copy_in=None, copy_out=None):
+    """Times `steps` replays of a one-step CUDA graph (and of a graph that adds the host
+    copies), with the clock window of measure(). Returns (ms, ms_e2e, clocks)."""
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            one_step()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            one_step()
+        ge = None
+        if copy_in is not None:
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge, stream=stream):
+                copy_in()
+                one_step()
+                copy_out()
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+        stream.synchronize()
+        barrier(world)
+        clocks = Clocks(local)
+        clocks.start()
+        w0 = time.perf_counter()
+        while (time.perf_counter() - w0) * 1e3 < args.clock_ms:
+            for _ in range(8):
+                g.replay()
+            stream.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        t1.record(stream)
+        stream.synchronize()
+        window = (time.perf_counter() - w0) * 1e3
+        ms = t0.elapsed_time(t1)
+        clk = clocks.stop()
+        if clk is not None:
+            clk["window_ms"] = round(window, 1)
+            clk["window"] = "back-to-back replays of the timed graph, ending with the timed region"
+        ms_e2e = None
+        if ge is not None:
+            for _ in range(2):
+                ge.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                ge.replay()
+            e1.record(stream)
+            stream.synchronize()
+            ms_e2e = e0.elapsed_time(e1)
+    return max_over_ranks(ms, world), (max_over_ranks(ms_e2e, world) if ms_e2e is not None else None), clk
+
+
+def measure_w8a16(args, name, steps, rank, world, local):
+    import w4a16_mixture_experts_gb300 as moe
+    moe.build()
+    moe.lib()
+    cfg = EXTRA[name]
+    T, layers, nsets = cfg["T"], cfg["layers"], cfg["sets"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    seed = args.seed + 1000 * rank
+    K0 = layers[0][1]
+    W = []
+    for s in range(nsets):
+        W.append([{k: v.to(dev) for k, v in synth.int8_weights(N, K, gs, seed=seed, layer=100 * s + j).items()}
+                  for j, (N, K, gs) in enumerate(layers)])
+    x = synth.hidden(T, K0, seed=seed).to(dev)
+    bufs = [torch.empty(T, N, dtype=torch.bfloat16, device=dev) for (N, K, gs) in layers]
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    h_in = x.cpu().pin_memory()
+    h_out = torch.empty_like(bufs[-1], device="cpu").pin_memory()
+
+    def one_step():
+        # one pass over the weight sets (the sets are consecutive layers of a model)
+        for s in range(nsets):
+            inp = x
+            for j, (N, K, gs) in enumerate(layers):
+                moe.moe_w8a16_linear(inp, W[s][j]["w_packed"], W[s][j]["scales"], gs, y=bufs[j], ws=ws)
+                inp = bufs[j]
+
+    ms, ms_e2e, clk = graph_timing(args, stream, one_step, steps, local, world,
+                                   copy_in=lambda: x.copy_(h_in, non_blocking=True),
+                                   copy_out=lambda: h_out.copy_(bufs[-1], non_blocking=True))
+    assert moe.moe_check_device_error(ws, stream) == 0
+    per_layer_ms = ms / steps / nsets
+    pk, pk_src = peaks()
+    nbytes = sum(N * K + N * (K // gs) * 2 for (N, K, gs) in layers)
+    flops = sum(2.0 * T * N * K for (N, K, gs) in layers)
+    gbs, tfl = nbytes / (per_layer_ms * 1e-3) / 1e9, flops / (per_layer_ms * 1e-3) / 1e12
+    kern = "w8a16_gemv_kernel" if T <= 8 else "prefill_kernel<true> (dense INT8 GEMM)"
+    if binding_roofline(nbytes, flops, pk["hbm_gbs"], pk["bf16_tflops"]) == "tensor":
+        roof = {"kernel": kern, "bound": "tensor", "achieved": tfl, "peak": pk["bf16_tflops"],
+                "peak_source": "%s bf16_tflops (cuBLAS bf16 dense, burst)" % pk_src, "unit": "TFLOP/s",
+                "frac": tfl / pk["bf16_tflops"], "hbm_achieved_gbs": gbs, "hbm_frac": gbs / pk["hbm_gbs"]}
+    else:
+        roof = {"kernel": kern, "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                "peak_source": pk_src + " hbm_gbs (copy)", "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                "tensor_achieved_tflops": tfl, "tensor_frac": tfl / pk["bf16_tflops"]}
+    roof.update({"traffic": recorded_counter(name, "dram_bytes_per_launch"), "algorithmic_bytes_per_launch": nbytes,
+                 "algorithmic_flops_per_launch": flops, "kernel_ms_per_launch": per_layer_ms,
+                 "launches_measured": steps * nsets,
+                 "timing": "the step's graph (the layer's launches only) over CUDA events"})
+    return {
+        "metric": "W8A16 layer tok/s (%s)" % name, "value": world * T * steps / (ms * 1e-3), "unit": "tok/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 activations x int8 weights, fp32 accumulate",
+        "data": "synthetic (seeded INT8 pack-quantized weights, N(0,1) activations)",
+        "config": {"workload": name, "T": T, "layers": [dict(N=N, K=K, gs=gs) for (N, K, gs) in layers],
+                   "weight_sets": nsets, "l2": "weights of a step exceed L2" if nbytes * nsets > L2_BYTES else
+                   "weights fit L2 (tensor-bound)", "graph": True},
+        "roofline": roof,
+        "e2e": {"value": world * T * steps / (ms_e2e * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": T * K0 * 2,
+                "d2h_bytes_per_step": bufs[-1].numel() * 2,
+                "copies": "pinned host buffers, copy in and out inside the replayed graph"},
+        "gpu_launches": steps * nsets * len(layers),
+        "clocks": clk,
+    }
+
+
+def measure_quant(args, name, steps, rank, world, local):
+    import w4a16_mixture_experts_gb300 as moe
+    moe.build()
+    moe.lib()
+    cfg = EXTRA[name]
+    N, K, nclip, nsets = cfg["N"], cfg["K"], cfg["nclip"], cfg["sets"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    seed = args.seed + 1000 * rank
+    Ws = [synth.bf16_weights(N, K, seed=seed, layer=s).to(dev) for s in range(nsets)]
+    packed = torch.empty(N, K // 8, dtype=torch.int32, device=dev)
+    scales = torch.empty(N, K // 128, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    h_in = Ws[0].cpu().pin_memory()
+    h_out = torch.empty_like(packed, device="cpu").pin_memory()
+
+    def one_step():
+        for s in range(nsets):
+            lib = moe.lib()
+            rc = lib.moe_quantize_int4(moe._p(Ws[s]), N, K, nclip, moe._p(packed), moe._p(scales), None,
+                                       moe._stream(None))
+            assert rc == 0
+
+    ms, ms_e2e, clk = graph_timing(args, stream, one_step, steps, local, world,
+                                   copy_in=lambda: Ws[0].copy_(h_in, non_blocking=True),
+                                   copy_out=lambda: h_out.copy_(packed, non_blocking=True))
+    per_launch_ms = ms / steps / nsets
+    pk, pk_src = peaks()
+    weights = N * K
+    inst = recorded_counter(name, "warp_instructions_per_launch")
+    clock_mhz = (clk or {}).get("sm_mhz") or pk.get("sm_max_mhz", 2070.0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_issue = sms * 4 * ISSUE_PER_SMSP * clock_mhz * 1e6   # warp instructions per second
+    roof = {"kernel": "quantize_int4_kernel", "bound": "alu",
+            "achieved": inst / (per_launch_ms * 1e-3) if inst else None,
+            "peak": peak_issue, "unit": "warp instructions/s",
+            "peak_source": "%d SMs x 4 sub-partitions x 1 warp instruction/cycle x %.0f MHz (sampled)" % (sms, clock_mhz),
+            "frac": inst / (per_launch_ms * 1e-3) / peak_issue if inst else None,
+            "warp_instructions_per_launch": inst,
+            "candidate_evaluations_per_s": weights * nclip / (per_launch_ms * 1e-3),
+            "hbm_bytes_per_launch": weights * 2 + weights // 2 + (weights // 128) * 2,
+            "hbm_frac": (weights * 2 + weights // 2 + (weights // 128) * 2) / (per_launch_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "traffic": recorded_counter(name, "dram_bytes_per_launch"), "kernel_ms_per_launch": per_launch_ms,
+            "launches_measured": steps * nsets}
+    return {
+        "metric": "INT4 quantiser weights/s (%s)" % name, "value": world * weights * nsets * steps / (ms * 1e-3),
+        "unit": "weights/s", "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 search, int4 out",
+        "data": "synthetic (seeded N(0, 0.02^2) bf16 weights with outliers)",
+        "config": {"workload": name, "N": N, "K": K, "nclip": nclip, "sets": nsets,
+                   "l2": "%d sets of %d MB rotated (> L2)" % (nsets, N * K * 2 >> 20), "graph": True},
+        "roofline": roof,
+        "e2e": {"value": world * weights * steps / (ms_e2e * 1e-3), "unit": "weights/s",
+                "h2d_bytes_per_step": N * K * 2, "d2h_bytes_per_step": N * K // 2,
+                "copies": "one weight set in and its packed words out, pinned host buffers, inside the graph",
+                "note": "the e2e step quantises the %d sets once each after the copy" % nsets},
+        "gpu_launches": steps * nsets,
+        "clocks": clk,
+    }
+
+
+def cpu_baseline_extra(name, seed, target_s):
+    """The oracle on a bounded sample of an EXTRA workload, scaled to its unit."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    cfg = EXTRA[name]
+    if cfg["kind"] == "w8a16":
+        T = cfg["T"]
+        # time each layer on a sample of its rows (T = 1) or of the tokens (T > 1), then scale up
+        total, parts = 0.0, []
+        for (N, K, gs) in cfg["layers"]:
+            n = min(N, 4096) if T == 1 else N
+            t_tok = T if T == 1 else min(T, 16)
+            d = synth.int8_weights(n, K, gs, seed=seed)
+            x = synth.hidden(t_tok, K, seed=seed)
+            t0 = time.perf_counter()
+            oracle.w8a16_linear(x, d["w_packed"], d["scales"], gs)
+            dt = time.perf_counter() - t0
+            total += dt * (N / n) * (T / t_tok)
+            parts.append("%d of %d rows x %d of %d tokens" % (n, N, t_tok, T))
+        nsets = cfg["sets"]
+        return {"value": T / (total * nsets), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                "sample": "fp64 oracle on " + "; ".join(parts) + ", scaled to the whole layer%s" %
+                          (" and to the %d layers of a step" % nsets if nsets > 1 else "")}
+    N, K, nclip = cfg["N"], cfg["K"], cfg["nclip"]
+    n = 64
+    w = synth.bf16_weights(n, K, seed=seed)
+    t0 = time.perf_counter()
+    oracle.quantize_int4(w, nclip)
+    dt = time.perf_counter() - t0
+    n = max(n, min(N, int(n * target_s / max(dt, 1e-3))))
+    w = synth.bf16_weights(n, K, seed=seed)
+    t0 = time.perf_counter()
+    oracle.quantize_int4(w, nclip)
+    dt = time.perf_counter() - t0
+    return {"value": n * K / dt, "unit": "weights/s", "cores": cores, "kind": "oracle",
+            "sample": "%d rows x %d of the quantiser input, %d clip candidates, %.1f s" % (n, K, nclip, dt)}
+
+
 # Workloads measured beside the headline one in a default run: the metric's other
 # two batch sizes (64 concurrent decode tokens; the 4096-token prefill on the
 # 48-layer stack).
-PER_CONFIG = ("decode64", "stack_prefill4096")
+PER_CONFIG = ("decode64", "stack_prefill4096", "shared_decode1", "w8a16_lm_head_decode1", "w8a16_hc_prefill512",
+              "quantize_experts")
+
+
+def measure_any(args, name, steps, rank, world, local):
+    if name in EXTRA:
+        fn = measure_w8a16 if EXTRA[name]["kind"] == "w8a16" else measure_quant
+        return fn(args, name, steps, rank, world, local)
+    return measure(args, synth.WORKLOADS[name], steps, rank, world, local)
 
 
 def run_ours(args, rank, world, local):
-    wl = synth.WORKLOADS[args.config]
-    res = measure(args, wl, args.steps, rank, world, local)
+    res = measure_any(args, args.config, args.steps, rank, world, local)
     if args.per_config and args.config == "decode1":
         res["per_config"] = {}
         for name in PER_CONFIG:
             torch.cuda.empty_cache()
-            r = measure(args, synth.WORKLOADS[name], args.steps, rank, world, local)
-            res["per_config"][name] = r
+            res["per_config"][name] = measure_any(args, name, args.steps, rank, world, local)
             torch.cuda.empty_cache()
     return res
 
 
+def baseline_any(name, seed, target_s):
+    if name in EXTRA:
+        return cpu_baseline_extra(name, seed, target_s)
+    return cpu_baseline(synth.WORKLOADS[name], seed, target_s)
+
+
 def main():
     args = parse()
-    wl = synth.WORKLOADS[args.config]
     if args.impl == "reference":
         # the oracle on the host cores: rank 0 alone runs it, the other ranks leave at once
         rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
         if rank == 0:
-            cb = cpu_baseline(wl, args.seed, args.cpu_seconds)
-            line = {"impl": "reference", "metric": "MoE layer tok/s (%s)" % wl.name, "value": cb["value"],
-                    "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            cb = baseline_any(args.config, args.seed, args.cpu_seconds)
+            metric = ("MoE layer tok/s (%s)" % args.config if args.config in synth.WORKLOADS else
+                      ("W8A16 layer tok/s (%s)" if EXTRA[args.config]["kind"] == "w8a16" else
+                       "INT4 quantiser weights/s (%s)") % args.config)
+            line = {"impl": "reference", "metric": metric, "value": cb["value"],
+                    "unit": cb["unit"], "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                    "data": "synthetic", "config": {"workload": wl.name},
+                    "data": "synthetic", "config": {"workload": args.config},
                     "cpu_baseline": cb,
-                    "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
             print(json.dumps(line), flush=True)
         return
     rank, world, local = dist_setup(args)
     res = run_ours(args, rank, world, local)
     if rank == 0:
-        res["cpu_baseline"] = cpu_baseline(wl, args.seed, args.cpu_seconds)
+        res["cpu_baseline"] = baseline_any(args.config, args.seed, args.cpu_seconds)
         for name, r in res.get("per_config", {}).items():
-            r["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[name], args.seed, args.cpu_seconds / 2)
+            r["cpu_baseline"] = baseline_any(name, args.seed, args.cpu_seconds / 2)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

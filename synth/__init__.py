@@ -59,6 +59,7 @@ class Workload:
     dims: Dims
     zipf: float | None = None   # exponent of the router-bias ranking, or None
     layers: int = 1
+    shared: bool = False        # a shared expert beside the routed ones (router row E, expert E)
 
 
 # The five workloads: tiny layer; one full-shape layer at decode T=1, 4, 64;
@@ -73,6 +74,8 @@ WORKLOADS = {
     "prefill512": Workload("prefill512", Dims(T=512, **FULL), zipf=1.1),
     "stack_prefill4096": Workload("stack_prefill4096", Dims(T=4096, **FULL), layers=48),
     "stack_decode4": Workload("stack_decode4", Dims(T=4, **FULL), layers=48),
+    # the layer with its shared expert (intermediate 640 like a routed one) at decode T = 1
+    "shared_decode1": Workload("shared_decode1", Dims(T=1, **FULL), shared=True),
 }
 
 
