@@ -20,13 +20,16 @@
 // g + 8, four steps ahead of use; the rows are the M = 16 side of
 // mma.sync m16n8k16 and the tokens the N = 8 side; each group's fp32 partial
 // product is scaled by the group's bf16 scale. x is staged once per CTA in
-// shared memory.
+// shared memory. Layers with few rows (the hyper-connection mixer [320, 10240]
+// has 20 blocks of 16 rows) split K: the 16 warps of a CTA take 16 / S blocks,
+// S warps each on consecutive ranges of whole scale groups, and the S partial
+// results of a block are summed in shared memory in a fixed order.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 
-constexpr int kW8Warps = 8;
+constexpr int kW8Warps = 16;
 constexpr int kW8Ahead = 4;          // 16-byte weight loads per row in flight per lane
 constexpr int kW8MaxSmem = 196608;   // bytes of staged x (T x K bf16)
 
@@ -47,6 +50,7 @@ struct W8Params {
     const uint16_t *s;      // bf16 [N][K/gs]
     uint16_t *y;            // bf16 [T][N]
     int T, N, K, gs;
+    int split;              // warps per 16-row block (a power of two <= kW8Warps)
 };
 
 // One warp per 16-row block (grid-stride over blocks). In each 64-wide K step,
@@ -58,7 +62,7 @@ struct W8Params {
 // k-step's 16 K values once; A and B agree, so the products are the dot
 // product's.) x rows are staged with a stride of K + 8, so that the eight
 // tokens' loads fall in different banks.
-__global__ void __launch_bounds__(kW8Warps * 32) w8a16_gemv_kernel(const __grid_constant__ W8Params p) {
+__global__ void __launch_bounds__(kW8Warps * 32, 2) w8a16_gemv_kernel(const __grid_constant__ W8Params p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, tig = lane & 3;
@@ -75,12 +79,19 @@ __global__ void __launch_bounds__(kW8Warps * 32) w8a16_gemv_kernel(const __grid_
     }
     __syncthreads();
     const uint16_t *xs = reinterpret_cast<const uint16_t *>(smem);
+    float4 *part = reinterpret_cast<float4 *>(smem + (size_t)p.T * kp * 2);   // [kW8Warps][32] partial sums
     const int tok = g < p.T ? g : 0;   // columns past T read token 0 and are not stored
-    const int nsteps = p.K / 64, steps_per_group = p.gs / 64;
+    const int steps_per_group = p.gs / 64;
     const int G = p.K / p.gs;
     const int nblocks = (p.N + 15) / 16;
+    const int S = p.split, bpc = kW8Warps / S;    // warps per block, blocks per CTA pass
+    const int piece = warp % S;
+    // this warp's K range: scale groups [G piece / S, G (piece + 1) / S)
+    const int st_lo = (G * piece / S) * steps_per_group, st_hi = (G * (piece + 1) / S) * steps_per_group;
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
-    for (int blk = blockIdx.x * kW8Warps + warp; blk < nblocks; blk += gridDim.x * kW8Warps) {
+    const int npass = (nblocks + bpc - 1) / bpc;
+    for (int pass = blockIdx.x; pass < npass; pass += gridDim.x) {
+        const int blk = pass * bpc + warp / S;
         const int r0 = blk * 16 + g, r1 = r0 + 8;
         const bool v0 = r0 < p.N, v1 = r1 < p.N;
         const uint4 *w0 = reinterpret_cast<const uint4 *>(p.w + (size_t)(v0 ? r0 : 0) * (p.K / 4)) + tig;
@@ -88,18 +99,18 @@ __global__ void __launch_bounds__(kW8Warps * 32) w8a16_gemv_kernel(const __grid_
         uint4 ring0[kW8Ahead], ring1[kW8Ahead];
 #pragma unroll
         for (int a = 0; a < kW8Ahead; ++a) {
-            ring0[a] = a < nsteps && v0 ? ld_nc_v4(w0 + 4 * a) : zero4;
-            ring1[a] = a < nsteps && v1 ? ld_nc_v4(w1 + 4 * a) : zero4;
+            ring0[a] = st_lo + a < st_hi && v0 ? ld_nc_v4(w0 + 4 * (st_lo + a)) : zero4;
+            ring1[a] = st_lo + a < st_hi && v1 ? ld_nc_v4(w1 + 4 * (st_lo + a)) : zero4;
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         float cc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int st0 = 0; st0 < nsteps; st0 += kW8Ahead) {
+        for (int st0 = st_lo; st0 < st_hi; st0 += kW8Ahead) {
 #pragma unroll
             for (int a = 0; a < kW8Ahead; ++a) {
                 const int st = st0 + a;
-                if (st < nsteps) {
+                if (st < st_hi) {
                     const uint4 q0 = ring0[a], q1 = ring1[a];
-                    if (st + kW8Ahead < nsteps) {
+                    if (st + kW8Ahead < st_hi) {
                         ring0[a] = v0 ? ld_nc_v4(w0 + 4 * (st + kW8Ahead)) : zero4;
                         ring1[a] = v1 ? ld_nc_v4(w1 + 4 * (st + kW8Ahead)) : zero4;
                     }
@@ -126,6 +137,20 @@ __global__ void __launch_bounds__(kW8Warps * 32) w8a16_gemv_kernel(const __grid_
                 }
             }
         }
+        // the block's S partial results, summed in piece order by the warp of piece 0
+        if (S > 1) {
+            part[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            __syncthreads();
+            if (piece == 0) {
+#pragma unroll 1
+                for (int j = 1; j < S; ++j) {
+                    const float4 o = part[(warp + j) * 32 + lane];
+                    acc[0] += o.x, acc[1] += o.y, acc[2] += o.z, acc[3] += o.w;
+                }
+            }
+            __syncthreads();
+            if (piece != 0) continue;
+        }
         // acc: (row g, tokens 2 tig, 2 tig + 1), (row g + 8, same tokens)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -146,17 +171,28 @@ __global__ void __launch_bounds__(kW8Warps * 32) w8a16_gemv_kernel(const __grid_
 
 bool w8a16_gemv_supported(int T, int K) { return T >= 1 && T <= 8 && (size_t)T * (K + 8) * 2 <= kW8MaxSmem; }
 
+// Warps per 16-row block: enough blocks x warps to give every SM's warps work,
+// never more pieces than scale groups.
+static int w8a16_split(int N, int K, int gs) {
+    const int nblocks = (N + 15) / 16, G = K / gs;
+    int S = 1;
+    while (S < kW8Warps && (long long)nblocks * S < 2LL * kW8Warps * sm_count() && 2 * S <= G) S *= 2;
+    return S;
+}
+
 cudaError_t launch_w8a16(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
                          int K, cudaStream_t st) {
     if (T == 0 || N == 0) return cudaSuccess;
     if (!w8a16_gemv_supported(T, K)) return cudaErrorInvalidValue;
-    W8Params p{x, reinterpret_cast<const uint32_t *>(w), s, y, T, N, K, gs};
-    const int smem = T * (K + 8) * 2;
-    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(w8a16_gemv_kernel), kW8MaxSmem);
+    const int S = w8a16_split(N, K, gs);
+    W8Params p{x, reinterpret_cast<const uint32_t *>(w), s, y, T, N, K, gs, S};
+    const int smem = T * (K + 8) * 2 + kW8Warps * 32 * 16;
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(w8a16_gemv_kernel), kW8MaxSmem + kW8Warps * 32 * 16);
     if (err != cudaSuccess) return err;
-    const int nblocks = (N + 15) / 16;
-    // enough warps to keep every SM's loads in flight, no more CTAs than blocks of rows need
-    long long grid = (nblocks + kW8Warps - 1) / kW8Warps;
+    const int nblocks = (N + 15) / 16, bpc = kW8Warps / S;
+    // two CTAs of 16 warps per SM (registers capped for it: measured 12% faster than one
+    // CTA per SM on lm_head), no more than the blocks need
+    long long grid = (nblocks + bpc - 1) / bpc;
     const long long cap = 2LL * sm_count();
     if (grid > cap) grid = cap;
     w8a16_gemv_kernel<<<(unsigned)grid, kW8Warps * 32, smem, st>>>(p);
