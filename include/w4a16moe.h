@@ -233,13 +233,20 @@ MOE_API int moe_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed
  * 65536); T <= 2^20.
  *  - 1 <= T <= 8: the decode GEMV (weights streamed from HBM, mma.sync), when
  *    T * (K + 8) * 2 <= 196608 (else MOE_ERR_UNSUPPORTED). ws may be NULL.
- *  - T > 8: the tcgen05 GEMM (tiles of 128 rows x 128 tokens). ws: at least
- *    256 bytes, 16-byte aligned, zero before its first use; it holds the error
- *    word that moe_check_device_error reads (a bounded wait that gave up).
+ *  - T > 8: the tcgen05 GEMM (tiles of 128 rows x 128 tokens; a layer with
+ *    fewer tiles than SMs is split over K, and the splits are summed in a
+ *    fixed order). ws: at least moe_w8a16_workspace_size() bytes, 16-byte
+ *    aligned, its first 256 bytes zero before its first use: they hold the
+ *    error word that moe_check_device_error reads (a bounded wait that gave
+ *    up); the rest holds the splits' f32 results.
  * T = 0 or N = 0 return MOE_OK with nothing enqueued.
  */
 MOE_API int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t *scales, int32_t gs,
                      uint16_t *y, int32_t T, int32_t N, int32_t K, void *ws, size_t ws_bytes, void *stream);
+
+/* Workspace bytes moe_w8a16_linear needs for these dims (256 for the GEMV and
+ * for GEMMs that are not split). Returns MOE_ERR_INVALID_ARG for bad dims. */
+MOE_API int moe_w8a16_workspace_size(int32_t T, int32_t N, int32_t K, int32_t gs, size_t *bytes);
 
 /*
  * INT4 quantiser of BF16 weights into the experts' storage ("vLLM

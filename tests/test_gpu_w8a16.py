@@ -82,14 +82,14 @@ def test_w8a16_every_byte_value():
 
 
 @pytest.mark.parametrize("T,N,K,gs", [
-    (512, 320, 10240, 64),    # the pages' batch: hyper-connection down mixer at 512 tokens
+    (512, 320, 10240, 64),    # the pages' batch: hyper-connection down mixer at 512 tokens (split over K)
     (512, 10240, 320, 64),    # up mixer: K = 320, the last 128-wide stage half full
     (9, 1000, 2560, 128),     # just above the GEMV, ragged rows
     (300, 2048, 2560, 128),   # lm_head rows, ragged token chunk
     (129, 130, 256, 64),      # one token past a chunk, two rows past a block
 ])
 def test_w8a16_gemm_parity(T, N, K, gs):
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.moe_w8a16_workspace_size(T, N, K, gs), dtype=torch.uint8, device="cuda")
     d = synth.int8_weights(N, K, gs, seed=T + N + K)
     x = synth.hidden(T, K, seed=T + N + K)
     y = moe.moe_w8a16_linear(x.cuda(), d["w_packed"].cuda(), d["scales"].cuda(), gs, ws=ws).float().cpu().numpy()
@@ -115,3 +115,17 @@ def test_w8a16_empty_batch():
     s = torch.ones(16, 1, dtype=torch.bfloat16, device="cuda")
     y = moe.moe_w8a16_linear(torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"), w, s, 64)
     assert y.shape == (0, 16)
+
+
+def test_w8a16_split_gemm_is_deterministic():
+    # the splits over K are summed in a fixed order: two calls give the same bits
+    T, N, K, gs = 256, 256, 8192, 64
+    assert moe.moe_w8a16_workspace_size(T, N, K, gs) > 256, "this shape should split over K"
+    d = synth.int8_weights(N, K, gs, seed=5)
+    x = synth.hidden(T, K, seed=5).cuda()
+    W = (d["w_packed"].cuda(), d["scales"].cuda())
+    a = moe.moe_w8a16_linear(x, *W, gs)
+    b = moe.moe_w8a16_linear(x, *W, gs)
+    assert torch.equal(a, b)
+    ref = oracle.w8a16_linear(x.cpu(), d["w_packed"], d["scales"], gs)
+    assert np.abs(a.float().cpu().numpy() - ref).max() <= OUT_TOL * np.abs(ref).max()

@@ -123,6 +123,13 @@ def test_argument_errors_are_synchronous(L):
                               ctypes.c_void_p(good[3]), 64, 16, 256, None, 0, None) == 1
     assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 64,
                               ctypes.c_void_p(good[3]), 64, 16, 256, ctypes.c_void_p(good[4]), 128, None) == 3
+    # the split GEMM needs its partial results' room: less than the reported size is refused
+    need = moe.moe_w8a16_workspace_size(512, 320, 10240, 64)
+    assert need >= 256 + 2 * 512 * 320 * 4
+    assert L.moe_w8a16_linear(ctypes.c_void_p(good[0]), ctypes.c_void_p(good[1]), ctypes.c_void_p(good[2]), 64,
+                              ctypes.c_void_p(good[3]), 512, 320, 10240, ctypes.c_void_p(good[4]), need - 16,
+                              None) == 3
+    assert moe.moe_w8a16_workspace_size(1, 320, 10240, 64) == 256
     # shared-expert routing: k + 1 must stay within 32 slots, E + 1 within 1024 experts
     assert L.moe_route_shared(*[ctypes.c_void_p(p) for p in good[:3]], moe.moe_dims(4, 256, 64, 32, 128),
                               ctypes.c_void_p(good[3]), ctypes.c_void_p(good[4]), ctypes.c_void_p(good[5]),

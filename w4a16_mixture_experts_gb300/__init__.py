@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "MoeError", "moe_dims", "lib", "build", "moe_status_str", "moe_version", "moe_workspace_size",
     "workspace", "moe_route", "moe_route_shared", "shared_workspace", "moe_w4a16_forward", "moe_w4a16_forward_rms", "moe_permute",
-    "moe_pack_int4", "moe_quantize_int4", "moe_w8a16_linear", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
+    "moe_pack_int4", "moe_quantize_int4", "moe_w8a16_linear", "moe_w8a16_workspace_size", "moe_check_device_error", "moe_profile_events", "moe_w4a16_forward_noalloc",
     "moe_noalloc_check_device_error", "moe_forward_plan", "STATUS",
 ]
 
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.moe_w8a16_linear.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, Z,
                                        P]
         L.moe_w8a16_linear.restype = I
+        L.moe_w8a16_workspace_size.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(Z)]
+        L.moe_w8a16_workspace_size.restype = I
         L.moe_check_device_error.argtypes, L.moe_check_device_error.restype = [P, Z, P], I
         L.moe_noalloc_check_device_error.argtypes, L.moe_noalloc_check_device_error.restype = [P], I
         L.moe_profile_events.argtypes, L.moe_profile_events.restype = [P, P], I
@@ -308,8 +310,8 @@ def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None
 def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, ws=None, stream=None):
     """bf16 y [T, N] = x . W^T for INT8 pack-quantized W (q + 128, four per int32 word, LSB first)
     with bf16 scales per gs (64 or 128) values of K. T <= 8: the decode GEMV; larger T: the
-    tensor-core GEMM, whose error word lives in ws (a zeroed uint8 tensor of >= 256 bytes;
-    allocated here when not given)."""
+    tensor-core GEMM, whose error word (and split partial results) live in ws (a zeroed uint8
+    tensor of moe_w8a16_workspace_size bytes; allocated here when not given)."""
     _need(x, "x", torch.bfloat16, 2)
     _need(w_packed, "w_packed", torch.int32, 2)
     _need(scales, "scales", torch.bfloat16, 2)
@@ -320,11 +322,17 @@ def moe_w8a16_linear(x, w_packed, scales, gs: int, y=None, ws=None, stream=None)
     if y is None:
         y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
     if ws is None and T > 8:
-        ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+        ws = torch.zeros(moe_w8a16_workspace_size(T, N, K, gs), dtype=torch.uint8, device=x.device)
     nbytes = 0 if ws is None else ws.numel()
     _check(lib().moe_w8a16_linear(_p(x), _p(w_packed), _p(scales), gs, _p(y), T, N, K, _p(ws), nbytes,
                                   _stream(stream)), "moe_w8a16_linear")
     return y
+
+
+def moe_w8a16_workspace_size(T: int, N: int, K: int, gs: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_w8a16_workspace_size(T, N, K, gs, ctypes.byref(n)), "moe_w8a16_workspace_size")
+    return n.value
 
 
 def moe_profile_events(before=None, after=None):

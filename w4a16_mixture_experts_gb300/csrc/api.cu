@@ -258,10 +258,25 @@ int moe_w8a16_linear(const uint16_t *x, const int32_t *w_packed, const uint16_t 
         if (!w8a16_gemv_supported(T, K)) return MOE_ERR_UNSUPPORTED;
         return cuda_status(launch_w8a16(x, w_packed, scales, gs, y, T, N, K, s));
     }
-    // the tensor-core GEMM records a wait that gave up in the workspace's error word
+    // the tensor-core GEMM records a wait that gave up in the workspace's error word, and
+    // keeps the partial results of a split over K after it
     if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
-    if (ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
-    return cuda_status(launch_w8a16_gemm(x, w_packed, scales, gs, y, T, N, K, reinterpret_cast<Ctrl *>(ws), s));
+    size_t need = 0;
+    moe_w8a16_workspace_size(T, N, K, gs, &need);
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_w8a16_gemm(x, w_packed, scales, gs, y, T, N, K, reinterpret_cast<Ctrl *>(ws),
+                                         ws_at<float>(ws, sizeof(Ctrl)), s));
+}
+
+int moe_w8a16_workspace_size(int32_t T, int32_t N, int32_t K, int32_t gs, size_t *bytes) {
+    if (!bytes || T < 0 || N < 0 || K <= 0 || (gs != 64 && gs != 128) || K % gs) return MOE_ERR_INVALID_ARG;
+    size_t n = sizeof(Ctrl);
+    if (T > 8 && N > 0) {
+        const int S = w8a16_gemm_splits(T, N, K);
+        if (S > 1) n += (size_t)S * T * N * 4;
+    }
+    *bytes = n;
+    return MOE_OK;
 }
 
 int moe_profile_events(void *before_experts, void *after_experts) {

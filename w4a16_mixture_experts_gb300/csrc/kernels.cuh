@@ -69,8 +69,11 @@ bool w8a16_gemv_supported(int T, int K);
 cudaError_t launch_w8a16(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
                          int K, cudaStream_t st);
 // ... and the tensor-core GEMM for larger T (prefill.cu, the INT8 instantiation).
+// K is split over CTAs when the layer has fewer tiles than SMs; the splits' f32
+// results go to part [splits][T][N] (the workspace after the control block).
+int w8a16_gemm_splits(int T, int N, int K);
 cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
-                              int K, struct Ctrl *ctrl, cudaStream_t st);
+                              int K, struct Ctrl *ctrl, float *part, cudaStream_t st);
 
 cudaError_t launch_pack_int4(const int8_t *q, int64_t N, int64_t K, int32_t *packed, int32_t *bad,
                              cudaStream_t s);

@@ -118,7 +118,9 @@ struct PrefillParams {
     const uint16_t *xs;        // gate_up input, bf16 [T*k][H] fragment order
     float *out_acc;            // down output, f32 [T][H]
     uint16_t *y;               // W8A16 output, bf16 [T][N]
+    float *part;               // W8A16 split over K: f32 [ksplit][T][N] partial results
     int N, gs, dense_chunks;   // W8A16: output features, scale group, token chunks of 128
+    int ksplit;                // W8A16: splits of K (1: the tile covers all of K)
     int T, H, E, k, I;
     int K;                     // reduction length: H (gate_up) or I (down)
     int mb;                    // row blocks per expert: I/64 (gate_up) or H/128 (down)
@@ -136,10 +138,25 @@ struct Tile {
 template <bool kW8>
 __device__ inline int4 chunk_of(const PrefillParams &p, int t) {
     if constexpr (kW8) {
-        const int c = t / p.mb;
+        const int c = (t / p.mb) % p.dense_chunks;
         return make_int4(0, c * kPN, min(kPN, p.T - c * kPN), 0);
     } else {
         return __ldg(p.chunk_info + t / p.mb);
+    }
+}
+
+// Stages [ks0, ks1) of tile t: all of K, or, for the dense GEMM split over K
+// (tiles t = split * (row blocks * chunks) + chunk * row blocks + row block),
+// the split's share.
+template <bool kW8>
+__device__ inline void tile_kspan(const PrefillParams &p, int t, int G, int &ks0, int &ks1) {
+    if constexpr (kW8) {
+        const int s = t / (p.mb * p.dense_chunks);
+        ks0 = G * s / p.ksplit;
+        ks1 = G * (s + 1) / p.ksplit;
+    } else {
+        ks0 = 0;
+        ks1 = G;
     }
 }
 
@@ -286,7 +303,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int ntiles = kW8 ? p.dense_chunks * p.mb : *p.n_chunks * p.mb;
+    const int ntiles = kW8 ? p.ksplit * p.dense_chunks * p.mb : *p.n_chunks * p.mb;
     const int G = (p.K + kKS - 1) / kKS;   // stages per tile (the dense GEMM's last one may be half)
 
     if (kW8 && warp < kWEpi) {
@@ -304,7 +321,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const int n = (t % p.mb) * 128 + r;   // this thread's weight row (output feature)
             const uint16_t *srow = p.scales + (size_t)(n < p.N ? n : 0) * nG;
             bool ok = true;
-            for (int ks = 0; ks < G; ++ks, ++g) {
+            int ks0, ks1;
+            tile_kspan<kW8>(p, t, G, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g) {
                 if ((int)(g & 1) != grp) continue;
                 const int sr = g % kRing, sa = g % kRS;
                 const int q0 = ks * kKS / p.gs, q1 = p.gs == kKS ? q0 : q0 + 1;
@@ -351,7 +370,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             if (!pwait(&sc_full[tb], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
             const uint16_t *sc = sSc + tb * (L.sc_bytes / 2) + (half * 64 + br) * G;
             bool ok = true;
-            for (int ks = 0; ks < G; ++ks, ++g) {
+            int ks0, ks1;
+            tile_kspan<kW8>(p, t, G, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g) {
                 if ((int)(g & 1) != grp) continue;
                 const int sr = g % kRR, sa = g % kRS;
                 if (!pwait(&raw_full[sr], (g / kRR) & 1, abort_flag)) { ok = false; break; }
@@ -410,20 +431,29 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kNEpi) : "memory");
             if (kW8) {
-                // y[token][n]: for each column the 32 lanes of a warp store 32 consecutive n
+                // y[token][n] (or, split over K, this split's f32 part): for each column the 32
+                // lanes of a warp store 32 consecutive n
                 const int n = T.m * 128 + et;
+                const int split = t / (p.mb * p.dense_chunks);
                 for (int c0 = 32 * eh; c0 < T.nv; c0 += 64) {
                     float v[32];
                     tc::ld_32x32b_x32(dbase + c0, v);
                     tc::wait_ld();
                     const int nu = min(32, T.nv - c0);
                     if (n < p.N) {
+                        if (p.ksplit > 1) {
+                            float *prow = p.part + ((size_t)split * p.T + T.s0 + c0) * p.N + n;
 #pragma unroll
-                        for (int u = 0; u < 32; ++u)
-                            if (u < nu) {
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(v[u]);
-                                p.y[(size_t)(T.s0 + c0 + u) * p.N + n] = *reinterpret_cast<const uint16_t *>(&hb);
-                            }
+                            for (int u = 0; u < 32; ++u)
+                                if (u < nu) prow[(size_t)u * p.N] = v[u];
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 32; ++u)
+                                if (u < nu) {
+                                    const __nv_bfloat16 hb = __float2bfloat16_rn(v[u]);
+                                    p.y[(size_t)(T.s0 + c0 + u) * p.N + n] = *reinterpret_cast<const uint16_t *>(&hb);
+                                }
+                        }
                     }
                 }
             } else if (p.down) {
@@ -487,7 +517,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     bulk_g2s(dst + 64 * G, p.scales + (size_t)row_b * G, 64 * G * 2, &sc_full[tb]);
                 }
                 bool ok = true;
-                for (int ks = 0; ks < G; ++ks, ++g) {
+                int ks0, ks1;
+            tile_kspan<kW8>(p, t, G, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g) {
                     const int sr = g % kRing;
                     if (!pwait(&raw_empty[sr], ((g / kRing) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&raw_full[sr], kStageBytes);
@@ -522,7 +554,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 const int t2 = t + 2 * grid;   // the tile after next
                 if (t2 < ntiles) ci2 = chunk_of<kW8>(p, t2);
                 bool ok = true;
-                for (int ks = 0; ks < G; ++ks, ++g) {
+                int ks0, ks1;
+            tile_kspan<kW8>(p, t, G, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g) {
                     const int sb = g % kRS;
                     if (!pwait(&ab_empty[sb], ((g / kRS) & 1) ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&b_full[sb], 2u * T.n16 * 128u);
@@ -569,7 +603,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const uint32_t d = tmem + b * kPN;
             const uint32_t idesc = tc::idesc_bf16(128, T.n16);
             bool ok = true;
-            for (int ks = 0; ks < G; ++ks, ++g) {
+            int ks0, ks1;
+            tile_kspan<kW8>(p, t, G, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g) {
                 const int s = g % kRS;
                 const uint32_t par = (g / kRS) & 1;
                 const bool ready = pwait(&a_full[s], par, abort_flag) && pwait(&b_full[s], par, abort_flag);
@@ -585,7 +621,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         tc::mma_ts(d, a0 + kk * 8, (kk < 4 ? bd0 : bd1) + (uint64_t)((kk & 3) * 2), idesc,
-                                   (ks | kk) != 0);
+                                   ks != ks0 || kk != 0);
                     tc::commit(&ab_empty[s]);   // one commit: A slot and activation stage share the index
                 }
                 __syncwarp();
@@ -864,8 +900,35 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
 
 // The W8A16 linear layer for batches: the dense INT8 instantiation, x and y the
 // caller's (token chunks of 128 consecutive tokens, row blocks of 128 weight rows).
+// A layer with fewer tiles than SMs (the hyper-connection mixer [320, 10240] at
+// 512 tokens has 12) splits K so that about one wave of CTAs runs, each split at
+// least kMinSplitStages stages long; the splits' f32 results are summed in split
+// order (deterministic) by w8a16_reduce_kernel.
+constexpr int kMinSplitStages = 4;
+// The split aims at one wave of CTAs on a 152-SM GB300; it is fixed rather than
+// read from the device so that the workspace size does not depend on it.
+constexpr int kSplitWave = 148;
+
+int w8a16_gemm_splits(int T, int N, int K) {
+    const long long tiles = (long long)((N + 127) / 128) * ((T + kPN - 1) / kPN);
+    const int G = (K + kKS - 1) / kKS;
+    long long s = kSplitWave / (tiles > 0 ? tiles : 1);
+    if (s > G / kMinSplitStages) s = G / kMinSplitStages;
+    return s < 1 ? 1 : (int)s;
+}
+
+__global__ void __launch_bounds__(256) w8a16_reduce_kernel(const float *__restrict__ part, int S, size_t n,
+                                                          uint16_t *__restrict__ y) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int j = 0; j < S; ++j) s += __ldcg(part + (size_t)j * n + i);
+        const __nv_bfloat16 h = __float2bfloat16_rn(s);
+        y[i] = *reinterpret_cast<const uint16_t *>(&h);
+    }
+}
+
 cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
-                              int K, Ctrl *ctrl, cudaStream_t st) {
+                              int K, Ctrl *ctrl, float *part, cudaStream_t st) {
     cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<true>), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
     PrefillParams p{};
@@ -877,20 +940,30 @@ cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_
     if (err != cudaSuccess) return err;
     p.scales = s;
     p.y = y;
+    p.part = part;
     p.N = N;
     p.gs = gs;
     p.T = T;
     p.K = K;
     p.mb = (N + 127) / 128;
     p.dense_chunks = (T + kPN - 1) / kPN;
+    p.ksplit = w8a16_gemm_splits(T, N, K);
     p.down = 1;
     p.ctrl = ctrl;
     p.ctrl_rw = ctrl;
     p.L = prefill_layout(0);
-    const long long tiles = (long long)p.mb * p.dense_chunks;
+    const long long tiles = (long long)p.ksplit * p.mb * p.dense_chunks;
     const unsigned grid = (unsigned)(tiles < sm_count() ? tiles : sm_count());
     prefill_kernel<true><<<grid, kPThreads, p.L.total, st>>>(p);
-    return cudaGetLastError();
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (p.ksplit > 1) {
+        const size_t n = (size_t)T * N;
+        const long long blocks = (long long)((n + 255) / 256);
+        w8a16_reduce_kernel<<<(unsigned)(blocks < 8LL * sm_count() ? blocks : 8LL * sm_count()), 256, 0, st>>>(
+            part, p.ksplit, n, y);
+        err = cudaGetLastError();
+    }
+    return err;
 }
 
 }  // namespace moe
