@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--sets", type=int, default=0, help="weight sets to rotate over (0: enough to exceed L2)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers of a stack workload (0: its own, 48); fewer only to profile a small case")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU-baseline sample")
     ap.add_argument("--clock-ms", type=float, default=1000.0,
@@ -262,7 +264,10 @@ def launches_per_layer(T: int, E: int) -> int:
 
 def measure(args, wl, steps, rank, world, local):
     """Times `steps` steps of workload wl on this rank; returns the JSON fields."""
+    import dataclasses
     import w4a16_mixture_experts_gb300 as moe
+    if wl.layers > 1 and args.layers:
+        wl = dataclasses.replace(wl, layers=args.layers)
     moe.build()
     moe.lib()
     T, H, E, k, I = wl.dims
@@ -659,7 +664,7 @@ def measure_w8a16(args, name, steps, rank, world, local):
     moe.build()
     moe.lib()
     cfg = EXTRA[name]
-    T, layers, nsets = cfg["T"], cfg["layers"], cfg["sets"]
+    T, layers, nsets = cfg["T"], cfg["layers"], args.sets or cfg["sets"]
     dev = torch.device("cuda", torch.cuda.current_device())
     seed = args.seed + 1000 * rank
     K0 = layers[0][1]
@@ -728,7 +733,7 @@ def measure_quant(args, name, steps, rank, world, local):
     moe.build()
     moe.lib()
     cfg = EXTRA[name]
-    N, K, nclip, nsets = cfg["N"], cfg["K"], cfg["nclip"], cfg["sets"]
+    N, K, nclip, nsets = cfg["N"], cfg["K"], cfg["nclip"], args.sets or cfg["sets"]
     dev = torch.device("cuda", torch.cuda.current_device())
     seed = args.seed + 1000 * rank
     Ws = [synth.bf16_weights(N, K, seed=seed, layer=s).to(dev) for s in range(nsets)]
