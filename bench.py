@@ -216,14 +216,6 @@ def cpu_baseline(wl, seed: int, target_s: float):
 
 # ------------------------------------------------------------- our arm -----
 
-# The sources that make up each captured kernel (its file and the headers it
-# includes): its recorded DRAM traffic holds while these are unchanged.
-KERNEL_SOURCES = {
-    "decode1": ["decode_fused.cu", "common.cuh", "kernels.cuh"],
-    "prefill512": ["prefill.cu", "common.cuh", "kernels.cuh", "tcgen05.cuh"],
-}
-
-
 def source_hash(names=None) -> str:
     """Hash of the named csrc files (all of them by default)."""
     h = hashlib.sha256()
@@ -235,17 +227,10 @@ def source_hash(names=None) -> str:
 
 
 def recorded_traffic(config: str):
-    """DRAM bytes per launch of the expert kernel from a committed ncu capture, if it
-    was taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    e = d.get(config)
-    if not e or config not in KERNEL_SOURCES or e.get("source_hash") != source_hash(KERNEL_SOURCES[config]):
-        return None
-    return e.get("dram_bytes_per_launch")
+    """DRAM bytes per launch of the workload's dominant kernel from a committed ncu capture
+    (profiles/traffic.json), if it was taken on the current sources of that kernel (its
+    file and the headers it includes, listed with the entry); else None."""
+    return recorded_counter(config, "dram_bytes_per_launch")
 
 
 def binding_roofline(bytes_per_launch, flops_per_launch, hbm_gbs, tc_tflops):
