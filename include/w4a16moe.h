@@ -271,9 +271,12 @@ MOE_API int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t n
  * Which kernels a forward call of dims `d` runs (a host-only query, no
  * counterpart on the pages; for tests and tuning). Writes *plan = 0 for the
  * tensor-core pipeline (permute, grouped gate_up and down GEMMs, conversion);
- * otherwise the fused decode kernel runs and *plan = s + 16 * g, where s = 1
- * if the activations are staged in shared memory and 2 if they are read from
- * global memory, and g is the number of 128-wide groups per gate_up chunk.
+ * otherwise the fused decode kernel runs and *plan = s + 16 * g + 256 * y,
+ * where s = 1 if the activations are staged in shared memory and 2 if they
+ * are read from global memory, g (at most 15) is the number of 128-wide
+ * groups per gate_up chunk, and y = 1 if the down outputs' block buffers have
+ * a shared-memory region of their own (0: they reuse the gate_up partial-sum
+ * area once the CTA's gate_up work is done).
  * Returns the shape checks' status.
  */
 MOE_API int moe_forward_plan(moe_dims d, int32_t *plan);

@@ -10,8 +10,8 @@ back as soon as its words are read; its partial sums then wait for the
 previous user of their buffer (task u - nb) to be finalised; the last of a
 task's chunks finalises it and counts the expert's gate_up task done. A down
 chunk holds its stage until all gate_up tasks of its expert, in every CTA,
-are done, until every gate_up task of its own CTA is finalised (its block
-buffer lives in the partial-sum area) and until the block that used its
+are done, (when its block buffer lives in the partial-sum area) until every
+gate_up task of its own CTA is finalised, and until the block that used its
 buffer before is combined; the chunk that completes a block combines it.
 
 This model plays that protocol for every CTA of a launch, in random order,
@@ -51,8 +51,9 @@ def _al(v, a):
     return (v + a - 1) // a * a
 
 
-def _layout_gc(T, H, E, k, I, gc_max):
-    """Mirror of fused_layout_gc: (fits, staged activations, gcw)."""
+def _layout_gc(T, H, E, k, I, gc_max, full=False):
+    """Mirror of fused_layout_gc: (fits, staged activations, gcw); with full, also
+    (output-block buffers, whether they have a region of their own)."""
     G1, G2 = H // 128, I // 128
     gc = min(G1, gc_max)
     gcw = gc * 16
@@ -75,20 +76,25 @@ def _layout_gc(T, H, E, k, I, gc_max):
     base = pro_off + _al(pro, 128)
     staged = base + xs <= C["kFusedSmem"]
     total = base + xs if staged else base
+    ys_start = _al(total, 128)
+    ysep = bool(yb) and ys_start + 2 * yb <= C["kFusedSmem"]
+    if ysep:
+        nyb, total = 2, ys_start + 2 * yb
     ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256 and \
         (nyb >= 1 or T == 0)
-    return ok, staged, gcw
+    return (ok, staged, gcw, nyb, ysep) if full else (ok, staged, gcw)
 
 
 def fused_plan(T, H, E, k, I):
     """Mirror of fused_layout: None if the decode kernel cannot take the shape,
-    else (staged, groups per chunk): which instantiation of the kernel runs."""
-    a = _layout_gc(T, H, E, k, I, C["kGC"])
+    else (staged, groups per chunk, separate block buffers): which
+    instantiation of the kernel runs, and which of its two buffer placements."""
+    a = _layout_gc(T, H, E, k, I, C["kGC"], full=True)
     if a[0] and a[1]:
-        return a[1], a[2] // 16
-    b = _layout_gc(T, H, E, k, I, C["kGCMin"])
+        return a[1], a[2] // 16, a[4]
+    b = _layout_gc(T, H, E, k, I, C["kGCMin"], full=True)
     pick = b if b[0] and (b[1] or not a[0]) else a
-    return (pick[1], pick[2] // 16) if pick[0] else None
+    return (pick[1], pick[2] // 16, pick[4]) if pick[0] else None
 
 
 def _launch(T, H, E, k, I, nact, gc_max, sms=152):
@@ -96,13 +102,12 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
     gc = min(G1, gc_max)
     nkc = -(-G1 // gc)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
-    yb = T * k * C["kP2Rows"] * 4
-    nyb = min(2, max(nb * nkc * 512, yb) // yb)
+    _, _, _, nyb, ysep = _layout_gc(T, H, E, k, I, gc_max, full=True)
     tp1 = I // 8
     n1 = nact * tp1
     chunks = min(T * k, E) * (tp1 * nkc + H // C["kP2Rows"])
     grid = max(1, min(sms, -(-chunks // C["kCons"])))
-    return nkc, nb, nyb, tp1, n1, grid
+    return nkc, nb, nyb, ysep, tp1, n1, grid
 
 
 def _split(H, I, nact, Cg, cb):
@@ -132,7 +137,7 @@ def _split(H, I, nact, Cg, cb):
 def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
-    nkc, nb, nyb, tp1, n1, grid = _launch(T, H, E, k, I, nact, gc_max)
+    nkc, nb, nyb, ysep, tp1, n1, grid = _launch(T, H, E, k, I, nact, gc_max)
     done1 = [0] * nact
     ctas = []
     covered_tasks, covered_blocks = [], []
@@ -174,7 +179,8 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
                     if kind == "dn":
                         a, lb = task, u
                         buf = lb % nyb
-                        if done1[a] < tp1 or cta["gu_done"] < cta["m1"] or cta["dfin"][buf] < lb // nyb:
+                        if done1[a] < tp1 or (not ysep and cta["gu_done"] < cta["m1"]) or \
+                                cta["dfin"][buf] < lb // nyb:
                             continue
                         cta["dcnt"][buf] += 1
                         if cta["dcnt"][buf] == nact:
@@ -212,6 +218,7 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
     (7, 3072, 64, 8, 256, 40),      # 5 or 6 K chunks per task, the last one shorter
     (2, 8064, 16, 4, 128, 8),       # 13 or 16 K chunks per task, 2 or 3 partial-sum buffers
     (7, 8064, 1024, 32, 640, 224),
+    (7, 4096, 8, 8, 128, 8),        # block buffers in the partial-sum area
 ])
 def test_decode_schedule_completes(T, H, E, k, I, nact):
     # either chunk size the launch may choose (the larger unless its stages
@@ -226,7 +233,11 @@ def test_decode_schedule_completes(T, H, E, k, I, nact):
 # The shapes of the GPU parity tests that run the decode kernel, and the
 # instantiation each one reaches: decode_fused_kernel<true> stages the
 # activations in shared memory, <false> reads them from global memory.
+# GPU_SHARED_AREA_SHAPES lists those whose down outputs' block buffers reuse
+# the gate_up partial-sum area (all others have a region of their own).
+GPU_SHARED_AREA_SHAPES = {(7, 4096, 8, 8, 128)}
 GPU_DECODE_SHAPES = {
+    (7, 4096, 8, 8, 128): True,        # block buffers in the partial-sum area
     (1, 2560, 512, 10, 640): True,     # decode1
     (4, 2560, 512, 10, 640): True,     # decode4
     (4, 256, 16, 2, 128): True,        # tiny
@@ -248,6 +259,7 @@ def test_decode_instantiation_of_gpu_shapes(shape, staged):
     plan = fused_plan(*shape)
     assert plan is not None, "the decode kernel must take %s" % (shape,)
     assert plan[0] == staged
+    assert plan[2] == (shape not in GPU_SHARED_AREA_SHAPES)
     if shape == (6, 6144, 32, 4, 256):
         assert plan[1] == C["kGCMin"]
     # the library's own choice (a host-only query) agrees with this mirror
@@ -267,6 +279,10 @@ def test_mirror_matches_library_plan_over_many_shapes():
         if k > E:
             continue
         assert _library_plan(T, H, E, k, I) == fused_plan(T, H, E, k, I), (T, H, E, k, I)
+    # shapes whose block buffers stay in the partial-sum area
+    for shape in ((7, 4096, 8, 8, 128), (6, 4608, 8, 8, 128), (5, 5888, 8, 4, 128), (4, 7296, 8, 8, 128)):
+        assert fused_plan(*shape)[2] is False
+        assert _library_plan(*shape) == fused_plan(*shape), shape
 
 
 def test_decode_takes_every_batch_up_to_seven_tokens_at_full_shape():

@@ -283,12 +283,13 @@ def moe_pack_int4(q, bad_count=None, stream=None):
 
 def moe_forward_plan(T: int, H: int, E: int, k: int, I: int):
     """None if a forward of these dims takes the tensor-core pipeline, else
-    (staged, groups_per_chunk) of the fused decode kernel it runs."""
+    (staged, groups_per_chunk, separate_block_buffers) of the fused decode
+    kernel it runs."""
     v = ctypes.c_int32(-1)
     _check(lib().moe_forward_plan(moe_dims(T, H, E, k, I), ctypes.byref(v)), "moe_forward_plan")
     if v.value == 0:
         return None
-    return (v.value & 15) == 1, v.value >> 4
+    return (v.value & 15) == 1, (v.value >> 4) & 15, bool(v.value & 256)
 
 
 def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None):

@@ -96,14 +96,15 @@ struct FusedParams {
     uint32_t stage_bytes;
     uint32_t red_off;    // offset of the gate_up partial sums and counters
     int nb;              // partial-sum buffers
-    int nyb;             // output-block buffers (in the partial-sum area, once gate_up is done)
+    int nyb;             // output-block buffers
     uint32_t red_area;   // bytes of the partial-sum area: the larger of the partial sums and one block buffer
     uint32_t pro_off;    // offset of the permutation arrays
     uint32_t xs_off;     // offset of the staged activations (0: not staged)
+    uint32_t ys_off;     // offset of the output-block buffers (0: in the partial-sum area)
 };
 
 struct FusedLayout {
-    uint32_t stage_bytes, red_off, red_area, pro_off, xs_off, total;
+    uint32_t stage_bytes, red_off, red_area, pro_off, xs_off, ys_off, total;
     int gcw, nkc, nb, nyb;
     bool ok;
 };
@@ -123,8 +124,10 @@ inline uint32_t fused_pro_bytes(const moe_dims &d) {
 // finalised tasks, the consumers' chunk ticket, per ring stage the chunk last
 // issued into it and the chunk it may take next, the CTA's count of finalised
 // gate_up tasks, and per output-block buffer a count of finished down chunks
-// and of combined blocks. Once every gate_up task of the CTA is finalised, the
-// partial-sum area holds nyb output-block buffers of [T*k slots][16 rows] f32.
+// and of combined blocks. The nyb output-block buffers of [T*k slots][16 rows]
+// f32 have a region of their own where shared memory allows; otherwise they lie
+// in the partial-sum area, which holds them once every gate_up task of the CTA
+// is finalised.
 constexpr int kRingWordsExtra = 5;
 inline uint32_t fused_red_bytes(uint32_t area, int nb) {
     return area + (uint32_t)(2 * nb * 4 + 4 + 2 * kNS * 4 + 4 * kRingWordsExtra);
@@ -148,7 +151,8 @@ __device__ inline RingWords ring_words(uint8_t *smem, const FusedParams &p) {
 }
 
 // Shared memory: the CTA's ring of kNS stages | partial sums | permutation
-// arrays | staged activations (if they fit). gc_max: groups per gate_up chunk.
+// arrays | staged activations (if they fit) | two output-block buffers (if
+// they fit). gc_max: groups per gate_up chunk.
 inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     FusedLayout L{};
     const int G1 = d.H / 128;
@@ -173,6 +177,15 @@ inline FusedLayout fused_layout_gc(const moe_dims &d, int gc_max) {
     const uint32_t base = L.pro_off + (uint32_t)align_up(fused_pro_bytes(d), 128);
     L.xs_off = base + xs_bytes <= (uint32_t)kFusedSmem ? base : 0;
     L.total = L.xs_off ? base + xs_bytes : base;
+    // the output-block buffers in a region of their own, so that a CTA's down
+    // chunks need not wait for its last gate_up task (measured at T = 1: the
+    // wait held each down chunk about 1 us after its expert was complete)
+    const uint32_t ys_start = (uint32_t)align_up(L.total, 128);
+    if (yb && ys_start + 2 * yb <= (uint32_t)kFusedSmem) {
+        L.ys_off = ys_start;
+        L.nyb = 2;
+        L.total = ys_start + 2 * yb;
+    }
     L.ok = L.total <= (uint32_t)kFusedSmem && d.T <= kDecodeMaxT && d.k <= kMaxK && d.I <= 1280 && L.gcw <= 256 &&
            (L.nyb >= 1 || d.T == 0);
     return L;
@@ -193,7 +206,7 @@ bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
 int fused_plan(const moe_dims &d) {
     const FusedLayout L = fused_layout(d);
     if (!L.ok) return 0;
-    return (L.xs_off ? 1 : 2) | ((L.gcw / 16) << 4);
+    return (L.xs_off ? 1 : 2) | ((L.gcw / 16) << 4) | (L.ys_off ? 256 : 0);
 }
 
 struct Pro {   // permutation arrays in shared memory
@@ -754,14 +767,14 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem,
             if (ns < 512) ns *= 2;
         }
     }
-    // the block's slot buffer lies in the gate_up partial-sum area: it is free
-    // once every gate_up task of this CTA is finalised, and once the block that
-    // used it before (nyb blocks earlier) is combined
+    // the block's slot buffer is free once the block that used it before (nyb
+    // blocks earlier) is combined, and, when it lies in the gate_up partial-sum
+    // area, once every gate_up task of this CTA is finalised
     const RingWords rw = ring_words(smem, p);
     const int lb = c - cb0, buf = lb % p.nyb;
     if (lane == 0 && ok) {
         uint32_t i = 0;
-        while (*rw.gu_done < m1 || rw.dfin[buf] < lb / p.nyb)
+        while ((!p.ys_off && *rw.gu_done < m1) || rw.dfin[buf] < lb / p.nyb)
             if (++i > kSpinLimit) {
                 ok = 0;
                 set_error(p.ctrl, MOE_ERR_TIMEOUT);
@@ -772,7 +785,7 @@ __device__ inline bool f_down(const FusedParams &p, const Pro &v, uint8_t *smem,
     __syncwarp();
     if (!ok) return false;
     __threadfence_block();
-    float *ys = reinterpret_cast<float *>(smem + p.red_off) + (size_t)buf * p.T * p.k * kP2Rows;
+    float *ys = reinterpret_cast<float *>(smem + (p.ys_off ? p.ys_off : p.red_off)) + (size_t)buf * p.T * p.k * kP2Rows;
 
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int np = 0; np < ne; np += 8) {
@@ -1115,6 +1128,7 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.red_area = L.red_area;
     p.pro_off = L.pro_off;
     p.xs_off = L.xs_off;
+    p.ys_off = L.ys_off;
 
     const bool staged = L.xs_off != 0;
     const void *fn = staged ? reinterpret_cast<const void *>(decode_fused_kernel<true>)
