@@ -20,6 +20,7 @@ processed (no cycle of waits). The constants are read from the kernel source
 so that the model follows it. Shapes include uneven K-chunk counts and the
 largest H and E.
 """
+import math
 import os
 import random
 import re
@@ -134,6 +135,23 @@ def _split(H, I, nact, Cg, cb):
     return s0, s1 - s0, cb0, cb1
 
 
+def task_stride(n1, nkc, grid):
+    """Mirror of task_stride: 0, or the multiplier M of the global task order."""
+    if n1 * nkc <= 2 * C["kCons"] * grid:
+        return 0
+    M = max(1, (n1 * 633) >> 10)
+    while math.gcd(M, n1) != 1:
+        M += 1
+    return M
+
+
+def cta_tasks(b1, m1, n1, M):
+    """The CTA's gate_up tasks in the order it takes them."""
+    if M == 0 or m1 > C["kFW"] * 32:
+        return list(range(b1, b1 + m1)) if M == 0 else [(x * M) % n1 for x in range(b1, b1 + m1)]
+    return sorted((x * M) % n1 for x in range(b1, b1 + m1))
+
+
 def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
@@ -143,9 +161,10 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
     covered_tasks, covered_blocks = [], []
     for cb in range(grid):
         b1, m1, cb0, cb1 = _split(H, I, nact, grid, cb)
-        covered_tasks += list(range(b1, b1 + m1))
+        tasks = cta_tasks(b1, m1, n1, task_stride(n1, nkc, grid))
+        covered_tasks += tasks
         covered_blocks += list(range(cb0, cb1))
-        seq = [("gu", b1 + u, u) for u in range(m1) for _ in range(nkc)] + \
+        seq = [("gu", tasks[u], u) for u in range(m1) for _ in range(nkc)] + \
               [("dn", a, c - cb0) for c in range(cb0, cb1) for a in range(nact)]
         ctas.append(dict(seq=seq, issued=set(), released=set(), ticket=0, held=[None] * kCons, cnt={}, fin=[0] * nb,
                          m1=m1, gu_done=0, dcnt=[0] * nyb, dfin=[0] * nyb))
@@ -231,8 +250,8 @@ def test_decode_schedule_completes(T, H, E, k, I, nact):
 
 
 # The shapes of the GPU parity tests that run the decode kernel, and the
-# instantiation each one reaches: decode_fused_kernel<true> stages the
-# activations in shared memory, <false> reads them from global memory.
+# instantiation each one reaches: decode_fused_kernel<true, *> stages the
+# activations in shared memory, <false, *> reads them from global memory.
 # GPU_SHARED_AREA_SHAPES lists those whose down outputs' block buffers reuse
 # the gate_up partial-sum area (all others have a region of their own).
 GPU_SHARED_AREA_SHAPES = {(7, 4096, 8, 8, 128)}

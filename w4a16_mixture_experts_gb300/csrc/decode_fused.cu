@@ -370,25 +370,28 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
 }
 
 // ---- the CTA's chunk sequence -----------------------------------------------
-// Chunk i of the CTA: for i < m1 * nkc, K chunk i % nkc of gate_up task
-// b1 + i / nkc (tasks in order); after them the down chunks b2, b2 + 1, ...
+// Chunk i of the CTA: for i < m1 * nkc, K chunk i % nkc of the CTA's gate_up
+// task u = i / nkc (tab[u], or b1 + u when tab is null; see task_stride);
+// after them the down chunks b2, b2 + 1, ...
 // Task ids: gate_up tasks 0..n1-1, down chunks n1, n1 + 1, ...; down chunk d
 // is (output block d / nact, active expert d % nact), and a CTA's down chunks
 // cover whole blocks. The producer issues the chunks in this order and the
 // consumers take them in this order.
 struct ChunkRef {
-    int task, chunk;
+    int task, chunk, u;   // u: the CTA's gate_up task index
 };
 
-__device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int nkc) {
+__device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int nkc, const uint16_t *tab) {
     ChunkRef r;
     if (i < m1 * nkc) {
         const int u = i / nkc;
-        r.task = b1 + u;
+        r.task = tab ? (int)tab[u] : b1 + u;
         r.chunk = i - u * nkc;
+        r.u = u;
     } else {
         r.task = n1 + b2 + (i - m1 * nkc);
         r.chunk = 0;
+        r.u = 0;
     }
     return r;
 }
@@ -909,7 +912,7 @@ __device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
 // (bounded) for the last copy issued into stage q, so that none lands after
 // the CTA has exited.
 __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8_t *smem, int b1, int m1, int b2,
-                                       int m2, int n1) {
+                                       int m2, int n1, const uint16_t *tab) {
     const int l = threadIdx.x & 31;
     const RingWords rw = ring_words(smem, p);
     const int nc = m1 * p.nkc + m2;
@@ -925,7 +928,7 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
                 // (the previous consumer's reads of the stage completed before it
                 // handed the stage back)
                 rw.issued[q] = i;
-                const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
+                const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc, tab);
                 f_issue(p, v, r.task, r.chunk, n1, smem + (size_t)q * p.stage_bytes, full_bar(v, q), 0);
                 i += 32;
             }
@@ -988,8 +991,41 @@ __device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb
     }
 }
 
+// The CTA's gate_up tasks are the positions b1 .. b1 + m1 - 1 of a global
+// order of all n1 tasks. When the gate_up work spans more than two rounds of
+// the consumer warps, position x holds task x * M mod n1 (M coprime to n1, about
+// 0.618 n1: consecutive positions land far apart), and each CTA takes its tasks
+// in increasing order, i.e. expert by expert: every expert's tasks are then
+// spread over many CTAs and sit at the same relative place in each CTA's
+// sequence, so the experts complete one after another through the gate_up
+// phase instead of all at its end, and a CTA whose gate_up work ends early
+// (one with two output blocks) finds early experts' h ready for its down
+// chunks. (Measured at T = 4 with the task order itself: the CTAs with two
+// output blocks ended 25% after the others.) Otherwise (M = 0) position x is
+// task x. The same in every CTA.
+static_assert(kFastN * 4 >= kFW * 32 * 2, "the sorted task list (one uint16 per thread) fits the prologue's scratch");
+static_assert(kDecodeMaxT * kMaxK * (1280 / 8) < 65536, "gate_up task ids fit 16 bits");
+__device__ inline int task_stride(int n1, int nkc, int C) {
+    if ((long long)n1 * nkc <= 2LL * kCons * C) return 0;
+    int M = (int)(((long long)n1 * 633) >> 10);
+    if (M < 1) M = 1;
+    for (;;) {   // ends at M = n1 - 1 at the latest
+        int a = M, b = n1;
+        while (b) {
+            const int t = a % b;
+            a = b;
+            b = t;
+        }
+        if (a == 1) return M;
+        ++M;
+    }
+}
+
 // ---- kernel -----------------------------------------------------------------
-template <bool kStaged>
+// kSpread: the launch may hold enough gate_up work for the spread task order
+// (see task_stride); without it the task order is the plain one, in code that
+// carries nothing of the other (measured: 0.3 us at T = 1 otherwise).
+template <bool kStaged, bool kSpread>
 __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_constant__ FusedParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1025,8 +1061,30 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     int b1, m1, cb0, cb1;
     fused_split(p, nact, gridDim.x, blockIdx.x, b1, m1, cb0, cb1);
     const int b2 = cb0 * nact, m2 = (cb1 - cb0) * nact;   // down chunks of whole blocks
+    // the CTA's gate_up tasks in increasing order (see task_stride), in the
+    // prologue's scratch array, free now; with M = 0, or more tasks than
+    // threads, the tasks are b1 + u (the partition is M's either way)
+    const int M = kSpread ? task_stride(n1, p.nkc, gridDim.x) : 0;
+    const uint16_t *tab = nullptr;
+    if (kSpread && M != 0 && m1 <= kFW * 32) {
+        uint16_t *t16 = reinterpret_cast<uint16_t *>(v.cnt);
+        const int j = threadIdx.x;
+        if (j < m1) {
+            const int tj = (int)(((unsigned)(b1 + j) * (unsigned)M) % (unsigned)n1);
+            int rank = 0;
+            int t2 = (int)(((unsigned)b1 * (unsigned)M) % (unsigned)n1);
+            for (int i2 = 0; i2 < m1; ++i2) {
+                rank += t2 < tj;
+                t2 += M;
+                if (t2 >= n1) t2 -= n1;
+            }
+            t16[rank] = (uint16_t)tj;
+        }
+        __syncthreads();
+        tab = t16;
+    }
     if (warp == kProd) {
-        f_produce(p, v, smem, b1, m1, b2, m2, n1);
+        f_produce(p, v, smem, b1, m1, b2, m2, n1, tab);
     } else {
         // the activations, converted while the producer requests the first chunks
         fused_stage(p, smem, v);
@@ -1045,7 +1103,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
             if (i >= nc) break;
             const int q = i % kNS;
             uint8_t *stage = smem + (size_t)q * p.stage_bytes;
-            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc);
+            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc, tab);
             // the chunk's scales travel while it waits for its weights
             uint32_t sk[2 * kScW];
             if (r.task < n1) gate_up_scales(p, v, r.task, r.chunk, lane, sk);
@@ -1074,7 +1132,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
                     __threadfence_block();
                     rw.next[q] = i + kNS;
                 }
-                if (!f_gu_reduce(p, v, smem, r.task, r.task - b1, r.chunk, lane, acc)) break;
+                if (!f_gu_reduce(p, v, smem, r.task, r.u, r.chunk, lane, acc)) break;
             } else {
                 f_down(p, v, smem, r.task - n1, cb0, m1, stage, lane, sk);
                 __syncwarp();
@@ -1131,16 +1189,19 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.ys_off = L.ys_off;
 
     const bool staged = L.xs_off != 0;
-    const void *fn = staged ? reinterpret_cast<const void *>(decode_fused_kernel<true>)
-                            : reinterpret_cast<const void *>(decode_fused_kernel<false>);
-    err = set_smem_once(fn, kFusedSmem);
-    if (err != cudaSuccess) return err;
     const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
     // enough CTAs that every consumer has a chunk
     const long long chunks = max_active * ((long long)(d.I / 8) * L.nkc + d.H / kP2Rows);
     long long grid = (chunks + kCons - 1) / kCons;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;
+    // the spread task order can only be chosen if the most active experts there can be give it enough work
+    const bool spread = max_active * (d.I / 8) * L.nkc > 2LL * kCons * grid;
+    const void *fn = staged ? (spread ? reinterpret_cast<const void *>(decode_fused_kernel<true, true>)
+                                      : reinterpret_cast<const void *>(decode_fused_kernel<true, false>))
+                            : reinterpret_cast<const void *>(decode_fused_kernel<false, true>);
+    err = set_smem_once(fn, kFusedSmem);
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kFW * 32);
@@ -1158,8 +1219,9 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, p);
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, p);
+    if (staged && spread) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, true>, p);
+    if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, false>, p);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false, true>, p);
 }
 
 }  // namespace moe
