@@ -35,7 +35,7 @@ def _constants():
     src = open(SRC).read()
     c = {}
     for name in ("kFW", "kCons", "kGC", "kGCMin", "kNS", "kRedMax", "kMaxNB", "kP2Rows", "kDecodeMaxT",
-                 "kFastN", "kRingWordsExtra"):
+                 "kFastN", "kRingWordsExtra", "kSpreadDownWeight"):
         m = re.search(r"constexpr int %s = (\d+);" % name, src)
         assert m, name
         c[name] = int(m.group(1))
@@ -108,20 +108,23 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
     n1 = nact * tp1
     chunks = min(T * k, E) * (tp1 * nkc + H // C["kP2Rows"])
     grid = max(1, min(sms, -(-chunks // C["kCons"])))
-    return nkc, nb, nyb, ysep, tp1, n1, grid
+    # the kernel instantiation with the spread task order and its split weight
+    spread = min(T * k, E) * tp1 * nkc > 2 * C["kCons"] * grid
+    return nkc, nb, nyb, ysep, tp1, n1, grid, spread
 
 
-def _split(H, I, nact, Cg, cb):
+def _split(H, I, nact, Cg, cb, w=1):
     """Mirror of fused_split (exact integer arithmetic, as the kernel's result):
-    (first gate_up task, tasks, first block, end block)."""
+    (first gate_up task, tasks, first block, end block); w weighs a CTA's own
+    down bytes."""
     B = H // C["kP2Rows"]
     n1 = nact * (I // 8)
     cb0, cb1 = B * cb // Cg, B * (cb + 1) // Cg
     blk = nact * I
     total = n1 * H + B * blk
     bmin = B // Cg
-    x0 = max(0, total - Cg * blk * bmin)
-    x1 = max(0, total - Cg * blk * (bmin + 1))
+    x0 = max(0, total - Cg * w * blk * bmin)
+    x1 = max(0, total - Cg * w * blk * (bmin + 1))
 
     def cum(c):
         nbig = B * c // Cg - bmin * c
@@ -155,17 +158,22 @@ def cta_tasks(b1, m1, n1, M):
 def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
-    nkc, nb, nyb, ysep, tp1, n1, grid = _launch(T, H, E, k, I, nact, gc_max)
+    nkc, nb, nyb, ysep, tp1, n1, grid, spread = _launch(T, H, E, k, I, nact, gc_max)
+    w = C["kSpreadDownWeight"] if spread else 1
     done1 = [0] * nact
     ctas = []
     covered_tasks, covered_blocks = [], []
     for cb in range(grid):
-        b1, m1, cb0, cb1 = _split(H, I, nact, grid, cb)
-        tasks = cta_tasks(b1, m1, n1, task_stride(n1, nkc, grid))
+        b1, m1, cb0, cb1 = _split(H, I, nact, grid, cb, w)
+        tasks = cta_tasks(b1, m1, n1, task_stride(n1, nkc, grid) if spread else 0)
         covered_tasks += tasks
         covered_blocks += list(range(cb0, cb1))
-        seq = [("gu", tasks[u], u) for u in range(m1) for _ in range(nkc)] + \
-              [("dn", a, c - cb0) for c in range(cb0, cb1) for a in range(nact)]
+        # down chunks block by block, or (spread order) expert by expert when every block has a buffer
+        if spread and cb1 - cb0 <= nyb:
+            down = [("dn", a, c - cb0) for a in range(nact) for c in range(cb0, cb1)]
+        else:
+            down = [("dn", a, c - cb0) for c in range(cb0, cb1) for a in range(nact)]
+        seq = [("gu", tasks[u], u) for u in range(m1) for _ in range(nkc)] + down
         ctas.append(dict(seq=seq, issued=set(), released=set(), ticket=0, held=[None] * kCons, cnt={}, fin=[0] * nb,
                          m1=m1, gu_done=0, dcnt=[0] * nyb, dfin=[0] * nyb))
     # the split covers every gate_up task and every output block exactly once

@@ -372,7 +372,12 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
 // ---- the CTA's chunk sequence -----------------------------------------------
 // Chunk i of the CTA: for i < m1 * nkc, K chunk i % nkc of the CTA's gate_up
 // task u = i / nkc (tab[u], or b1 + u when tab is null; see task_stride);
-// after them the down chunks b2, b2 + 1, ...
+// after them the down chunks of its nblk output blocks from cb0: block by block
+// (each block's chunk for every active expert a), or, with the spread task
+// order when every block has a buffer of its own (nblk <= nyb, emaj), expert
+// by expert (each expert's chunk for every block), so that a CTA with two
+// blocks runs both blocks' chunks of an expert as soon as the expert is
+// complete.
 // Task ids: gate_up tasks 0..n1-1, down chunks n1, n1 + 1, ...; down chunk d
 // is (output block d / nact, active expert d % nact), and a CTA's down chunks
 // cover whole blocks. The producer issues the chunks in this order and the
@@ -381,7 +386,8 @@ struct ChunkRef {
     int task, chunk, u;   // u: the CTA's gate_up task index
 };
 
-__device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int nkc, const uint16_t *tab) {
+__device__ inline ChunkRef chunk_at(int i, int b1, int m1, int cb0, int nblk, int nact, int n1, int nkc,
+                                    const uint16_t *tab, bool emaj) {
     ChunkRef r;
     if (i < m1 * nkc) {
         const int u = i / nkc;
@@ -389,7 +395,9 @@ __device__ inline ChunkRef chunk_at(int i, int b1, int m1, int b2, int n1, int n
         r.chunk = i - u * nkc;
         r.u = u;
     } else {
-        r.task = n1 + b2 + (i - m1 * nkc);
+        const int d = i - m1 * nkc;
+        const int c = emaj ? cb0 + d % nblk : cb0 + d / nact, a = emaj ? d / nblk : d % nact;
+        r.task = n1 + c * nact + a;
         r.chunk = 0;
         r.u = 0;
     }
@@ -911,11 +919,12 @@ __device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
 // chunks only. The loop is bounded. Before the warp leaves, lane q waits
 // (bounded) for the last copy issued into stage q, so that none lands after
 // the CTA has exited.
-__device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8_t *smem, int b1, int m1, int b2,
-                                       int m2, int n1, const uint16_t *tab) {
+__device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8_t *smem, int b1, int m1, int cb0,
+                                       int nblk, int n1, const uint16_t *tab, bool emaj) {
     const int l = threadIdx.x & 31;
     const RingWords rw = ring_words(smem, p);
-    const int nc = m1 * p.nkc + m2;
+    const int nact = *v.nact;
+    const int nc = m1 * p.nkc + nblk * nact;
     int i = l;   // next chunk of this lane
     uint32_t polls = 0;
     bool ok = true;
@@ -928,7 +937,7 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
                 // (the previous consumer's reads of the stage completed before it
                 // handed the stage back)
                 rw.issued[q] = i;
-                const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc, tab);
+                const ChunkRef r = chunk_at(i, b1, m1, cb0, nblk, nact, n1, p.nkc, tab, emaj);
                 f_issue(p, v, r.task, r.chunk, n1, smem + (size_t)q * p.stage_bytes, full_bar(v, q), 0);
                 i += 32;
             }
@@ -949,8 +958,8 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
 // ---- work split ---------------------------------------------------------------
 // CTA cb of C owns output blocks [cb0, cb1) = [B cb / C, B (cb + 1) / C), B = H/16.
 // The gate_up tasks are shared out in proportion to each CTA's capacity: an
-// equal share of all the bytes (gate_up tasks and down chunks) minus the bytes
-// of its own blocks' down chunks (at least 0). CTAs own B / C or B / C + 1
+// equal share of all the bytes (gate_up tasks and down chunks) minus w times the
+// bytes of its own blocks' down chunks (at least 0). CTAs own B / C or B / C + 1
 // blocks, so the capacities take two values and their prefix sums have a
 // closed form, computed exactly in 64-bit integers (units of 8 bytes: a gate_up
 // task is H, a block's down chunks nact * I). CTA c's tasks start at
@@ -970,7 +979,14 @@ __device__ inline int floor_ratio(long long num, long long den) {   // floor(num
     return q;
 }
 
-__device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int &b1, int &m1, int &cb0,
+// w: the weight of a CTA's own down bytes in its capacity. With the spread
+// task order (see task_stride) and the down chunks expert by expert, the down
+// work of a CTA with more blocks runs while the experts complete, so such CTAs
+// take less gate_up work (w = 2; measured at T = 4: the CTAs with two blocks,
+// then without gate_up work, end with the others; route + forward 56.9 ->
+// 55.2 us at T = 4, 83.9 -> 81.7 us at T = 7).
+constexpr int kSpreadDownWeight = 2;
+__device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int w, int &b1, int &m1, int &cb0,
                                    int &cb1) {
     const int B = p.H / kP2Rows;
     const int n1 = nact * (p.I / 8);
@@ -979,8 +995,8 @@ __device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb
     const long long blk = (long long)nact * p.I;
     const long long total = (long long)n1 * p.H + (long long)B * blk;
     const int bmin = B / C;
-    const long long x0 = max(0LL, total - (long long)C * blk * bmin);
-    const long long x1 = max(0LL, total - (long long)C * blk * (bmin + 1));
+    const long long x0 = max(0LL, total - (long long)C * w * blk * bmin);
+    const long long x1 = max(0LL, total - (long long)C * w * blk * (bmin + 1));
     const long long all = split_cum(C, C, B, bmin, x0, x1);
     if (all > 0) {
         b1 = floor_ratio((long long)n1 * split_cum(cb, C, B, bmin, x0, x1), all);
@@ -1005,19 +1021,33 @@ __device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb
 // task x. The same in every CTA.
 static_assert(kFastN * 4 >= kFW * 32 * 2, "the sorted task list (one uint16 per thread) fits the prologue's scratch");
 static_assert(kDecodeMaxT * kMaxK * (1280 / 8) < 65536, "gate_up task ids fit 16 bits");
-__device__ inline int task_stride(int n1, int nkc, int C) {
-    if ((long long)n1 * nkc <= 2LL * kCons * C) return 0;
-    int M = (int)(((long long)n1 * 633) >> 10);
-    if (M < 1) M = 1;
-    for (;;) {   // ends at M = n1 - 1 at the latest
-        int a = M, b = n1;
-        while (b) {
-            const int t = a % b;
+// gcd(a, b) == 1 for 0 < a, b < 2^16, by the binary method (shifts and
+// subtractions: a chain of integer divisions cost about 3 us here, measured).
+__device__ inline bool coprime(uint32_t a, uint32_t b) {
+    if (((a | b) & 1u) == 0) return false;
+    a >>= __ffs(a) - 1;
+    while (b) {
+        b >>= __ffs(b) - 1;
+        if (a > b) {
+            const uint32_t t = a;
             a = b;
             b = t;
         }
-        if (a == 1) return M;
-        ++M;
+        b -= a;
+    }
+    return a == 1;
+}
+
+// Called by whole warps: the lanes test 32 candidates at a time.
+__device__ inline int task_stride(int n1, int nkc, int C) {
+    if ((long long)n1 * nkc <= 2LL * kCons * C) return 0;
+    if (n1 <= 2) return 1;
+    const int M0 = (int)(((long long)n1 * 633) >> 10);   // about 0.618 n1, at least 1
+    const int lane = threadIdx.x & 31;
+    for (int base = M0;; base += 32) {   // ends by M = n1 - 1, coprime to n1
+        const int M = base + lane;
+        const unsigned ok = __ballot_sync(0xffffffffu, M < n1 && coprime((uint32_t)M, (uint32_t)n1));
+        if (ok) return base + __ffs(ok) - 1;
     }
 }
 
@@ -1059,8 +1089,9 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     const int nact = *v.nact;
     const int n1 = nact * (p.I / 8);
     int b1, m1, cb0, cb1;
-    fused_split(p, nact, gridDim.x, blockIdx.x, b1, m1, cb0, cb1);
-    const int b2 = cb0 * nact, m2 = (cb1 - cb0) * nact;   // down chunks of whole blocks
+    fused_split(p, nact, gridDim.x, blockIdx.x, kSpread ? kSpreadDownWeight : 1, b1, m1, cb0, cb1);
+    const int nblk = cb1 - cb0, m2 = nblk * nact;   // down chunks of whole blocks
+    const bool emaj = kSpread && nblk <= p.nyb;   // (block by block measured faster at T = 1)
     // the CTA's gate_up tasks in increasing order (see task_stride), in the
     // prologue's scratch array, free now; with M = 0, or more tasks than
     // threads, the tasks are b1 + u (the partition is M's either way)
@@ -1084,7 +1115,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         tab = t16;
     }
     if (warp == kProd) {
-        f_produce(p, v, smem, b1, m1, b2, m2, n1, tab);
+        f_produce(p, v, smem, b1, m1, cb0, nblk, n1, tab, emaj);
     } else {
         // the activations, converted while the producer requests the first chunks
         fused_stage(p, smem, v);
@@ -1103,7 +1134,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
             if (i >= nc) break;
             const int q = i % kNS;
             uint8_t *stage = smem + (size_t)q * p.stage_bytes;
-            const ChunkRef r = chunk_at(i, b1, m1, b2, n1, p.nkc, tab);
+            const ChunkRef r = chunk_at(i, b1, m1, cb0, nblk, nact, n1, p.nkc, tab, emaj);
             // the chunk's scales travel while it waits for its weights
             uint32_t sk[2 * kScW];
             if (r.task < n1) gate_up_scales(p, v, r.task, r.chunk, lane, sk);
