@@ -3,6 +3,8 @@
 // moe_check_device_error, which exists to synchronise).
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "w4a16moe.h"
@@ -18,8 +20,10 @@ struct SmemAttr {
     int bytes;
     bool done[kMaxDevices];
 };
-SmemAttr g_attrs[8];
+constexpr int kMaxSmemKernels = 16;   // kernels that raise their shared-memory limit (9 today)
+SmemAttr g_attrs[kMaxSmemKernels];
 int g_nattrs = 0;
+std::mutex g_attrs_mu;   // callers may launch from several host threads
 
 int current_device() {
     int dev = 0;
@@ -40,11 +44,13 @@ int sm_count() {
 
 cudaError_t set_smem_once(const void *func, int bytes) {
     const int dev = current_device();
+    std::lock_guard<std::mutex> lock(g_attrs_mu);
     int i = 0;
     for (; i < g_nattrs; ++i)
         if (g_attrs[i].func == func) break;
     if (i == g_nattrs) {
-        if (g_nattrs == 8) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (g_nattrs == kMaxSmemKernels)
+            return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         g_attrs[i].func = func;
         g_attrs[i].bytes = bytes;
         ++g_nattrs;
