@@ -378,10 +378,10 @@ __device__ inline uint32_t fw_word(const uint4 &v, int m) {
 // by expert (each expert's chunk for every block), so that a CTA with two
 // blocks runs both blocks' chunks of an expert as soon as the expert is
 // complete.
-// Task ids: gate_up tasks 0..n1-1, down chunks n1, n1 + 1, ...; down chunk d
-// is (output block d / nact, active expert d % nact), and a CTA's down chunks
-// cover whole blocks. The producer issues the chunks in this order and the
-// consumers take them in this order.
+// Task ids: gate_up tasks 0..n1-1; the down chunk of output block c and active
+// expert a is n1 + c * nact + a, and a CTA's down chunks cover whole blocks.
+// The producer issues the chunks in this order and the consumers take them in
+// this order.
 struct ChunkRef {
     int task, chunk, u;   // u: the CTA's gate_up task index
 };
@@ -1226,7 +1226,9 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     long long grid = (chunks + kCons - 1) / kCons;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;
-    // the spread task order can only be chosen if the most active experts there can be give it enough work
+    // the instantiation with the spread task order, where the gate_up work of the most
+    // active experts there can be spans more than two rounds (the kernel decides on the
+    // experts actually active)
     const bool spread = max_active * (d.I / 8) * L.nkc > 2LL * kCons * grid;
     const void *fn = staged ? (spread ? reinterpret_cast<const void *>(decode_fused_kernel<true, true>)
                                       : reinterpret_cast<const void *>(decode_fused_kernel<true, false>))
