@@ -84,22 +84,38 @@ static_assert(kRR8 * kRawBytes8 == kRR * kRawBytes, "one raw ring size for both 
 constexpr uint32_t kPrefillSmemMax = 232448 - 1024;   // dynamic; the static part is a few bytes
 static_assert(kAStage0 + kRS * kACols <= kTmemCols, "tensor memory budget");
 
+// A tile's scales (128 rows x G) go to one of nsc buffers: 2 at least, up to
+// kMaxSC where shared memory allows. With 2, the scale copy of a tile waited
+// for the dequantisation of the tile two before it, which held back the
+// weight stream of short tiles (down: 5 stages a tile; measured at T = 64: the
+// weight copies waited 24% of the kernel for a free scale buffer).
+constexpr int kMaxSC = 4;
 struct PrefillLayout {   // shared-memory offsets from the 1024-aligned base; scales sized by K
     uint32_t b, raw, sc, sc_bytes, cols, bars, tmem_slot, total;
+    int nsc;
 };
-constexpr int kNBars = 2 * kRR + 3 * kRS + 8;
+constexpr int kNBars = 2 * kRR + 3 * kRS + 4 + 2 * kMaxSC;
 
-__host__ __device__ inline PrefillLayout prefill_layout(int G) {
+__host__ __device__ inline PrefillLayout prefill_layout_n(int G, int nsc) {
     PrefillLayout L;
     L.b = 0;
     L.raw = L.b + kRS * kBBytes;
     L.sc = L.raw + kRR * kRawBytes;
     L.sc_bytes = (uint32_t)(128 * G * 2 + 127) / 128 * 128;
-    L.cols = L.sc + 2 * L.sc_bytes;           // per token column: f32 weight, i32 token
+    L.nsc = nsc;
+    L.cols = L.sc + nsc * L.sc_bytes;         // per token column: f32 weight, i32 token
     L.bars = L.cols + 2 * 4 * kPN;
     L.tmem_slot = L.bars + kNBars * 8;
     L.total = L.tmem_slot + 16 + 1024;   // + alignment slack
     return L;
+}
+
+__host__ __device__ inline PrefillLayout prefill_layout(int G) {
+    for (int n = kMaxSC; n > 2; --n) {
+        const PrefillLayout L = prefill_layout_n(G, n);
+        if (L.total <= kPrefillSmemMax) return L;
+    }
+    return prefill_layout_n(G, 2);
 }
 
 struct PrefillParams {
@@ -264,8 +280,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     uint64_t *ab_empty = a_full + kRS;      // [kRS] MMA commit: A slot and activation stage are free
     uint64_t *acc_full = ab_empty + kRS;    // [2] MMA commit
     uint64_t *acc_empty = acc_full + 2;     // [2] the epilogue threads
-    uint64_t *sc_full = acc_empty + 2;      // [2] scale copy (+tx)
-    uint64_t *sc_empty = sc_full + 2;       // [2] the 256 dequant threads
+    uint64_t *sc_full = acc_empty + 2;      // [nsc] scale copy (+tx)
+    uint64_t *sc_empty = sc_full + kMaxSC;  // [nsc] the 256 dequant threads
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
     float *col_w = reinterpret_cast<float *>(smem + L.cols);     // epilogue (gate_up): routing weight
     uint32_t *col_off = reinterpret_cast<uint32_t *>(col_w + kPN);   // epilogue (down): token * H (< 2^32)
@@ -287,6 +303,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kNEpi);
+        }
+        for (int b = 0; b < kMaxSC; ++b) {
             mbar_init(&sc_full[b], 1);
             mbar_init(&sc_empty[b], 256);
         }
@@ -366,8 +384,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         uint32_t g = 0;
         int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            const int tb = lt & 1;
-            if (!pwait(&sc_full[tb], (lt >> 1) & 1, abort_flag)) { fail(p, abort_flag); break; }
+            const int tb = lt % L.nsc;
+            if (!pwait(&sc_full[tb], (lt / L.nsc) & 1, abort_flag)) { fail(p, abort_flag); break; }
             const uint16_t *sc = sSc + tb * (L.sc_bytes / 2) + (half * 64 + br) * G;
             bool ok = true;
             int ks0, ks1;
@@ -505,12 +523,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
                 const Tile T = make_tile(ci, t % p.mb);
                 if (t + (int)gridDim.x < ntiles) ci = chunk_of<kW8>(p, t + gridDim.x);
-                const int tb = lt & 1;
+                const int tb = lt % L.nsc;
                 // weight rows of TMEM lanes 0-63 and 64-127
                 const int row_a = kW8 ? T.m * 128 : p.down ? T.e * p.H + T.m * 128 : T.e * 2 * p.I + T.m * 64;
                 const int row_b = row_a + (p.down ? 64 : p.I);
                 if (!kW8) {
-                    if (!pwait(&sc_empty[tb], ((lt >> 1) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
+                    if (!pwait(&sc_empty[tb], ((lt / L.nsc) & 1) ^ 1, abort_flag)) { fail(p, abort_flag); break; }
                     uint16_t *dst = sSc + tb * (L.sc_bytes / 2);
                     mbar_arrive_expect_tx(&sc_full[tb], 128 * G * 2);
                     bulk_g2s(dst, p.scales + (size_t)row_a * G, 64 * G * 2, &sc_full[tb]);
