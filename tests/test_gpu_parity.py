@@ -302,6 +302,46 @@ def test_forward_edge_shapes(T, H, E, k, I):
     assert_close(out.float().cpu().numpy(), ref, "T=%d H=%d E=%d k=%d I=%d" % (T, H, E, k, I))
 
 
+def _random_shape(seed):
+    """A seeded random layer shape within the library's rules, small enough for the oracle:
+    half decode batches (T <= 7), half tensor-core batches."""
+    g = np.random.default_rng(5000 + seed)
+    T = int(g.integers(1, 8)) if seed % 2 == 0 else int(g.integers(8, 41))
+    H = 128 * int(g.integers(1, 17))
+    I = 128 * int(g.integers(1, 6))
+    E = int(g.integers(1, 161))
+    k = int(g.integers(1, min(E, 12) + 1))
+    return T, H, E, k, I
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_forward_random_shapes(seed):
+    """Random shapes (both kernels, every decode instantiation the shape selects, ragged
+    groups, few and many experts) against the oracle; only the routed experts are drawn,
+    into full-size device tensors."""
+    T, H, E, k, I = _random_shape(seed)
+    x = synth.hidden(T, H, seed=seed)
+    ids, w = synth.random_topk(T, E, k, seed=seed)
+    held = np.unique(ids.numpy())
+    part = synth.expert_weights(E, H, I, seed=seed, experts=held)
+    W = [torch.zeros(E, 2 * I, H // 8, dtype=torch.int32, device="cuda"),
+         torch.zeros(E, 2 * I, H // 128, dtype=torch.bfloat16, device="cuda"),
+         torch.zeros(E, H, I // 8, dtype=torch.int32, device="cuda"),
+         torch.zeros(E, H, I // 128, dtype=torch.bfloat16, device="cuda")]
+    idx = torch.from_numpy(held).long().cuda()
+    for dst, n in zip(W, ("w1_packed", "w1_scales", "w2_packed", "w2_scales")):
+        dst[idx] = part[n].cuda()
+    ws = moe.workspace(T, H, E, k, I)
+    out = moe.moe_w4a16_forward(x.cuda(), ids.cuda(), w.cuda(), *W, ws=ws)
+    assert moe.moe_check_device_error(ws) == 0
+    row = np.full(E, -1, np.int32)
+    row[held] = np.arange(len(held))
+    ref = oracle.expert_forward(x, ids, w, part["w1_packed"], part["w1_scales"], part["w2_packed"],
+                                part["w2_scales"], E, I, expert_row=row)
+    assert_close(out.float().cpu().numpy(), ref, "T=%d H=%d E=%d k=%d I=%d plan %s" % (
+        T, H, E, k, I, moe.moe_forward_plan(T, H, E, k, I)))
+
+
 def test_forward_empty_batch():
     wl, h, g = layer("tiny")
     T, H, E, k, I = wl.dims
