@@ -242,7 +242,7 @@ def binding_roofline(bytes_per_launch, flops_per_launch, hbm_gbs, tc_tflops):
 def launches_per_layer(T: int, E: int) -> int:
     """Kernels one layer launches: route is one kernel for T <= 8 (logits, then
     top-k in the last CTA), else logits + top-k; the forward is one fused kernel
-    (the library's decode path, T <= 7), or permute 3 + x gather + chunk table +
+    (the library's decode path, T <= 8), or permute 3 + x gather + chunk table +
     gate_up + down + conversion."""
     return (1 if T <= 8 else 2) + (1 if T <= FUSED_MAX_T else 8)
 

@@ -174,10 +174,10 @@ MOE_API int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_id
  * Same computation and arguments as moe_w4a16_forward minus ws/ws_bytes. The
  * scratch is a 1 MiB array that the library holds in device memory, one per
  * device per process; the call allocates and frees nothing.
- *  - Served shapes: those of the fused decode path (T <= 7) whose
+ *  - Served shapes: those of the fused decode path (T <= 8) whose
  *    moe_workspace_size() is at most 1 MiB (T = 7 at H 2560, E 512, k 10,
  *    I 640 needs about 0.45 MiB). A larger workspace size returns
- *    MOE_ERR_WORKSPACE and T > 7 returns MOE_ERR_UNSUPPORTED, in both cases
+ *    MOE_ERR_WORKSPACE and T > 8 returns MOE_ERR_UNSUPPORTED, in both cases
  *    before anything is enqueued. T = 0 returns MOE_OK.
  *  - The first call on a device looks up the array's device address (which
  *    may load the module that holds it); make that call before any stream

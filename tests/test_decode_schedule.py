@@ -312,7 +312,7 @@ def test_mirror_matches_library_plan_over_many_shapes():
         assert _library_plan(*shape) == fused_plan(*shape), shape
 
 
-def test_decode_takes_every_batch_up_to_seven_tokens_at_full_shape():
+def test_decode_takes_every_batch_up_to_its_limit_at_full_shape():
     for T in range(1, C["kDecodeMaxT"] + 1):
         for k in (1, 10, 32):
             for E in (k, 512, 1024):

@@ -55,7 +55,7 @@ def _built():
 
 def test_noalloc_rejects_shapes_before_any_cuda_call(_built):
     # T beyond the decode path
-    assert _call(8, 2560, 512, 10, 640) == 2                       # MOE_ERR_UNSUPPORTED
+    assert _call(9, 2560, 512, 10, 640) == 2                       # MOE_ERR_UNSUPPORTED
     # a decode shape whose workspace exceeds the 1 MiB static scratch
     assert moe.moe_forward_plan(7, 6144, 1024, 32, 640) is not None
     need = moe.moe_workspace_size(7, 6144, 1024, 32, 640)

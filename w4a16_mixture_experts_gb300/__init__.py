@@ -225,7 +225,7 @@ def moe_w4a16_forward(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed,
 
 def moe_w4a16_forward_noalloc(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales,
                               out=None, stream=None):
-    """moe_w4a16_forward for decode batches (T <= 7) with the library's own static scratch.
+    """moe_w4a16_forward for decode batches (T <= 8) with the library's own static scratch.
 
     No workspace is passed or allocated; calls on one device must not overlap.
     """

@@ -77,7 +77,7 @@ inline int router_ksplit(const moe_dims &d) {   // at most 16
     return 1;
 }
 
-// True when the forward calls take the fused decode kernel (T <= 7 and its
+// True when the forward calls take the fused decode kernel (T <= 8 and its
 // shared-memory layout fits); otherwise they take the prefill pipeline. The
 // workspace holds the regions of the path that will run.
 bool fused_supported(const moe_dims &d);

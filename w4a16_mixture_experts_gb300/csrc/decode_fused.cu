@@ -2,7 +2,7 @@
 //
 // Computes the fused Marlin MoE of "Running 125B MoE on Three 3090s - vLLM
 // Optimization Edition", section 3.3 "MoE block" (moe_align_block_size,
-// gate_up, SiluAndMul, down, moe_sum) for decode batches (T <= 7), on
+// gate_up, SiluAndMul, down, moe_sum) for decode batches (T <= 8), on
 // symmetric INT4 group-128 weights (model card, "What is quantized", group A).
 // At decode the layer streams ~2.5 MB of packed weights per active expert
 // and does a few FLOPs per byte, so everything here serves the byte stream:
@@ -64,10 +64,11 @@ constexpr int kNS = 29;              // stages of the CTA's chunk ring
 constexpr int kRedMax = 20480;       // bytes for the gate_up partial-sum buffers
 constexpr int kMaxNB = 8;            // partial-sum buffers (gate_up tasks in flight)
 constexpr int kP2Rows = 16;          // output rows per down item
-// Batches of up to 7 tokens. From 8 tokens on, the tensor-core grouped GEMM
-// (prefill.cu) is as fast on GB300 and grows faster (measured: T = 8 at 114
-// us either way, T = 64 at 378 us there against 662 us here).
-constexpr int kDecodeMaxT = 7;
+// Batches of up to 8 tokens (route + forward at T = 8: 88.6 us here against
+// 96.9 us on the tensor-core grouped GEMM of prefill.cu, measured). Beyond, an
+// expert can hold more than one 8-token MMA tile, which the gate_up reduction
+// slots do not provide for, and the tensor-core path grows more slowly.
+constexpr int kDecodeMaxT = 8;
 constexpr int kMaxNT = (kDecodeMaxT + 7) / 8;   // token tiles of 8 per expert
 static_assert(kMaxNT == 1, "the gate_up reduction slots hold one token tile");
 constexpr int kFastN = 256;          // assignments ranked by comparison: one thread each

@@ -51,7 +51,7 @@ bool prefill_supported(const moe_dims &d);
 cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next, float eps,
                            cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t s);
 
-// Fused decode forward (T <= 7): permute, experts and combine in one launch.
+// Fused decode forward (T <= 8): permute, experts and combine in one launch.
 bool fused_supported(const moe_dims &d);
 // 0 if the forward takes the tensor-core pipeline; else 1 (activations staged
 // in shared memory) or 2 (read from global memory), plus 16 * quantisation

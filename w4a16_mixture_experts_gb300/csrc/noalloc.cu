@@ -13,7 +13,7 @@
 // library.
 //
 // Limits and rules (also stated in w4a16moe.h):
-//  - Only the fused decode path (T <= 7) is served, and only when the
+//  - Only the fused decode path (T <= 8) is served, and only when the
 //    workspace layout of the shape fits in kStaticScratchBytes (1 MiB);
 //    larger shapes are rejected with MOE_ERR_WORKSPACE before anything is
 //    enqueued.
