@@ -159,17 +159,18 @@ def _simulate(T, H, E, k, I, nact, seed, gc_max):
     rng = random.Random(seed)
     kCons, kNS = C["kCons"], C["kNS"]
     nkc, nb, nyb, ysep, tp1, n1, grid, spread = _launch(T, H, E, k, I, nact, gc_max)
-    w = C["kSpreadDownWeight"] if spread else 1
+    M = task_stride(n1, nkc, grid) if spread else 0
+    w = C["kSpreadDownWeight"] if M else 1
     done1 = [0] * nact
     ctas = []
     covered_tasks, covered_blocks = [], []
     for cb in range(grid):
         b1, m1, cb0, cb1 = _split(H, I, nact, grid, cb, w)
-        tasks = cta_tasks(b1, m1, n1, task_stride(n1, nkc, grid) if spread else 0)
+        tasks = cta_tasks(b1, m1, n1, M)
         covered_tasks += tasks
         covered_blocks += list(range(cb0, cb1))
         # down chunks block by block, or (spread order) expert by expert when every block has a buffer
-        if spread and cb1 - cb0 <= nyb:
+        if M and cb1 - cb0 <= nyb:
             down = [("dn", a, c - cb0) for a in range(nact) for c in range(cb0, cb1)]
         else:
             down = [("dn", a, c - cb0) for c in range(cb0, cb1) for a in range(nact)]

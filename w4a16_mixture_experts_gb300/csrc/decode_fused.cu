@@ -1090,13 +1090,16 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     const int nact = *v.nact;
     const int n1 = nact * (p.I / 8);
     int b1, m1, cb0, cb1;
-    fused_split(p, nact, gridDim.x, blockIdx.x, kSpread ? kSpreadDownWeight : 1, b1, m1, cb0, cb1);
-    const int nblk = cb1 - cb0, m2 = nblk * nact;   // down chunks of whole blocks
-    const bool emaj = kSpread && nblk <= p.nyb;   // (block by block measured faster at T = 1)
-    // the CTA's gate_up tasks in increasing order (see task_stride), in the
-    // prologue's scratch array, free now; with M = 0, or more tasks than
-    // threads, the tasks are b1 + u (the partition is M's either way)
+    // the task order (see task_stride; the same in every CTA), then the split,
+    // whose weight w and the down order follow it: with the plain order,
+    // w = 1 and block by block (measured faster at T = 1)
     const int M = kSpread ? task_stride(n1, p.nkc, gridDim.x) : 0;
+    fused_split(p, nact, gridDim.x, blockIdx.x, M != 0 ? kSpreadDownWeight : 1, b1, m1, cb0, cb1);
+    const int nblk = cb1 - cb0, m2 = nblk * nact;   // down chunks of whole blocks
+    const bool emaj = M != 0 && nblk <= p.nyb;
+    // the CTA's gate_up tasks in increasing order, in the prologue's scratch
+    // array, free now; with M = 0, or more tasks than threads, the tasks are
+    // b1 + u (the partition is M's either way)
     const uint16_t *tab = nullptr;
     if (kSpread && M != 0 && m1 <= kFW * 32) {
         uint16_t *t16 = reinterpret_cast<uint16_t *>(v.cnt);
