@@ -7,8 +7,9 @@
 // At decode the layer streams ~2.5 MB of packed weights per active expert
 // and does a few FLOPs per byte, so everything here serves the byte stream:
 //
-//  * One persistent CTA per SM, launched programmatically behind the router,
-//    so that it takes its SM and sets up while the router finishes. Each CTA
+//  * One persistent CTA per SM, launched cooperatively (the CTAs wait on one
+//    another, so all must be resident) and programmatically behind the
+//    router, so that the launch is under way while the router finishes. Each CTA
 //    first derives the whole token-to-expert permutation from topk_ids in
 //    shared memory (every CTA computes the same result), so no separate
 //    permute launch sits on the critical path. Each assignment is ranked by
@@ -21,17 +22,20 @@
 //    expert's W2, all of K = I), so the sum over experts never leaves the
 //    CTA. The gate_up tasks are shared out so that every CTA streams about
 //    the same number of bytes. A CTA runs its work as one sequence of
-//    chunks: all its gate_up chunks first, then its down chunks, block by
-//    block.
+//    chunks: all its gate_up chunks first, then its down chunks. From two
+//    rounds of work on, the tasks are dealt in a stride order and each CTA
+//    takes them expert by expert, so that experts complete one after another
+//    (see task_stride).
 //  * One producer warp issues the copies of the sequence (two 2-D TMA boxes
 //    per gate_up chunk, one bulk copy per down chunk) into a ring of kNS
 //    shared-memory stages completed on mbarriers; its lanes issue side by
 //    side. The copy instructions themselves are the limit of this stream (a
 //    few tens of ns each per SM, measured), so the small scale rows do not
-//    take copies of their own: each consumer loads its chunk's scales with
-//    plain loads before it waits for the chunk's data. The kCons consumer warps take chunks in
-//    sequence order by a shared ticket and hand each stage back as soon as
-//    they are done with it, so up to kNS copies are in flight per SM.
+//    take copies of their own: the producer prefetches them into L2, and
+//    each consumer loads its chunk's scales with plain loads before it waits
+//    for the chunk's data. The kCons consumer warps take chunks in sequence
+//    order by a shared ticket and hand each stage back as soon as they are
+//    done with it, so up to kNS copies are in flight per SM.
 //  * Weights are dequantised in registers into mma.sync m16n8k16 A fragments
 //    (bf16 holds 128 + n exactly, and one lop3 makes a pair); each group's
 //    fp32 partial sum is corrected by 136 * sum(x) over the group and scaled
