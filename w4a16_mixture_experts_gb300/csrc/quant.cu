@@ -21,8 +21,8 @@
 // which neither underflows for tiny weights nor overflows for large ones.
 //
 // One warp per group: lane l holds values 4l .. 4l + 3 (one 8-byte load), the
-// warp forms amax, then for each candidate the lanes' partial errors are summed
-// by shuffles. The work is arithmetic (nclip quotients per value): the kernel is
+// warp forms amax, the lanes prepare one candidate scale each (32 at a time),
+// then for each candidate the lanes' partial errors are summed by shuffles. The work is arithmetic (nclip quotients per value): the kernel is
 // bound by the ALU, not by HBM. Lanes 2m and 2m + 1 together fill word m.
 //
 // The quotient w / s of the search is formed as w * RN(1 / s): within 2^-23
@@ -83,34 +83,51 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_int4_kernel(const uint1
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         int best = 0;
         float best_err = 0.f;
-        for (int j = 0; j < nclip; ++j) {
-            const float s = clip_scale_dev(amax, j);
-            float e = 0.f;
-            if (s != 0.0f) {
-                // in units of s: d = w/s - q, then scaled by (s / amax)^2
-                const float inv = __frcp_rn(s);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float q;
-                    const float r = quotient(v[i], s, inv, q);
-                    const float d = r - fminf(fmaxf(q, -8.0f), 7.0f);
-                    e = fmaf(d, d, e);
-                }
-                const float ratio = __fdiv_rn(s, amax);
-                e *= ratio * ratio;
-            } else if (amax != 0.0f) {
-                // a scale that underflowed: every code is 0, the error is the group itself
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float d = __fdiv_rn(v[i], amax);
-                    e = fmaf(d, d, e);
+        for (int jb = 0; jb < nclip; jb += 32) {
+            // lane l prepares candidate jb + l (its scale, the reciprocal and (s / amax)^2,
+            // the same for every lane), and the candidates are taken from their lanes in
+            // turn: half of a candidate's instructions were these warp-uniform divisions
+            const int jl = jb + lane;
+            float ls = 0.f, linv = 0.f, lr2 = 0.f;
+            if (jl < nclip) {
+                ls = clip_scale_dev(amax, jl);
+                if (ls != 0.0f) {
+                    linv = __frcp_rn(ls);
+                    const float ratio = __fdiv_rn(ls, amax);
+                    lr2 = ratio * ratio;
                 }
             }
+            const int jn = nclip - jb < 32 ? nclip - jb : 32;
+            for (int jj = 0; jj < jn; ++jj) {
+                const int j = jb + jj;
+                const float s = __shfl_sync(0xffffffffu, ls, jj);
+                const float inv = __shfl_sync(0xffffffffu, linv, jj);
+                const float r2 = __shfl_sync(0xffffffffu, lr2, jj);
+                float e = 0.f;
+                if (s != 0.0f) {
+                    // in units of s: d = w/s - q, then scaled by (s / amax)^2
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
-            if (j == 0 || e < best_err) {
-                best = j;
-                best_err = e;
+                    for (int i = 0; i < 4; ++i) {
+                        float q;
+                        const float r = quotient(v[i], s, inv, q);
+                        const float d = r - fminf(fmaxf(q, -8.0f), 7.0f);
+                        e = fmaf(d, d, e);
+                    }
+                    e *= r2;
+                } else if (amax != 0.0f) {
+                    // a scale that underflowed: every code is 0, the error is the group itself
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float d = __fdiv_rn(v[i], amax);
+                        e = fmaf(d, d, e);
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+                if (j == 0 || e < best_err) {
+                    best = j;
+                    best_err = e;
+                }
             }
         }
         const float s = clip_scale_dev(amax, best);
