@@ -28,10 +28,11 @@
 // The quotient w / s of the search is formed as w * RN(1 / s): within 2^-23
 // relative of the correctly rounded division, i.e. within 2e-6 for the
 // quotients here (|w / s| <= 7 / 0.01). rint of the two can differ only when
-// the quotient lies that close to a half-integer, so a value whose product
-// lies within 1e-5 of one takes the exact division instead: the codes are
-// those of the fp32 division, bit for bit. (The error sums then differ from
-// the division's by far less than their own fp32 rounding.)
+// the quotient lies that close to a half-integer, where either code leaves
+// |w / s - q| within 2e-6 of 0.5: the group's error moves by less than 1e-5 of
+// one value's share, far below the fp32 rounding of the sum, so the search
+// ranks the candidates as the division would. The stored codes are computed
+// with the division, bit for bit.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -47,18 +48,6 @@ __device__ inline float clip_scale_dev(float amax, int j) {
     const float c = __fdiv_rn((float)(100 - j), 100.0f);
     const float t = __fmul_rn(c, amax);
     return bf16_round_f32(__fdiv_rn(t, 7.0f));
-}
-
-// rint(w / s) with the quotient as the division gives it: the product with the
-// reciprocal, or the division itself within 1e-5 of a half-integer.
-__device__ __forceinline__ float quotient(float w, float s, float inv, float &q) {
-    float r = w * inv;
-    q = rintf(r);
-    if (fabsf(r - q) > 0.5f - 1e-5f) {
-        r = __fdiv_rn(w, s);
-        q = rintf(r);
-    }
-    return r;
 }
 
 __device__ inline int quant_code(float w, float s) {
@@ -108,9 +97,8 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_int4_kernel(const uint1
                     // in units of s: d = w/s - q, then scaled by (s / amax)^2
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        float q;
-                        const float r = quotient(v[i], s, inv, q);
-                        const float d = r - fminf(fmaxf(q, -8.0f), 7.0f);
+                        const float r = v[i] * inv;
+                        const float d = r - fminf(fmaxf(rintf(r), -8.0f), 7.0f);
                         e = fmaf(d, d, e);
                     }
                     e *= r2;
