@@ -262,7 +262,7 @@ __device__ inline void dequant8_w8(const uint4 &a, const uint4 &b, const uint4 &
     }
 }
 
-template <bool kW8>
+template <bool kW8, bool kRed4>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int kRing = kW8 ? kRR8 : kRR;                       // raw weight stages
     constexpr uint32_t kStageBytes = kW8 ? kRawBytes8 : kRawBytes;
@@ -478,14 +478,48 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 // one reduction per (row, token): the 32 lanes of a warp cover 128 consecutive
                 // bytes of the token's output row; the routing weight is already in h
                 float *orow = p.out_acc + T.m * 128 + et;
+                // with kRed4, one 16-byte reduction per (4 rows, token): the 4 lanes of a row
+                // quad swap values in two butterfly stages, so that lane r of the quad holds
+                // rows 4j .. 4j + 3 of token 4i + r. A quarter of the reduction requests at
+                // the cost of the swaps: measured 5% faster for a 4096-token layer, where the
+                // reductions (105 M a layer) bind, and 2-3% slower for 64 to 2048 tokens.
+                float *obase = p.out_acc + T.m * 128 + 32 * q + (lane & ~3);
+                const int r = lane & 3;
+                const bool b1 = (r & 2) != 0, b0 = (r & 1) != 0;
+                (void)orow, (void)obase, (void)b1, (void)b0;
                 for (int c0 = 32 * eh; c0 < T.nv; c0 += 64) {
                     float v[32];
                     tc::ld_32x32b_x32(dbase + c0, v);
                     tc::wait_ld();
                     const int nu = min(32, T.nv - c0);
+                    if constexpr (!kRed4) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        if (u < nu) atomicAdd(orow + (size_t)col_off[c0 + u], v[u]);
+                        for (int u = 0; u < 32; ++u)
+                            if (u < nu) atomicAdd(orow + (size_t)col_off[c0 + u], v[u]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (4 * i < nu) {
+                                const float a0 = v[4 * i], a1 = v[4 * i + 1], a2 = v[4 * i + 2], a3 = v[4 * i + 3];
+                                // stage 1 (lanes r, r ^ 2): keep columns 2 b1, 2 b1 + 1 of rows r, r ^ 2
+                                const float k0 = b1 ? a2 : a0, k1 = b1 ? a3 : a1;
+                                const float g0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
+                                const float g1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
+                                // stage 2 (lanes r, r ^ 1): keep column r of all four rows
+                                const float kr = b0 ? k1 : k0, kq = b0 ? g1 : g0;
+                                const float h1 = __shfl_xor_sync(0xffffffffu, b0 ? k0 : k1, 1);
+                                const float h3 = __shfl_xor_sync(0xffffffffu, b0 ? g0 : g1, 1);
+                                // row k of token 4i + r is [kr, h1, kq, h3][k ^ r]
+                                float4 o;
+                                o.x = b1 ? (b0 ? h3 : kq) : (b0 ? h1 : kr);
+                                o.y = b1 ? (b0 ? kq : h3) : (b0 ? kr : h1);
+                                o.z = b1 ? (b0 ? h1 : kr) : (b0 ? h3 : kq);
+                                o.w = b1 ? (b0 ? kr : h1) : (b0 ? kq : h3);
+                                if (4 * i + r < nu)
+                                    atomicAdd(reinterpret_cast<float4 *>(obase + (size_t)col_off[c0 + 4 * i + r]), o);
+                            }
+                        }
+                    }
                 }
             } else {
                 uint16_t *hrow = p.hbuf + (size_t)T.s0 * p.I + T.m * 64 + pl;
@@ -657,6 +691,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc::fence_after();
     if (warp == kWMma) tc::dealloc(tmem, kTmemCols);
 }
+// Batches from which the down epilogue reduces 4 rows at a time (measured:
+// slower at 2048 tokens, faster at 4096).
+constexpr int kRed4MinT = 4096;
+
 // ---------------------------------------------------------------------------
 // xs[slot] = x[token of slot] in fragment order within each 8-element chunk
 // (0,4,1,5,2,6,3,7), for the offsets[E] slots that hold a valid assignment.
@@ -842,7 +880,11 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     uint16_t *xperm = ws_at<uint16_t>(ws, W.xperm);
     float *out_acc = ws_at<float>(ws, W.out_acc);
     int32_t *n_chunks = ws_at<int32_t>(ws, W.n_chunks);
-    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<false>), (int)kPrefillSmemMax);
+    // the down launch of a large batch takes the instantiation with 16-byte reductions
+    const bool red4 = d.T >= kRed4MinT;
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<false, false>), (int)kPrefillSmemMax);
+    if (err == cudaSuccess && red4)
+        err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<false, true>), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
 
     {
@@ -892,7 +934,7 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.mb = d.I / 64;
     p.down = 0;
     p.L = prefill_layout(p.K / kKS);
-    prefill_kernel<false><<<grid, kPThreads, p.L.total, s>>>(p);
+    prefill_kernel<false, false><<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // down: K = I, 128 output rows per tile
@@ -908,7 +950,8 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
     p.mb = d.H / 128;
     p.down = 1;
     p.L = prefill_layout(p.K / kKS);
-    prefill_kernel<false><<<grid, kPThreads, p.L.total, s>>>(p);
+    if (red4) prefill_kernel<false, true><<<grid, kPThreads, p.L.total, s>>>(p);
+    else prefill_kernel<false, false><<<grid, kPThreads, p.L.total, s>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = record_profile_event(ev_after, s)) != cudaSuccess) return err;
 
@@ -947,7 +990,7 @@ __global__ void __launch_bounds__(256) w8a16_reduce_kernel(const float *__restri
 
 cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_t *s, int gs, uint16_t *y, int T, int N,
                               int K, Ctrl *ctrl, float *part, cudaStream_t st) {
-    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<true>), (int)kPrefillSmemMax);
+    cudaError_t err = set_smem_once(reinterpret_cast<const void *>(prefill_kernel<true, false>), (int)kPrefillSmemMax);
     if (err != cudaSuccess) return err;
     PrefillParams p{};
     err = encode_tmap_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, w, (uint64_t)K / 4, (uint64_t)N, (uint64_t)K, 32u,
@@ -972,7 +1015,7 @@ cudaError_t launch_w8a16_gemm(const uint16_t *x, const int32_t *w, const uint16_
     p.L = prefill_layout(0);
     const long long tiles = (long long)p.ksplit * p.mb * p.dense_chunks;
     const unsigned grid = (unsigned)(tiles < sm_count() ? tiles : sm_count());
-    prefill_kernel<true><<<grid, kPThreads, p.L.total, st>>>(p);
+    prefill_kernel<true, false><<<grid, kPThreads, p.L.total, st>>>(p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (p.ksplit > 1) {
         const size_t n = (size_t)T * N;
