@@ -682,7 +682,7 @@ def measure_w8a16(args, name, steps, rank, world, local):
     nbytes = sum(N * K + N * (K // gs) * 2 for (N, K, gs) in layers)
     flops = sum(2.0 * T * N * K for (N, K, gs) in layers)
     gbs, tfl = nbytes / (per_layer_ms * 1e-3) / 1e9, flops / (per_layer_ms * 1e-3) / 1e12
-    kern = "w8a16_gemv_kernel" if T <= 8 else "prefill_kernel<true> (dense INT8 GEMM, split over K where it has few tiles)"
+    kern = "w8a16_gemv_kernel" if T <= 8 else "prefill_kernel<true, false> (dense INT8 GEMM, split over K where it has few tiles)"
     if binding_roofline(nbytes, flops, pk["hbm_gbs"], pk["bf16_tflops"]) == "tensor":
         roof = {"kernel": kern, "bound": "tensor", "achieved": tfl, "peak": pk["bf16_tflops"],
                 "peak_source": "%s bf16_tflops (cuBLAS bf16 dense, burst)" % pk_src, "unit": "TFLOP/s",
