@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Throughput of the W4A16 routed-expert MoE layer on GB300.
 
-One step = the whole layer on one batch of synthetic tokens: moe_route
-(router GEMM, softmax, top-k, renormalised weights) then moe_w4a16_forward
-(permute, INT4 expert GEMMs with SiLU*up, weighted combine). The stack
+One step = the whole layer on one batch of synthetic tokens, one
+moe_layer_forward call: the router (GEMM, softmax, top-k, renormalised
+weights) and the routed experts (permute, INT4 expert GEMMs with SiLU*up,
+weighted combine); for decode batches one kernel runs both. The stack
 workloads run 48 such layers, each followed by the residual + RMS rescale.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
@@ -239,11 +240,14 @@ def binding_roofline(bytes_per_launch, flops_per_launch, hbm_gbs, tc_tflops):
     return "tensor" if flops_per_launch / (tc_tflops * 1e12) > bytes_per_launch / (hbm_gbs * 1e9) else "hbm"
 
 
-def launches_per_layer(T: int, E: int) -> int:
-    """Kernels one layer launches: route is one kernel for T <= 8 (logits, then
-    top-k in the last CTA), else logits + top-k; the forward is one fused kernel
-    (the library's decode path, T <= 8), or permute 3 + x gather + chunk table +
+def launches_per_layer(T: int, E: int, routes_itself: bool = False) -> int:
+    """Kernels one layer launches: one when the decode kernel runs the router
+    itself; else the router is one kernel for T <= 8 (logits, then top-k in the
+    last CTA), or logits + top-k, and the forward one fused kernel (the
+    library's decode path, T <= 8), or permute 3 + x gather + chunk table +
     gate_up + down + conversion."""
+    if routes_itself:
+        return 1
     return (1 if T <= 8 else 2) + (1 if T <= FUSED_MAX_T else 8)
 
 
@@ -292,16 +296,16 @@ def measure(args, wl, steps, rank, world, local):
     for e in ev_b + ev_a:       # torch only lets recorded events be timed; the library re-records them
         e.record(stream)
 
-    route = moe.moe_route_shared if wl.shared else moe.moe_route
+    # one call per layer: where the decode kernel runs the router itself, that
+    # one kernel is the layer, and its time includes the router's bytes
+    plan = moe.moe_forward_plan(T, H, Ef, kf, I)
+    routes_itself = bool(plan and plan[3])
+    router_bytes = Ef * H * 2 + (E * 4 if wl.zipf else 0)
 
     def layer_call(x, s, nxt=None, out=None):
-        route(x, s["router_w"], k, bias=s["bias"], ws=ws, topk_ids=ids, topk_w=w)
-        if nxt is not None:
-            moe.moe_w4a16_forward_rms(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                                      s["w2_scales"], eps=1e-6, next=nxt, ws=ws)
-        else:
-            moe.moe_w4a16_forward(x, ids, w, s["w1_packed"], s["w1_scales"], s["w2_packed"],
-                                  s["w2_scales"], out=out, ws=ws)
+        moe.moe_layer_forward(x, s["router_w"], k, s["w1_packed"], s["w1_scales"], s["w2_packed"], s["w2_scales"],
+                              bias=s["bias"], shared=wl.shared, rms=nxt is not None, eps=1e-6,
+                              out=nxt if nxt is not None else out, topk_ids=ids, topk_w=w, ws=ws)
 
     def step(i, profile=False, x_in=None):
         """Enqueue one step (set i for single layers; all layers for the stack)."""
@@ -455,12 +459,13 @@ def measure(args, wl, steps, rank, world, local):
             else:
                 enqueue([i], profile=True)
         stream.synchronize()
+        extra = router_bytes if routes_itself else 0
         if stack:
             durs = [ev_b[l].elapsed_time(ev_a[l]) for l in range(wl.layers)]
-            bytes_l = [u * EXPERT_BYTES for u in unique]
+            bytes_l = [u * EXPERT_BYTES + extra for u in unique]
         else:
             durs = [ev_b[i].elapsed_time(ev_a[i]) for i in range(per)]
-            bytes_l = [unique[i] * EXPERT_BYTES for i in range(per)]
+            bytes_l = [unique[i] * EXPERT_BYTES + extra for i in range(per)]
 
         # end to end through the same calls, with the host copies inside the timed region
         run_steps(per, e2e=True)
@@ -499,10 +504,18 @@ def measure(args, wl, steps, rank, world, local):
     ms_e2e = max_over_ranks(ms_e2e, world)
     ms_eager = max_over_ranks(ms_eager, world)
     fused = T <= FUSED_MAX_T
+    kernel_timing = "CUDA events around the kernel, in one-step graphs replayed after the timed region"
+    if routes_itself:
+        # the step is this one launch (per layer): its duration is the timed region's
+        # events over the launches it holds (the one-step graphs would add a graph
+        # launch's start-up to each)
+        durs = [ms / (steps * wl.layers)] * len(bytes_l)
+        kernel_timing = "CUDA events over the timed region, which holds one launch per layer"
     pk, pk_src = peaks()
     hbm_gbs = sum(bytes_l) / (sum(durs) * 1e-3) / 1e9
     flops_launch = 2.0 * 3 * H * I * T * kf          # algorithmic: gate, up and down over all slots
-    expert_kernel = "decode_fused_kernel" if fused else "prefill_kernel (gate_up + down launches)"
+    expert_kernel = ("decode_fused_kernel (the router inside)" if routes_itself else "decode_fused_kernel") if fused \
+        else "prefill_kernel (gate_up + down launches)"
     if wl.shared:
         expert_kernel += ", shared expert as expert E"
     # the binding roofline: whichever of the unique weight bytes at the copy rate
@@ -524,8 +537,10 @@ def measure(args, wl, steps, rank, world, local):
                 "tensor_achieved_tflops": tflops, "tensor_frac": tflops / pk["bf16_tflops"]}
     roof.update({"algorithmic_bytes_per_launch": statistics.mean(bytes_l),
                  "kernel_ms_per_launch": statistics.mean(durs), "launches_measured": len(durs),
-                 "unique_experts_per_launch": statistics.mean(bytes_l) / EXPERT_BYTES})
-    nlaunch = steps * wl.layers * launches_per_layer(T, E)
+                 "unique_experts_per_launch": statistics.mean(unique[:len(durs)]),
+                 "router_bytes_per_launch": router_bytes if routes_itself else 0,
+                 "kernel_timing": kernel_timing})
+    nlaunch = steps * wl.layers * launches_per_layer(T, E, routes_itself)
     return {
         "metric": "MoE layer tok/s (%s)" % wl.name,
         "value": world * T * steps / (ms * 1e-3),
@@ -553,9 +568,9 @@ def measure(args, wl, steps, rank, world, local):
                           "the steps replayed from CUDA graphs",
                 "eager": {"value": world * T * steps / (ms_eager * 1e-3), "unit": "tok/s",
                           "ms_per_step": ms_eager / steps,
-                          "how": "per step: copy in from pinned host memory, moe_route + moe_w4a16_forward%s "
+                          "how": "per step: copy in from pinned host memory, moe_layer_forward%s "
                                  "called through the C ABI from the host (no graph), copy out; one stream"
-                                 % ("_rms x %d layers" % wl.layers if stack else "")}},
+                                 % (" (with the RMS step) x %d layers" % wl.layers if stack else "")}},
         "gpu_launches": nlaunch,
         "clocks": clk,
     }

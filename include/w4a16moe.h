@@ -31,8 +31,10 @@
  *    workspace's error word and reported by moe_check_device_error.
  *  - Workspace: `ws` must hold at least moe_workspace_size() bytes and must
  *    be all zero before its first use (the library leaves the counters it
- *    uses at zero when a call completes). One workspace must not be used by
- *    two calls that may run concurrently. A call whose bounded wait gave up
+ *    uses at zero when a call completes, at offsets that depend on no
+ *    dimension, so calls of different dims may share a workspace large
+ *    enough for each). One workspace must not be used by two calls that may
+ *    run concurrently. A call whose bounded wait gave up
  *    (MOE_ERR_TIMEOUT) can leave counters non-zero: moe_check_device_error
  *    then clears the whole workspace before it returns, and a caller that
  *    does not call it must clear the workspace itself before reusing it.
@@ -165,6 +167,38 @@ MOE_API int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_id
                           void *stream);
 
 /*
+ * The whole MoE block in one call ("vLLM Optimization Edition", section 3.3
+ * "MoE block (decode-05)": the router GEMV, topk_softmax, the fused experts and
+ * moe_sum; with `shared`, the shared expert's gate as one more router row):
+ *
+ *   moe_route (shared = 0) or moe_route_shared (shared = 1) with dims d,
+ *   then moe_w4a16_forward (out not NULL) or moe_w4a16_forward_rms (next not
+ *   NULL) with dims (T, H, E + shared, k + shared, I).
+ *
+ * Arguments are those of the calls above: router_w bf16 [E + shared][H], bias
+ * f32 [E] or NULL, the weights of E + shared experts, topk_ids int32 and
+ * topk_w f32 [T][k + shared] (outputs: the selection, as the router calls
+ * write it), and exactly one of out / next (the other NULL; eps is read only
+ * with next). The workspace must hold max(moe_workspace_size(d),
+ * moe_workspace_size(T, H, E + shared, k + shared, I)) bytes; the rules on
+ * zeroing are those of every call.
+ *
+ * Where moe_forward_plan reports bit 512 for the forward's dims (decode
+ * batches, T <= 8, whose activations the expert kernel stages in shared
+ * memory), one cooperative kernel runs the block: each CTA computes a few
+ * router rows with the small-batch router's own arithmetic, the CTAs meet at a
+ * grid-wide barrier, every CTA selects the top-k from all logits, and the
+ * experts follow in the same launch. Selection, weights and outputs are then
+ * bit-identical to the separate calls. Otherwise the router's kernels run,
+ * then the forward's.
+ */
+MOE_API int moe_layer_forward(const uint16_t *hidden, const uint16_t *router_w, const float *bias, int32_t shared,
+                      const int32_t *w1_packed, const uint16_t *w1_scales,
+                      const int32_t *w2_packed, const uint16_t *w2_scales,
+                      uint16_t *out, uint16_t *next, float eps, int32_t *topk_ids, float *topk_w,
+                      moe_dims d, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_w4a16_forward for decode batches without a caller workspace. The pages
  * have no counterpart: this entry point exists for callers that cannot
  * provide or allocate a device scratch buffer where they run the layer (a
@@ -271,12 +305,13 @@ MOE_API int moe_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int32_t n
  * Which kernels a forward call of dims `d` runs (a host-only query, no
  * counterpart on the pages; for tests and tuning). Writes *plan = 0 for the
  * tensor-core pipeline (permute, grouped gate_up and down GEMMs, conversion);
- * otherwise the fused decode kernel runs and *plan = s + 16 * g + 256 * y,
+ * otherwise the fused decode kernel runs and *plan = s + 16 * g + 256 * y + 512 * r,
  * where s = 1 if the activations are staged in shared memory and 2 if they
  * are read from global memory, g (at most 15) is the number of 128-wide
  * groups per gate_up chunk, and y = 1 if the down outputs' block buffers have
  * a shared-memory region of their own (0: they reuse the gate_up partial-sum
- * area once the CTA's gate_up work is done).
+ * area once the CTA's gate_up work is done), and r = 1 if moe_layer_forward
+ * runs the router inside the same kernel for these (forward) dims.
  * Returns the shape checks' status.
  */
 MOE_API int moe_forward_plan(moe_dims d, int32_t *plan);

@@ -83,19 +83,35 @@ def _layout_gc(T, H, E, k, I, gc_max, full=False):
         nyb, total = 2, ys_start + 2 * yb
     ok = total <= C["kFusedSmem"] and T <= C["kDecodeMaxT"] and k <= 32 and I <= 1280 and gcw <= 256 and \
         (nyb >= 1 or T == 0)
-    return (ok, staged, gcw, nyb, ysep) if full else (ok, staged, gcw)
+    return (ok, staged, gcw, nyb, ysep, red_off) if full else (ok, staged, gcw)
+
+
+def _route_scratch_start():
+    m = re.search(r"constexpr uint32_t kRtLogit = (\d+);", open(SRC).read())
+    assert m, "kRtLogit"
+    return int(m.group(1))
+
+
+def _route_max_t():
+    m = re.search(r"constexpr int kRouteFusedMaxT = (\d+);", open(SRC).read())
+    assert m, "kRouteFusedMaxT"
+    return int(m.group(1))
 
 
 def fused_plan(T, H, E, k, I):
     """Mirror of fused_layout: None if the decode kernel cannot take the shape,
-    else (staged, groups per chunk, separate block buffers): which
-    instantiation of the kernel runs, and which of its two buffer placements."""
+    else (staged, groups per chunk, separate block buffers, routes itself):
+    which instantiation of the kernel runs, which of its two buffer
+    placements, and whether the router's scratch (the logits after a fixed
+    head) fits the ring, which it occupies before the first weight copy."""
     a = _layout_gc(T, H, E, k, I, C["kGC"], full=True)
-    if a[0] and a[1]:
-        return a[1], a[2] // 16, a[4]
-    b = _layout_gc(T, H, E, k, I, C["kGCMin"], full=True)
-    pick = b if b[0] and (b[1] or not a[0]) else a
-    return (pick[1], pick[2] // 16, pick[4]) if pick[0] else None
+    if not (a[0] and a[1]):
+        b = _layout_gc(T, H, E, k, I, C["kGCMin"], full=True)
+        a = b if b[0] and (b[1] or not a[0]) else a
+    if not a[0]:
+        return None
+    route = a[1] and T <= _route_max_t() and T * k <= C["kFastN"] and _route_scratch_start() + 4 * T * E <= a[5]
+    return a[1], a[2] // 16, a[4], route
 
 
 def _launch(T, H, E, k, I, nact, gc_max, sms=152):
@@ -103,7 +119,7 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
     gc = min(G1, gc_max)
     nkc = -(-G1 // gc)
     nb = max(1, min(C["kMaxNB"], C["kRedMax"] // (nkc * 512)))
-    _, _, _, nyb, ysep = _layout_gc(T, H, E, k, I, gc_max, full=True)
+    _, _, _, nyb, ysep, _ = _layout_gc(T, H, E, k, I, gc_max, full=True)
     tp1 = I // 8
     n1 = nact * tp1
     chunks = min(T * k, E) * (tp1 * nkc + H // C["kP2Rows"])
@@ -114,27 +130,33 @@ def _launch(T, H, E, k, I, nact, gc_max, sms=152):
 
 
 def _split(H, I, nact, Cg, cb, w=1):
-    """Mirror of fused_split (exact integer arithmetic, as the kernel's result):
-    (first gate_up task, tasks, first block, end block); w weighs a CTA's own
-    down bytes."""
+    """Mirror of fused_split and its host constants: (first gate_up task, tasks,
+    first block, end block); w weighs a CTA's own down bytes. The task bounds
+    are f(c) = floor(n1 * (fp32(cum(c)) * fp32(1 / cum(Cg)))), in fp32 as the
+    kernel computes them."""
+    import numpy as np
     B = H // C["kP2Rows"]
     n1 = nact * (I // 8)
     cb0, cb1 = B * cb // Cg, B * (cb + 1) // Cg
-    blk = nact * I
-    total = n1 * H + B * blk
     bmin = B // Cg
-    x0 = max(0, total - Cg * w * blk * bmin)
-    x1 = max(0, total - Cg * w * blk * (bmin + 1))
+    unit = (I // 8) * H + B * I
+    x0 = max(0, unit - Cg * w * I * bmin)
+    x1 = max(0, unit - Cg * w * I * (bmin + 1))
+    allv = Cg * x0 + (B - bmin * Cg) * (x1 - x0)
+    r = np.float32(1.0 / allv) if allv > 0 else np.float32(0.0)
 
-    def cum(c):
+    def at(c):
+        if c <= 0:
+            return 0
+        if c >= Cg:
+            return n1
+        if r == 0:
+            return n1 * c // Cg
         nbig = B * c // Cg - bmin * c
-        return c * x0 + nbig * (x1 - x0)
+        cum = c * x0 + nbig * (x1 - x0)
+        return int(np.floor(np.float32(n1) * (np.float32(cum) * r)))
 
-    a = cum(Cg)
-    if a > 0:
-        s0, s1 = n1 * cum(cb) // a, n1 * cum(cb + 1) // a
-    else:
-        s0, s1 = n1 * cb // Cg, n1 * (cb + 1) // Cg
+    s0, s1 = at(cb), at(cb + 1)
     return s0, s1 - s0, cb0, cb1
 
 
@@ -311,6 +333,19 @@ def test_mirror_matches_library_plan_over_many_shapes():
     for shape in ((7, 4096, 8, 8, 128), (6, 4608, 8, 8, 128), (5, 5888, 8, 4, 128), (4, 7296, 8, 8, 128)):
         assert fused_plan(*shape)[2] is False
         assert _library_plan(*shape) == fused_plan(*shape), shape
+
+
+def test_router_runs_inside_the_decode_kernel_at_the_benchmark_shapes():
+    # the full layer shape (with and without the shared expert) up to the
+    # kernel's batch limit for it, and the largest router there (1024 experts)
+    tmax = _route_max_t()
+    for T in range(1, C["kDecodeMaxT"] + 1):
+        assert fused_plan(T, 2560, 512, 10, 640)[3] == (T <= tmax), T
+        assert fused_plan(T, 2560, 513, 11, 640)[3] == (T <= tmax), T
+    assert fused_plan(tmax, 2560, 1024, 32, 640)[3]
+    # the smallest ring (H = I = 128) still holds the logits of tmax tokens x 1024 experts
+    assert fused_plan(tmax, 128, 1024, 8, 128)[3]
+    assert not fused_plan(tmax + 1, 2560, 512, 10, 640)[3]
 
 
 def test_decode_takes_every_batch_up_to_its_limit_at_full_shape():

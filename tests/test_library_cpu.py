@@ -153,4 +153,6 @@ def test_workspace_holds_the_regions_of_the_path_taken():
     big = moe.moe_workspace_size(T, H, E, k, 1408)
     small = moe.moe_workspace_size(T, H, E, k, 128)
     assert big >= T * k * H * 2 + T * H * 4 + T * k * 1408 * 2
-    assert small < T * k * H * 2 + T * H * 4 + T * k * 128 * 2 + 64 * 1024
+    # the same fixed head (control block, per-expert counters for every id) in
+    # both; only the prefill one adds the per-slot activations and the accumulator
+    assert small + T * k * H * 2 + T * H * 4 <= big

@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.moe_w4a16_forward.restype = I
         L.moe_w4a16_forward_rms.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, D, P, Z, P]
         L.moe_w4a16_forward_rms.restype = I
+        L.moe_layer_forward.argtypes = [P, P, P, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_float, P, P, D, P, Z, P]
+        L.moe_layer_forward.restype = I
         L.moe_w4a16_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, D, P]
         L.moe_w4a16_forward_noalloc.restype = I
         L.moe_permute.argtypes, L.moe_permute.restype = [P, D, P, P, P, Z, P], I
@@ -257,6 +259,43 @@ def moe_w4a16_forward_rms(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_pac
     return next
 
 
+def moe_layer_forward(hidden, router_w, k: int, w1_packed, w1_scales, w2_packed, w2_scales, bias=None,
+                      shared: bool = False, rms: bool = False, eps: float = 1e-6, out=None, topk_ids=None,
+                      topk_w=None, ws=None, stream=None):
+    """Router and experts in one call: moe_route (moe_route_shared with shared)
+    then moe_w4a16_forward (moe_w4a16_forward_rms with rms), one kernel for
+    decode batches. router_w [E (+1), H]; the weights hold E (+1) experts.
+
+    Returns (out or next bf16 [T, H], topk_ids int32 [T, k (+1)], topk_w f32 [T, k (+1)]).
+    """
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(router_w, "router_w", torch.bfloat16, 2)
+    _need(w1_packed, "w1_packed", torch.int32, 3)
+    _need(w2_packed, "w2_packed", torch.int32, 3)
+    _need(w1_scales, "w1_scales", torch.bfloat16, 3)
+    _need(w2_scales, "w2_scales", torch.bfloat16, 3)
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+    T, H = hidden.shape
+    g = 1 if shared else 0
+    E = router_w.shape[0] - g
+    I = w1_packed.shape[1] // 2
+    dims = moe_dims(T, H, E, k, I)
+    if ws is None:
+        ws = shared_workspace(T, H, E, k, I, hidden.device) if shared else workspace(T, H, E, k, I, hidden.device)
+    if topk_ids is None:
+        topk_ids = torch.empty(T, k + g, dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, k + g, dtype=torch.float32, device=hidden.device)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(lib().moe_layer_forward(_p(hidden), _p(router_w), _p(bias), g, _p(w1_packed), _p(w1_scales),
+                                   _p(w2_packed), _p(w2_scales), None if rms else _p(out), _p(out) if rms else None,
+                                   float(eps), _p(topk_ids), _p(topk_w), dims, _p(ws), ws.numel(), _stream(stream)),
+           "moe_layer_forward")
+    return out, topk_ids, topk_w
+
+
 def moe_permute(topk_ids, E: int, H: int = 128, I: int = 128, ws=None, stream=None):
     """(offsets int32 [E+1], perm int32 [T*k]) of the stable token-to-expert permutation."""
     _need(topk_ids, "topk_ids", torch.int32, 2)
@@ -283,13 +322,14 @@ def moe_pack_int4(q, bad_count=None, stream=None):
 
 def moe_forward_plan(T: int, H: int, E: int, k: int, I: int):
     """None if a forward of these dims takes the tensor-core pipeline, else
-    (staged, groups_per_chunk, separate_block_buffers) of the fused decode
-    kernel it runs."""
+    (staged, groups_per_chunk, separate_block_buffers, routes_itself) of the
+    fused decode kernel it runs; routes_itself: moe_layer_forward runs the
+    router in the same kernel for these (forward) dims."""
     v = ctypes.c_int32(-1)
     _check(lib().moe_forward_plan(moe_dims(T, H, E, k, I), ctypes.byref(v)), "moe_forward_plan")
     if v.value == 0:
         return None
-    return (v.value & 15) == 1, (v.value >> 4) & 15, bool(v.value & 256)
+    return (v.value & 15) == 1, (v.value >> 4) & 15, bool(v.value & 256), bool(v.value & 512)
 
 
 def moe_quantize_int4(w, nclip: int = 50, with_choice: bool = False, stream=None):

@@ -206,6 +206,46 @@ int moe_w4a16_forward_rms(const uint16_t *hidden, const int32_t *topk_ids, const
                         ws, ws_bytes, stream);
 }
 
+int moe_layer_forward(const uint16_t *hidden, const uint16_t *router_w, const float *bias, int32_t shared,
+                      const int32_t *w1_packed, const uint16_t *w1_scales, const int32_t *w2_packed,
+                      const uint16_t *w2_scales, uint16_t *out, uint16_t *next, float eps, int32_t *topk_ids,
+                      float *topk_w, moe_dims d, void *ws, size_t ws_bytes, void *stream) {
+    if (shared != 0 && shared != 1) return MOE_ERR_INVALID_ARG;
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (shared && (d.k + 1 > kMaxK || d.E + 1 > kMaxE)) return MOE_ERR_UNSUPPORTED;
+    // the forward's dims: the shared expert is one more expert and one more slot
+    const moe_dims df{d.T, d.H, d.E + shared, d.k + shared, d.I};
+    if ((rc = check_dims(df))) return rc;
+    const bool empty = d.T == 0;
+    if (!empty && (out != nullptr) == (next != nullptr)) return MOE_ERR_INVALID_ARG;   // exactly one output
+    if (!ptr_ok(hidden, empty) || !ptr_ok(router_w, false) || !ptr_ok(topk_ids, empty) || !ptr_ok(topk_w, empty))
+        return MOE_ERR_INVALID_ARG;
+    if (!ptr_ok(w1_packed, false) || !ptr_ok(w1_scales, false) || !ptr_ok(w2_packed, false) ||
+        !ptr_ok(w2_scales, false))
+        return MOE_ERR_INVALID_ARG;
+    if (!ptr_ok(next ? (const void *)next : (const void *)out, empty)) return MOE_ERR_INVALID_ARG;
+    if (next && !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+    if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+    // one workspace serves the router (dims d) and the forward (dims df)
+    if ((rc = check_ws(d, ws, ws_bytes)) || (rc = check_ws(df, ws, ws_bytes))) return rc;
+    if (empty) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fused_route_supported(df)) {
+        const ExpertArgs a{hidden, nullptr, nullptr, w1_packed, w1_scales, w2_packed, w2_scales};
+        const RouteArgs r{router_w, bias, topk_ids, topk_w, shared};
+        cudaError_t err = record_profile_event(g_ev_before, s);
+        if (err == cudaSuccess) err = launch_decode_fused(a, df, ws, out, next, eps, s, &r);
+        if (err == cudaSuccess) err = record_profile_event(g_ev_after, s);
+        return cuda_status(err);
+    }
+    // otherwise the router's kernels, then the forward's
+    const cudaError_t err = launch_route(hidden, router_w, bias, d, topk_ids, topk_w, ws, s, shared != 0);
+    if (err != cudaSuccess) return cuda_status(err);
+    return forward_impl(hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales, out, next, eps, df, ws,
+                        ws_bytes, stream);
+}
+
 int moe_permute(const int32_t *topk_ids, moe_dims d, int32_t *offsets, int32_t *perm, void *ws, size_t ws_bytes,
                 void *stream) {
     int rc = check_dims(d);

@@ -20,6 +20,7 @@ constexpr uint32_t kSpinLimit = 1u << 22;   // polls before a wait gives up (~0.
 // Per-expert completion counters sit one 128-byte line apart, so that the
 // pollers and the increments of different experts do not share a line.
 constexpr int kCtrStride = 32;
+constexpr int kRowssMax = 8;   // tokens of the decode stack step's per-token sums
 
 struct Ctrl {
     uint32_t error;          // first MOE_ERR_DEVICE / MOE_ERR_TIMEOUT seen
@@ -28,7 +29,8 @@ struct Ctrl {
     uint32_t bar_arrive;     // grid barrier of the decode stack step: CTAs arrived
     uint32_t bar_depart;     // ... and CTAs done with the rows after it (the last resets both)
     uint32_t exit_count;     // decode CTAs finished (the last resets the per-expert counters)
-    uint32_t pad1[58];
+    uint32_t route_arrive;   // grid barrier of the decode kernel that routes itself: CTAs with their logits stored
+    uint32_t pad1[57];
 };
 static_assert(sizeof(Ctrl) == 256, "control block");
 
@@ -90,13 +92,18 @@ inline WsLayout ws_layout(const moe_dims &d) {
     const size_t H = (size_t)d.H, I = (size_t)d.I;
     L.ksplit = router_ksplit(d);
     L.nchunk = (int)((T * k + kPermChunk - 1) / kPermChunk);
+    // the regions that must be zero when a call starts (each call leaves them
+    // so) come first, with sizes and offsets that depend on no dimension, so
+    // that calls of different dims can share one workspace (a router call of
+    // dims (E, k) and the forward of its layer with a shared expert, dims
+    // (E + 1, k + 1), among them)
     L.ctrl = take(sizeof(Ctrl));
+    L.rowss = take(kRowssMax * 4);
+    L.done1 = take((size_t)kMaxE * kCtrStride * 4);   // every expert id a call can have
     L.partial = take((size_t)L.ksplit * T * (E + 1) * 4);   // (+1: a shared expert's gate row)
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.active = take(E * 4);
-    L.done1 = take((size_t)E * kCtrStride * 4);
-    L.rowss = take(T * 4);
     const bool small = fused_supported(d);
     L.rbuf = take(small ? T * H * 4 : 0);
     L.chunk = take((size_t)(L.nchunk > 0 ? L.nchunk : 1) * E * 4);

@@ -9,7 +9,11 @@
 //
 //  * One persistent CTA per SM, launched cooperatively (the CTAs wait on one
 //    another, so all must be resident) and programmatically behind the
-//    router, so that the launch is under way while the router finishes. Each CTA
+//    router, so that the launch is under way while the router finishes. Or
+//    the kernel runs the router itself (moe_layer_forward): each CTA computes
+//    a few router rows, the CTAs meet at a grid-wide barrier, and each selects
+//    the top-k from all logits (see f_route); this removes the router's own
+//    launch, its last-CTA hand-over and the wait between the kernels. Each CTA
 //    first derives the whole token-to-expert permutation from topk_ids in
 //    shared memory (every CTA computes the same result), so no separate
 //    permute launch sits on the critical path. Each assignment is ranked by
@@ -56,6 +60,7 @@
 //    barrier). All counters reset themselves.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -73,6 +78,7 @@ constexpr int kP2Rows = 16;          // output rows per down item
 // expert can hold more than one 8-token MMA tile, which the gate_up reduction
 // slots do not provide for, and the tensor-core path grows more slowly.
 constexpr int kDecodeMaxT = 8;
+static_assert(kDecodeMaxT <= kRowssMax, "the stack step's per-token sums fit their region");
 constexpr int kMaxNT = (kDecodeMaxT + 7) / 8;   // token tiles of 8 per expert
 static_assert(kMaxNT == 1, "the gate_up reduction slots hold one token tile");
 constexpr int kFastN = 256;          // assignments ranked by comparison: one thread each
@@ -106,6 +112,17 @@ struct FusedParams {
     uint32_t pro_off;    // offset of the permutation arrays
     uint32_t xs_off;     // offset of the staged activations (0: not staged)
     uint32_t ys_off;     // offset of the output-block buffers (0: in the partial-sum area)
+    // the router, when the kernel runs it (E, k above count the shared expert)
+    const uint16_t *wr;  // bf16 [E][H] router rows (row E - 1 the shared gate if rgate)
+    const float *rbias;  // f32 [E - rgate] or null
+    float *logits;       // f32 [T][E] (workspace)
+    int32_t *ids_out;    // int32 [T][k] selection (output)
+    float *w_out;        // f32 [T][k]
+    int rgate;           // 1: a shared expert (slot k - 1 of each token, expert E - 1)
+    // the work split's constants per unit of active experts, for the down
+    // weights w = 1 and w = kSpreadDownWeight (see fused_split)
+    long long sx0[2], sx1[2];
+    float sr[2];         // 1 / (the sum of all capacities), or 0: an even split
 };
 
 struct FusedLayout {
@@ -208,10 +225,37 @@ inline FusedLayout fused_layout(const moe_dims &d) {
 
 bool fused_supported(const moe_dims &d) { return fused_layout(d).ok; }
 
+// Scratch of the router phase at the start of the ring (free until the first
+// weight copy): candidate keys, quarter sums, the selection, the logits.
+constexpr uint32_t kRtCand = 0;       // uint64 [kRouteWarps][32]
+constexpr uint32_t kRtPart = 4096;    // f32 [kRouteWarps][kRouteInlineMaxT]
+constexpr uint32_t kRtIds = 4608;     // int32 [T * k] <= kFastN
+constexpr uint32_t kRtW = 5632;       // f32 [T * k]
+constexpr uint32_t kRtLogit = 6656;   // f32 [T][E]
+static_assert(kRtPart >= kRouteWarps * 32 * 8 && kRtIds - kRtPart >= kRouteWarps * kRouteInlineMaxT * 4 &&
+                  kRtW - kRtIds >= kFastN * 4 && kRtLogit - kRtW >= kFastN * 4,
+              "router scratch");
+static_assert(kFW == kRouteWarps, "the router selection runs on the kernel's warps");
+
+// The kernel runs the router itself for batches of up to kRouteFusedMaxT
+// tokens. Measured (route + forward in one graph of 10 layers, H 2560, E 512,
+// k 10, I 640; separate calls -> one kernel): T = 1 29.91 -> 29.42 us, T = 2
+// 36.92 -> 36.63, T = 4 54.75 -> 54.88, T = 7 81.19 -> 82.09, T = 8 88.76 ->
+// 89.60. Each CTA reads all T x E logits after the barrier (the same lines,
+// from every SM) and selects for every token, which outweighs the saved
+// hand-over from 4 tokens on.
+constexpr int kRouteFusedMaxT = 2;
+
+bool fused_route_supported(const moe_dims &d) {
+    const FusedLayout L = fused_layout(d);
+    return L.ok && L.xs_off && d.T <= kRouteFusedMaxT && (size_t)d.T * d.k <= kFastN &&
+           kRtLogit + (size_t)d.T * d.E * 4 <= L.red_off;
+}
+
 int fused_plan(const moe_dims &d) {
     const FusedLayout L = fused_layout(d);
     if (!L.ok) return 0;
-    return (L.xs_off ? 1 : 2) | ((L.gcw / 16) << 4) | (L.ys_off ? 256 : 0);
+    return (L.xs_off ? 1 : 2) | ((L.gcw / 16) << 4) | (L.ys_off ? 256 : 0) | (fused_route_supported(d) ? 512 : 0);
 }
 
 struct Pro {   // permutation arrays in shared memory
@@ -908,7 +952,10 @@ __device__ __noinline__ void f_exit(const FusedParams &p, const Pro &v) {
     if (!s_last) return;
     const int nact = *v.nact;
     for (int a = threadIdx.x; a < nact; a += blockDim.x) p.done1[(size_t)v.act[a] * kCtrStride] = 0;
-    if (threadIdx.x == 0) p.ctrl->exit_count = 0;
+    if (threadIdx.x == 0) {
+        p.ctrl->route_arrive = 0;
+        p.ctrl->exit_count = 0;
+    }
 }
 
 // The producer warp: lane l issues chunks l, l + 32, ... of the CTA's
@@ -960,55 +1007,133 @@ __device__ __noinline__ void f_produce(const FusedParams &p, const Pro &v, uint8
     }
 }
 
+// ---- the router, run by the kernel itself ------------------------------------
+// Router rows 4 (C r + b) .. 4 (C r + b) + 3 go to CTA b of C in pass r, four
+// warps a row, with the small-batch router's own code (route_dev.cuh), so the
+// logits, the selected experts and their weights are those of moe_route bit
+// for bit. The logits go to the workspace; the CTAs meet at a grid-wide
+// barrier (a count on the control block: each CTA adds itself with release
+// semantics after its stores, thread 0 polls with acquire, bounded); then
+// every CTA loads all T x E logits into its ring (free until the first weight
+// copy) and selects for itself, so that no second hand-over follows. CTA 0
+// writes the selection out. Thread a < T k leaves with assignment a's id and
+// weight. The activations were copied into shared memory (row-major) at entry
+// and are rewritten in fragment order only later (fused_stage). Inlined, so
+// that its shared-memory accesses are known to be shared (a call passes a
+// generic pointer).
+__device__ __forceinline__ void f_route(const FusedParams &p, uint8_t *smem, const Pro &v, int &id_reg,
+                                        float &w_reg) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Eg = p.E, Er = p.E - p.rgate, kr = p.k - p.rgate;
+    uint64_t(*s_cand)[32] = reinterpret_cast<uint64_t(*)[32]>(smem + kRtCand);
+    float(*s_part)[kRouteInlineMaxT] = reinterpret_cast<float(*)[kRouteInlineMaxT]>(smem + kRtPart);
+    int32_t *s_ids = reinterpret_cast<int32_t *>(smem + kRtIds);
+    float *s_w = reinterpret_cast<float *>(smem + kRtW);
+    float *s_logit = reinterpret_cast<float *>(smem + kRtLogit);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(smem + p.xs_off);
+    const int C = gridDim.x, b4 = 4 * (int)blockIdx.x;
+    // the first pass's row loads go out before the wait for the activations
+    RouteQuarter rq = route_quarter(p.wr, b4 + (warp >> 2), Eg, p.H, warp & 3);
+    uint4 wv[kRouteLoads];
+    route_quarter_load(rq, rq.c_lo, lane, wv);
+    if (!mbar_wait(x_bar(v), 0) && tid == 0) set_error(p.ctrl, MOE_ERR_TIMEOUT);
+    for (int e0 = b4; e0 < Eg; e0 += 4 * C) {
+        if (e0 != b4) {
+            rq = route_quarter(p.wr, e0 + (warp >> 2), Eg, p.H, warp & 3);
+            route_quarter_load(rq, rq.c_lo, lane, wv);
+        }
+        float acc[kRouteInlineMaxT];
+        route_quarter_dot(rq, xs, p.T, p.H, lane, wv, acc);
+#pragma unroll
+        for (int t = 0; t < kRouteInlineMaxT; ++t) {
+            if (t >= p.T) break;
+            if (lane == 0) s_part[warp][t] = acc[t];
+        }
+        __syncthreads();
+        if (tid < 4 * kRouteInlineMaxT) {
+            const int jj = tid / kRouteInlineMaxT, t = tid % kRouteInlineMaxT;
+            const int ee = e0 + jj;
+            if (t < p.T && ee < Eg) p.logits[(size_t)t * Eg + ee] = route_logit(s_part, jj, t, p.rbias, ee, Er);
+        }
+        __syncthreads();   // (orders the logit stores before the release below, and s_part's reuse)
+    }
+    if (tid == 0) {
+        red_release_add_u32(&p.ctrl->route_arrive, 1u);
+        uint32_t i = 0;
+        while (ld_acquire_u32(&p.ctrl->route_arrive) < (uint32_t)C)
+            if (++i > kSpinLimit) {
+                set_error(p.ctrl, MOE_ERR_TIMEOUT);
+                break;
+            }
+    }
+    __syncthreads();
+    route_load_logits(s_logit, p.logits, p.T * Eg);
+    __syncthreads();
+    route_select(s_logit, p.T, Er, kr, p.rgate, s_cand, s_ids, s_w);
+    __syncthreads();
+    if (tid < p.T * p.k) {
+        id_reg = s_ids[tid];
+        w_reg = s_w[tid];
+        if (blockIdx.x == 0) {
+            p.ids_out[tid] = id_reg;
+            p.w_out[tid] = w_reg;
+        }
+    }
+}
+
 // ---- work split ---------------------------------------------------------------
 // CTA cb of C owns output blocks [cb0, cb1) = [B cb / C, B (cb + 1) / C), B = H/16.
 // The gate_up tasks are shared out in proportion to each CTA's capacity: an
 // equal share of all the bytes (gate_up tasks and down chunks) minus w times the
-// bytes of its own blocks' down chunks (at least 0). CTAs own B / C or B / C + 1
-// blocks, so the capacities take two values and their prefix sums have a
-// closed form, computed exactly in 64-bit integers (units of 8 bytes: a gate_up
-// task is H, a block's down chunks nact * I). CTA c's tasks start at
-// floor(n1 * cum(c) / cum(C)): non-decreasing in c, 0 at c = 0, n1 at c = C,
-// and the same value in every CTA that evaluates it. The split runs on the
-// critical path of every CTA, so the quotient is estimated in fp32 and made
-// exact with 64-bit multiplies (a 64-bit division is a long dependent chain).
-__device__ inline long long split_cum(int c, int C, int B, int bmin, long long x0, long long x1) {
-    const int nbig = B * c / C - bmin * c;   // CTAs among [0, c) with bmin + 1 blocks
-    return (long long)c * x0 + (long long)nbig * (x1 - x0);
+// bytes of its own blocks' down chunks (at least 0). Every term is a multiple of
+// the number of active experts, so the capacities' prefix sums are those of
+// launch constants (x0, x1: the capacity of a CTA with bmin or bmin + 1 blocks,
+// per active expert, in units of 8 bytes): cum(c) = c x0 + nbig(c) (x1 - x0),
+// nbig(c) the CTAs among [0, c) with bmin + 1 blocks. CTA c's tasks start at
+// f(c) = floor(n1 * (fp32(cum(c)) * r)), r = fp32(1 / cum(C)) from the host,
+// with f(0) = 0 and f(C) = n1: non-decreasing in c and the same value in every
+// CTA that evaluates it, so the CTAs' ranges tile [0, n1) exactly. (A few
+// multiplies on the critical path of every CTA; the exact quotient in 64-bit
+// integers cost about 1 us at T = 1, measured.)
+__device__ inline int split_at(const FusedParams &p, int c, int C, int n1, int wi) {
+    if (c <= 0) return 0;
+    if (c >= C) return n1;
+    const float r = p.sr[wi];
+    if (r == 0.f) return n1 * c / C;
+    const int B = p.H / kP2Rows, bmin = B / C;
+    const int nbig = B * c / C - bmin * c;
+    const long long cum = (long long)c * p.sx0[wi] + (long long)nbig * (p.sx1[wi] - p.sx0[wi]);
+    return __float2int_rd(__fmul_rn((float)n1, __fmul_rn((float)cum, r)));
 }
 
-__device__ inline int floor_ratio(long long num, long long den) {   // floor(num / den), 0 <= num / den < 2^24
-    int q = __float2int_rd(__fdiv_rn((float)num, (float)den));
-    while ((long long)(q + 1) * den <= num) ++q;
-    while (q > 0 && (long long)q * den > num) --q;
-    return q;
-}
-
-// w: the weight of a CTA's own down bytes in its capacity. With the spread
-// task order (see task_stride) and the down chunks expert by expert, the down
-// work of a CTA with more blocks runs while the experts complete, so such CTAs
-// take less gate_up work (w = 2; measured at T = 4: the CTAs with two blocks,
-// then without gate_up work, end with the others; route + forward 56.9 ->
-// 55.2 us at T = 4, 83.9 -> 81.7 us at T = 7).
+// wi = 1: with the spread task order (see task_stride) and the down chunks
+// expert by expert, the down work of a CTA with more blocks runs while the
+// experts complete, so such CTAs take less gate_up work (w = 2; measured at
+// T = 4: the CTAs with two blocks, then without gate_up work, end with the
+// others; route + forward 56.9 -> 55.2 us at T = 4, 83.9 -> 81.7 us at T = 7).
 constexpr int kSpreadDownWeight = 2;
-__device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int w, int &b1, int &m1, int &cb0,
+__device__ inline void fused_split(const FusedParams &p, int nact, int C, int cb, int wi, int &b1, int &m1, int &cb0,
                                    int &cb1) {
     const int B = p.H / kP2Rows;
     const int n1 = nact * (p.I / 8);
     cb0 = B * cb / C;
     cb1 = B * (cb + 1) / C;
-    const long long blk = (long long)nact * p.I;
-    const long long total = (long long)n1 * p.H + (long long)B * blk;
-    const int bmin = B / C;
-    const long long x0 = max(0LL, total - (long long)C * w * blk * bmin);
-    const long long x1 = max(0LL, total - (long long)C * w * blk * (bmin + 1));
-    const long long all = split_cum(C, C, B, bmin, x0, x1);
-    if (all > 0) {
-        b1 = floor_ratio((long long)n1 * split_cum(cb, C, B, bmin, x0, x1), all);
-        m1 = floor_ratio((long long)n1 * split_cum(cb + 1, C, B, bmin, x0, x1), all) - b1;
-    } else {
-        b1 = n1 * cb / C;
-        m1 = n1 * (cb + 1) / C - b1;
+    b1 = split_at(p, cb, C, n1, wi);
+    m1 = split_at(p, cb + 1, C, n1, wi) - b1;
+}
+
+// The host's half of the split: x0, x1 and r for w = 1 and w = kSpreadDownWeight.
+void fused_split_constants(const moe_dims &d, int C, FusedParams &p) {
+    const long long B = d.H / kP2Rows, bmin = B / C;
+    const long long unit = (long long)(d.I / 8) * d.H + B * d.I;   // all bytes / 8, per active expert
+    for (int wi = 0; wi < 2; ++wi) {
+        const long long w = wi ? kSpreadDownWeight : 1;
+        const long long c0 = unit - C * w * d.I * bmin, c1 = unit - C * w * d.I * (bmin + 1);
+        const long long x0 = c0 > 0 ? c0 : 0, x1 = c1 > 0 ? c1 : 0;
+        const long long all = C * x0 + (B - bmin * C) * (x1 - x0);
+        p.sx0[wi] = x0;
+        p.sx1[wi] = x1;
+        p.sr[wi] = all > 0 ? (float)(1.0 / (double)all) : 0.f;
     }
 }
 
@@ -1060,8 +1185,10 @@ __device__ inline int task_stride(int n1, int nkc, int C) {
 // kSpread: the launch may hold enough gate_up work for the spread task order
 // (see task_stride); without it the task order is the plain one, in code that
 // carries nothing of the other (measured: 0.3 us at T = 1 otherwise).
-template <bool kStaged, bool kSpread>
+// kRoute: the kernel runs the router itself (f_route; needs kStaged).
+template <bool kStaged, bool kSpread, bool kRoute>
 __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_constant__ FusedParams p) {
+    static_assert(!kRoute || kStaged, "the router reads the staged activations");
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_w1) : "memory");
@@ -1070,7 +1197,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_init(x_bar(v), 1);
         fence_mbar_init();
     }
-    if (p.xs_off && threadIdx.x == 0) {
+    if (!kRoute && p.xs_off && threadIdx.x == 0) {
         // The activations start moving at once: x is an input of the layer,
         // complete before the router (the kernel ahead of this one) began, so
         // it may be read before the wait below. Nothing of the router's
@@ -1079,13 +1206,35 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_arrive_expect_tx(x_bar(v), xb);
         bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
     }
-    // The launch is programmatic: the CTAs may start while the router still
-    // runs, and read its outputs (and the workspace) only once it has finished.
+    if (kRoute && threadIdx.x < 5) {
+        // the CTA's first router rows and the activations head for L2 while the
+        // kernel ahead finishes (a prefetch into L2, the point of coherence,
+        // reads nothing stale; the loads themselves come after the wait)
+        const int e = 4 * (int)blockIdx.x + (int)threadIdx.x;
+        if (threadIdx.x < 4 && e < p.E)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.wr + (size_t)e * p.H),
+                         "r"((uint32_t)p.H * 2) : "memory");
+        if (threadIdx.x == 4)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.x), "r"((uint32_t)p.T * p.H * 2)
+                         : "memory");
+    }
+    // The launch is programmatic: the CTAs may start while the kernel ahead
+    // (the router, or the layer before) still runs, and read its outputs (and
+    // the workspace) only once it has finished.
     pdl_wait();
     // the ids are the first thing every path needs
     int id_reg = -1;
     float w_reg = 0.f;
-    if ((int)threadIdx.x < p.T * p.k) {
+    if constexpr (kRoute) {
+        // here x may come from the kernel ahead, so it is copied only now
+        if (threadIdx.x == 0) {
+            const uint32_t xb = (uint32_t)p.T * p.H * 2;
+            mbar_arrive_expect_tx(x_bar(v), xb);
+            bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
+        }
+        __syncthreads();   // (the barrier's initialisation is visible to every thread)
+        f_route(p, smem, v, id_reg, w_reg);
+    } else if ((int)threadIdx.x < p.T * p.k) {
         id_reg = p.ids[threadIdx.x];
         w_reg = p.topk_w[threadIdx.x];
     }
@@ -1098,7 +1247,7 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     // whose weight w and the down order follow it: with the plain order,
     // w = 1 and block by block (measured faster at T = 1)
     const int M = kSpread ? task_stride(n1, p.nkc, gridDim.x) : 0;
-    fused_split(p, nact, gridDim.x, blockIdx.x, M != 0 ? kSpreadDownWeight : 1, b1, m1, cb0, cb1);
+    fused_split(p, nact, gridDim.x, blockIdx.x, M != 0 ? 1 : 0, b1, m1, cb0, cb1);
     const int nblk = cb1 - cb0, m2 = nblk * nact;   // down chunks of whole blocks
     const bool emaj = M != 0 && nblk <= p.nyb;
     // the CTA's gate_up tasks in increasing order, in the prologue's scratch
@@ -1188,10 +1337,10 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
 }
 
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
-                                float eps, cudaStream_t s) {
+                                float eps, cudaStream_t s, const RouteArgs *r) {
     const WsLayout W = ws_layout(d);
     const FusedLayout L = fused_layout(d);
-    if (!L.ok) return cudaErrorInvalidValue;
+    if (!L.ok || (r && !fused_route_supported(d))) return cudaErrorInvalidValue;
     FusedParams p;
     cudaError_t err = encode_tmap_2d(&p.tm_w1, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, a.w1p, (uint64_t)d.H / 8,
                                      (uint64_t)d.E * 2 * d.I, (uint64_t)d.H / 2, (uint32_t)L.gcw, 8u,
@@ -1226,6 +1375,12 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     p.pro_off = L.pro_off;
     p.xs_off = L.xs_off;
     p.ys_off = L.ys_off;
+    p.wr = r ? r->wr : nullptr;
+    p.rbias = r ? r->bias : nullptr;
+    p.logits = ws_at<float>(ws, W.partial);
+    p.ids_out = r ? r->ids : nullptr;
+    p.w_out = r ? r->w : nullptr;
+    p.rgate = r ? r->gate : 0;
 
     const bool staged = L.xs_off != 0;
     const long long max_active = (long long)d.T * d.k < d.E ? (long long)d.T * d.k : d.E;
@@ -1234,13 +1389,16 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     long long grid = (chunks + kCons - 1) / kCons;
     if (grid > sm_count()) grid = sm_count();
     if (grid < 1) grid = 1;
+    fused_split_constants(d, (int)grid, p);
     // the instantiation with the spread task order, where the gate_up work of the most
     // active experts there can be spans more than two rounds (the kernel decides on the
     // experts actually active)
     const bool spread = max_active * (d.I / 8) * L.nkc > 2LL * kCons * grid;
-    const void *fn = staged ? (spread ? reinterpret_cast<const void *>(decode_fused_kernel<true, true>)
-                                      : reinterpret_cast<const void *>(decode_fused_kernel<true, false>))
-                            : reinterpret_cast<const void *>(decode_fused_kernel<false, true>);
+    const void *fn = r ? (spread ? reinterpret_cast<const void *>(decode_fused_kernel<true, true, true>)
+                                 : reinterpret_cast<const void *>(decode_fused_kernel<true, false, true>))
+                       : staged ? (spread ? reinterpret_cast<const void *>(decode_fused_kernel<true, true, false>)
+                                          : reinterpret_cast<const void *>(decode_fused_kernel<true, false, false>))
+                                : reinterpret_cast<const void *>(decode_fused_kernel<false, true, false>);
     err = set_smem_once(fn, kFusedSmem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -1260,9 +1418,11 @@ cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (staged && spread) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, true>, p);
-    if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, false>, p);
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false, true>, p);
+    if (r && spread) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, true, true>, p);
+    if (r) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, false, true>, p);
+    if (staged && spread) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, true, false>, p);
+    if (staged) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true, false, false>, p);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false, true, false>, p);
 }
 
 }  // namespace moe

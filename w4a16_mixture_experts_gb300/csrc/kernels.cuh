@@ -55,10 +55,26 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
 bool fused_supported(const moe_dims &d);
 // 0 if the forward takes the tensor-core pipeline; else 1 (activations staged
 // in shared memory) or 2 (read from global memory), plus 16 * quantisation
-// groups per gate_up chunk.
+// groups per gate_up chunk, plus 256 if the down outputs' block buffers have a
+// region of their own, plus 512 if the kernel can also run the router.
 int fused_plan(const moe_dims &d);
+// The router run by the fused decode kernel itself (moe_layer_forward): the
+// router weights [E + gate][H] and bias, and the selection's outputs.
+struct RouteArgs {
+    const uint16_t *wr;
+    const float *bias;
+    int32_t *ids;
+    float *w;
+    int gate;
+};
+// True when the fused decode kernel can also run the router for the forward
+// dims d (experts E + gate, slots k + gate): the activations are staged and its
+// ring holds the router's scratch.
+bool fused_route_supported(const moe_dims &d);
+// With r, the kernel routes itself (d: the forward's dims) and a.ids / a.topk_w
+// are not read.
 cudaError_t launch_decode_fused(const ExpertArgs &a, const moe_dims &d, void *ws, uint16_t *out, uint16_t *next,
-                                float eps, cudaStream_t s);
+                                float eps, cudaStream_t s, const RouteArgs *r = nullptr);
 
 // RTN INT4 g128 quantiser with the per-group clip search (quant.cu).
 cudaError_t launch_quantize_int4(const uint16_t *w, int64_t N, int64_t K, int nclip, int32_t *packed,

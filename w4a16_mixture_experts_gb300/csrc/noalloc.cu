@@ -24,7 +24,7 @@
 //    may load this module); make that first call outside any stream capture.
 //  - The fused kernel needs its completion counters and the control block
 //    (error word, exit and barrier counts) at zero when it starts. Each call
-//    clears both itself with two small cudaMemsetAsync on its stream, so
+//    clears both itself with one small cudaMemsetAsync on its stream, so
 //    neither the module-load zero fill nor what an earlier call (of any shape,
 //    finished or given up) left behind matters. Nothing else in the array must
 //    start at zero.
@@ -99,11 +99,10 @@ extern "C" int moe_w4a16_forward_noalloc(const uint16_t *hidden, const int32_t *
     cudaError_t err = static_scratch(&ws);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the control block, then done1 and rowss, which are adjacent in
-    // the layout (rbuf follows them)
+    // the control block, rowss and the counters of experts [0, E), the first
+    // regions of the layout
     const WsLayout W = ws_layout(d);
-    err = cudaMemsetAsync(ws_at<char>(ws, W.ctrl), 0, sizeof(Ctrl), s);
-    if (err == cudaSuccess) err = cudaMemsetAsync(ws_at<char>(ws, W.done1), 0, W.rbuf - W.done1, s);
+    err = cudaMemsetAsync(ws_at<char>(ws, W.ctrl), 0, W.done1 + (size_t)d.E * kCtrStride * 4 - W.ctrl, s);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     const ExpertArgs a{hidden, topk_ids, topk_w, w1_packed, w1_scales, w2_packed, w2_scales};
     err = launch_decode_fused(a, d, ws, out, nullptr, 0.f, s);

@@ -700,14 +700,16 @@ constexpr int kRed4MinT = 4096;
 // (0,4,1,5,2,6,3,7), for the offsets[E] slots that hold a valid assignment.
 // A warp copies whole rows: the row's token is read once (the next row's is
 // fetched while this one moves), then up to kXgLoads 16-byte chunks per lane
-// are in flight at once.
+// are in flight at once. The same warps then clear the T rows of the down
+// kernel's fp32 accumulator.
 constexpr int kXgThreads = 256;
 constexpr int kXgLoads = 10;   // a 2560-wide row in one pass
 
 __global__ void __launch_bounds__(kXgThreads) xgather_kernel(const uint16_t *__restrict__ x,
                                                              const int32_t *__restrict__ perm,
                                                              const int32_t *__restrict__ offsets, int E, int H, int k,
-                                                             uint16_t *__restrict__ xs) {
+                                                             uint16_t *__restrict__ xs, float *__restrict__ out_acc,
+                                                             int T) {
     const int nslots = offsets[E];
     const int cpr = H / 8;   // 16-byte chunks per row
     const int lane = threadIdx.x & 31;
@@ -734,6 +736,13 @@ __global__ void __launch_bounds__(kXgThreads) xgather_kernel(const uint16_t *__r
             }
         }
         tok = nxt;
+    }
+    // the down kernel's accumulator starts at zero: the warps clear its T rows
+    // (so that nothing depends on what an earlier call left in the workspace)
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = blockIdx.x * (kXgThreads / 32) + (threadIdx.x >> 5); t < T; t += nw) {
+        float4 *row = reinterpret_cast<float4 *>(out_acc + (size_t)t * H);
+        for (int c = lane; c < H / 4; c += 32) row[c] = z4;
     }
 }
 
@@ -800,7 +809,8 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *__rest
     }
 }
 
-// out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue), then out_acc = 0.
+// out[t][n] = bf16(out_acc[t][n]) (or the stack epilogue); out_acc was
+// cleared by the gather kernel at the start of the call.
 // One CTA per token, 16-byte accesses; the stack variant keeps the token's
 // row in registers between the sum of squares and the rescale.
 constexpr int kConvThreads = 256;
@@ -831,11 +841,6 @@ __global__ void __launch_bounds__(kConvThreads) acc_convert_kernel(float *__rest
         const int i = threadIdx.x + kConvThreads * j;
         r[j] = i < n4 ? row[i] : zero;
         xv[j] = next && i < n4 ? xr[i] : make_uint2(0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kConvPer; ++j) {
-        const int i = threadIdx.x + kConvThreads * j;
-        if (i < n4) row[i] = zero;
     }
     if (!next) {
         uint2 *o = reinterpret_cast<uint2 *>(out + (size_t)t * H);
@@ -894,7 +899,8 @@ cudaError_t launch_prefill(const ExpertArgs &a, const moe_dims &d, void *ws, uin
         if (grid > 8LL * sm_count()) grid = 8LL * sm_count();
         if (grid < 1) grid = 1;
         xgather_kernel<<<(unsigned)grid, kXgThreads, 0, s>>>(a.x, ws_at<int32_t>(ws, W.perm),
-                                                             ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm);
+                                                             ws_at<int32_t>(ws, W.offsets), d.E, d.H, d.k, xperm,
+                                                             out_acc, d.T);
     }
     int4 *chunk_info = ws_at<int4>(ws, W.chunk_info);
     chunk_table_kernel<<<1, 1024, 0, s>>>(ws_at<int32_t>(ws, W.counts), ws_at<int32_t>(ws, W.offsets), d.E, n_chunks,

@@ -10,6 +10,7 @@
 // far below a bf16 ulp.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -87,85 +88,6 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t *__res
     route_logits_tile<NT>(x, wr, partial, T, H, E);
 }
 
-// Order-preserving map of an fp32 value onto uint32.
-__device__ inline uint32_t f32_order_key(float v) {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ inline float f32_from_order_key(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// ---------------------------------------------------------------------------
-// Top-k: keys pack an order key of the fp32 logit above 0xffffffff - id, so
-// keys are unique and one maximum gives value and id (ties to the lower id).
-// A warp's k largest: every lane sorts its keys, then k rounds of a two-step
-// warp max with redux.sync (first the logit half, then the id half among the
-// lanes holding that logit); the lane that held the maximum moves to its next
-// key. Weights: softmax over the selected logits in fp32.
-__device__ inline uint64_t warp_max_key(uint64_t m) {
-    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
-    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32) == hi ? (uint32_t)m : 0u);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-// Size-generic forms for lanes holding N keys each (N a power of two): sort,
-// k rounds of the heads' warp maximum (lane j < k ends with the j-th largest),
-// and the softmax over the selected logits with the writes.
-template <int N>
-__device__ inline void sort_desc_n(uint64_t (&key)[N]) {
-#pragma unroll
-    for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-        for (int stride = size / 2; stride > 0; stride >>= 1)
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int l = i ^ stride;
-                if (l > i) {
-                    const bool up = (i & size) != 0;
-                    const uint64_t a = key[i], b = key[l];
-                    if (up ? a > b : a < b) {
-                        key[i] = b;
-                        key[l] = a;
-                    }
-                }
-            }
-}
-
-template <int N>
-__device__ inline uint64_t warp_topk_n(uint64_t (&key)[N], int k, int lane) {
-    sort_desc_n<N>(key);
-    uint64_t mine = 0;
-    for (int j = 0; j < k; ++j) {
-        const uint64_t m = warp_max_key(key[0]);
-        if (key[0] == m) {
-#pragma unroll
-            for (int i = 0; i + 1 < N; ++i) key[i] = key[i + 1];
-            key[N - 1] = 0;
-        }
-        if (lane == j) mine = m;
-    }
-    return mine;
-}
-
-__device__ inline void topk_finish(uint64_t mine, int k, int lane, int32_t *ids_row, float *w_row) {
-    const float lmax = f32_from_order_key((uint32_t)(__shfl_sync(0xffffffffu, mine, 0) >> 32));
-    const float l = f32_from_order_key((uint32_t)(mine >> 32));
-    const float p = lane < k ? expf(l - lmax) : 0.f;
-    float z = p;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane < k) {
-        ids_row[lane] = (int32_t)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
-        w_row[lane] = p / z;
-    }
-}
-
-__device__ inline uint64_t topk_key(float logit, int e) {
-    return ((uint64_t)f32_order_key(logit) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
-}
-
 // Top-k for T > 8 tokens: one CTA of four warps per token. Warp w takes the
 // experts [w * ep, (w + 1) * ep), ep = ceil(E / 4) <= 256: lane l sums the
 // K-split partial logits of experts lo + l, lo + l + 32, ... (all loads of a
@@ -224,8 +146,6 @@ __device__ inline float gate_dot_cta(const uint16_t *__restrict__ xrow, const ui
     return g;
 }
 
-__device__ inline float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
-
 __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float *__restrict__ partial, int ksplit,
                                                                      const float *__restrict__ bias, int T, int E,
                                                                      int k, int32_t *__restrict__ ids,
@@ -277,11 +197,8 @@ __global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float
 // T x E of them into shared memory and selects: each token's experts are
 // split over wpt warps (4 for T <= 4, else 2), each takes the k largest of
 // its part, and one warp takes the k largest of their candidates. The ticket
-// is reset for the next launch.
-constexpr int kRouteInlineMaxT = 8;
-constexpr int kRouteWarps = 16;
-constexpr int kRouteLoads = 3;   // 16-byte loads per lane in flight (a quarter row of H <= 3072 in one pass)
-constexpr int kRouteMaxWpt = 4;
+// is reset for the next launch. The row arithmetic and the selection live in
+// route_dev.cuh, shared with the decode kernel that routes itself.
 
 inline size_t route_small_smem(const moe_dims &d) {
     const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * (d.E + 1) * 4;
@@ -308,16 +225,10 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Eg = E + gate;   // router rows, and the row stride of the logits
-    const int e = blockIdx.x * 4 + (warp >> 2);
-    const int q4 = H / 4, c_lo = (warp & 3) * q4, c_hi = c_lo + q4;
-    const uint16_t *row = wr + (size_t)(e < Eg ? e : 0) * H;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const RouteQuarter rq = route_quarter(wr, blockIdx.x * 4 + (warp >> 2), Eg, H, warp & 3);
     uint4 wv[kRouteLoads];
-#pragma unroll
-    for (int i = 0; i < kRouteLoads; ++i) {
-        const int c = c_lo + 256 * i + 8 * lane;
-        wv[i] = e < Eg && c < c_hi ? ld_nc_v4(row + c) : zero;
-    }
+    route_quarter_load(rq, rq.c_lo, lane, wv);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
     uint4 *xs = reinterpret_cast<uint4 *>(s_raw);
     const int nx = T * H / 8;
     for (int i0 = threadIdx.x; i0 < nx; i0 += 4 * blockDim.x) {
@@ -335,117 +246,28 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(const uin
     }
     __syncthreads();
     float acc[kRouteInlineMaxT];
-#pragma unroll
-    for (int t = 0; t < kRouteInlineMaxT; ++t) acc[t] = 0.f;
-    for (int c0 = c_lo; c0 < c_hi; c0 += 256 * kRouteLoads) {
-        if (c0 != c_lo) {
-#pragma unroll
-            for (int i = 0; i < kRouteLoads; ++i) {
-                const int c = c0 + 256 * i + 8 * lane;
-                wv[i] = e < Eg && c < c_hi ? ld_nc_v4(row + c) : zero;
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kRouteInlineMaxT; ++t) {
-            if (t >= T) break;
-#pragma unroll
-            for (int i = 0; i < kRouteLoads; ++i) {
-                const int c = c0 + 256 * i + 8 * lane;
-                const uint4 xv = c < c_hi ? xs[((size_t)t * H + c) / 8] : zero;
-                const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-                const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc[t] = fmaf(__uint_as_float(ww[j] << 16), __uint_as_float(xx[j] << 16), acc[t]);
-                    acc[t] = fmaf(__uint_as_float(ww[j] & 0xffff0000u), __uint_as_float(xx[j] & 0xffff0000u), acc[t]);
-                }
-            }
-        }
-    }
+    route_quarter_dot(rq, xs, T, H, lane, wv, acc);
 #pragma unroll
     for (int t = 0; t < kRouteInlineMaxT; ++t) {
         if (t >= T) break;
-        float v = acc[t];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) s_part[warp][t] = v;
+        if (lane == 0) s_part[warp][t] = acc[t];
     }
     __syncthreads();
     if (threadIdx.x < 4 * kRouteInlineMaxT) {
         const int jj = threadIdx.x / kRouteInlineMaxT, t = threadIdx.x % kRouteInlineMaxT;
         const int ee = blockIdx.x * 4 + jj;
-        if (t < T && ee < Eg) {
-            const float v = ((s_part[4 * jj][t] + s_part[4 * jj + 1][t]) + s_part[4 * jj + 2][t]) + s_part[4 * jj + 3][t];
-            logits[(size_t)t * Eg + ee] = bias && ee < E ? v + bias[ee] : v;
-        }
+        if (t < T && ee < Eg) logits[(size_t)t * Eg + ee] = route_logit(s_part, jj, t, bias, ee, E);
     }
     // the CTA barrier orders the logit stores before thread 0's release
     __syncthreads();
     if (threadIdx.x == 0) s_last = atom_acq_rel_add_u32(&ctrl->route_ticket, 1u) + 1 == gridDim.x;
     __syncthreads();
     if (!s_last) return;
-    // the last CTA: all logits at once (8 loads per thread in flight), then top-k
+    // the last CTA: all logits at once, then top-k
     float *s_logit = reinterpret_cast<float *>(s_raw);
-    const int n = T * Eg;
-    for (int i0 = 0; i0 < n; i0 += 8 * blockDim.x) {
-        float lv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * blockDim.x + threadIdx.x;
-            lv[u] = i < n ? __ldcg(logits + i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * blockDim.x + threadIdx.x;
-            if (i < n) s_logit[i] = lv[u];
-        }
-    }
+    route_load_logits(s_logit, logits, T * Eg);
     __syncthreads();
-    const int wpt = T <= kRouteWarps / kRouteMaxWpt ? kRouteMaxWpt : kRouteWarps / kRouteInlineMaxT;
-    const int t = warp / wpt, part = warp % wpt;
-    const int ep = (E + wpt - 1) / wpt, lo = part * ep, hi = min(E, lo + ep);
-    if (t < T) {
-        uint64_t mine;
-        if (ep <= 128) {
-            uint64_t key[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
-            }
-            mine = warp_topk_n<4>(key, k, lane);
-        } else if (ep <= 256) {
-            uint64_t key[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
-            }
-            mine = warp_topk_n<8>(key, k, lane);
-        } else {
-            uint64_t key[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int ee = lo + lane + 32 * i;
-                key[i] = ee < hi ? topk_key(s_logit[t * Eg + ee], ee) : 0;
-            }
-            mine = warp_topk_n<16>(key, k, lane);
-        }
-        s_cand[warp][lane] = lane < k ? mine : 0;
-    }
-    __syncthreads();
-    if (t < T && part == 0) {
-        uint64_t c[kRouteMaxWpt];
-#pragma unroll
-        for (int q = 0; q < kRouteMaxWpt; ++q) c[q] = q < wpt ? s_cand[warp + q][lane] : 0;
-        const uint64_t mine = warp_topk_n<kRouteMaxWpt>(c, k, lane);
-        const int ldk = k + gate;
-        topk_finish(mine, k, lane, ids + (size_t)t * ldk, w + (size_t)t * ldk);
-        if (gate && lane == 0) {
-            ids[(size_t)t * ldk + k] = E;
-            w[(size_t)t * ldk + k] = sigmoidf_(s_logit[t * Eg + E]);
-        }
-    }
+    route_select(s_logit, T, E, k, gate, s_cand, ids, w);
     if (threadIdx.x == 0) ctrl->route_ticket = 0;
 }
 
