@@ -156,3 +156,46 @@ def test_workspace_holds_the_regions_of_the_path_taken():
     # the same fixed head (control block, per-expert counters for every id) in
     # both; only the prefill one adds the per-slot activations and the accumulator
     assert small + T * k * H * 2 + T * H * 4 <= big
+
+
+def _call_layer(L, dims, p, ws_bytes, shared=0, out=True, nxt=False, eps=1e-6, bias=None):
+    """moe_layer_forward with fake, never-dereferenced addresses p[0..12]."""
+    v = lambda i: ctypes.c_void_p(p[i])
+    return L.moe_layer_forward(v(0), v(1), None if bias is None else ctypes.c_void_p(bias), shared, v(2), v(3), v(4),
+                               v(5), v(6) if out else None, v(7) if nxt else None, eps, v(8), v(9), dims, v(10),
+                               ws_bytes, None)
+
+
+def test_layer_call_argument_errors_are_synchronous(L):
+    """moe_layer_forward's checks: every refusal comes before any CUDA work."""
+    d = moe.moe_dims(2, 256, 16, 2, 128)
+    need = max(moe.moe_workspace_size(2, 256, 16, 2, 128), moe.moe_workspace_size(2, 256, 17, 3, 128))
+    good = [0x10000 * (i + 1) for i in range(11)]
+    # `shared` is 0 or 1
+    assert _call_layer(L, d, good, need, shared=2) == 1
+    # exactly one of out and next
+    assert _call_layer(L, d, good, need, out=True, nxt=True) == 1
+    assert _call_layer(L, d, good, need, out=False, nxt=False) == 1
+    # the stack step needs eps >= 0
+    assert _call_layer(L, d, good, need, out=False, nxt=True, eps=-1.0) == 1
+    # a null weight, a misaligned router, a misaligned bias
+    p = list(good)
+    p[4] = 0
+    assert _call_layer(L, d, p, need) == 1
+    p = list(good)
+    p[1] += 8
+    assert _call_layer(L, d, p, need) == 1
+    assert _call_layer(L, d, good, need, bias=good[0] + 4) == 1
+    # the shared expert: k + 1 within 32 slots, E + 1 within 1024 experts
+    assert _call_layer(L, moe.moe_dims(2, 256, 64, 32, 128), good, 1 << 30, shared=1) == 2
+    assert _call_layer(L, moe.moe_dims(2, 256, 1024, 8, 128), good, 1 << 30, shared=1) == 2
+    # the workspace must serve the router's dims and the forward's (one more expert and slot)
+    small = moe.moe_workspace_size(2, 256, 16, 2, 128)
+    big = moe.moe_workspace_size(2, 256, 17, 3, 128)
+    assert big > small
+    assert _call_layer(L, d, good, big - 16, shared=1) == 3
+    assert _call_layer(L, d, good, small - 16) == 3
+    # an empty batch: nothing to do (no output needed)
+    e = moe.moe_dims(0, 256, 16, 2, 128)
+    assert _call_layer(L, e, [0, good[1], good[2], good[3], good[4], good[5], 0, 0, 0, 0, good[10]], need,
+                       out=False) == 0
