@@ -9,7 +9,9 @@
 //
 //  * One persistent CTA per SM, launched cooperatively (the CTAs wait on one
 //    another, so all must be resident) and programmatically behind the
-//    router, so that the launch is under way while the router finishes. Or
+//    router, so that the launch is under way while the router finishes (and
+//    the kernel lets the next one launch at its own entry: the next layer's
+//    CTAs take the SMs this one frees and prefetch their inputs). Or
 //    the kernel runs the router itself (moe_layer_forward): each CTA computes
 //    a few router rows, the CTAs meet at a grid-wide barrier, and each selects
 //    the top-k from all logits (see f_route); this removes the router's own
@@ -1197,15 +1199,13 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
         mbar_init(x_bar(v), 1);
         fence_mbar_init();
     }
-    if (!kRoute && p.xs_off && threadIdx.x == 0) {
-        // The activations start moving at once: x is an input of the layer,
-        // complete before the router (the kernel ahead of this one) began, so
-        // it may be read before the wait below. Nothing of the router's
-        // output or the workspace is touched before it.
-        const uint32_t xb = (uint32_t)p.T * p.H * 2;
-        mbar_arrive_expect_tx(x_bar(v), xb);
-        bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
-    }
+    // The kernel behind this one may launch now: its CTAs take the SMs that
+    // this grid's CTAs free and set up, and wait for this grid's end before
+    // they read anything (every input of this kernel, too, is read only after
+    // its own wait below, since the kernel ahead may be one of these).
+    pdl_launch_dependents();
+    if (!kRoute && p.xs_off && threadIdx.x == 4)   // x heads for L2 (read after the wait)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.x), "r"((uint32_t)p.T * p.H * 2) : "memory");
     if (kRoute && threadIdx.x < 5) {
         // the CTA's first router rows and the activations head for L2 while the
         // kernel ahead finishes (a prefetch into L2, the point of coherence,
@@ -1225,13 +1225,13 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     // the ids are the first thing every path needs
     int id_reg = -1;
     float w_reg = 0.f;
+    if (p.xs_off && threadIdx.x == 0) {
+        // x may come from the kernel ahead, so it is copied only now
+        const uint32_t xb = (uint32_t)p.T * p.H * 2;
+        mbar_arrive_expect_tx(x_bar(v), xb);
+        bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
+    }
     if constexpr (kRoute) {
-        // here x may come from the kernel ahead, so it is copied only now
-        if (threadIdx.x == 0) {
-            const uint32_t xb = (uint32_t)p.T * p.H * 2;
-            mbar_arrive_expect_tx(x_bar(v), xb);
-            bulk_g2s(smem + p.xs_off, p.x, xb, x_bar(v));
-        }
         __syncthreads();   // (the barrier's initialisation is visible to every thread)
         f_route(p, smem, v, id_reg, w_reg);
     } else if ((int)threadIdx.x < p.T * p.k) {
