@@ -20,7 +20,8 @@ CUDA graph holds one pass over the sets (consecutive steps, as consecutive
 layers of a model run), and K steps are whole replays plus one graph of the
 remainder; CUDA events on the launching stream; >= 3 warm-up steps. The
 expert kernel's own time is taken from events that the library records
-around it in separate one-step graphs, replayed after the timed region.
+around it in separate one-step graphs, replayed after the timed region; where
+the layer is that one kernel (the router inside), from the timed region.
 `e2e` repeats the timing through the same public calls with every step's
 tokens copied in from pinned host memory and its output copied back, inside
 the timed region; the copies run on a second stream, so that a step's kernels
