@@ -354,3 +354,53 @@ def test_decode_takes_every_batch_up_to_its_limit_at_full_shape():
             for E in (k, 512, 1024):
                 assert fused_plan(T, 2560, E, k, 640) is not None, (T, E, k)
     assert fused_plan(C["kDecodeMaxT"] + 1, 2560, 512, 10, 640) is None
+
+
+def _warp_prologue(ids):
+    """Mirror of f_route_prologue's warp: bitonic sort of (expert << 5 | a) over 32
+    lanes by xor-shuffles, then the slots and the runs of equal experts."""
+    n = len(ids)
+    key = [(ids[l] << 5) | l if l < n else 0x7fffffff for l in range(32)]
+    kk = 2
+    while kk <= 32:
+        j = kk >> 1
+        while j > 0:
+            o = [key[l ^ j] for l in range(32)]
+            key = [min(key[l], o[l]) if ((l & j) == 0) == ((l & kk) == 0) else max(key[l], o[l]) for l in range(32)]
+            j >>= 1
+        kk <<= 1
+    e = [k >> 5 for k in key]
+    a = [k & 31 for k in key]
+    starts = [l < n and (l == 0 or e[l - 1] != e[l]) for l in range(32)]
+    perm = a[:n]
+    inv = [0] * n
+    for s in range(n):
+        inv[a[s]] = s
+    act, aoff, acnt = [], [], []
+    pos = [l for l in range(32) if starts[l]]
+    for i, l in enumerate(pos):
+        act.append(e[l])
+        aoff.append(l)
+        acnt.append((pos[i + 1] if i + 1 < len(pos) else n) - l)
+    return perm, inv, act, aoff, acnt
+
+
+def test_route_prologue_network_matches_the_ranking():
+    # the general prologue's definition: slot = #ids below e + #earlier equal ids;
+    # the active list in increasing expert order with first slot and count
+    rng = random.Random(7)
+    for trial in range(300):
+        T = rng.choice([1, 2])
+        k = rng.randint(1, 32 // T)
+        E = rng.choice([k, max(k, 16), 64, 512, 1024])
+        ids = []
+        for t in range(T):
+            ids += rng.sample(range(E), k)   # distinct within a token, repeats across tokens
+        n = len(ids)
+        perm, inv, act, aoff, acnt = _warp_prologue(ids)
+        for a in range(n):
+            slot = sum(1 for x in ids if x < ids[a]) + sum(1 for b in range(a) if ids[b] == ids[a])
+            assert inv[a] == slot and perm[slot] == a, (trial, ids)
+        assert act == sorted(set(ids))
+        assert aoff == [sum(1 for x in ids if x < e) for e in act]
+        assert acnt == [ids.count(e) for e in act]

@@ -300,6 +300,23 @@ static_assert(kNS + 1 <= 4 * kFW, "mbarrier slots");
 __device__ inline uint64_t *full_bar(const Pro &v, int q) { return v.bar + q; }
 __device__ inline uint64_t *x_bar(const Pro &v) { return v.bar + kNS; }
 
+// The ring's shared words and full barriers, set by the CTA's threads before
+// the barrier that ends either prologue.
+__device__ __forceinline__ void fused_ring_init(const FusedParams &p, uint8_t *smem, const Pro &v, int tid) {
+    const RingWords rw = ring_words(smem, p);
+    if (tid < 2 * p.nb + 1) rw.cnt[tid] = 0;   // chunks done, tasks finalised, the ticket
+    if (tid < kRingWordsExtra) rw.gu_done[tid] = 0;   // tasks finalised, block counts
+    if (tid < kNS) {
+        rw.issued[tid] = -1;
+        rw.next[tid] = tid;
+    }
+    // the ring's full barriers (one arrival: the producer's expect_tx)
+    if (tid < kNS) {
+        mbar_init(v.bar + tid, 1);
+        fence_mbar_init();
+    }
+}
+
 // The stable permutation, in every CTA: the slot of assignment a is
 // #{valid a' with a lower expert} + #{a' < a with the same expert}. Thread a
 // ranks assignment a (id_reg: its id, already loaded by the caller); the
@@ -361,20 +378,59 @@ __device__ __forceinline__ void fused_prologue(const FusedParams &p, uint8_t *sm
         v.acnt[ai] = (int16_t)ct;
     }
     if (tid == 0) *v.nact = nact_s;
-    {
-        const RingWords rw = ring_words(smem, p);
-        if (tid < 2 * p.nb + 1) rw.cnt[tid] = 0;   // chunks done, tasks finalised, the ticket
-        if (tid < kRingWordsExtra) rw.gu_done[tid] = 0;   // tasks finalised, block counts
-        if (tid < kNS) {
-            rw.issued[tid] = -1;
-            rw.next[tid] = tid;
+    fused_ring_init(p, smem, v, tid);
+    __syncthreads();
+}
+
+// The permutation for the kernel's own selection (f_route) when it has at most
+// 32 assignments: every id is valid, so warp 0 sorts the keys (expert << 5 |
+// assignment) across its lanes with a bitonic network of shuffles and reads
+// the slots, the active-expert list, the first slots and the counts off the
+// sorted order: the arrays of fused_prologue, without its three CTA barriers
+// (the other warps set up the ring meanwhile). Ties of the expert go by the
+// assignment, as there.
+__device__ __forceinline__ void f_route_prologue(const FusedParams &p, uint8_t *smem, const Pro &v) {
+    const int tid = threadIdx.x;
+    const int n = p.T * p.k;   // <= 32
+    if (tid < 32) {
+        const int lane = tid;
+        const int32_t *s_ids = reinterpret_cast<const int32_t *>(smem + kRtIds);
+        const float *s_w = reinterpret_cast<const float *>(smem + kRtW);
+        int key = 0x7fffffff;   // lanes past n sort last
+        if (lane < n) {
+            const int e = s_ids[lane];
+            v.ids[lane] = (int16_t)e;
+            v.wv[lane] = s_w[lane];
+            key = (e << 5) | lane;
         }
+#pragma unroll
+        for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+            for (int j = kk >> 1; j > 0; j >>= 1) {
+                const int o = __shfl_xor_sync(0xffffffffu, key, j);
+                const bool up = (lane & kk) == 0, low = (lane & j) == 0;
+                key = low == up ? min(key, o) : max(key, o);
+            }
+        const int e = key >> 5, a = key & 31;
+        const int eprev = __shfl_up_sync(0xffffffffu, e, 1);
+        const bool valid = lane < n;
+        const bool start = valid && (lane == 0 || eprev != e);   // the first slot of an expert
+        const unsigned starts = __ballot_sync(0xffffffffu, start);
+        if (valid) {
+            v.perm[lane] = (int16_t)a;
+            v.inv[a] = (int16_t)lane;
+        }
+        if (start) {
+            const int ai = __popc(starts & ((1u << lane) - 1u));
+            const unsigned later = starts & ~((2u << lane) - 1u);
+            v.act[ai] = (int16_t)e;
+            v.aoff[ai] = (int16_t)lane;
+            v.acnt[ai] = (int16_t)((later ? __ffs(later) - 1 : n) - lane);
+        }
+        if (lane < p.T) v.kv[lane] = (int16_t)p.k;   // every slot valid
+        if (lane == 0) *v.nact = __popc(starts);
     }
-    // the ring's full barriers (one arrival: the producer's expect_tx)
-    if (tid < kNS) {
-        mbar_init(v.bar + tid, 1);
-        fence_mbar_init();
-    }
+    fused_ring_init(p, smem, v, tid);
     __syncthreads();
 }
 
@@ -1234,11 +1290,17 @@ __global__ void __launch_bounds__(kFW * 32, 1) decode_fused_kernel(const __grid_
     if constexpr (kRoute) {
         __syncthreads();   // (the barrier's initialisation is visible to every thread)
         f_route(p, smem, v, id_reg, w_reg);
-    } else if ((int)threadIdx.x < p.T * p.k) {
-        id_reg = p.ids[threadIdx.x];
-        w_reg = p.topk_w[threadIdx.x];
+        if (p.T * p.k <= 32)
+            f_route_prologue(p, smem, v);
+        else
+            fused_prologue(p, smem, v, id_reg, w_reg);
+    } else {
+        if ((int)threadIdx.x < p.T * p.k) {
+            id_reg = p.ids[threadIdx.x];
+            w_reg = p.topk_w[threadIdx.x];
+        }
+        fused_prologue(p, smem, v, id_reg, w_reg);
     }
-    fused_prologue(p, smem, v, id_reg, w_reg);
 
     const int nact = *v.nact;
     const int n1 = nact * (p.I / 8);
