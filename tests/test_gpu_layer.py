@@ -94,6 +94,7 @@ CASES = [
     (2, 256, 16, 2, 128, False, False, False, True),       # a small grid, 4 rows a CTA
     (1, 512, 777, 31, 128, True, False, True, True),       # ragged rows, k + 1 = 32 slots
     (2, 128, 1024, 8, 128, False, True, False, True),      # the smallest ring holds the logits
+    (2, 512, 256, 24, 128, False, False, True, True),      # 48 assignments: the CTA-wide prologue after the selection
     (4, 2560, 512, 10, 640, False, False, True, False),    # from 3 tokens: the router's kernel, then the forward's
     (8, 2560, 512, 10, 640, True, True, False, False),
     (9, 2560, 512, 10, 640, False, False, False, False),   # T > 8: router kernels, tensor-core pipeline
