@@ -210,7 +210,7 @@ MOE_API int moe_layer_forward(const uint16_t *hidden, const uint16_t *router_w, 
  * device per process; the call allocates and frees nothing.
  *  - Served shapes: those of the fused decode path (T <= 8) whose
  *    moe_workspace_size() is at most 1 MiB (T = 7 at H 2560, E 512, k 10,
- *    I 640 needs about 0.45 MiB). A larger workspace size returns
+ *    I 640 needs about 0.51 MiB). A larger workspace size returns
  *    MOE_ERR_WORKSPACE and T > 8 returns MOE_ERR_UNSUPPORTED, in both cases
  *    before anything is enqueued. T = 0 returns MOE_OK.
  *  - The first call on a device looks up the array's device address (which
