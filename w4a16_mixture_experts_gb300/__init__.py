@@ -280,6 +280,10 @@ def moe_layer_forward(hidden, router_w, k: int, w1_packed, w1_scales, w2_packed,
     g = 1 if shared else 0
     E = router_w.shape[0] - g
     I = w1_packed.shape[1] // 2
+    if w1_packed.shape[0] != E + g or w2_packed.shape[0] != E + g:
+        raise ValueError("the weights must hold %d experts (router rows %d%s), got %d and %d"
+                         % (E + g, router_w.shape[0], ", the last the shared gate" if g else "",
+                            w1_packed.shape[0], w2_packed.shape[0]))
     dims = moe_dims(T, H, E, k, I)
     if ws is None:
         ws = shared_workspace(T, H, E, k, I, hidden.device) if shared else workspace(T, H, E, k, I, hidden.device)
